@@ -1,0 +1,269 @@
+"""fp64 CPU oracle for the fused quantized LM-head -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
+library never calls it and shares no code with it.
+
+The arithmetic lives in ``qhead_oracle.c`` (plain C, fp64, OpenMP over
+independent outputs); this module only builds that file with gcc, marshals
+numpy arrays and strings the steps together in the order the method defines
+them (page "mlx-bun 0.0.4 -> 0.0.6", src/train/flash-cce.ts):
+
+1. dequantize  w[v,d] = scale[v,d//group] * q[v,d] + bias[v,d//group]
+2. raw = h @ w.T
+3. z = cap*tanh(raw/cap) if cap > 0 else raw
+4. lse = logsumexp_v z;  logp = z[target] - lse;  argmax = first argmax of raw
+5. dh = sum_v dlogp*(onehot - exp(z - lse))*sech2 * w[v,:]
+
+Masked rows (mask == 0) are skipped: logp = lse = 0, argmax = -1, dh = 0.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qhead_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_f64p = ctypes.POINTER(ctypes.c_double)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+
+def build(force: bool = False) -> str:
+    """Compile qhead_oracle.c into liboracle.so (gcc, -O2, OpenMP, no fast-math,
+    no FMA contraction so x86 and Arm hosts give the same bits)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    lib.oracle_widen_bf16.argtypes = [_u16p, _f64p, _i64]
+    lib.oracle_widen_f16.argtypes = [_u16p, _f64p, _i64]
+    lib.oracle_codes.argtypes = [_u32p, _i64, _i64, _int, _u32p]
+    lib.oracle_dequant.argtypes = [_u32p, _f64p, _f64p, _i64, _i64, _int, _int, _f64p]
+    lib.oracle_logits.argtypes = [_i64, _i64, _i64, _int, _int, _f64p, _u32p, _f64p, _f64p,
+                                  _f64p, _int]
+    lib.oracle_row_stats.argtypes = [_i64, _i64, ctypes.c_double, _f64p, _i32p, _u8p, _f64p,
+                                     _f64p, _i64p, _f64p, _f64p, _int]
+    lib.oracle_coeff.argtypes = [_i64, _i64, ctypes.c_double, _f64p, _f64p, _i32p, _u8p,
+                                 _f64p, _int]
+    lib.oracle_dh.argtypes = [_i64, _i64, _i64, _int, _int, _u32p, _f64p, _f64p, _f64p,
+                              _f64p, _int]
+    lib.oracle_num_threads.argtypes = [_int]
+    lib.oracle_num_threads.restype = _int
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray | None, ctype):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctype)
+
+
+def num_threads(threads: int = 0) -> int:
+    """Threads the oracle's OpenMP loops use for ``threads`` (0 = all cores)."""
+    return int(_load().oracle_num_threads(threads))
+
+
+# ------------------------------------------------------------------ widening
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_widen_bf16(_ptr(b, _u16p), _ptr(out, _f64p), b.size)
+    return out
+
+
+def widen_f16(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bit patterns (uint16, or a float16 array) -> float64, exactly."""
+    b = np.ascontiguousarray(bits)
+    if b.dtype == np.float16:
+        b = b.view(np.uint16)
+    b = np.ascontiguousarray(b.astype(np.uint16, copy=False))
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_widen_f16(_ptr(b, _u16p), _ptr(out, _f64p), b.size)
+    return out
+
+
+def _as_f64_h(h: np.ndarray) -> np.ndarray:
+    """Hidden states: uint16 arrays are bf16 bit patterns; float64 is taken as is."""
+    if h.dtype == np.uint16:
+        return widen_bf16(h)
+    if h.dtype == np.float64:
+        return np.ascontiguousarray(h)
+    raise TypeError(f"oracle: h must be bf16 bits (uint16) or float64, got {h.dtype}")
+
+
+def _as_f64_sb(x: np.ndarray) -> np.ndarray:
+    """Scales/biases: float16 (or its uint16 bits) is widened; float64 is taken as is."""
+    if x.dtype in (np.float16, np.uint16):
+        return widen_f16(x)
+    if x.dtype == np.float64:
+        return np.ascontiguousarray(x)
+    raise TypeError(f"oracle: scales/biases must be float16 or float64, got {x.dtype}")
+
+
+# -------------------------------------------------------------------- head
+
+@dataclass
+class Head:
+    """The quantized head (FlashCceHead on the page): packed codes, per-group
+    affine scale and bias, bit width, group size and the optional soft cap."""
+    wq: np.ndarray          # uint32 [V, H*bits/32]
+    scales: np.ndarray      # float16 or float64 [V, H/group]
+    biases: np.ndarray      # float16 or float64 [V, H/group]
+    bits: int
+    group: int = 64
+    softcap: float = 0.0
+
+    @property
+    def V(self) -> int:
+        return int(self.wq.shape[0])
+
+    @property
+    def H(self) -> int:
+        return int(self.wq.shape[1]) * 32 // self.bits
+
+
+def codes(wq: np.ndarray, H: int, bits: int) -> np.ndarray:
+    """Unpacked codes q[v,d] (uint32 [V,H])."""
+    wq = np.ascontiguousarray(wq, dtype=np.uint32)
+    V = wq.shape[0]
+    out = np.empty((V, H), dtype=np.uint32)
+    _load().oracle_codes(_ptr(wq, _u32p), V, H, bits, _ptr(out, _u32p))
+    return out
+
+
+def dequant(head: Head) -> np.ndarray:
+    """Dense fp64 head w[v,d] (for small heads only: V*H doubles)."""
+    wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
+    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    out = np.empty((head.V, head.H), dtype=np.float64)
+    _load().oracle_dequant(_ptr(wq, _u32p), _ptr(s, _f64p), _ptr(b, _f64p), head.V, head.H,
+                           head.bits, head.group, _ptr(out, _f64p))
+    return out
+
+
+def _check(head: Head, hf: np.ndarray):
+    if head.bits not in (2, 4, 8):
+        raise ValueError(f"oracle: bits={head.bits}")
+    if head.H % head.group or head.group % (32 // head.bits):
+        raise ValueError("oracle: H must be a multiple of group, group of 32/bits")
+    if hf.ndim != 2 or hf.shape[1] != head.H:
+        raise ValueError(f"oracle: h shape {hf.shape} vs H={head.H}")
+
+
+def logits(h: np.ndarray, head: Head, threads: int = 0) -> np.ndarray:
+    """raw[m,v] = sum_d h[m,d] w[v,d]  (fp64 [M,V])."""
+    hf = _as_f64_h(h)
+    _check(head, hf)
+    wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
+    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    M = hf.shape[0]
+    raw = np.empty((M, head.V), dtype=np.float64)
+    _load().oracle_logits(M, head.H, head.V, head.bits, head.group, _ptr(hf, _f64p),
+                          _ptr(wq, _u32p), _ptr(s, _f64p), _ptr(b, _f64p), _ptr(raw, _f64p),
+                          threads)
+    return raw
+
+
+@dataclass
+class Forward:
+    logp: np.ndarray | None  # float64 [M] (None when no targets)
+    lse: np.ndarray          # float64 [M]
+    argmax: np.ndarray       # int64 [M], -1 on masked rows
+    gap: np.ndarray          # float64 [M], top-2 gap of the capped logits
+    zmax: np.ndarray         # float64 [M]
+    raw: np.ndarray | None   # float64 [M,V] when keep_raw
+
+
+def _targets(targets, M):
+    if targets is None:
+        return None
+    t = np.ascontiguousarray(targets, dtype=np.int32)
+    if t.shape != (M,):
+        raise ValueError("oracle: targets must be [M]")
+    return t
+
+
+def _mask(mask, M):
+    if mask is None:
+        return None
+    mk = np.ascontiguousarray(mask, dtype=np.uint8)
+    if mk.shape != (M,):
+        raise ValueError("oracle: mask must be [M]")
+    return mk
+
+
+def forward(h: np.ndarray, head: Head, targets=None, mask=None, threads: int = 0,
+            keep_raw: bool = False) -> Forward:
+    """logp, lse, argmax (and the top-2 gap of z) for every row of h."""
+    raw = logits(h, head, threads)
+    M, V = raw.shape
+    t = _targets(targets, M)
+    if t is not None and M and (t.min() < 0 or t.max() >= V):
+        raise ValueError("oracle: target out of range")
+    mk = _mask(mask, M)
+    logp = np.empty(M) if t is not None else None
+    lse, gap, zmax = np.empty(M), np.empty(M), np.empty(M)
+    am = np.empty(M, dtype=np.int64)
+    _load().oracle_row_stats(M, V, float(head.softcap), _ptr(raw, _f64p), _ptr(t, _i32p),
+                             _ptr(mk, _u8p), _ptr(logp, _f64p), _ptr(lse, _f64p),
+                             _ptr(am, _i64p), _ptr(gap, _f64p), _ptr(zmax, _f64p), threads)
+    return Forward(logp, lse, am, gap, zmax, raw if keep_raw else None)
+
+
+def backward(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
+             threads: int = 0) -> np.ndarray:
+    """dh = d(sum_m dlogp[m] * logp[m]) / dh  (fp64 [M,H]).  When ``lse`` is None
+    it is recomputed by the forward definition (the same value the forward
+    returns)."""
+    raw = logits(h, head, threads)
+    M, V = raw.shape
+    t = _targets(targets, M)
+    if t is None:
+        raise ValueError("oracle: backward needs targets")
+    mk = _mask(mask, M)
+    if lse is None:
+        tmp_lse, gap, zmax = np.empty(M), np.empty(M), np.empty(M)
+        am = np.empty(M, dtype=np.int64)
+        _load().oracle_row_stats(M, V, float(head.softcap), _ptr(raw, _f64p), None,
+                                 _ptr(mk, _u8p), None, _ptr(tmp_lse, _f64p), _ptr(am, _i64p),
+                                 _ptr(gap, _f64p), _ptr(zmax, _f64p), threads)
+        lse = tmp_lse
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    g = np.ascontiguousarray(np.broadcast_to(np.asarray(dlogp, dtype=np.float64), (M,)))
+    _load().oracle_coeff(M, V, float(head.softcap), _ptr(raw, _f64p), _ptr(lse, _f64p),
+                         _ptr(t, _i32p), _ptr(mk, _u8p), _ptr(g, _f64p), threads)
+    wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
+    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    dh = np.empty((M, head.H), dtype=np.float64)
+    _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
+                      _ptr(b, _f64p), _ptr(raw, _f64p), _ptr(dh, _f64p), threads)
+    return dh

@@ -1,0 +1,304 @@
+"""Pins for the fp64 oracle, each against something other than the oracle itself.
+
+* the packed layout against hand-packed words (tests/golden/pack_layout.txt);
+* fp16 / bf16 widening against numpy's and torch's own conversions, on every
+  bit pattern;
+* hand-derivable worked examples (closed forms for lse, logp, argmax, dh,
+  with and without the soft cap);
+* special cases: V = 1, identical vocab rows, a very large cap equals no cap,
+  a shared bias shift leaves logp / argmax / dh unchanged;
+* a library cross-check: torch fp64 log_softmax / logsumexp / argmax and
+  autograd's dh on an independently unpacked head;
+* finite differences of sum_m dlogp_m * logp_m against dh;
+* invariants: logp <= 0, max z <= lse <= max z + ln V, z at the argmax is the
+  row maximum.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from verify_vocab_blocked_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_layout():
+    rows = []
+    with open(os.path.join(GOLDEN, "pack_layout.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            bits, words, codes = line.rstrip("\n").split("\t")
+            rows.append((int(bits), [int(w, 16) for w in words.split()],
+                         [int(c) for c in codes.split()]))
+    return rows
+
+
+@pytest.mark.parametrize("case", _read_layout())
+def test_pack_layout_golden(case):
+    bits, words, expect = case
+    wq = np.array([words], dtype=np.uint32)
+    H = len(words) * 32 // bits
+    got = oracle.codes(wq, H, bits)[0]
+    assert got.tolist() == expect
+
+
+def _unpack_independent(wq: np.ndarray, bits: int) -> np.ndarray:
+    """Unpack through the little-endian bit string of each row (np.unpackbits),
+    not through shifts and masks."""
+    V, wpr = wq.shape
+    b = np.unpackbits(wq.astype("<u4").view(np.uint8).reshape(V, wpr * 4), axis=1,
+                      bitorder="little")
+    fields = b.reshape(V, wpr * 32 // bits, bits).astype(np.int64)
+    return (fields * (1 << np.arange(bits))).sum(axis=2)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_unpack_matches_bitstring_expansion(bits):
+    head = synth.make_head(37, 128, bits, seed=3)
+    assert np.array_equal(oracle.codes(head.wq, 128, bits), _unpack_independent(head.wq, bits))
+
+
+def test_widen_f16_all_patterns():
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.widen_f16(pats)
+    ref = pats.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_widen_bf16_all_patterns():
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.widen_bf16(pats)
+    ref = torch.from_numpy(pats.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+# ------------------------------------------------------------ worked examples
+
+def _const_code_head(codes_per_row, H=64, scale=1.0 / 64, bias=0.0, softcap=0.0):
+    """Row v has every 4-bit code equal to codes_per_row[v] (word = c * 0x11111111)."""
+    V = len(codes_per_row)
+    wq = np.array([[c * 0x11111111] * (H // 8) for c in codes_per_row], dtype=np.uint32)
+    s = np.full((V, H // 64), scale, dtype=np.float64)
+    b = np.full((V, H // 64), bias, dtype=np.float64)
+    return oracle.Head(wq, s, b, 4, 64, softcap)
+
+
+def test_worked_example_no_cap():
+    # h = ones(64), w_v = c_v / 64 everywhere, so raw = [0, 1, 2].
+    head = _const_code_head([0, 1, 2])
+    h = np.ones((1, 64), dtype=np.float64)
+    f = oracle.forward(h, head, targets=[1], keep_raw=True)
+    assert np.allclose(f.raw[0], [0.0, 1.0, 2.0], atol=1e-15)
+    lse = math.log(1 + math.e + math.e ** 2)
+    assert abs(f.lse[0] - lse) < 1e-14
+    assert abs(f.logp[0] - (1.0 - lse)) < 1e-14
+    assert f.argmax[0] == 2
+    assert abs(f.gap[0] - 1.0) < 1e-14
+    # dh = sum_v (onehot_v - p_v) w_v = (c_t - E_p[c]) / 64 in every column.
+    p = np.exp(np.array([0.0, 1.0, 2.0]) - lse)
+    expect = (1.0 - (p * [0, 1, 2]).sum()) / 64
+    dh = oracle.backward(h, head, [1], 1.0)
+    assert np.allclose(dh, expect, atol=1e-15, rtol=1e-13)
+    # The sign follows d(dlogp * logp)/dh: a negative cotangent flips it.
+    dh_neg = oracle.backward(h, head, [1], -2.5)
+    assert np.allclose(dh_neg, -2.5 * expect, atol=1e-15, rtol=1e-13)
+
+
+def test_worked_example_softcap():
+    # cap = 1: z = tanh(raw); sech2 = 1 - tanh(raw)^2 scales every coefficient.
+    head = _const_code_head([0, 1, 2], softcap=1.0)
+    h = np.ones((1, 64), dtype=np.float64)
+    f = oracle.forward(h, head, targets=[2])
+    z = np.tanh([0.0, 1.0, 2.0])
+    lse = math.log(np.exp(z).sum())
+    assert abs(f.lse[0] - lse) < 1e-14
+    assert abs(f.logp[0] - (z[2] - lse)) < 1e-14
+    assert f.argmax[0] == 2
+    assert abs(f.gap[0] - (z[2] - z[1])) < 1e-14
+    p = np.exp(z - lse)
+    sech2 = 1 - z ** 2
+    coeff = (np.array([0.0, 0.0, 1.0]) - p) * sech2
+    expect = (coeff * np.array([0, 1, 2]) / 64).sum()
+    dh = oracle.backward(h, head, [2], 1.0)
+    assert np.allclose(dh, expect, atol=1e-15, rtol=1e-12)
+
+
+def test_worked_example_group_scales():
+    # Two groups with different scales and biases; h = ones(128); row 0 has code 3
+    # in group 0 and code 5 in group 1, row 1 is all zeros.
+    wq = np.zeros((2, 16), dtype=np.uint32)
+    wq[0, :8] = 3 * 0x11111111
+    wq[0, 8:] = 5 * 0x11111111
+    s = np.array([[0.25, 0.5], [1.0, 1.0]])
+    b = np.array([[-0.5, 0.125], [0.0, -0.25]])
+    head = oracle.Head(wq, s, b, 4, 64, 0.0)
+    raw = oracle.logits(np.ones((1, 128)), head)[0]
+    assert np.allclose(raw, [64 * (0.25 * 3 - 0.5) + 64 * (0.5 * 5 + 0.125),
+                             64 * 0.0 + 64 * (-0.25)], atol=1e-12)
+
+
+# -------------------------------------------------------------- special cases
+
+@pytest.mark.parametrize("cap", [0.0, 30.0])
+def test_single_vocab_row(cap):
+    head = synth.make_head(1, 128, 4, softcap=cap, seed=1)
+    ohead = oracle.Head(head.wq, head.scales, head.biases, 4, 64, cap)
+    h = synth.make_hidden(3, 128, seed=1)
+    f = oracle.forward(h, ohead, targets=[0, 0, 0], keep_raw=True)
+    z = cap * np.tanh(f.raw[:, 0] / cap) if cap else f.raw[:, 0]
+    assert np.allclose(f.lse, z, atol=1e-13)
+    assert np.allclose(f.logp, 0.0, atol=1e-13)
+    assert (f.argmax == 0).all()
+    dh = oracle.backward(h, ohead, [0, 0, 0], 1.0)
+    assert np.abs(dh).max() < 1e-13
+
+
+@pytest.mark.parametrize("cap", [0.0, 5.0])
+def test_identical_rows(cap):
+    base = synth.make_head(1, 128, 4, seed=2)
+    V = 7
+    head = oracle.Head(np.repeat(base.wq, V, 0), np.repeat(base.scales, V, 0),
+                       np.repeat(base.biases, V, 0), 4, 64, cap)
+    h = synth.make_hidden(4, 128, seed=2)
+    t = np.array([0, 3, 6, 2])
+    f = oracle.forward(h, head, targets=t)
+    assert np.allclose(f.logp, -math.log(V), atol=1e-13)
+    assert (f.argmax == 0).all()
+    assert np.allclose(f.gap, 0.0)
+    dh = oracle.backward(h, head, t, 1.0)
+    assert np.abs(dh).max() < 1e-13
+
+
+def test_huge_cap_equals_no_cap():
+    wl = synth.make_workload("tiny")
+    h0 = oracle.Head(wl.head.wq, wl.head.scales, wl.head.biases, 4, 64, 0.0)
+    h1 = oracle.Head(wl.head.wq, wl.head.scales, wl.head.biases, 4, 64, 1e9)
+    f0 = oracle.forward(wl.h, h0, wl.targets)
+    f1 = oracle.forward(wl.h, h1, wl.targets)
+    assert np.allclose(f0.lse, f1.lse, atol=1e-9)
+    assert np.allclose(f0.logp, f1.logp, atol=1e-9)
+    assert np.array_equal(f0.argmax, f1.argmax)
+    d0 = oracle.backward(wl.h, h0, wl.targets, 1.0)
+    d1 = oracle.backward(wl.h, h1, wl.targets, 1.0)
+    assert np.allclose(d0, d1, atol=1e-9)
+
+
+def test_shared_bias_shift_invariance():
+    # Adding delta to every bias shifts every logit of token m by delta * sum_d h[m,d]:
+    # lse shifts by that amount, logp / argmax / dh (no cap) are unchanged.
+    wl = synth.make_workload("tiny")
+    s = oracle.widen_f16(wl.head.scales).reshape(wl.head.scales.shape)
+    b = oracle.widen_f16(wl.head.biases).reshape(wl.head.biases.shape)
+    delta = 0.0371
+    ha = oracle.Head(wl.head.wq, s, b, 4, 64, 0.0)
+    hb = oracle.Head(wl.head.wq, s, b + delta, 4, 64, 0.0)
+    fa = oracle.forward(wl.h, ha, wl.targets)
+    fb = oracle.forward(wl.h, hb, wl.targets)
+    hsum = oracle.widen_bf16(wl.h).sum(axis=1)
+    assert np.allclose(fb.lse - fa.lse, delta * hsum, atol=1e-10)
+    assert np.allclose(fa.logp, fb.logp, atol=1e-10)
+    assert np.array_equal(fa.argmax, fb.argmax)
+    g = synth.make_dlogp(wl.M, seed=4)
+    da = oracle.backward(wl.h, ha, wl.targets, g)
+    db = oracle.backward(wl.h, hb, wl.targets, g)
+    assert np.allclose(da, db, atol=1e-10)
+
+
+# ----------------------------------------------------- library cross-check
+
+def _torch_reference(h64, head: oracle.Head, targets, dlogp):
+    """torch fp64: dense head from the bit-string unpack, log_softmax, autograd."""
+    q = torch.from_numpy(_unpack_independent(head.wq, head.bits)).double()
+    s = torch.from_numpy(head.scales.astype(np.float64))
+    b = torch.from_numpy(head.biases.astype(np.float64))
+    w = q * s.repeat_interleave(head.group, 1) + b.repeat_interleave(head.group, 1)
+    h = torch.from_numpy(h64).clone().requires_grad_(True)
+    raw = h @ w.T
+    z = head.softcap * torch.tanh(raw / head.softcap) if head.softcap > 0 else raw
+    lp = torch.log_softmax(z, dim=1)
+    t = torch.from_numpy(np.asarray(targets, dtype=np.int64))
+    logp = lp.gather(1, t[:, None])[:, 0]
+    (torch.from_numpy(np.asarray(dlogp, dtype=np.float64)) * logp).sum().backward()
+    return (logp.detach().numpy(), torch.logsumexp(z, 1).detach().numpy(),
+            torch.argmax(raw, 1).numpy(), h.grad.numpy())
+
+
+@pytest.mark.parametrize("name,V,cap", [("tiny", None, None), ("gemma512", 4096, None),
+                                        ("mid8", 2048, None), ("gemma512", 1500, 0.0)])
+def test_against_torch_autograd(name, V, cap):
+    cfg = synth.CONFIGS[name]
+    V = V or cfg["V"]
+    cap = cfg["softcap"] if cap is None else cap
+    head = synth.make_head(V, cfg["H"], cfg["bits"], softcap=cap, seed=11)
+    ohead = oracle.Head(head.wq, head.scales, head.biases, cfg["bits"], 64, cap)
+    M = 6
+    h = synth.make_hidden(M, cfg["H"], seed=11)
+    t = synth.make_targets(M, V, seed=11)
+    g = synth.make_dlogp(M, seed=11).astype(np.float64)
+    f = oracle.forward(h, ohead, t)
+    dh = oracle.backward(h, ohead, t, g)
+    r_logp, r_lse, r_am, r_dh = _torch_reference(oracle.widen_bf16(h), ohead, t, g)
+    assert np.allclose(f.logp, r_logp, atol=1e-10, rtol=0)
+    assert np.allclose(f.lse, r_lse, atol=1e-10, rtol=0)
+    assert np.array_equal(f.argmax, r_am)
+    assert np.abs(dh - r_dh).max() <= 1e-10 * max(1.0, np.abs(r_dh).max())
+
+
+# ---------------------------------------------------------- finite differences
+
+@pytest.mark.parametrize("cap", [0.0, 2.0])
+def test_finite_differences(cap):
+    head = synth.make_head(300, 128, 4, softcap=cap, seed=5)
+    ohead = oracle.Head(head.wq, head.scales, head.biases, 4, 64, cap)
+    M = 5
+    h = oracle.widen_bf16(synth.make_hidden(M, 128, seed=5)) * 3.0
+    t = synth.make_targets(M, 300, seed=5)
+    g = synth.make_dlogp(M, seed=5).astype(np.float64)
+    mask = np.array([1, 0, 1, 1, 0], dtype=np.uint8)
+    dh = oracle.backward(h, ohead, t, g, mask=mask)
+    assert np.all(dh[mask == 0] == 0.0)
+
+    def f(x):
+        return float((g * oracle.forward(x, ohead, t, mask=mask).logp).sum())
+
+    rng = np.random.default_rng(0)
+    for _ in range(3):
+        u = rng.standard_normal(h.shape)
+        eps = 1e-5
+        fd = (f(h + eps * u) - f(h - eps * u)) / (2 * eps)
+        an = float((dh * u).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (fd, an)
+
+
+# ------------------------------------------------------------------ invariants
+
+@pytest.mark.parametrize("name", ["tiny", "gemma512"])
+def test_invariants(name):
+    cfg = synth.CONFIGS[name]
+    V = min(cfg["V"], 8192)
+    head = synth.make_head(V, cfg["H"], cfg["bits"], softcap=cfg["softcap"], seed=9)
+    ohead = oracle.Head(head.wq, head.scales, head.biases, cfg["bits"], 64, cfg["softcap"])
+    M = 8
+    h = synth.make_hidden(M, cfg["H"], seed=9)
+    t = synth.make_targets(M, V, seed=9)
+    mask = np.array([1, 1, 0, 1, 1, 1, 0, 1], dtype=np.uint8)
+    f = oracle.forward(h, ohead, t, mask=mask, keep_raw=True)
+    act = mask == 1
+    assert (f.logp[act] <= 0).all()
+    assert (f.lse[act] >= f.zmax[act]).all()
+    assert (f.lse[act] <= f.zmax[act] + math.log(V) + 1e-12).all()
+    cap = cfg["softcap"]
+    z = cap * np.tanh(f.raw / cap) if cap else f.raw
+    for m in np.nonzero(act)[0]:
+        assert abs(z[m, f.argmax[m]] - f.zmax[m]) <= 1e-12
+        assert f.argmax[m] == int(np.argmax(f.raw[m]))
+    assert (f.argmax[~act] == -1).all() and (f.logp[~act] == 0).all()
