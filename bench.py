@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the fused quantized LM-head on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+  * verify (default; the gamma+1 speculative-decode window): one forward
+    (lse + argmax of every position) over M = 5 rows;
+  * training configs (gemma512, mid8, gemma8k_masked, tiny): forward (logp,
+    lse, argmax) + backward (dh) over all rows.
+`value` is tokens/s over all ranks with inputs already resident in HBM;
+`e2e` is the same metric through the C ABI with the step's inputs copied from
+pinned host memory and its results read back inside the timed region.
+Multi-GPU runs are replicas (weak scaling): every rank runs the same
+workload on its own GPU, timed between barriers, max over ranks.
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from verify_vocab_blocked_gb300 import synth  # noqa: E402
+
+METRIC = "fused qhead logp tokens/s (fwd, fwd+bwd) + % of tensor-core / HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = "verify"
+# The pages' own time for the e4b-class head at M=512 (forward 180 ms, backward
+# 754 ms, Apple M1 Max, fp32 operands): the only workload they time that
+# matches one of ours (gemma512, forward + backward).
+PAGES_TOKENS_PER_S = {"gemma512": 512 / (0.180 + 0.754)}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _traffic(kernel: str):
+    """ncu DRAM bytes per launch for `kernel`, if recorded for the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "verify_vocab_blocked_gb300", "csrc", e["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != e["sha256_16"]:
+            return None
+    return e
+
+
+def workload_desc(name: str, cfg: dict) -> dict:
+    d = {"workload": f"{name}: {cfg['desc']}", "M": cfg["M"], "H": cfg["H"], "V": cfg["V"],
+         "bits": cfg["bits"], "group": cfg["group"], "softcap": cfg["softcap"],
+         "pass": "fwd+bwd" if cfg["bwd"] else "fwd",
+         "l2": "inputs larger than L2 (packed head %.1f MB > 129 MB L2)"
+               % (cfg["V"] * (cfg["H"] * cfg["bits"] / 8 + 4 * cfg["H"] / 64) / 1e6),
+         "parallelism": "replicas"}
+    if cfg.get("mask"):
+        d["mask"] = "30%% masked: prompt prefix of %d tokens per %d-token sequence" % (
+            round(cfg["mask"][1] * cfg["mask"][0]), cfg["mask"][0])
+    return d
+
+
+def head_bytes(cfg: dict) -> int:
+    """Algorithmic bytes of one pass over the head: packed codes + fp16 scales and biases."""
+    V, H = cfg["V"], cfg["H"]
+    return V * (H * cfg["bits"] // 8 + 2 * 2 * (H // 64))
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Runner:
+    """Device buffers for one workload and the C-ABI calls of one step."""
+
+    def __init__(self, wl: synth.Workload, device):
+        import torch
+        from verify_vocab_blocked_gb300 import qhead
+        self.torch, self.q = torch, qhead
+        self.wl = wl
+        self.dev = device
+        self.head = qhead.Head.from_numpy(wl.head.wq, wl.head.scales, wl.head.biases,
+                                          wl.head.bits, wl.head.group, wl.head.softcap,
+                                          device=device)
+        M = wl.M
+        self.M = M
+        self.h_host = torch.from_numpy(wl.h.astype(np.int16)).view(torch.bfloat16).pin_memory()
+        self.h = self.h_host.to(device)
+        self.bwd = bool(wl.cfg["bwd"])
+        self.t_host = (torch.from_numpy(wl.targets).pin_memory()
+                       if wl.targets is not None else None)
+        self.t = self.t_host.to(device) if self.t_host is not None else None
+        self.m_host = torch.from_numpy(wl.mask).pin_memory() if wl.mask is not None else None
+        self.mk = self.m_host.to(device) if self.m_host is not None else None
+        self.g_host = torch.from_numpy(wl.dlogp).pin_memory()
+        self.g = self.g_host.to(device)
+        f32, i32 = torch.float32, torch.int32
+        self.logp = torch.empty(M, dtype=f32, device=device) if self.t is not None else None
+        self.lse = torch.empty(M, dtype=f32, device=device)
+        self.am = torch.empty(M, dtype=i32, device=device)
+        self.dh = torch.empty(M, wl.head.H, dtype=f32, device=device) if self.bwd else None
+        n = qhead.fwd_workspace(self.head, M)
+        if self.bwd:
+            n = max(n, qhead.bwd_workspace(self.head, M))
+        self.ws = qhead.alloc_workspace(n, device)
+        self.chead = self.head.c()
+        self.stream = torch.cuda.current_stream(device)
+        # pinned outputs for the end-to-end leg
+        self.out_host = {k: torch.empty_like(v, device="cpu").pin_memory()
+                         for k, v in (("lse", self.lse), ("am", self.am), ("logp", self.logp),
+                                      ("dh", self.dh)) if v is not None}
+        self.launches_per_step = 4 + (3 if self.bwd else 0)
+        self.active = int(wl.mask.sum()) if wl.mask is not None else M
+
+    def _ptr(self, t):
+        return None if t is None else t.data_ptr()
+
+    def step(self, ev_fwd=None, ev_bwd=None):
+        import ctypes
+        L = self.q.lib()
+        if ev_fwd is not None:
+            L.qhead_time_next_head_kernel(ev_fwd[0].cuda_event, ev_fwd[1].cuda_event)
+        rc = L.qhead_fwd(ctypes.byref(self.chead), self.h.data_ptr(), self.M, self._ptr(self.t),
+                         self._ptr(self.mk), self._ptr(self.logp), self.lse.data_ptr(),
+                         self.am.data_ptr(), self.ws.data_ptr(), self.ws.numel(),
+                         self.stream.cuda_stream)
+        if rc:
+            raise RuntimeError(self.q.last_error())
+        if self.bwd:
+            if ev_bwd is not None:
+                L.qhead_time_next_head_kernel(ev_bwd[0].cuda_event, ev_bwd[1].cuda_event)
+            rc = L.qhead_bwd(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
+                             self.t.data_ptr(), self._ptr(self.mk), self.lse.data_ptr(),
+                             self.g.data_ptr(), self.dh.data_ptr(), self.ws.data_ptr(),
+                             self.ws.numel(), self.stream.cuda_stream)
+            if rc:
+                raise RuntimeError(self.q.last_error())
+
+    def h2d(self):
+        n = 0
+        for src, dst in ((self.h_host, self.h), (self.t_host, self.t), (self.m_host, self.mk),
+                         (self.g_host if self.bwd else None, self.g)):
+            if src is not None:
+                dst.copy_(src, non_blocking=True)
+                n += src.numel() * src.element_size()
+        return n
+
+    def d2h(self):
+        n = 0
+        for k, dev in (("lse", self.lse), ("am", self.am), ("logp", self.logp), ("dh", self.dh)):
+            if dev is not None:
+                self.out_host[k].copy_(dev, non_blocking=True)
+                n += dev.numel() * dev.element_size()
+        return n
+
+
+def aggregate(elapsed_ms: float, units: float, world: int, dist=None) -> tuple[float, float]:
+    """Max of the ranks' elapsed time and the sum of their units (replicas)."""
+    if world > 1 and dist is not None:
+        import torch
+        t = torch.tensor([elapsed_ms], dtype=torch.float64)
+        u = torch.tensor([units], dtype=torch.float64)
+        if dist.get_backend() == "nccl":
+            t, u = t.cuda(), u.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        return float(t.item()), float(u.item())
+    return elapsed_ms, units
+
+
+def cpu_baseline(wl: synth.Workload, budget_s: float = 12.0, max_reps: int = 64) -> dict:
+    """The fp64 oracle, as it stands, on a bounded sample: one row of the
+    workload (full vocab), forward (+ backward for training configs), repeated
+    until the budget is spent."""
+    import oracle
+    oh = oracle.Head(wl.head.wq, wl.head.scales, wl.head.biases, wl.head.bits, wl.head.group,
+                     wl.head.softcap)
+    bwd = bool(wl.cfg["bwd"])
+    act = np.nonzero(wl.mask)[0] if wl.mask is not None else np.arange(wl.M)
+    t0 = time.perf_counter()
+    reps = 0
+    while reps < max_reps:
+        r = act[reps % len(act):reps % len(act) + 1]
+        tg = wl.targets[r] if wl.targets is not None else None
+        f = oracle.forward(wl.h[r], oh, tg)
+        if bwd:
+            oracle.backward(wl.h[r], oh, tg, wl.dlogp[r].astype(np.float64), lse=f.lse)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": reps / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} x 1 row of the workload (full V={wl.head.V}), "
+                      f"{'fwd+bwd' if bwd else 'fwd'}, fp64, {el:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = synth.CONFIGS[args.config]
+    wl = synth.make_workload(args.config, seed=0)
+    R = Runner(wl, dev)
+    K, W = args.steps, args.warmup
+
+    # warm-up (also creates the timing events)
+    mk_ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev_f = [(mk_ev(), mk_ev()) for _ in range(K)]
+    ev_b = [(mk_ev(), mk_ev()) for _ in range(K)] if R.bwd else [None] * K
+    for pair in ev_f + [p for p in ev_b if p]:
+        pair[0].record()
+        pair[1].record()
+    for _ in range(W):
+        R.step()
+    torch.cuda.synchronize()
+
+    # device-resident timed region
+    t0, t1 = mk_ev(), mk_ev()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record()
+        for i in range(K):
+            R.step(ev_f[i], ev_b[i])
+        t1.record()
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    el = t0.elapsed_time(t1)
+    el_max, units = aggregate(el, R.active * K, world, dist)
+    value = units / (el_max / 1e3)
+    fwd_ms = [a.elapsed_time(b) for a, b in ev_f]
+    bwd_ms = [a.elapsed_time(b) for a, b in ev_b if ev_b[0] is not None] if R.bwd else []
+
+    # end-to-end timed region: pinned host inputs -> C ABI -> host outputs
+    Ke = K
+    torch.cuda.synchronize()
+    e0, e1 = mk_ev(), mk_ev()
+    if dist:
+        dist.barrier()
+    e0.record()
+    h2d = d2h = 0
+    for _ in range(Ke):
+        h2d = R.h2d()
+        R.step()
+        d2h = R.d2h()
+    e1.record()
+    torch.cuda.synchronize()
+    el_e = e0.elapsed_time(e1)
+    el_e_max, units_e = aggregate(el_e, R.active * Ke, world, dist)
+
+    hbm, tf_burst, tf_sus, peak_src = _peaks()
+    if R.bwd:
+        # dominant kernel: the backward contraction (recompute + dh): 4*Ma*V*H flop
+        dom = "bwd_simt_kernel"
+        flops = 4.0 * R.active * cfg["V"] * cfg["H"]
+        kms = statistics.mean(bwd_ms)
+        achieved = flops / (kms / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tf_sus,
+                "unit": "TFLOP/s", "frac": achieved / tf_sus,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (dense, same rate as fp16)",
+                "work_per_launch": f"{flops:.3e} flop (4*Ma*V*H)", "ms_per_launch": kms}
+        fms = statistics.mean(fwd_ms)
+        ff = 2.0 * R.active * cfg["V"] * cfg["H"]
+        roof["fwd_kernel"] = {"kernel": "stream_fwd_kernel", "ms_per_launch": fms,
+                              "achieved_tflops": ff / (fms / 1e3) / 1e12}
+    else:
+        dom = "stream_fwd_kernel"
+        nbytes = head_bytes(cfg)
+        kms = statistics.mean(fwd_ms)
+        achieved = nbytes / (kms / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                "work_per_launch": f"{nbytes} bytes (packed head + fp16 scales/biases)",
+                "ms_per_launch": kms}
+    tr = _traffic(dom)
+    roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": el_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / PAGES_TOKENS_PER_S[args.config]
+                        if args.config in PAGES_TOKENS_PER_S else None),
+        "dtype": "f16", "data": "synthetic (seeded; no real weights or data)",
+        "config": workload_desc(args.config, cfg),
+        "roofline": roof,
+        "e2e": {"value": units_e / (el_e_max / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": R.launches_per_step * K,
+        "clocks": clk.summary(),
+        "impl": "ours",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, each step a bounded sample (one row of
+    the workload over the full vocab), stopped early past a time cap."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cfg = synth.CONFIGS[args.config]
+    wl = synth.make_workload(args.config, seed=0)
+    oracle.build()
+    oh = oracle.Head(wl.head.wq, wl.head.scales, wl.head.biases, wl.head.bits, wl.head.group,
+                     wl.head.softcap)
+    bwd = bool(cfg["bwd"])
+    act = np.nonzero(wl.mask)[0] if wl.mask is not None else np.arange(wl.M)
+
+    def one(i):
+        r = act[i % len(act):i % len(act) + 1]
+        tg = wl.targets[r] if wl.targets is not None else None
+        f = oracle.forward(wl.h[r], oh, tg)
+        if bwd:
+            oracle.backward(wl.h[r], oh, tg, wl.dlogp[r].astype(np.float64), lse=f.lse)
+
+    cap_s = 180.0
+    w0 = time.perf_counter()
+    for i in range(args.warmup):
+        one(i)
+        if time.perf_counter() - w0 > cap_s / 4:
+            break
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        one(i)
+        done += 1
+        if time.perf_counter() - t0 > cap_s:
+            break
+    el = time.perf_counter() - t0
+    value = done / el
+    sample = (f"{done} of {args.steps} steps (time cap {cap_s:.0f} s), each 1 row of the workload "
+              f"(full V={cfg['V']}), {'fwd+bwd' if bwd else 'fwd'}, fp64")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", 1)),
+        "steps": done, "warmup": args.warmup, "ms_per_step": el / max(done, 1) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; no real weights or data)",
+        "config": workload_desc(args.config, cfg), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    fwd_only = not synth.CONFIGS[args.config]["bwd"]
+    if args.steps is None:
+        args.steps = 3000 if fwd_only else 5
+    if args.warmup is None:
+        args.warmup = 50 if fwd_only else 3
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

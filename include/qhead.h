@@ -1,0 +1,164 @@
+/*
+ * qhead.h -- C ABI of the GB300 fused quantized LM-head ("Flash Cut-Cross-
+ * Entropy" over a frozen 4/8-bit affine-quantized head).
+ *
+ * The operation is the one described on the page "mlx-bun 0.0.4 -> 0.0.6"
+ * (src/train/flash-cce.ts): for hidden states h[M,H] and a quantized head W
+ * (FlashCceHead: packed uint32 codes, per-group scales and biases, bits,
+ * group size, optional final-logit soft cap)
+ *
+ *     w[v,d]   = scale[v, d/group] * q[v,d] + bias[v, d/group]
+ *     raw[m,v] = sum_d h[m,d] * w[v,d]
+ *     z[m,v]   = cap * tanh(raw[m,v] / cap)      (z = raw when cap <= 0)
+ *     lse[m]   = log sum_v exp(z[m,v])
+ *     logp[m]  = z[m, target[m]] - lse[m]
+ *
+ * and, for the frozen head, the gradient of sum_m dlogp[m] * logp[m]:
+ *
+ *     dh[m,:]  = sum_v dlogp[m] * (1[v == target[m]] - exp(z[m,v] - lse[m]))
+ *                              * sech2[m,v] * w[v,:]
+ *     sech2    = 1 - tanh^2(raw / cap)           (1 when the cap is off)
+ *
+ * The vocab loop runs inside the kernels: neither the [M,V] logits nor a
+ * dequantized [V,H] head is ever written to device memory.  The same call
+ * with targets == NULL is the speculative-decode verify step of the page
+ * "mlx-bun 0.0.8 -> 0.0.10" (src/spec/generate.ts, picksBatched): one head
+ * pass over the gamma+1 window, then the argmax of every position (argmax of
+ * the raw logits; the soft cap and the lse shift are monotone, so it is also
+ * the argmax of z and of logp).
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers unless stated otherwise.
+ *   - The caller owns and allocates every input, output and workspace; the
+ *     library allocates nothing and keeps no per-call state.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  Nothing synchronizes.
+ *   - Return value: QHEAD_OK or an error code; on error nothing was launched
+ *     (argument errors) or a launch failed (QHEAD_ECUDA).  A message for the
+ *     calling thread is available from qhead_last_error().
+ *   - There is no fallback path: unsupported shapes are rejected.
+ */
+#ifndef QHEAD_H
+#define QHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define QHEAD_OK 0
+#define QHEAD_EINVAL 1        /* null required pointer, misalignment, bad size, small workspace */
+#define QHEAD_EUNSUPPORTED 2  /* bits / group / H / dtype this build does not implement */
+#define QHEAD_ECUDA 3         /* a CUDA launch or runtime call failed */
+
+/* Element type of scales and biases. */
+#define QHEAD_SB_F16 0
+
+/*
+ * The frozen quantized head (FlashCceHead on the page "mlx-bun 0.0.4 ->
+ * 0.0.6", src/train/flash-cce.ts).
+ *   wq       device, uint32 [V, H*bits/32], row-major.  Word j of row v holds
+ *            elements j*(32/bits) + k, k = 0 .. 32/bits - 1, element k in bits
+ *            bits*k .. bits*k + bits - 1 (least-significant field first).
+ *            16-byte aligned.
+ *   scales   device, fp16 [V, H/group], row-major.  2-byte aligned.
+ *   biases   device, fp16 [V, H/group], row-major.  2-byte aligned.
+ *   V        vocab rows, 1 <= V < 2^31.
+ *   H        hidden size: a multiple of 128, 128 <= H <= 8192.
+ *   bits     4 or 8.
+ *   group    64 (the only group size implemented).
+ *   sb_dtype QHEAD_SB_F16.
+ *   softcap  final-logit soft cap; <= 0 turns it off.
+ */
+typedef struct qhead_head {
+    const uint32_t* wq;
+    const void* scales;
+    const void* biases;
+    int64_t V;
+    int32_t H;
+    int32_t bits;
+    int32_t group;
+    int32_t sb_dtype;
+    float softcap;
+} qhead_head;
+
+/*
+ * Workspace bytes qhead_fwd / qhead_bwd need for M rows with this head on the
+ * current device (the plan depends on M, the head's shape and the SM count).
+ * Returns 0 for M == 0 and (size_t)-1 if the arguments are invalid (see
+ * qhead_last_error()).  Host-only; launches nothing.
+ */
+size_t qhead_fwd_workspace(const qhead_head* head, int64_t M);
+size_t qhead_bwd_workspace(const qhead_head* head, int64_t M);
+
+/*
+ * Forward: logp, lse and argmax for every row of h.
+ * Definition: flashCceForward on the page "mlx-bun 0.0.4 -> 0.0.6"
+ * (src/train/flash-cce.ts, per-vocab-block partials merged into lse and
+ * logp = target logit - lse); argmax as in picksBatched on the page
+ * "mlx-bun 0.0.8 -> 0.0.10" (src/spec/generate.ts).
+ *   h         device, bf16 [M, H] row-major, 16-byte aligned.
+ *   M         rows, >= 0 (M == 0 returns QHEAD_OK and launches nothing).
+ *   targets   device, int32 [M], or NULL (verify: no logp).  Each active
+ *             row's target must lie in [0, V); a row whose target does not
+ *             gets logp = NaN (no out-of-range read happens).
+ *   mask      device, uint8 [M], or NULL (all rows active).  mask[m] != 0
+ *             means row m is active; inactive rows are skipped and written as
+ *             logp = 0, lse = 0, argmax = -1.
+ *   logp      device, float [M], or NULL.  Requires targets.
+ *   lse       device, float [M], or NULL.
+ *   argmax    device, int32 [M], or NULL.  The lowest vocab index attaining
+ *             the row's maximum logit (ties within float rounding of each
+ *             other may resolve to either index).
+ *   workspace device, >= qhead_fwd_workspace(head, M) bytes, 256-byte
+ *             aligned; contents on entry are ignored.
+ * Outputs may not alias inputs or each other.
+ */
+int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+              const uint8_t* mask, float* logp, float* lse, int32_t* argmax, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of the frozen head: dh = d(sum_m dlogp[m] * logp[m]) / dh.
+ * Definition: flashCceBackward on the page "mlx-bun 0.0.4 -> 0.0.6"
+ * (src/train/flash-cce.ts: logits recomputed per vocab tile, coefficient
+ * dlogp * (onehot - softmax) * sech2, dh accumulated over all vocab blocks),
+ * with the forward's lse reused.
+ *   h, M, targets, mask  as for qhead_fwd; targets is required.
+ *   lse       device, float [M]: the lse qhead_fwd returned for the same
+ *             h / head / mask.
+ *   dlogp     device, float [M]: the cotangent of each row's logp.
+ *   dh        device, float [M, H] row-major, 16-byte aligned.  Every row is
+ *             written; inactive rows are exactly 0.
+ *   workspace device, >= qhead_bwd_workspace(head, M) bytes, 256-byte aligned.
+ * The result is deterministic: fixed-order reductions, no float atomics.
+ */
+int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+              const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Message for the last error on the calling thread ("" if none).  The
+ * pointer stays valid until the thread's next qhead_* call. */
+const char* qhead_last_error(void);
+
+/*
+ * Instrumentation (no counterpart on the pages): arm a one-shot hook on the
+ * calling thread.  The thread's next qhead_fwd or qhead_bwd call records the
+ * CUDA event `start` on its stream immediately before its head kernel (the
+ * vocab-streaming contraction that dominates the call) and `stop`
+ * immediately after it, then disarms the hook.  start and stop are
+ * cudaEvent_t handles passed as void*; passing NULL for both disarms.
+ */
+void qhead_time_next_head_kernel(void* start, void* stop);
+
+/* Library version string, e.g. "qhead 0.1.0 sm_103a". */
+const char* qhead_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QHEAD_H */

@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+symbol include/qhead.h declares, and argument errors come back as the
+documented status codes before anything touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from verify_vocab_blocked_gb300 import build as qbuild
+from verify_vocab_blocked_gb300 import qhead
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qhead.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return qhead.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qhead_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_lists():
+    assert set(_declared_functions()) == set(qhead.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version(L):
+    assert L.qhead_version().decode().startswith("qhead ")
+
+
+def _head(**kw):
+    # Plausible-looking, never-dereferenced device addresses: every case below
+    # fails argument checks before any CUDA call.
+    base = dict(wq=0x10000, scales=0x20000, biases=0x30000, V=1000, H=256, bits=4, group=64,
+                sb_dtype=qhead.QHEAD_SB_F16, softcap=0.0)
+    base.update(kw)
+    return qhead.CHead(**base)
+
+
+FWD_ARGS = dict(h=0x40000, M=4, targets=None, mask=None, logp=None, lse=0x50000, argmax=None,
+                ws=0x60000, ws_bytes=1 << 20, stream=None)
+
+
+def _fwd(L, head, **kw):
+    a = dict(FWD_ARGS)
+    a.update(kw)
+    return L.qhead_fwd(ctypes.byref(head) if head is not None else None, a["h"], a["M"],
+                       a["targets"], a["mask"], a["logp"], a["lse"], a["argmax"], a["ws"],
+                       a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), qhead.QHEAD_EUNSUPPORTED),
+    (dict(bits=2), qhead.QHEAD_EUNSUPPORTED),
+    (dict(group=32), qhead.QHEAD_EUNSUPPORTED),
+    (dict(sb_dtype=7), qhead.QHEAD_EUNSUPPORTED),
+    (dict(H=192), qhead.QHEAD_EUNSUPPORTED),
+    (dict(H=64), qhead.QHEAD_EUNSUPPORTED),
+    (dict(H=8320), qhead.QHEAD_EUNSUPPORTED),
+    (dict(V=0), qhead.QHEAD_EINVAL),
+    (dict(V=1 << 31), qhead.QHEAD_EINVAL),
+    (dict(wq=0x10004), qhead.QHEAD_EINVAL),
+    (dict(scales=0x20001), qhead.QHEAD_EINVAL),
+    (dict(wq=None), qhead.QHEAD_EINVAL),
+    (dict(biases=None), qhead.QHEAD_EINVAL),
+    (dict(softcap=float("nan")), qhead.QHEAD_EINVAL),
+])
+def test_bad_head(L, kw, code):
+    assert _fwd(L, _head(**kw)) == code
+    assert L.qhead_last_error().decode() != ""
+    assert L.qhead_fwd_workspace(ctypes.byref(_head(**kw)), 4) == ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("kw", [
+    dict(M=-1), dict(h=None), dict(h=0x40008), dict(logp=0x70000),
+    dict(lse=None), dict(ws=None), dict(ws=0x60080),
+])
+def test_bad_fwd_args(L, kw):
+    assert _fwd(L, _head(), **kw) == qhead.QHEAD_EINVAL
+    assert L.qhead_last_error().decode() != ""
+
+
+def test_null_head(L):
+    assert _fwd(L, None) == qhead.QHEAD_EINVAL
+
+
+def test_zero_rows_is_a_no_op(L):
+    assert _fwd(L, _head(), M=0, ws=None, ws_bytes=0) == qhead.QHEAD_OK
+    assert L.qhead_fwd_workspace(ctypes.byref(_head()), 0) == 0
+    assert L.qhead_bwd(ctypes.byref(_head()), None, 0, None, None, None, None, None, None, 0,
+                       None) == qhead.QHEAD_OK
+
+
+@pytest.mark.parametrize("drop", ["h", "targets", "lse", "dlogp", "dh"])
+def test_bad_bwd_args(L, drop):
+    a = dict(h=0x40000, targets=0x41000, lse=0x42000, dlogp=0x43000, dh=0x44000)
+    a[drop] = None
+    rc = L.qhead_bwd(ctypes.byref(_head()), a["h"], 4, a["targets"], None, a["lse"],
+                     a["dlogp"], a["dh"], 0x60000, 1 << 20, None)
+    assert rc == qhead.QHEAD_EINVAL
+
+
+def test_error_message_is_per_call(L):
+    assert _fwd(L, _head(bits=3)) != 0
+    assert "bits" in L.qhead_last_error().decode()
+    assert _fwd(L, _head(), M=0) == 0
+    assert L.qhead_last_error().decode() == ""

@@ -1,0 +1,58 @@
+"""Host-side pieces of bench.py: the replica aggregation over ranks (gloo,
+world size 2), the algorithmic byte count and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    el, units = bench.aggregate(10.0 + 5.0 * rank, 100.0 * (rank + 1), world, dist)
+    q.put((rank, el, units))
+    dist.destroy_process_group()
+
+
+def test_aggregate_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 1000)
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get() for _ in range(2))
+    for _, el, units in res:
+        assert el == 15.0 and units == 300.0
+
+
+def test_single_rank_aggregate_is_identity():
+    assert bench.aggregate(3.0, 7.0, 1) == (3.0, 7.0)
+
+
+def test_head_bytes_verify():
+    cfg = bench.synth.CONFIGS["verify"]
+    # 262144 rows x (2560*4/8 packed bytes + 2 arrays x 40 groups x 2 bytes)
+    assert bench.head_bytes(cfg) == 262144 * (1280 + 160) == 377_487_360
+
+
+def test_reference_arm_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"

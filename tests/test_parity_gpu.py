@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases are compared on every row; the full-size workloads on sampled rows
+(rows are independent, so a sampled row is an exact check of that row) plus
+properties that hold on every row.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import check_dh, check_fwd, gpu_fwd, oracle_head, to_dev
+from verify_vocab_blocked_gb300 import build as qbuild
+from verify_vocab_blocked_gb300 import qhead, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qbuild.build()
+    qhead.lib()
+
+
+def _custom(M, H, V, bits, cap, seed=0, mask=None, targets=None, dlogp=None):
+    head = synth.make_head(V, H, bits, softcap=cap, seed=seed)
+    h = synth.make_hidden(M, H, seed=seed)
+    t = synth.make_targets(M, V, seed=seed) if targets is None else np.asarray(targets, np.int32)
+    g = synth.make_dlogp(M, seed=seed) if dlogp is None else np.asarray(dlogp, np.float32)
+    return synth.Workload("custom", head, h, t, mask, g, dict(M=M, H=H, V=V, bits=bits))
+
+
+def _run_all(wl, bwd=True):
+    head, h, t, mk, g = to_dev(wl)
+    logp, lse, am = gpu_fwd(head, h, t, mk)
+    rows = np.arange(wl.M)
+    check_fwd(wl, rows, logp, lse, am)
+    if bwd:
+        lse_d = torch.from_numpy(lse).cuda()
+        dh = qhead.bwd(head, h, t, lse_d, g, mk)
+        torch.cuda.synchronize()
+        check_dh(wl, rows, dh.cpu().numpy())
+
+
+def test_tiny_config():
+    wl = synth.make_workload("tiny")
+    wl.dlogp = np.ones(wl.M, np.float32)
+    _run_all(wl)
+
+
+def test_tiny_random_cotangent():
+    wl = synth.make_workload("tiny", seed=3)
+    wl.dlogp = synth.make_dlogp(wl.M, seed=3)
+    _run_all(wl)
+
+
+EDGE = [
+    # M, H, V, bits, cap
+    (1, 256, 2048, 4, 0.0),
+    (2, 256, 2048, 4, 30.0),
+    (3, 256, 2048, 8, 0.0),
+    (4, 128, 1000, 4, 5.0),
+    (5, 384, 4099, 4, 30.0),
+    (7, 128, 130, 8, 0.0),
+    (8, 256, 127, 4, 0.0),
+    (9, 512, 3000, 8, 30.0),
+    (17, 128, 1, 4, 0.0),
+    (33, 256, 16, 4, 2.0),
+    (127, 128, 777, 8, 0.0),
+    (128, 256, 515, 4, 30.0),
+    (129, 128, 2049, 4, 0.0),
+]
+
+
+@pytest.mark.parametrize("M,H,V,bits,cap", EDGE)
+def test_edge_shapes(M, H, V, bits, cap):
+    _run_all(_custom(M, H, V, bits, cap, seed=M + V))
+
+
+@pytest.mark.parametrize("pattern", ["all", "none", "alternate", "spans"])
+def test_masks(pattern):
+    M = 40
+    mask = {"all": np.zeros(M, np.uint8), "none": np.ones(M, np.uint8),
+            "alternate": (np.arange(M) % 2).astype(np.uint8),
+            "spans": synth.make_mask(M, 16, 0.3)}[pattern]
+    _run_all(_custom(M, 256, 1500, 4, 30.0, seed=7, mask=mask))
+
+
+def test_target_at_both_ends():
+    M, V = 6, 3001
+    _run_all(_custom(M, 256, V, 4, 30.0, seed=8, targets=[0, V - 1, 0, V - 1, 5, V - 2]))
+
+
+def test_tied_rows_pick_lowest_index():
+    # Vocab rows 17, 250 and 251 are identical and carry a large bias, so they
+    # are the exact maximum of every token with equal value: argmax must be 17.
+    M, H, V = 12, 256, 300
+    wl = _custom(M, H, V, 4, 0.0, seed=9)
+    hh = wl.head
+    for r in (250, 251):
+        hh.wq[r] = hh.wq[17]
+        hh.scales[r] = hh.scales[17]
+    hh.biases[17] = np.float16(0.5)
+    for r in (250, 251):
+        hh.biases[r] = hh.biases[17]
+    # make sum_d h positive so the bias term dominates
+    hf = oracle.widen_bf16(wl.h)
+    hf = np.abs(hf)
+    wl.h = synth.f32_to_bf16_bits(hf.astype(np.float32))
+    head, h, t, mk, g = to_dev(wl)
+    logp, lse, am = gpu_fwd(head, h, t, mk)
+    assert (am == 17).all()
+    check_fwd(wl, np.arange(M), logp, lse, am)
+
+
+def test_verify_no_targets():
+    wl = _custom(5, 512, 5000, 4, 30.0, seed=10)
+    wl.targets = None
+    head, h, t, mk, g = to_dev(wl)
+    logp, lse, am = qhead.fwd(head, h, None, None)
+    assert logp is None
+    check_fwd(wl, np.arange(5), None, lse.cpu().numpy(), am.cpu().numpy())
+
+
+def test_invalid_target_gives_nan_not_a_fault():
+    wl = _custom(4, 256, 1000, 4, 0.0, seed=11, targets=[0, 1000, -3, 999])
+    head, h, t, mk, g = to_dev(wl)
+    logp, lse, am = gpu_fwd(head, h, t, mk)
+    assert np.isnan(logp[1]) and np.isnan(logp[2])
+    assert np.isfinite(logp[0]) and np.isfinite(logp[3])
+
+
+def test_deterministic():
+    wl = _custom(70, 256, 4000, 4, 30.0, seed=12, mask=synth.make_mask(70, 32, 0.25))
+    head, h, t, mk, g = to_dev(wl)
+    a = qhead.fwd(head, h, t, mk)
+    b = qhead.fwd(head, h, t, mk)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    d1 = qhead.bwd(head, h, t, a[1], g, mk)
+    d2 = qhead.bwd(head, h, t, a[1], g, mk)
+    assert torch.equal(d1, d2)
+
+
+def test_workspace_too_small_is_rejected():
+    wl = _custom(9, 256, 2048, 4, 0.0, seed=13)
+    head, h, t, mk, g = to_dev(wl)
+    need = qhead.fwd_workspace(head, 9)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qhead.QheadError) as e:
+        qhead.fwd(head, h, t, mk, workspace=ws)
+    assert e.value.code == qhead.QHEAD_EINVAL
+
+
+# ------------------------------------------------------------ full-size configs
+
+_FULL = {}
+
+
+def _full(name):
+    if name not in _FULL:
+        wl = synth.make_workload(name, seed=0)
+        _FULL[name] = (wl, to_dev(wl))
+    return _FULL[name]
+
+
+def _sample_rows(wl, n, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(wl.M, size=min(n, wl.M), replace=False).tolist())
+    rows |= {0, wl.M - 1}
+    if wl.mask is not None:
+        # both sides of every prompt / response boundary in the first sequence
+        idx = np.nonzero(np.diff(wl.mask.astype(int)))[0]
+        for i in idx[:4]:
+            rows |= {int(i), int(i) + 1}
+    return np.array(sorted(rows))
+
+
+def test_full_verify_window():
+    wl, (head, h, t, mk, g) = _full("verify")
+    logp, lse, am = qhead.fwd(head, h, None, None)
+    torch.cuda.synchronize()
+    check_fwd(wl, np.arange(wl.M), None, lse.cpu().numpy(), am.cpu().numpy())
+
+
+@pytest.mark.parametrize("name,n", [("gemma512", 24), ("mid8", 16), ("gemma8k_masked", 16)])
+def test_full_training_configs(name, n):
+    wl, (head, h, t, mk, g) = _full(name)
+    logp, lse, am = qhead.fwd(head, h, t, mk)
+    dh = qhead.bwd(head, h, t, lse, g, mk)
+    torch.cuda.synchronize()
+    logp, lse_h, am = logp.cpu().numpy(), lse.cpu().numpy(), am.cpu().numpy()
+    act = np.ones(wl.M, bool) if wl.mask is None else wl.mask.astype(bool)
+    # properties on every row
+    assert np.all(np.isfinite(logp)) and np.all(logp[act] <= 1e-6)
+    assert np.all((am[act] >= 0) & (am[act] < wl.head.V)) and np.all(am[~act] == -1)
+    dh_h = dh.cpu().numpy()
+    assert np.all(dh_h[~act] == 0.0) and np.all(np.isfinite(dh_h))
+    rows = _sample_rows(wl, n)
+    check_fwd(wl, rows, logp, lse_h, am)
+    check_dh(wl, rows[:8], dh_h)

@@ -1,0 +1,268 @@
+// qh_api.cu -- the C ABI of include/qhead.h: argument checks, the launch plan,
+// workspace layout and the kernel sequence of each entry point.
+//
+// Forward sequence:  compact (mask -> active rows) -> convert (bf16 -> fp16 rows)
+//                    -> head kernel (per-split partials) -> finalize (merge,
+//                    exact target logit, argmax recheck, scatter).
+// Backward sequence: compact -> head backward (per-split partial dh) ->
+//                    finalize (fixed-order sum, exact one-hot term, zeros for
+//                    masked rows).
+#include <stdio.h>
+
+#include <string>
+
+#include "../../include/qhead.h"
+#include "qh_internal.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+
+// Records the armed "before head kernel" event (if any).
+void hook_before(cudaStream_t st) {
+    if (g_ev_start) cudaEventRecord(g_ev_start, st);
+}
+void hook_after(cudaStream_t st) {
+    if (g_ev_stop) cudaEventRecord(g_ev_stop, st);
+    g_ev_start = g_ev_stop = nullptr;
+}
+
+int fail(int code, const std::string& msg) {
+    g_err = msg;
+    return code;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DevInfo {
+    int sms = 0;
+};
+
+int device_info(DevInfo* info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(QHEAD_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return fail(QHEAD_ECUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    return QHEAD_OK;
+}
+
+int check_head(const qhead_head* hd) {
+    if (!hd) return fail(QHEAD_EINVAL, "head is NULL");
+    if (!hd->wq || !hd->scales || !hd->biases) return fail(QHEAD_EINVAL, "head pointer is NULL");
+    if (hd->bits != 4 && hd->bits != 8) return fail(QHEAD_EUNSUPPORTED, "bits must be 4 or 8");
+    if (hd->group != 64) return fail(QHEAD_EUNSUPPORTED, "group size must be 64");
+    if (hd->sb_dtype != QHEAD_SB_F16) return fail(QHEAD_EUNSUPPORTED, "scales/biases must be fp16");
+    if (hd->H < 128 || hd->H > qh::kMaxH || hd->H % 128)
+        return fail(QHEAD_EUNSUPPORTED, "H must be a multiple of 128 in [128, 8192]");
+    if (hd->V < 1 || hd->V >= ((int64_t)1 << 31)) return fail(QHEAD_EINVAL, "V must be in [1, 2^31)");
+    if (reinterpret_cast<uintptr_t>(hd->wq) % 16) return fail(QHEAD_EINVAL, "wq must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(hd->scales) % 2 || reinterpret_cast<uintptr_t>(hd->biases) % 2)
+        return fail(QHEAD_EINVAL, "scales/biases must be 2-byte aligned");
+    if (hd->softcap != hd->softcap) return fail(QHEAD_EINVAL, "softcap is NaN");
+    return QHEAD_OK;
+}
+
+// ---------------------------------------------------------------- plans
+
+struct FwdPlan {
+    int64_t M = 0, Mpad = 0;
+    int S = 1;           // vocab splits of the partials
+    int cand_width = 1;  // argmax candidate run length
+    size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_part = 0, total = 0;
+};
+
+struct BwdPlan {
+    int64_t M = 0, Mpad = 0;
+    int S = 1;
+    size_t off_count = 0, off_rows = 0, off_pos = 0, off_dhp = 0, total = 0;
+};
+
+int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
+    DevInfo di;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    p->M = M;
+    p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
+    const int64_t groups = (M + qh::kTokGroup - 1) / qh::kTokGroup;
+    // Enough CTAs to fill every SM several times over; each split keeps at
+    // least 128 vocab rows (16 per warp).
+    const int64_t want = (int64_t)di.sms * 4;
+    int64_t S = (want + groups - 1) / groups;
+    const int64_t max_s = (hd->V + 127) / 128;
+    if (S > max_s) S = max_s;
+    if (S < 1) S = 1;
+    p->S = (int)S;
+    p->cand_width = 1;
+    size_t off = 0;
+    p->off_count = off; off = align_up(off + 4, 256);
+    p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
+    p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 256);
+    p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 256);
+    p->off_part = off;  off = align_up(off + sizeof(qh::Partial) * (size_t)p->Mpad * p->S, 256);
+    p->total = off;
+    return QHEAD_OK;
+}
+
+int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p) {
+    DevInfo di;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    p->M = M;
+    p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
+    const int tb = qh::bwd_simt_tokens(hd->H);
+    const int64_t groups = (M + tb - 1) / tb;
+    const int64_t want = (int64_t)di.sms * 4;
+    int64_t S = (want + groups - 1) / groups;
+    const int64_t max_s = (hd->V + 255) / 256;
+    if (S > max_s) S = max_s;
+    if (S < 1) S = 1;
+    p->S = (int)S;
+    size_t off = 0;
+    p->off_count = off; off = align_up(off + 4, 256);
+    p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
+    p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 256);
+    p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 256);
+    p->total = off;
+    return QHEAD_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(QHEAD_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qhead_last_error(void) { return g_err.c_str(); }
+
+const char* qhead_version(void) { return "qhead 0.1.0 sm_103a"; }
+
+void qhead_time_next_head_kernel(void* start, void* stop) {
+    g_ev_start = static_cast<cudaEvent_t>(start);
+    g_ev_stop = static_cast<cudaEvent_t>(stop);
+}
+
+size_t qhead_fwd_workspace(const qhead_head* head, int64_t M) {
+    g_err.clear();
+    if (check_head(head)) return (size_t)-1;
+    if (M < 0) { fail(QHEAD_EINVAL, "M < 0"); return (size_t)-1; }
+    if (M == 0) return 0;
+    FwdPlan p;
+    if (plan_fwd(head, M, &p)) return (size_t)-1;
+    return p.total;
+}
+
+size_t qhead_bwd_workspace(const qhead_head* head, int64_t M) {
+    g_err.clear();
+    if (check_head(head)) return (size_t)-1;
+    if (M < 0) { fail(QHEAD_EINVAL, "M < 0"); return (size_t)-1; }
+    if (M == 0) return 0;
+    BwdPlan p;
+    if (plan_bwd(head, M, &p)) return (size_t)-1;
+    return p.total;
+}
+
+int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+              const uint8_t* mask, float* logp, float* lse, int32_t* argmax, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    g_err.clear();
+    int rc = check_head(head);
+    if (rc) return rc;
+    if (M < 0) return fail(QHEAD_EINVAL, "M < 0");
+    if (M >= ((int64_t)1 << 31) - qh::kRowPad) return fail(QHEAD_EINVAL, "M too large");
+    if (M == 0) return QHEAD_OK;
+    if (!h) return fail(QHEAD_EINVAL, "h is NULL");
+    if (reinterpret_cast<uintptr_t>(h) % 16) return fail(QHEAD_EINVAL, "h must be 16-byte aligned");
+    if (logp && !targets) return fail(QHEAD_EINVAL, "logp requested without targets");
+    if (!logp && !lse && !argmax) return fail(QHEAD_EINVAL, "no output requested");
+    if (!workspace) return fail(QHEAD_EINVAL, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(QHEAD_EINVAL, "workspace must be 256-byte aligned");
+    FwdPlan p;
+    rc = plan_fwd(head, M, &p);
+    if (rc) return rc;
+    if (workspace_bytes < p.total)
+        return fail(QHEAD_EINVAL, "workspace too small: need " + std::to_string(p.total) + " bytes");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const auto* wq = head->wq;
+    const auto* sc = static_cast<const __half*>(head->scales);
+    const auto* bi = static_cast<const __half*>(head->biases);
+    const auto* hb = static_cast<const __nv_bfloat16*>(h);
+    int* count = at<int>(workspace, p.off_count);
+    int* rows = at<int>(workspace, p.off_rows);
+    int* pos = at<int>(workspace, p.off_pos);
+    __half* h16 = at<__half>(workspace, p.off_h16);
+    qh::Partial* part = at<qh::Partial>(workspace, p.off_part);
+
+    cudaError_t e;
+    if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, st))) return cuda_fail(e, "compact");
+    if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
+        return cuda_fail(e, "convert_h");
+    hook_before(st);
+    e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, h16, count,
+                              M, part, p.S, st);
+    hook_after(st);
+    if (e) return cuda_fail(e, "stream_fwd");
+    if ((e = qh::launch_fwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+                                     pos, targets, part, p.S, p.cand_width, logp, lse, argmax, M,
+                                     st)))
+        return cuda_fail(e, "fwd_finalize");
+    return QHEAD_OK;
+}
+
+int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+              const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
+              void* workspace, size_t workspace_bytes, void* stream) {
+    g_err.clear();
+    int rc = check_head(head);
+    if (rc) return rc;
+    if (M < 0) return fail(QHEAD_EINVAL, "M < 0");
+    if (M >= ((int64_t)1 << 31) - qh::kRowPad) return fail(QHEAD_EINVAL, "M too large");
+    if (M == 0) return QHEAD_OK;
+    if (!h || !targets || !lse || !dlogp || !dh)
+        return fail(QHEAD_EINVAL, "h, targets, lse, dlogp and dh are required");
+    if (reinterpret_cast<uintptr_t>(h) % 16) return fail(QHEAD_EINVAL, "h must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(dh) % 16) return fail(QHEAD_EINVAL, "dh must be 16-byte aligned");
+    if (!workspace) return fail(QHEAD_EINVAL, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(QHEAD_EINVAL, "workspace must be 256-byte aligned");
+    BwdPlan p;
+    rc = plan_bwd(head, M, &p);
+    if (rc) return rc;
+    if (workspace_bytes < p.total)
+        return fail(QHEAD_EINVAL, "workspace too small: need " + std::to_string(p.total) + " bytes");
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const auto* wq = head->wq;
+    const auto* sc = static_cast<const __half*>(head->scales);
+    const auto* bi = static_cast<const __half*>(head->biases);
+    const auto* hb = static_cast<const __nv_bfloat16*>(h);
+    int* count = at<int>(workspace, p.off_count);
+    int* rows = at<int>(workspace, p.off_rows);
+    int* pos = at<int>(workspace, p.off_pos);
+    float* dhp = at<float>(workspace, p.off_dhp);
+
+    cudaError_t e;
+    if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, st))) return cuda_fail(e, "compact");
+    hook_before(st);
+    e = qh::launch_bwd_simt(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb, rows,
+                            count, lse, dlogp, dhp, p.S, M, p.Mpad, st);
+    hook_after(st);
+    if (e) return cuda_fail(e, "bwd_simt");
+    if ((e = qh::launch_bwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+                                     pos, targets, dlogp, dhp, p.S, p.Mpad, dh, M, st)))
+        return cuda_fail(e, "bwd_finalize");
+    return QHEAD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,154 @@
+// qh_finalize.cu -- steps a6/a7 (forward) and a11 (backward) of the hot path.
+//
+// Forward: merge the per-(row, vocab split) partials in a fixed order,
+//   gMax = max_b m_b;  lse = gMax + log(sum_b s_b * exp(m_b - gMax))
+// (the cross-vocab-block merge of flashCceForward on the page "mlx-bun 0.0.4
+// -> 0.0.6", src/train/flash-cce.ts, done here on device in a fixed order
+// instead of in MLX ops), then
+//   * the target logit is recomputed exactly in fp32 (h widened from bf16,
+//     w = fmaf(scale, q, bias)), so logp = softcap(raw_target) - lse carries
+//     no fp16 operand rounding;
+//   * the argmax candidates (the two best raw logits over all splits, as runs
+//     of `cand_width` indices) are recomputed the same way and the best exact
+//     value wins, lowest index on ties (argmax over the raw logits, which
+//     picksBatched on the page "mlx-bun 0.0.8 -> 0.0.10" notes is the argmax of
+//     the capped, lse-shifted log-probs too);
+//   * masked rows get logp = 0, lse = 0, argmax = -1.
+// Backward: dh[r,:] = sum_s dh_partial[s, i, :] (fixed order) plus the one-hot
+// term dlogp * sech2(raw_target) * w[target, :] added exactly in fp32; masked
+// rows are written as exact zeros.
+#include "qh_internal.cuh"
+
+namespace qh {
+
+namespace {
+
+constexpr int kFinThreads = 128;
+
+__global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
+    const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
+    const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
+    const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
+    const int32_t* __restrict__ targets, const Partial* __restrict__ part, int S, int cand_width,
+    float* __restrict__ logp, float* __restrict__ lse, int32_t* __restrict__ argmax) {
+    const int64_t r = blockIdx.x;
+    const int i = pos[r];
+    if (i < 0) {
+        if (threadIdx.x == 0) {
+            if (logp) logp[r] = 0.f;
+            if (lse) lse[r] = 0.f;
+            if (argmax) argmax[r] = -1;
+        }
+        return;
+    }
+    __shared__ Partial red[kFinThreads / 32];
+    __shared__ float exact[2 * 32 + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    RowState st;
+    st.init();
+    for (int s = threadIdx.x; s < S; s += kFinThreads) st.merge(part[(int64_t)i * S + s]);
+#pragma unroll
+    for (int o = 1; o <= 16; o <<= 1) st.shfl_merge(o);
+    if (lane == 0) red[warp] = st.to_partial();
+    __syncthreads();
+    RowState fin;
+    fin.init();
+    for (int w = 0; w < kFinThreads / 32; ++w) fin.merge(red[w]);
+
+    const __nv_bfloat16* hrow = h + r * (int64_t)H;
+    const int32_t t = targets ? targets[r] : -1;
+    const bool t_ok = t >= 0 && (int64_t)t < V;
+    // Work items: candidate indices of run 1, run 2, then the target.
+    const int n1 = fin.i1 == INT32_MAX ? 0 : (int)min((int64_t)cand_width, V - fin.i1);
+    const int n2 = fin.i2 == INT32_MAX ? 0 : (int)min((int64_t)cand_width, V - fin.i2);
+    const int nitems = n1 + n2 + 1;
+    for (int it = warp; it < nitems; it += kFinThreads / 32) {
+        int64_t v;
+        if (it < n1) v = fin.i1 + it;
+        else if (it < n1 + n2) v = fin.i2 + (it - n1);
+        else v = t_ok ? t : -1;
+        float x = 0.f;
+        if (v >= 0) x = warp_exact_logit(hrow, wq, scales, biases, v, H, bits);
+        if (lane == 0) exact[it] = x;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const float l = fin.m + logf(fin.s);
+        float best = -INFINITY;
+        int bi = INT32_MAX;
+        for (int it = 0; it < n1 + n2; ++it) {
+            const int v = it < n1 ? fin.i1 + it : fin.i2 + (it - n1);
+            if (better(exact[it], v, best, bi)) { best = exact[it]; bi = v; }
+        }
+        if (lse) lse[r] = l;
+        if (argmax) argmax[r] = bi == INT32_MAX ? -1 : bi;
+        if (logp) logp[r] = t_ok ? softcap_exact(exact[n1 + n2], cap) - l : __int_as_float(0x7fc00000);
+    }
+}
+
+constexpr int kBwdFinThreads = 256;
+
+__global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
+    const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
+    const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
+    const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
+    const int32_t* __restrict__ targets, const float* __restrict__ dlogp,
+    const float* __restrict__ dhp, int S, int64_t Mpad, float* __restrict__ dh) {
+    const int64_t r = blockIdx.x;
+    const int i = pos[r];
+    float* out = dh + r * (int64_t)H;
+    if (i < 0) {
+        for (int d = threadIdx.x; d < H; d += kBwdFinThreads) out[d] = 0.f;
+        return;
+    }
+    __shared__ float coef_sh;
+    const int32_t t = targets[r];
+    const bool t_ok = t >= 0 && (int64_t)t < V;
+    if (threadIdx.x < 32) {
+        float raw = 0.f;
+        if (t_ok) raw = warp_exact_logit(h + r * (int64_t)H, wq, scales, biases, t, H, bits);
+        if (threadIdx.x == 0) {
+            float sech2 = 1.f;
+            if (cap > 0.f) {
+                const float th = tanhf(raw / cap);
+                sech2 = 1.f - th * th;
+            }
+            coef_sh = t_ok ? dlogp[r] * sech2 : __int_as_float(0x7fc00000);
+        }
+    }
+    __syncthreads();
+    const float coef = coef_sh;
+    for (int d = threadIdx.x; d < H; d += kBwdFinThreads) {
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) acc += dhp[((int64_t)s * Mpad + i) * H + d];
+        const float wt = t_ok ? dequant_elem(wq, scales, biases, t, d, H, bits) : 0.f;
+        out[d] = fmaf(coef, wt, acc);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+                                int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                                const int* pos, const int32_t* targets, const Partial* part, int S,
+                                int cand_width, float* logp, float* lse, int32_t* argmax,
+                                int64_t M, cudaStream_t st) {
+    fwd_finalize_kernel<<<(unsigned)M, kFinThreads, 0, st>>>(wq, scales, biases, V, H, bits, cap,
+                                                              h, pos, targets, part, S, cand_width,
+                                                              logp, lse, argmax);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+                                int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                                const int* pos, const int32_t* targets, const float* dlogp,
+                                const float* dhp, int S, int64_t Mpad, float* dh, int64_t M,
+                                cudaStream_t st) {
+    bwd_finalize_kernel<<<(unsigned)M, kBwdFinThreads, 0, st>>>(wq, scales, biases, V, H, bits,
+                                                                 cap, h, pos, targets, dlogp, dhp,
+                                                                 S, Mpad, dh);
+    return cudaGetLastError();
+}
+
+}  // namespace qh

@@ -1,0 +1,159 @@
+// qh_internal.cuh -- declarations shared by the translation units of libqhead.so.
+// Not a public header: the public C ABI is include/qhead.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qh {
+
+// Per-(row, vocab split) partial of the forward: online-softmax state over the
+// split's vocab rows (m = max z, s = sum exp(z - m)) and the split's two best
+// raw logits with their vocab indices (i = start of a candidate run of
+// `cand_width` indices; empty entries hold v = -inf, i = INT32_MAX).
+struct __align__(32) Partial {
+    float m, s, v1, v2;
+    int i1, i2, pad0, pad1;
+};
+
+constexpr int kTokGroup = 8;      // tokens per weight-streaming CTA (mma n = 8)
+constexpr int kMaxH = 8192;
+constexpr int kRowPad = 128;      // compacted row count is padded to this
+
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+// Soft cap z = cap * tanh(raw / cap) (cap <= 0: identity), accurate tanhf.
+__device__ __forceinline__ float softcap_exact(float raw, float cap) {
+    return cap > 0.f ? cap * tanhf(raw / cap) : raw;
+}
+
+struct RowState {
+    float m, s, v1, v2;
+    int i1, i2;
+    __device__ __forceinline__ void init() {
+        m = -INFINITY; s = 0.f; v1 = -INFINITY; v2 = -INFINITY; i1 = INT32_MAX; i2 = INT32_MAX;
+    }
+    // One logit: z (capped) feeds the softmax state, raw feeds the top-2.
+    __device__ __forceinline__ void push(float z, float raw, int idx) {
+        if (z > m) { s = s * expf(m - z) + 1.f; m = z; }
+        else       { s += expf(z - m); }
+        if (better(raw, idx, v1, i1))      { v2 = v1; i2 = i1; v1 = raw; i1 = idx; }
+        else if (better(raw, idx, v2, i2)) { v2 = raw; i2 = idx; }
+    }
+    __device__ __forceinline__ void merge(float om, float os, float ov1, int oi1, float ov2, int oi2) {
+        const float nm = fmaxf(m, om);
+        if (nm == -INFINITY) { s = 0.f; }
+        else { s = s * expf(m - nm) + os * expf(om - nm); }
+        m = nm;
+        if (better(ov1, oi1, v1, i1)) {
+            if (better(v1, i1, ov2, oi2)) { v2 = v1; i2 = i1; } else { v2 = ov2; i2 = oi2; }
+            v1 = ov1; i1 = oi1;
+        } else if (better(ov1, oi1, v2, i2)) {
+            v2 = ov1; i2 = oi1;
+        }
+    }
+    __device__ __forceinline__ void merge(const RowState& o) { merge(o.m, o.s, o.v1, o.i1, o.v2, o.i2); }
+    __device__ __forceinline__ void merge(const Partial& o) { merge(o.m, o.s, o.v1, o.i1, o.v2, o.i2); }
+    __device__ __forceinline__ void shfl_merge(int lane_mask) {
+        RowState o;
+        o.m = __shfl_xor_sync(0xffffffffu, m, lane_mask);
+        o.s = __shfl_xor_sync(0xffffffffu, s, lane_mask);
+        o.v1 = __shfl_xor_sync(0xffffffffu, v1, lane_mask);
+        o.v2 = __shfl_xor_sync(0xffffffffu, v2, lane_mask);
+        o.i1 = __shfl_xor_sync(0xffffffffu, i1, lane_mask);
+        o.i2 = __shfl_xor_sync(0xffffffffu, i2, lane_mask);
+        // Merge in a lane-order-independent way so both partners end equal:
+        // the lower lane's state always comes first.
+        const int lane = threadIdx.x & 31;
+        if (lane & lane_mask) { RowState mine = *this; *this = o; merge(mine); }
+        else { merge(o); }
+    }
+    __device__ __forceinline__ Partial to_partial() const {
+        Partial p; p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.pad0 = 0; p.pad1 = 0;
+        return p;
+    }
+};
+
+// Exact fp32 logit of one (row of h, vocab row) pair, computed by one warp:
+// h widened from bf16 exactly, w = fmaf(scale, q, bias) in fp32.  Every lane
+// returns the same value (fixed butterfly order).
+__device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restrict__ hrow,
+                                                  const uint32_t* __restrict__ wq,
+                                                  const __half* __restrict__ scales,
+                                                  const __half* __restrict__ biases,
+                                                  int64_t v, int H, int bits) {
+    const int lane = threadIdx.x & 31;
+    const int wpr = H * bits / 32;
+    const int G = H / 64;
+    const uint32_t* wrow = wq + v * (int64_t)wpr;
+    const __half* srow = scales + v * (int64_t)G;
+    const __half* brow = biases + v * (int64_t)G;
+    float acc = 0.f;
+    for (int u = lane; u < H / 8; u += 32) {  // unit of 8 consecutive elements
+        const int d0 = u * 8;
+        const uint4 hv = *reinterpret_cast<const uint4*>(hrow + d0);
+        const __nv_bfloat16* hp = reinterpret_cast<const __nv_bfloat16*>(&hv);
+        const float s = __half2float(srow[d0 / 64]);
+        const float b = __half2float(brow[d0 / 64]);
+        uint32_t w0, w1 = 0;
+        if (bits == 4) { w0 = wrow[u]; }
+        else { w0 = wrow[2 * u]; w1 = wrow[2 * u + 1]; }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            uint32_t q;
+            if (bits == 4) q = (w0 >> (4 * k)) & 15u;
+            else q = ((k < 4 ? w0 : w1) >> (8 * (k & 3))) & 255u;
+            const float w = fmaf(s, (float)q, b);
+            acc = fmaf(__bfloat162float(hp[k]), w, acc);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc;
+}
+
+// fp32 dequantized element w[v,d].
+__device__ __forceinline__ float dequant_elem(const uint32_t* __restrict__ wq,
+                                              const __half* __restrict__ scales,
+                                              const __half* __restrict__ biases,
+                                              int64_t v, int d, int H, int bits) {
+    const int per = 32 / bits;
+    const uint32_t word = wq[v * (int64_t)(H * bits / 32) + d / per];
+    const uint32_t q = (word >> (bits * (d % per))) & ((1u << bits) - 1u);
+    const int64_t gi = v * (int64_t)(H / 64) + d / 64;
+    return fmaf(__half2float(scales[gi]), (float)q, __half2float(biases[gi]));
+}
+
+// ------------------------------------------------------------- launchers
+// Each returns the cudaError_t of its launch.
+
+cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* rows, int* pos,
+                           int* count, cudaStream_t st);
+cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
+                             const int* count, __half* h16, cudaStream_t st);
+cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
+                              int64_t V, int H, int bits, float cap, const __half* h16,
+                              const int* count, int64_t M, Partial* part, int S, cudaStream_t st);
+cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+                                int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                                const int* pos, const int32_t* targets, const Partial* part, int S,
+                                int cand_width, float* logp, float* lse, int32_t* argmax,
+                                int64_t M, cudaStream_t st);
+cudaError_t launch_bwd_simt(const uint32_t* wq, const __half* scales, const __half* biases,
+                            int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                            const int* rows, const int* count, const float* lse,
+                            const float* dlogp, float* dhp, int S, int64_t M, int64_t Mpad,
+                            cudaStream_t st);
+cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+                                int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                                const int* pos, const int32_t* targets, const float* dlogp,
+                                const float* dhp, int S, int64_t Mpad, float* dh, int64_t M,
+                                cudaStream_t st);
+
+int bwd_simt_tokens(int H);  // tokens per CTA of the SIMT backward
+
+}  // namespace qh

@@ -1,0 +1,185 @@
+"""Thin ctypes binding of libqhead.so (include/qhead.h).
+
+Argument marshalling only: every step of the head runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  If the
+library has not been built, the first call raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqhead.so")
+
+QHEAD_OK, QHEAD_EINVAL, QHEAD_EUNSUPPORTED, QHEAD_ECUDA = 0, 1, 2, 3
+QHEAD_SB_F16 = 0
+
+# Every symbol include/qhead.h declares.
+EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd",
+           "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel")
+
+
+class CHead(ctypes.Structure):
+    _fields_ = [("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("V", ctypes.c_int64), ("H", ctypes.c_int32),
+                ("bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("sb_dtype", ctypes.c_int32), ("softcap", ctypes.c_float)]
+
+
+class QheadError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"qhead error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libqhead.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m verify_vocab_blocked_gb300.build` (no CPU fallback exists)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    hp = ctypes.POINTER(CHead)
+    L.qhead_fwd_workspace.argtypes = [hp, i64]
+    L.qhead_fwd_workspace.restype = sz
+    L.qhead_bwd_workspace.argtypes = [hp, i64]
+    L.qhead_bwd_workspace.restype = sz
+    L.qhead_fwd.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.qhead_fwd.restype = ctypes.c_int
+    L.qhead_bwd.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.qhead_bwd.restype = ctypes.c_int
+    L.qhead_last_error.argtypes = []
+    L.qhead_last_error.restype = ctypes.c_char_p
+    L.qhead_version.argtypes = []
+    L.qhead_version.restype = ctypes.c_char_p
+    L.qhead_time_next_head_kernel.argtypes = [vp, vp]
+    L.qhead_time_next_head_kernel.restype = None
+    _lib = L
+    return L
+
+
+def time_next_head_kernel(start: torch.cuda.Event, stop: torch.cuda.Event) -> None:
+    """Arm the library's one-shot hook: the next fwd/bwd call on this thread
+    records `start` / `stop` around its head kernel on the call's stream.
+    Both events must already exist (record them once beforehand)."""
+    lib().qhead_time_next_head_kernel(start.cuda_event, stop.cuda_event)
+
+
+def last_error() -> str:
+    return lib().qhead_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != QHEAD_OK:
+        raise QheadError(rc, last_error())
+
+
+@dataclass
+class Head:
+    """A quantized head resident on the GPU (FlashCceHead layout)."""
+    wq: torch.Tensor        # int32 (uint32 bit patterns) [V, H*bits/32]
+    scales: torch.Tensor    # float16 [V, H/group]
+    biases: torch.Tensor    # float16 [V, H/group]
+    bits: int
+    group: int = 64
+    softcap: float = 0.0
+
+    @property
+    def V(self) -> int:
+        return int(self.wq.shape[0])
+
+    @property
+    def H(self) -> int:
+        return int(self.wq.shape[1]) * 32 // self.bits
+
+    def c(self) -> CHead:
+        for t in (self.wq, self.scales, self.biases):
+            if not t.is_contiguous():
+                raise ValueError("head tensors must be contiguous")
+        if self.scales.dtype != torch.float16 or self.biases.dtype != torch.float16:
+            raise ValueError("scales/biases must be float16")
+        return CHead(self.wq.data_ptr(), self.scales.data_ptr(), self.biases.data_ptr(),
+                     self.V, self.H, self.bits, self.group, QHEAD_SB_F16, float(self.softcap))
+
+    @staticmethod
+    def from_numpy(wq, scales, biases, bits, group=64, softcap=0.0, device="cuda"):
+        import numpy as np
+        return Head(torch.from_numpy(np.ascontiguousarray(wq).view(np.int32)).to(device),
+                    torch.from_numpy(np.ascontiguousarray(scales)).to(device),
+                    torch.from_numpy(np.ascontiguousarray(biases)).to(device),
+                    bits, group, softcap)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def fwd_workspace(head: Head, M: int) -> int:
+    n = lib().qhead_fwd_workspace(ctypes.byref(head.c()), M)
+    if n == ctypes.c_size_t(-1).value:
+        raise QheadError(QHEAD_EINVAL, last_error())
+    return int(n)
+
+
+def bwd_workspace(head: Head, M: int) -> int:
+    n = lib().qhead_bwd_workspace(ctypes.byref(head.c()), M)
+    if n == ctypes.c_size_t(-1).value:
+        raise QheadError(QHEAD_EINVAL, last_error())
+    return int(n)
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte aligned device buffer of at least nbytes (torch allocations are)."""
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def fwd(head: Head, h: torch.Tensor, targets: torch.Tensor | None = None,
+        mask: torch.Tensor | None = None, *, want_logp: bool = True, want_lse: bool = True,
+        want_argmax: bool = True, workspace: torch.Tensor | None = None, stream=None):
+    """Returns (logp or None, lse or None, argmax or None) for every row of h."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
+    M = h.shape[0]
+    dev = h.device
+    want_logp = want_logp and targets is not None
+    logp = torch.empty(M, dtype=torch.float32, device=dev) if want_logp else None
+    lse = torch.empty(M, dtype=torch.float32, device=dev) if want_lse else None
+    am = torch.empty(M, dtype=torch.int32, device=dev) if want_argmax else None
+    if workspace is None:
+        workspace = alloc_workspace(fwd_workspace(head, M), dev)
+    _check(lib().qhead_fwd(ctypes.byref(head.c()), h.data_ptr(), M, _ptr(targets), _ptr(mask),
+                           _ptr(logp), _ptr(lse), _ptr(am), workspace.data_ptr(),
+                           workspace.numel(), _stream(stream)))
+    return logp, lse, am
+
+
+def bwd(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+        dlogp: torch.Tensor, mask: torch.Tensor | None = None, *,
+        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dh [M, H] float32 of sum_m dlogp[m] * logp[m]."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
+    M = h.shape[0]
+    dev = h.device
+    dh = torch.empty(M, head.H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(bwd_workspace(head, M), dev)
+    _check(lib().qhead_bwd(ctypes.byref(head.c()), h.data_ptr(), M, _ptr(targets), _ptr(mask),
+                           lse.data_ptr(), dlogp.data_ptr(), dh.data_ptr(), workspace.data_ptr(),
+                           workspace.numel(), _stream(stream)))
+    return dh
