@@ -184,7 +184,9 @@ class Runner:
         self.out_host = {k: torch.empty_like(v, device="cpu").pin_memory()
                          for k, v in (("lse", self.lse), ("am", self.am), ("logp", self.logp),
                                       ("dh", self.dh)) if v is not None}
-        self.launches_per_step = 4 + (3 if self.bwd else 0)
+        # fwd: prologue (1 fused launch up to 256 rows, else 2) + head + finalize;
+        # bwd: compact + head + finalize
+        self.launches_per_step = (3 if M <= 256 else 4) + (3 if self.bwd else 0)
         self.active = int(wl.mask.sum()) if wl.mask is not None else M
 
     def _ptr(self, t):

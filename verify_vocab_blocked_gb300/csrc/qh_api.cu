@@ -87,9 +87,9 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
     const int64_t groups = (M + qh::kTokGroup - 1) / qh::kTokGroup;
-    // Enough CTAs to fill every SM several times over; each split keeps at
+    // One full wave: every SM holds as many CTAs as fit; each split keeps at
     // least 128 vocab rows (16 per warp).
-    const int64_t want = (int64_t)di.sms * 4;
+    const int64_t want = (int64_t)di.sms * qh::stream_fwd_ctas_per_sm(hd->bits, hd->H);
     int64_t S = (want + groups - 1) / groups;
     const int64_t max_s = (hd->V + 127) / 128;
     if (S > max_s) S = max_s;
@@ -205,9 +205,16 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     qh::Partial* part = at<qh::Partial>(workspace, p.off_part);
 
     cudaError_t e;
-    if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, st))) return cuda_fail(e, "compact");
-    if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
-        return cuda_fail(e, "convert_h");
+    if (M <= qh::kFusedPrologueMaxM) {
+        if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
+                                           count, h16, st)))
+            return cuda_fail(e, "prologue");
+    } else {
+        if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, st)))
+            return cuda_fail(e, "compact");
+        if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
+            return cuda_fail(e, "convert_h");
+    }
     hook_before(st);
     e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, h16, count,
                               M, part, p.S, st);

@@ -93,22 +93,35 @@ __device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restric
     const __half* srow = scales + v * (int64_t)G;
     const __half* brow = biases + v * (int64_t)G;
     float acc = 0.f;
-    for (int u = lane; u < H / 8; u += 32) {  // unit of 8 consecutive elements
-        const int d0 = u * 8;
-        const uint4 hv = *reinterpret_cast<const uint4*>(hrow + d0);
-        const __nv_bfloat16* hp = reinterpret_cast<const __nv_bfloat16*>(&hv);
-        const float s = __half2float(srow[d0 / 64]);
-        const float b = __half2float(brow[d0 / 64]);
-        uint32_t w0, w1 = 0;
-        if (bits == 4) { w0 = wrow[u]; }
-        else { w0 = wrow[2 * u]; w1 = wrow[2 * u + 1]; }
+    // Units of 8 consecutive elements, 4 per lane per round, loads of a round
+    // issued together.
+    for (int u0 = lane; u0 < H / 8; u0 += 4 * 32) {
+        uint4 hv[4];
+        uint32_t w0[4], w1[4];
+        float s[4], b[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            uint32_t q;
-            if (bits == 4) q = (w0 >> (4 * k)) & 15u;
-            else q = ((k < 4 ? w0 : w1) >> (8 * (k & 3))) & 255u;
-            const float w = fmaf(s, (float)q, b);
-            acc = fmaf(__bfloat162float(hp[k]), w, acc);
+        for (int i = 0; i < 4; ++i) {
+            const int u = u0 + 32 * i;
+            if (u < H / 8) {
+                hv[i] = *reinterpret_cast<const uint4*>(hrow + 8 * u);
+                s[i] = __half2float(srow[u / 8]);
+                b[i] = __half2float(brow[u / 8]);
+                if (bits == 4) { w0[i] = wrow[u]; w1[i] = 0u; }
+                else { w0[i] = wrow[2 * u]; w1[i] = wrow[2 * u + 1]; }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (u0 + 32 * i < H / 8) {
+                const __nv_bfloat16* hp = reinterpret_cast<const __nv_bfloat16*>(&hv[i]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t q;
+                    if (bits == 4) q = (w0[i] >> (4 * k)) & 15u;
+                    else q = ((k < 4 ? w0[i] : w1[i]) >> (8 * (k & 3))) & 255u;
+                    acc = fmaf(__bfloat162float(hp[k]), fmaf(s[i], (float)q, b[i]), acc);
+                }
+            }
         }
     }
 #pragma unroll
@@ -133,6 +146,11 @@ __device__ __forceinline__ float dequant_elem(const uint32_t* __restrict__ wq,
 
 cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* rows, int* pos,
                            int* count, cudaStream_t st);
+// Compaction and conversion in one single-CTA launch (small M only).
+constexpr int64_t kFusedPrologueMaxM = 256;
+cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
+                                  int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
+                                  __half* h16, cudaStream_t st);
 cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
                              const int* count, __half* h16, cudaStream_t st);
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
@@ -154,6 +172,7 @@ cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const 
                                 const float* dhp, int S, int64_t Mpad, float* dh, int64_t M,
                                 cudaStream_t st);
 
-int bwd_simt_tokens(int H);  // tokens per CTA of the SIMT backward
+int bwd_simt_tokens(int H);
+int stream_fwd_ctas_per_sm(int bits, int H);  // occupancy of the weight-streaming kernel  // tokens per CTA of the SIMT backward
 
 }  // namespace qh

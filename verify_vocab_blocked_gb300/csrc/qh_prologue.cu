@@ -13,9 +13,9 @@ namespace qh {
 // One CTA of 1024 threads scans the mask in chunks of 1024 rows.
 // rows[i] = original index of the i-th active row (ascending), rows[i] = -1 for
 // i in [count, Mpad); pos[r] = compact index of row r, or -1 if r is masked.
-__global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ mask, int64_t M,
-                                                       int64_t Mpad, int* __restrict__ rows,
-                                                       int* __restrict__ pos, int* __restrict__ count) {
+// Must be called by all 1024 threads of the CTA; returns the active count.
+__device__ int compact_rows(const uint8_t* __restrict__ mask, int64_t M, int64_t Mpad,
+                            int* __restrict__ rows, int* __restrict__ pos, int* __restrict__ count) {
     __shared__ int warp_tot[32];
     __shared__ int base_sh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -52,6 +52,13 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
     const int n = base_sh;
     for (int64_t i = n + tid; i < Mpad; i += 1024) rows[i] = -1;
     if (tid == 0) *count = n;
+    return n;
+}
+
+__global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ mask, int64_t M,
+                                                       int64_t Mpad, int* __restrict__ rows,
+                                                       int* __restrict__ pos, int* __restrict__ count) {
+    compact_rows(mask, M, Mpad, rows, pos, count);
 }
 
 // h16[i, :] = fp16(h[rows[i], :]) for i < count, zeros for count <= i < Mpad.
@@ -60,6 +67,21 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
 // dequantizer yields (q_k, q_k+4) pairs out of one packed word, so the B
 // operand of every mma sees the same permutation of the K axis as the A
 // operand.  8-bit heads keep the natural order.
+__device__ __forceinline__ uint4 convert_unit(const __nv_bfloat16* __restrict__ src, int bits) {
+    const uint4 in = *reinterpret_cast<const uint4*>(src);
+    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&in);
+    __half y[8];
+    if (bits == 4) {
+        const int perm[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = __float2half_rn(__bfloat162float(x[perm[k]]));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = __float2half_rn(__bfloat162float(x[k]));
+    }
+    return *reinterpret_cast<const uint4*>(y);
+}
+
 __global__ void convert_h_kernel(const __nv_bfloat16* __restrict__ h, int H, int bits,
                                  const int* __restrict__ rows, const int* __restrict__ count,
                                  __half* __restrict__ h16) {
@@ -67,22 +89,34 @@ __global__ void convert_h_kernel(const __nv_bfloat16* __restrict__ h, int H, int
     const int u = threadIdx.x;  // 8-element unit
     if (u >= H / 8) return;
     uint4 out = make_uint4(0u, 0u, 0u, 0u);
-    if (i < *count) {
-        const int64_t r = rows[i];
-        const uint4 in = *reinterpret_cast<const uint4*>(h + r * H + 8 * u);
-        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&in);
-        __half y[8];
-        if (bits == 4) {
-            const int perm[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) y[k] = __float2half_rn(__bfloat162float(x[perm[k]]));
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) y[k] = __float2half_rn(__bfloat162float(x[k]));
-        }
-        out = *reinterpret_cast<const uint4*>(y);
-    }
+    if (i < *count) out = convert_unit(h + (int64_t)rows[i] * H + 8 * u, bits);
     *reinterpret_cast<uint4*>(h16 + i * H + 8 * u) = out;
+}
+
+// Small M: one CTA compacts, then converts every (row, 8-unit) of the padded
+// tile (the weight-streaming kernel reads rows in groups of 8).
+__global__ void __launch_bounds__(1024) prologue_fused_kernel(
+    const uint8_t* __restrict__ mask, const __nv_bfloat16* __restrict__ h, int64_t M, int64_t Mpad,
+    int H, int bits, int* __restrict__ rows, int* __restrict__ pos, int* __restrict__ count,
+    __half* __restrict__ h16) {
+    const int n = compact_rows(mask, M, Mpad, rows, pos, count);
+    __syncthreads();  // rows[] written by other threads
+    const int units = H / 8;
+    const int64_t nrows = (M + kTokGroup - 1) / kTokGroup * kTokGroup;
+    for (int64_t idx = threadIdx.x; idx < nrows * units; idx += 1024) {
+        const int64_t i = idx / units;
+        const int u = (int)(idx - i * units);
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (i < n) out = convert_unit(h + (int64_t)rows[i] * H + 8 * u, bits);
+        *reinterpret_cast<uint4*>(h16 + i * H + 8 * u) = out;
+    }
+}
+
+cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
+                                  int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
+                                  __half* h16, cudaStream_t st) {
+    prologue_fused_kernel<<<1, 1024, 0, st>>>(mask, h, M, Mpad, H, bits, rows, pos, count, h16);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* rows, int* pos,

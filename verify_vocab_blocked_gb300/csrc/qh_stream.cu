@@ -42,19 +42,28 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 x) { return *reinterpret_cast<uint32_t*>(&x); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t x) { return *reinterpret_cast<__half2*>(&x); }
 
-// (1024 + q_lo, 1024 + q_hi) -> (s*q_lo + b, s*q_hi + b), fp16, one rounding.
-__device__ __forceinline__ uint32_t affine(uint32_t magic_pair, __half2 s, __half2 b) {
-    const __half2 k1024 = __float2half2_rn(1024.f);
-    const __half2 q = __hsub2(u32_as_h2(magic_pair), k1024);  // exact: integers < 2048
+// (M + q_lo, M + q_hi) -> (s*q_lo + b, s*q_hi + b), fp16, one rounding: the
+// subtraction of the magic M (1024 or 64) is exact for integers q < 256.
+__device__ __forceinline__ uint32_t affine(uint32_t magic_pair, float magic, __half2 s, __half2 b) {
+    const __half2 q = __hsub2(u32_as_h2(magic_pair), __float2half2_rn(magic));
     return h2_as_u32(__hfma2(q, s, b));
 }
 
-__device__ __forceinline__ uint32_t deq4(uint32_t w, int k, __half2 s, __half2 b) {
-    return affine(lop3_and_or(w >> (4 * k), 0x000F000Fu, 0x64006400u), s, b);
+// 4-bit codes of one word as fp16 pairs (q_k, q_k+4), k = 0..3, without a
+// shift per pair: codes in bits 0-3 of each 16-bit half become the mantissa
+// of 1024 + q (magic 0x6400), codes in bits 4-7 the mantissa of 64 + q (magic
+// 0x5400: exponent 2^6, mantissa step 16 -> 1).  One shift by 8 brings codes
+// 2, 3, 6, 7 down to the same two positions.
+__device__ __forceinline__ void deq4_word(uint32_t w, __half2 s, __half2 b, uint32_t (&p)[4]) {
+    const uint32_t w8 = w >> 8;
+    p[0] = affine(lop3_and_or(w, 0x000F000Fu, 0x64006400u), 1024.f, s, b);
+    p[1] = affine(lop3_and_or(w, 0x00F000F0u, 0x54005400u), 64.f, s, b);
+    p[2] = affine(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), 1024.f, s, b);
+    p[3] = affine(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), 64.f, s, b);
 }
 
 __device__ __forceinline__ uint32_t deq8(uint32_t w, uint32_t sel, __half2 s, __half2 b) {
-    return affine(__byte_perm(w, 0x64646464u, sel), s, b);
+    return affine(__byte_perm(w, 0x64646464u, sel), 1024.f, s, b);
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -68,7 +77,7 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
@@ -88,15 +97,12 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& a0, cons
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint4 bq = *reinterpret_cast<const uint4*>(hb + 8 * j);
-            const uint32_t w0 = u4_at(a0, j), w1 = u4_at(a1, j);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const uint32_t A0 = deq4(w0, 2 * e, s0, b0);
-                const uint32_t A2 = deq4(w0, 2 * e + 1, s0, b0);
-                const uint32_t A1 = deq4(w1, 2 * e, s1, b1);
-                const uint32_t A3 = deq4(w1, 2 * e + 1, s1, b1);
-                mma16816(acc, A0, A1, A2, A3, e ? bq.z : bq.x, e ? bq.w : bq.y);
-            }
+            uint32_t p0[4], p1[4];
+            deq4_word(u4_at(a0, j), s0, b0, p0);
+            deq4_word(u4_at(a1, j), s1, b1, p1);
+            // step e = 0 uses pairs (0,4) and (1,5); e = 1 uses (2,6) and (3,7)
+            mma16816(acc, p0[0], p1[0], p0[1], p1[1], bq.x, bq.y);
+            mma16816(acc, p0[2], p1[2], p0[3], p1[3], bq.z, bq.w);
         }
     } else {
 #pragma unroll
@@ -115,8 +121,15 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& a0, cons
     }
 }
 
+// One packed chunk of a warp's work: A words of rows g and g+8 and their
+// (scale, bias) pairs, packed as half2 (scale, bias).
+struct Item {
+    uint4 a0, a1;
+    uint32_t sb0, sb1;
+};
+
 template <int BITS>
-__global__ void __launch_bounds__(kThreads) stream_fwd_kernel(
+__global__ void __launch_bounds__(kThreads, 3) stream_fwd_kernel(
     const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, float cap,
     const __half* __restrict__ h16, const int* __restrict__ count, Partial* __restrict__ part,
@@ -131,15 +144,6 @@ __global__ void __launch_bounds__(kThreads) stream_fwd_kernel(
     const int hstride = H + 8;  // halves; +16 bytes per row spreads the banks
     __shared__ Partial red[kWarps][kTokGroup];
 
-    // Stage the group's 8 rows of h (fp16, K-permuted for 4-bit) in shared memory.
-    const int units = H / 8;
-    for (int idx = threadIdx.x; idx < kTokGroup * units; idx += kThreads) {
-        const int r = idx / units, c = idx - r * units;
-        const uint4 v = *reinterpret_cast<const uint4*>(h16 + (int64_t)(tok0 + r) * H + 8 * c);
-        *reinterpret_cast<uint4*>(hs + r * hstride + 8 * c) = v;
-    }
-    __syncthreads();
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int64_t cta_v0 = V * split / S, cta_v1 = V * (split + 1) / S;
@@ -148,46 +152,92 @@ __global__ void __launch_bounds__(kThreads) stream_fwd_kernel(
     const int wpr = H * BITS / 32;
     const int G = H / 64;
     const int nchunks = wpr / 16;
-    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+    const int ntiles = (int)((wv1 - wv0 + 15) / 16);
+    const int nitems = ntiles * nchunks;
+
+    // Item loader.  Rows past the warp's range are clamped to its last row (a
+    // valid address); their logits are discarded in the epilogue.  Only two
+    // row indices are kept; addresses are formed at fetch time.
+    int pf_c = 0;
+    int64_t pf_r0 = wv0 + g;
+    int rc0 = 0, rc1 = 0;
+    const int wpr4 = wpr / 4;                      // uint4 per row
+    const int go = BITS == 4 ? (t >> 1) : 0;      // group offset of this lane
+    auto set_rows = [&]() {
+        const int64_t last = wv1 - 1;
+        rc0 = (int)min(pf_r0, last);
+        rc1 = (int)min(pf_r0 + 8, last);
+    };
+    const uint4* wq4 = reinterpret_cast<const uint4*>(wq) + t;
+    auto fetch = [&](Item& it) {
+        it.a0 = ld_stream(wq4 + ((int64_t)rc0 * wpr4 + 4 * pf_c));
+        it.a1 = ld_stream(wq4 + ((int64_t)rc1 * wpr4 + 4 * pf_c));
+        const int gi = (BITS == 4 ? 2 * pf_c : pf_c) + go;
+        const int64_t o0 = (int64_t)rc0 * G + gi, o1 = (int64_t)rc1 * G + gi;
+        it.sb0 = h2_as_u32(__halves2half2(scales[o0], biases[o0]));
+        it.sb1 = h2_as_u32(__halves2half2(scales[o1], biases[o1]));
+        if (++pf_c == nchunks) {
+            pf_c = 0;
+            pf_r0 += 16;
+            set_rows();
+        }
+    };
+
+    Item A, B, C;
+    if (nitems > 0) {
+        set_rows();
+        fetch(A);
+    }
+    if (nitems > 1) fetch(B);
+
+    // Stage the group's 8 rows of h (fp16, K-permuted for 4-bit) in shared memory.
+    const int units = H / 8;
+    for (int idx = threadIdx.x; idx < kTokGroup * units; idx += kThreads) {
+        const int r = idx / units, c = idx - r * units;
+        const uint4 v = *reinterpret_cast<const uint4*>(h16 + (int64_t)(tok0 + r) * H + 8 * c);
+        *reinterpret_cast<uint4*>(hs + r * hstride + 8 * c) = v;
+    }
+    __syncthreads();
     const __half* hrow = hs + g * hstride + (BITS == 4 ? 32 * t : 16 * t);
+    constexpr int kChunkHalves = BITS == 4 ? 128 : 64;
 
     RowState st[2];
     st[0].init();
     st[1].init();
-
-    for (int64_t tile = wv0; tile < wv1; tile += 16) {
-        const int64_t r0 = tile + g, r1 = tile + g + 8;
-        const bool ok0 = r0 < wv1, ok1 = r1 < wv1;
-        const uint4* p0 = reinterpret_cast<const uint4*>(wq + (ok0 ? r0 : wv0) * wpr) + t;
-        const uint4* p1 = reinterpret_cast<const uint4*>(wq + (ok1 ? r1 : wv0) * wpr) + t;
-        const __half* sc0 = scales + (ok0 ? r0 : wv0) * G;
-        const __half* sc1 = scales + (ok1 ? r1 : wv0) * G;
-        const __half* bi0 = biases + (ok0 ? r0 : wv0) * G;
-        const __half* bi1 = biases + (ok1 ? r1 : wv0) * G;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-
-        uint4 na0 = ok0 ? ld_stream(p0) : zero4;
-        uint4 na1 = ok1 ? ld_stream(p1) : zero4;
-        for (int c = 0; c < nchunks; ++c) {
-            const uint4 a0 = na0, a1 = na1;
-            if (c + 1 < nchunks) {
-                na0 = ok0 ? ld_stream(p0 + 4 * (c + 1)) : zero4;
-                na1 = ok1 ? ld_stream(p1 + 4 * (c + 1)) : zero4;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int c = 0;
+    int64_t tile_r0 = wv0 + g;
+    auto compute = [&](const Item& it) {
+        const __half2 sb0 = u32_as_h2(it.sb0), sb1 = u32_as_h2(it.sb1);
+        chunk_mma<BITS>(acc, it.a0, it.a1, __low2half2(sb0), __high2half2(sb0), __low2half2(sb1),
+                        __high2half2(sb1), hrow + kChunkHalves * c);
+        if (++c == nchunks) {
+            // acc: (row g, tok 2t), (row g, tok 2t+1), (row g+8, tok 2t), (row g+8, tok 2t+1)
+            const int64_t r0 = tile_r0, r1 = tile_r0 + 8;
+            if (r0 < wv1) {
+                st[0].push(softcap_exact(acc[0], cap), acc[0], (int)r0);
+                st[1].push(softcap_exact(acc[1], cap), acc[1], (int)r0);
             }
-            const int gi = BITS == 4 ? (2 * c + (t >> 1)) : c;
-            const __half2 s0 = __half2half2(sc0[gi]), b0 = __half2half2(bi0[gi]);
-            const __half2 s1 = __half2half2(sc1[gi]), b1 = __half2half2(bi1[gi]);
-            chunk_mma<BITS>(acc, a0, a1, s0, b0, s1, b1, hrow + (BITS == 4 ? 128 : 64) * c);
+            if (r1 < wv1) {
+                st[0].push(softcap_exact(acc[2], cap), acc[2], (int)r1);
+                st[1].push(softcap_exact(acc[3], cap), acc[3], (int)r1);
+            }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            c = 0;
+            tile_r0 += 16;
         }
-        // acc: (row g, token 2t), (row g, token 2t+1), (row g+8, token 2t), (row g+8, token 2t+1)
-        if (ok0) {
-            st[0].push(softcap_exact(acc[0], cap), acc[0], (int)r0);
-            st[1].push(softcap_exact(acc[1], cap), acc[1], (int)r0);
-        }
-        if (ok1) {
-            st[0].push(softcap_exact(acc[2], cap), acc[2], (int)r1);
-            st[1].push(softcap_exact(acc[3], cap), acc[3], (int)r1);
-        }
+    };
+    // Three-slot ring, unrolled so no slot is ever copied: item k is computed
+    // while item k+2 is in flight.
+    for (int k = 0; k < nitems; k += 3) {
+        if (k + 2 < nitems) fetch(C);
+        compute(A);
+        if (k + 1 >= nitems) break;
+        if (k + 3 < nitems) fetch(A);
+        compute(B);
+        if (k + 2 >= nitems) break;
+        if (k + 4 < nitems) fetch(B);
+        compute(C);
     }
 
     // Merge the 8 lanes that share t (lanes t, t+4, ..., t+28), then the warps.
@@ -211,6 +261,20 @@ __global__ void __launch_bounds__(kThreads) stream_fwd_kernel(
 }
 
 }  // namespace
+
+int stream_fwd_ctas_per_sm(int bits, int H) {
+    const size_t smem = (size_t)kTokGroup * (H + 8) * sizeof(__half);
+    int n = 0;
+    cudaError_t e;
+    if (bits == 4) {
+        cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stream_fwd_kernel<4>, kThreads, smem);
+    } else {
+        cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stream_fwd_kernel<8>, kThreads, smem);
+    }
+    return (e == cudaSuccess && n > 0) ? n : 1;
+}
 
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
                               int64_t V, int H, int bits, float cap, const __half* h16,
