@@ -47,7 +47,17 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
 
     RowState st;
     st.init();
-    for (int s = threadIdx.x; s < S; s += kFinThreads) st.merge(part[(int64_t)i * S + s]);
+    // Up to 4 partials per thread per round, loads issued before the merges.
+    const Partial* prow = part + (int64_t)i * S;
+    for (int s0 = threadIdx.x; s0 < S; s0 += 4 * kFinThreads) {
+        Partial buf[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k * kFinThreads < S) buf[k] = prow[s0 + k * kFinThreads];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (s0 + k * kFinThreads < S) st.merge(buf[k]);
+    }
 #pragma unroll
     for (int o = 1; o <= 16; o <<= 1) st.shfl_merge(o);
     if (lane == 0) red[warp] = st.to_partial();

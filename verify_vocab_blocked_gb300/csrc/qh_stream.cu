@@ -44,8 +44,10 @@ __device__ __forceinline__ __half2 u32_as_h2(uint32_t x) { return *reinterpret_c
 
 // (M + q_lo, M + q_hi) -> (s*q_lo + b, s*q_hi + b), fp16, one rounding: the
 // subtraction of the magic M (1024 or 64) is exact for integers q < 256.
-__device__ __forceinline__ uint32_t affine(uint32_t magic_pair, float magic, __half2 s, __half2 b) {
-    const __half2 q = __hsub2(u32_as_h2(magic_pair), __float2half2_rn(magic));
+// The magic constant is passed as its fp16x2 bit pattern so it stays a
+// compile-time immediate (0x64006400 = (1024, 1024), 0x54005400 = (64, 64)).
+__device__ __forceinline__ uint32_t affine(uint32_t magic_pair, uint32_t magic, __half2 s, __half2 b) {
+    const __half2 q = __hsub2(u32_as_h2(magic_pair), u32_as_h2(magic));
     return h2_as_u32(__hfma2(q, s, b));
 }
 
@@ -56,14 +58,14 @@ __device__ __forceinline__ uint32_t affine(uint32_t magic_pair, float magic, __h
 // 2, 3, 6, 7 down to the same two positions.
 __device__ __forceinline__ void deq4_word(uint32_t w, __half2 s, __half2 b, uint32_t (&p)[4]) {
     const uint32_t w8 = w >> 8;
-    p[0] = affine(lop3_and_or(w, 0x000F000Fu, 0x64006400u), 1024.f, s, b);
-    p[1] = affine(lop3_and_or(w, 0x00F000F0u, 0x54005400u), 64.f, s, b);
-    p[2] = affine(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), 1024.f, s, b);
-    p[3] = affine(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), 64.f, s, b);
+    p[0] = affine(lop3_and_or(w, 0x000F000Fu, 0x64006400u), 0x64006400u, s, b);
+    p[1] = affine(lop3_and_or(w, 0x00F000F0u, 0x54005400u), 0x54005400u, s, b);
+    p[2] = affine(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), 0x64006400u, s, b);
+    p[3] = affine(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), 0x54005400u, s, b);
 }
 
 __device__ __forceinline__ uint32_t deq8(uint32_t w, uint32_t sel, __half2 s, __half2 b) {
-    return affine(__byte_perm(w, 0x64646464u, sel), 1024.f, s, b);
+    return affine(__byte_perm(w, 0x64646464u, sel), 0x64006400u, s, b);
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
