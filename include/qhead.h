@@ -140,6 +140,33 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
               const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
               void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Forward without a workspace argument, for callers that cannot allocate
+ * device memory (no counterpart on the pages: it is an addition for this
+ * library's users).  Engines that run the verify step inside a pre-sized
+ * memory arena, plugins hosted by frameworks that forbid allocation after
+ * start-up, and latency-critical loops that must not enter the allocator
+ * cannot call cudaMalloc to provide qhead_fwd's workspace.  This call takes
+ * the same arguments as qhead_fwd minus the workspace and computes the same
+ * outputs, using instead a fixed scratch array of 8 MiB (8388608 bytes) that
+ * lives in the library on every device that loads it, until the process
+ * exits.  It allocates
+ * nothing and calls no allocating routine.
+ *   - The first call with a given device current looks up the array's device
+ *     address (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture on the device.
+ *   - M rows whose workspace (qhead_fwd_workspace) exceeds the scratch size
+ *     are rejected with QHEAD_EINVAL and a message; nothing is launched.
+ *     With H = 2560 that is roughly M > 1500.
+ *   - Every call shares the one array.  No byte of it needs to start at zero
+ *     (a call writes all scratch it reads), but calls whose kernels may
+ *     overlap on the GPU (e.g. issued on different streams without ordering)
+ *     race on it: order them on one stream or with events.
+ */
+int qhead_fwd_noalloc(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                      const uint8_t* mask, float* logp, float* lse, int32_t* argmax,
+                      void* stream);
+
 /* Message for the last error on the calling thread ("" if none).  The
  * pointer stays valid until the thread's next qhead_* call. */
 const char* qhead_last_error(void);

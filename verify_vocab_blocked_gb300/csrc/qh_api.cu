@@ -140,6 +140,8 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 }  // namespace
 
+void qh::set_error(const std::string& msg) { g_err = msg; }
+
 extern "C" {
 
 const char* qhead_last_error(void) { return g_err.c_str(); }

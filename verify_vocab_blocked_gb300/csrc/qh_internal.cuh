@@ -7,7 +7,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace qh {
+
+// Sets the calling thread's qhead_last_error() message.
+void set_error(const std::string& msg);
 
 // Per-(row, vocab split) partial of the forward: online-softmax state over the
 // split's vocab rows (m = max z, s = sum exp(z - m)) and the split's two best

@@ -20,7 +20,8 @@ QHEAD_SB_F16 = 0
 
 # Every symbol include/qhead.h declares.
 EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd",
-           "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel")
+           "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel",
+           "qhead_fwd_noalloc")
 
 
 class CHead(ctypes.Structure):
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
     L.qhead_version.restype = ctypes.c_char_p
     L.qhead_time_next_head_kernel.argtypes = [vp, vp]
     L.qhead_time_next_head_kernel.restype = None
+    L.qhead_fwd_noalloc.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp]
+    L.qhead_fwd_noalloc.restype = ctypes.c_int
     _lib = L
     return L
 
