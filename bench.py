@@ -347,7 +347,8 @@ def run_ours(args):
                 "work_per_launch": f"{flops:.3e} flop (4*Ma*V*H)", "ms_per_launch": kms}
         fms = statistics.mean(fwd_ms)
         ff = 2.0 * R.active * cfg["V"] * cfg["H"]
-        roof["fwd_kernel"] = {"kernel": "stream_fwd_kernel", "ms_per_launch": fms,
+        roof["fwd_kernel"] = {"kernel": "tc_fwd_kernel" if R.M >= 64 else "stream_fwd_kernel",
+                              "ms_per_launch": fms,
                               "achieved_tflops": ff / (fms / 1e3) / 1e12}
     else:
         dom = "stream_fwd_kernel"

@@ -79,6 +79,30 @@ def test_edge_shapes(M, H, V, bits, cap):
     _run_all(_custom(M, H, V, bits, cap, seed=M + V))
 
 
+# Shapes on the tensor-core forward (M >= 64): partial 128-row tiles, vocab
+# sizes that are not multiples of the 256-row tile or of the 32-column argmax
+# chunk, 4 and 8 bits, cap on and off.
+TC_SHAPES = [
+    (64, 256, 1000, 4, 30.0),
+    (128, 128, 256, 4, 0.0),
+    (130, 384, 4099, 8, 30.0),
+    (200, 256, 257, 8, 0.0),
+    (300, 512, 3000, 4, 5.0),
+    (257, 128, 31, 4, 0.0),
+]
+
+
+@pytest.mark.parametrize("M,H,V,bits,cap", TC_SHAPES)
+def test_tensor_core_forward_shapes(M, H, V, bits, cap):
+    _run_all(_custom(M, H, V, bits, cap, seed=M * 7 + V))
+
+
+def test_tensor_core_forward_masked():
+    M = 333
+    mask = synth.make_mask(M, 64, 0.4)
+    _run_all(_custom(M, 256, 2000, 4, 30.0, seed=21, mask=mask))
+
+
 @pytest.mark.parametrize("pattern", ["all", "none", "alternate", "spans"])
 def test_masks(pattern):
     M = 40

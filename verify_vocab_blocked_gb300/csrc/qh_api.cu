@@ -13,6 +13,7 @@
 
 #include "../../include/qhead.h"
 #include "qh_internal.cuh"
+#include "qh_tmap.h"
 
 namespace {
 
@@ -67,10 +68,17 @@ int check_head(const qhead_head* hd) {
 
 // ---------------------------------------------------------------- plans
 
+// Rows from which the forward runs on the tensor-core kernel (below: the
+// weight-streaming kernel, whose cost is one pass over the head per 8 rows).
+constexpr int64_t kTcMinM = 64;
+
 struct FwdPlan {
     int64_t M = 0, Mpad = 0;
-    int S = 1;           // vocab splits of the partials
+    bool tc = false;     // tensor-core path
+    int grid = 0;        // persistent CTAs of the tensor-core kernel
+    int S = 1;           // vocab splits of the partials (weight-streaming path)
     int cand_width = 1;  // argmax candidate run length
+    size_t records = 0;  // partial records
     size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_part = 0, total = 0;
 };
 
@@ -86,22 +94,33 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    const int64_t groups = (M + qh::kTokGroup - 1) / qh::kTokGroup;
-    // One full wave: every SM holds as many CTAs as fit; each split keeps at
-    // least 128 vocab rows (16 per warp).
-    const int64_t want = (int64_t)di.sms * qh::stream_fwd_ctas_per_sm(hd->bits, hd->H);
-    int64_t S = (want + groups - 1) / groups;
-    const int64_t max_s = (hd->V + 127) / 128;
-    if (S > max_s) S = max_s;
-    if (S < 1) S = 1;
-    p->S = (int)S;
-    p->cand_width = 1;
+    p->tc = M >= kTcMinM;
+    if (p->tc) {
+        // One persistent CTA per SM; the kernel picks the number of vocab
+        // segments S from the active-row count so that n_tiles * S is about
+        // 8 * grid, hence at most 128 * (8 * grid + n_tiles) records.
+        p->grid = di.sms;
+        p->cand_width = 32;
+        p->records = (size_t)128 * (8 * (size_t)p->grid + (size_t)(p->Mpad / 128));
+    } else {
+        const int64_t groups = (M + qh::kTokGroup - 1) / qh::kTokGroup;
+        // One full wave: every SM holds as many CTAs as fit; each split keeps at
+        // least 128 vocab rows (16 per warp).
+        const int64_t want = (int64_t)di.sms * qh::stream_fwd_ctas_per_sm(hd->bits, hd->H);
+        int64_t S = (want + groups - 1) / groups;
+        const int64_t max_s = (hd->V + 127) / 128;
+        if (S > max_s) S = max_s;
+        if (S < 1) S = 1;
+        p->S = (int)S;
+        p->cand_width = 1;
+        p->records = (size_t)p->Mpad * p->S;
+    }
     size_t off = 0;
-    p->off_count = off; off = align_up(off + 4, 256);
+    p->off_count = off; off = align_up(off + 16, 256);  // count, error word, segment count
     p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
     p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 256);
-    p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 256);
-    p->off_part = off;  off = align_up(off + sizeof(qh::Partial) * (size_t)p->Mpad * p->S, 256);
+    p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
+    p->off_part = off;  off = align_up(off + sizeof(qh::Partial) * p->records, 256);
     p->total = off;
     return QHEAD_OK;
 }
@@ -201,6 +220,8 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     const auto* bi = static_cast<const __half*>(head->biases);
     const auto* hb = static_cast<const __nv_bfloat16*>(h);
     int* count = at<int>(workspace, p.off_count);
+    int* err = count + 1;
+    int* S_dev = count + 2;
     int* rows = at<int>(workspace, p.off_rows);
     int* pos = at<int>(workspace, p.off_pos);
     __half* h16 = at<__half>(workspace, p.off_h16);
@@ -208,22 +229,37 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
 
     cudaError_t e;
     if (M <= qh::kFusedPrologueMaxM) {
+        const int64_t nrows = p.tc ? p.Mpad : (M + qh::kTokGroup - 1) / qh::kTokGroup * qh::kTokGroup;
         if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
-                                           count, h16, st)))
+                                           count, h16, nrows, err, st)))
             return cuda_fail(e, "prologue");
     } else {
-        if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, st)))
+        if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
             return cuda_fail(e, "compact");
         if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
             return cuda_fail(e, "convert_h");
     }
-    hook_before(st);
-    e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, h16, count,
-                              M, part, p.S, st);
-    hook_after(st);
-    if (e) return cuda_fail(e, "stream_fwd");
+    if (p.tc) {
+        CUtensorMap th, tw;
+        const int words = 64 * head->bits / 32;
+        if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
+            !qh::tmap_packed_rows(&tw, wq, head->H * head->bits / 32, head->V, words, 256))
+            return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
+        hook_before(st);
+        e = qh::launch_tc_fwd(th, tw, sc, bi, head->V, head->H, head->bits, head->softcap, count,
+                              part, S_dev, err, p.grid, st);
+        hook_after(st);
+        if (e) return cuda_fail(e, "tc_fwd");
+    } else {
+        hook_before(st);
+        e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, h16,
+                                  count, M, part, p.S, st);
+        hook_after(st);
+        if (e) return cuda_fail(e, "stream_fwd");
+    }
     if ((e = qh::launch_fwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
-                                     pos, targets, part, p.S, p.cand_width, logp, lse, argmax, M,
+                                     pos, targets, part, p.S, p.tc ? S_dev : nullptr,
+                                     p.tc ? err : nullptr, p.cand_width, logp, lse, argmax, M,
                                      st)))
         return cuda_fail(e, "fwd_finalize");
     return QHEAD_OK;
@@ -262,7 +298,8 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     float* dhp = at<float>(workspace, p.off_dhp);
 
     cudaError_t e;
-    if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, st))) return cuda_fail(e, "compact");
+    if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, nullptr, st)))
+        return cuda_fail(e, "compact");
     hook_before(st);
     e = qh::launch_bwd_simt(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb, rows,
                             count, lse, dlogp, dhp, p.S, M, p.Mpad, st);

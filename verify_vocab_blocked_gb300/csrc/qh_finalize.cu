@@ -29,10 +29,21 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
     const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
-    const int32_t* __restrict__ targets, const Partial* __restrict__ part, int S, int cand_width,
+    const int32_t* __restrict__ targets, const Partial* __restrict__ part, int S,
+    const int* __restrict__ S_dev, const int* __restrict__ err, int cand_width,
     float* __restrict__ logp, float* __restrict__ lse, int32_t* __restrict__ argmax) {
     const int64_t r = blockIdx.x;
     const int i = pos[r];
+    if (S_dev) S = *S_dev;
+    if (err && *err != 0 && i >= 0) {
+        // The head kernel gave up (a bounded wait expired): poison the row.
+        if (threadIdx.x == 0) {
+            if (logp) logp[r] = __int_as_float(0x7fc00000);
+            if (lse) lse[r] = __int_as_float(0x7fc00000);
+            if (argmax) argmax[r] = -1;
+        }
+        return;
+    }
     if (i < 0) {
         if (threadIdx.x == 0) {
             if (logp) logp[r] = 0.f;
@@ -142,11 +153,11 @@ __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
-                                int cand_width, float* logp, float* lse, int32_t* argmax,
-                                int64_t M, cudaStream_t st) {
+                                const int* S_dev, const int* err, int cand_width, float* logp,
+                                float* lse, int32_t* argmax, int64_t M, cudaStream_t st) {
     fwd_finalize_kernel<<<(unsigned)M, kFinThreads, 0, st>>>(wq, scales, biases, V, H, bits, cap,
-                                                              h, pos, targets, part, S, cand_width,
-                                                              logp, lse, argmax);
+                                                              h, pos, targets, part, S, S_dev, err,
+                                                              cand_width, logp, lse, argmax);
     return cudaGetLastError();
 }
 

@@ -150,12 +150,12 @@ __device__ __forceinline__ float dequant_elem(const uint32_t* __restrict__ wq,
 // Each returns the cudaError_t of its launch.
 
 cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* rows, int* pos,
-                           int* count, cudaStream_t st);
+                           int* count, int* err, cudaStream_t st);
 // Compaction and conversion in one single-CTA launch (small M only).
 constexpr int64_t kFusedPrologueMaxM = 256;
 cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
                                   int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
-                                  __half* h16, cudaStream_t st);
+                                  __half* h16, int64_t nrows, int* err, cudaStream_t st);
 cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
                              const int* count, __half* h16, cudaStream_t st);
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
@@ -164,8 +164,8 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
-                                int cand_width, float* logp, float* lse, int32_t* argmax,
-                                int64_t M, cudaStream_t st);
+                                const int* S_dev, const int* err, int cand_width, float* logp,
+                                float* lse, int32_t* argmax, int64_t M, cudaStream_t st);
 cudaError_t launch_bwd_simt(const uint32_t* wq, const __half* scales, const __half* biases,
                             int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                             const int* rows, const int* count, const float* lse,

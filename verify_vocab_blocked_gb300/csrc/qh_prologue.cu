@@ -57,7 +57,9 @@ __device__ int compact_rows(const uint8_t* __restrict__ mask, int64_t M, int64_t
 
 __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ mask, int64_t M,
                                                        int64_t Mpad, int* __restrict__ rows,
-                                                       int* __restrict__ pos, int* __restrict__ count) {
+                                                       int* __restrict__ pos, int* __restrict__ count,
+                                                       int* __restrict__ err) {
+    if (err && threadIdx.x == 0) *err = 0;
     compact_rows(mask, M, Mpad, rows, pos, count);
 }
 
@@ -93,16 +95,17 @@ __global__ void convert_h_kernel(const __nv_bfloat16* __restrict__ h, int H, int
     *reinterpret_cast<uint4*>(h16 + i * H + 8 * u) = out;
 }
 
-// Small M: one CTA compacts, then converts every (row, 8-unit) of the padded
-// tile (the weight-streaming kernel reads rows in groups of 8).
+// Small M: one CTA compacts, then converts rows [0, nrows) (zeros past the
+// active count): groups of 8 for the weight-streaming kernel, whole 128-row
+// tiles for the tensor-core kernel.
 __global__ void __launch_bounds__(1024) prologue_fused_kernel(
     const uint8_t* __restrict__ mask, const __nv_bfloat16* __restrict__ h, int64_t M, int64_t Mpad,
     int H, int bits, int* __restrict__ rows, int* __restrict__ pos, int* __restrict__ count,
-    __half* __restrict__ h16) {
+    __half* __restrict__ h16, int64_t nrows, int* __restrict__ err) {
+    if (err && threadIdx.x == 0) *err = 0;
     const int n = compact_rows(mask, M, Mpad, rows, pos, count);
     __syncthreads();  // rows[] written by other threads
     const int units = H / 8;
-    const int64_t nrows = (M + kTokGroup - 1) / kTokGroup * kTokGroup;
     for (int64_t idx = threadIdx.x; idx < nrows * units; idx += 1024) {
         const int64_t i = idx / units;
         const int u = (int)(idx - i * units);
@@ -114,14 +117,15 @@ __global__ void __launch_bounds__(1024) prologue_fused_kernel(
 
 cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
                                   int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
-                                  __half* h16, cudaStream_t st) {
-    prologue_fused_kernel<<<1, 1024, 0, st>>>(mask, h, M, Mpad, H, bits, rows, pos, count, h16);
+                                  __half* h16, int64_t nrows, int* err, cudaStream_t st) {
+    prologue_fused_kernel<<<1, 1024, 0, st>>>(mask, h, M, Mpad, H, bits, rows, pos, count, h16,
+                                              nrows, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* rows, int* pos,
-                           int* count, cudaStream_t st) {
-    compact_kernel<<<1, 1024, 0, st>>>(mask, M, Mpad, rows, pos, count);
+                           int* count, int* err, cudaStream_t st) {
+    compact_kernel<<<1, 1024, 0, st>>>(mask, M, Mpad, rows, pos, count, err);
     return cudaGetLastError();
 }
 

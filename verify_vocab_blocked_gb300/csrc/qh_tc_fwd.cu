@@ -1,0 +1,371 @@
+// qh_tc_fwd.cu -- tensor-core forward for large M (steps a2-a5 of the hot path).
+//
+// Computes the same per-(row, vocab segment) partials as the vocab-parallel
+// forward on the page "mlx-bun 0.0.4 -> 0.0.6" (src/train/flash-cce.ts,
+// FWD_STEEL_SOURCE: a quantized block GEMM whose epilogue soft-caps each
+// logit tile and folds it into a running max / sum-exp), re-designed for
+// sm_103a:
+//
+//   * one persistent CTA per SM walks units (128 token rows x a segment of
+//     256-row vocab tiles), chosen on the device from the active-row count;
+//   * a TMA warp streams the fp16 h tile (128 x 64, 128-byte swizzle) and the
+//     packed weight tile (256 rows x 64 codes) into a 3-stage ring;
+//   * four dequant warps turn the packed tile into fp16 in the tensor core's
+//     K-major 128-byte-swizzled layout (w = fma(q, scale, bias), one rounding);
+//   * one thread issues tcgen05.mma (M=128, N=256, K=16, fp32 accumulate) into
+//     one of two 256-column TMEM accumulators;
+//   * four epilogue warps read the accumulator with tcgen05.ld (one row per
+//     thread), apply the soft cap, update the row's online softmax and track
+//     the two 32-column chunks with the largest raw logit (argmax candidates,
+//     rechecked exactly by the finalize kernel).
+// The [M,V] logits and the dequantized head never leave the SM.
+#include <stdio.h>
+
+#include "qh_dequant.cuh"
+#include "qh_tc.cuh"
+
+namespace qh {
+
+namespace {
+
+constexpr int BM = 128;   // token rows per tile (MMA M)
+constexpr int BN = 256;   // vocab rows per tile (MMA N)
+constexpr int BK = 64;    // K per stage (one quantization group, one swizzle atom)
+constexpr int NS = 3;     // pipeline stages
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;  // two 256-column fp32 accumulators
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr uint32_t kIdesc = tc::idesc_f16_f32(BM, BN, false, false);
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int BITS>
+struct Layout {
+    static constexpr int P_ROW = BK * BITS / 8;  // packed bytes per row per stage
+    static constexpr int P_BYTES = BN * P_ROW;
+    static constexpr int WORDS = BK * BITS / 32;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + NS * A_BYTES;
+    static constexpr int OFF_P = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_BAR = OFF_P + NS * P_BYTES;
+    static constexpr int BAR_BYTES = 8 * (3 * NS + 4) + 16;
+    static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+};
+
+struct Work {
+    int n_mt, n_vt, n_seg, units;
+};
+
+__device__ __forceinline__ Work plan_work(int n_active, int64_t V) {
+    Work w;
+    w.n_mt = (n_active + BM - 1) / BM;
+    w.n_vt = (int)((V + BN - 1) / BN);
+    const int target = 8 * (int)gridDim.x;  // about 8 units per CTA
+    int seg = w.n_mt > 0 ? (target + w.n_mt - 1) / w.n_mt : 1;
+    if (seg > w.n_vt) seg = w.n_vt;
+    if (seg < 1) seg = 1;
+    w.n_seg = seg;
+    w.units = w.n_mt * w.n_seg;
+    return w;
+}
+
+__device__ __forceinline__ void unit_coords(const Work& w, int u, int& mt, int& seg, int& vt0,
+                                            int& vt1) {
+    seg = u / w.n_mt;
+    mt = u - seg * w.n_mt;
+    vt0 = (int)((int64_t)seg * w.n_vt / w.n_seg);
+    vt1 = (int)((int64_t)(seg + 1) * w.n_vt / w.n_seg);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
+    const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+    const __half* __restrict__ scales, const __half* __restrict__ biases, int64_t V, int H,
+    float cap, const int* __restrict__ count, Partial* __restrict__ part, int* __restrict__ S_out,
+    int* __restrict__ err) {
+    using L = Layout<BITS>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+    uint64_t* dq = full + NS;
+    uint64_t* empty = dq + NS;
+    uint64_t* accf = empty + NS;
+    uint64_t* acce = accf + 2;
+    uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_active = *count;
+    const Work W = plan_work(n_active, V);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *S_out = W.n_seg;
+    if (W.units == 0 || (int)blockIdx.x >= W.units) return;
+    const int KSTEPS = H / BK;
+    const int G = H / 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&dq[i], 4);
+            tc::mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&accf[i], 1);
+            tc::mbar_init(&acce[i], 4);
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_tmap(&tmap_h);
+        tc::prefetch_tmap(&tmap_w);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_base_sh, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_sh;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
+                int mt, seg, vt0, vt1;
+                unit_coords(W, u, mt, seg, vt0, vt1);
+                for (int vt = vt0; vt < vt1; ++vt) {
+                    for (int kk = 0; kk < KSTEPS; ++kk) {
+                        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
+                                           tc::kErrTimeoutEmpty))
+                            goto producer_done;
+                        tc::mbar_arrive_expect_tx(&full[stage], A_BYTES + L::P_BYTES);
+                        tc::tma_load_2d(smem + L::OFF_A + stage * A_BYTES, &tmap_h, &full[stage],
+                                        kk * BK, mt * BM);
+                        tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w,
+                                        &full[stage], kk * L::WORDS, vt * BN);
+                        if (++stage == NS) { stage = 0; phase ^= 1; }
+                    }
+                }
+            }
+            // Drain: wait until the loads of the last stages have landed.
+            for (int i = 0; i < NS; ++i) {
+                if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
+                                   tc::kErrTimeoutEmpty))
+                    break;
+                if (++stage == NS) { stage = 0; phase ^= 1; }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, aphase = 0;
+            for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
+                int mt, seg, vt0, vt1;
+                unit_coords(W, u, mt, seg, vt0, vt1);
+                for (int vt = vt0; vt < vt1; ++vt) {
+                    if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
+                                       tc::kErrTimeoutAccEmpty))
+                        goto mma_done;
+                    tc::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    for (int kk = 0; kk < KSTEPS; ++kk) {
+                        if (!tc::mbar_wait(&full[stage], phase, abort_flag, err,
+                                           tc::kErrTimeoutFull))
+                            goto mma_done;
+                        if (!tc::mbar_wait(&dq[stage], phase, abort_flag, err,
+                                           tc::kErrTimeoutDequant))
+                            goto mma_done;
+                        tc::tc_fence_after();
+                        const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * A_BYTES);
+                        const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + stage * B_BYTES);
+#pragma unroll
+                        for (int ks = 0; ks < BK / 16; ++ks) {
+                            const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks, 16, 1024);
+                            const uint64_t bd = tc::sdesc_sw128(b0 + 32 * ks, 16, 1024);
+                            tc::umma_f16(d_tmem, ad, bd, kIdesc, (kk | ks) != 0);
+                        }
+                        tc::umma_commit(&empty[stage]);
+                        if (++stage == NS) { stage = 0; phase ^= 1; }
+                    }
+                    tc::umma_commit(&accf[buf]);
+                    if (++buf == 2) { buf = 0; aphase ^= 1; }
+                }
+            }
+        mma_done:;
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ dequant warps
+        const int t = threadIdx.x - 64;  // 0..127: rows t and t + 128 of the tile
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
+            int mt, seg, vt0, vt1;
+            unit_coords(W, u, mt, seg, vt0, vt1);
+            for (int vt = vt0; vt < vt1; ++vt) {
+                const int64_t v0 = (int64_t)vt * BN + t, v1 = v0 + 128;
+                const bool ok0 = v0 < V, ok1 = v1 < V;
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const __half z = __float2half(0.f);
+                    const __half s0 = ok0 ? scales[v0 * G + kk] : z, b0 = ok0 ? biases[v0 * G + kk] : z;
+                    const __half s1 = ok1 ? scales[v1 * G + kk] : z, b1 = ok1 ? biases[v1 * G + kk] : z;
+                    if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
+                        goto dq_done;
+                    const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
+                    unsigned char* Bs = smem + L::OFF_B + stage * B_BYTES;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int r = t + 128 * rr;
+                        const __half2 s2 = __half2half2(rr ? s1 : s0);
+                        const __half2 b2 = __half2half2(rr ? b1 : b0);
+                        const uint4* prow = reinterpret_cast<const uint4*>(P + r * L::P_ROW);
+                        unsigned char* brow = Bs + r * 128;
+                        if constexpr (BITS == 4) {
+#pragma unroll
+                            for (int hq = 0; hq < 2; ++hq) {
+                                const uint4 wv = prow[hq];
+                                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const int c = hq * 4 + j;  // 16-byte chunk = one word
+                                    uint32_t p[4];
+                                    deq4_word(wd[j], s2, b2, p);
+                                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) =
+                                        make_uint4(p[0], p[1], p[2], p[3]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int hq = 0; hq < 4; ++hq) {
+                                const uint4 wv = prow[hq];
+                                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                                for (int j = 0; j < 2; ++j) {
+                                    const int c = hq * 2 + j;  // 16-byte chunk = two words
+                                    const uint32_t w0 = wd[2 * j], w1 = wd[2 * j + 1];
+                                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) =
+                                        make_uint4(deq8(w0, 0x5140u, s2, b2),
+                                                   deq8(w0, 0x7362u, s2, b2),
+                                                   deq8(w1, 0x5140u, s2, b2),
+                                                   deq8(w1, 0x7362u, s2, b2));
+                                }
+                            }
+                        }
+                    }
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&dq[stage]);
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    dq_done:;
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int sub = warp & 3;  // TMEM sub-partition of this warp
+        const int row = sub * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
+        const float k2 = cap > 0.f ? 2.f * kLog2e / cap : 0.f;
+        int buf = 0;
+        uint32_t aphase = 0;
+        for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
+            int mt, seg, vt0, vt1;
+            unit_coords(W, u, mt, seg, vt0, vt1);
+            float m = -INFINITY, s = 0.f, v1 = -INFINITY, v2 = -INFINITY;
+            int i1 = INT32_MAX, i2 = INT32_MAX;
+            for (int vt = vt0; vt < vt1; ++vt) {
+                if (!tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
+                    goto epi_done;
+                tc::tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, r);
+                    tc::tmem_wait_ld();
+                    const int64_t col0 = (int64_t)vt * BN + c * 32;
+                    const int nvalid = (int)min((int64_t)32, V - col0);
+                    if (nvalid <= 0) continue;
+                    float x[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+                    float rmax = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nvalid) rmax = fmaxf(rmax, x[j]);
+                    // argmax candidates: the two chunks with the largest raw logit
+                    const int ci = (int)col0;
+                    if (better(rmax, ci, v1, i1)) { v2 = v1; i2 = i1; v1 = rmax; i1 = ci; }
+                    else if (better(rmax, ci, v2, i2)) { v2 = rmax; i2 = ci; }
+                    // soft cap z = cap * tanh(x / cap) = cap - 2 cap / (exp(2x/cap) + 1)
+                    float zmax = rmax;
+                    if (cap > 0.f) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            x[j] = fmaf(-2.f * cap, tc::rcp_approx(tc::ex2_approx(x[j] * k2) + 1.f), cap);
+                        zmax = fmaf(-2.f * cap, tc::rcp_approx(tc::ex2_approx(rmax * k2) + 1.f), cap);
+                    }
+                    const float mn = fmaxf(m, zmax);
+                    const float mb = mn * kLog2e;
+                    float acc = 0.f;
+                    if (nvalid == 32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc += tc::ex2_approx(fmaf(x[j], kLog2e, -mb));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nvalid) acc += tc::ex2_approx(fmaf(x[j], kLog2e, -mb));
+                    }
+                    s = s * tc::ex2_approx((m - mn) * kLog2e) + acc;
+                    m = mn;
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&acce[buf]);
+                if (++buf == 2) { buf = 0; aphase ^= 1; }
+            }
+            {
+                const int i = mt * BM + row;
+                if (i < n_active) {
+                    Partial p;
+                    p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.pad0 = 0; p.pad1 = 0;
+                    part[(int64_t)i * W.n_seg + seg] = p;
+                }
+            }
+        }
+    epi_done:;
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+int tc_fwd_smem_bytes(int bits) { return bits == 4 ? Layout<4>::SMEM : Layout<8>::SMEM; }
+
+cudaError_t launch_tc_fwd(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
+                          const __half* scales, const __half* biases, int64_t V, int H, int bits,
+                          float cap, const int* count, Partial* part, int* S_out, int* err,
+                          int grid, cudaStream_t st) {
+    if (bits == 4) {
+        cudaFuncSetAttribute(tc_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<4>::SMEM);
+        tc_fwd_kernel<4><<<grid, kThreads, Layout<4>::SMEM, st>>>(
+            tmap_h, tmap_w, scales, biases, V, H, cap, count, part, S_out, err);
+    } else {
+        cudaFuncSetAttribute(tc_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<8>::SMEM);
+        tc_fwd_kernel<8><<<grid, kThreads, Layout<8>::SMEM, st>>>(
+            tmap_h, tmap_w, scales, biases, V, H, cap, count, part, S_out, err);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace qh
