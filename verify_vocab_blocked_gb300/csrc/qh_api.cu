@@ -84,9 +84,17 @@ struct FwdPlan {
 
 struct BwdPlan {
     int64_t M = 0, Mpad = 0;
-    int S = 1;
-    size_t off_count = 0, off_rows = 0, off_pos = 0, off_dhp = 0, total = 0;
+    bool tc = false;
+    int grid = 0;
+    int S = 1;               // vocab splits of the CUDA-core path
+    int64_t chunk = 0;       // vocab rows per coefficient block (tensor-core path)
+    size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_coeff = 0, off_dhp = 0,
+           total = 0;
 };
+
+// Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block
+// (about 94 MB at 5736 rows) stays mostly in L2 between the two phases.
+constexpr int64_t kBwdChunk = 8192;
 
 int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
     DevInfo di;
@@ -131,19 +139,30 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p) {
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    const int tb = qh::bwd_simt_tokens(hd->H);
-    const int64_t groups = (M + tb - 1) / tb;
-    const int64_t want = (int64_t)di.sms * 4;
-    int64_t S = (want + groups - 1) / groups;
-    const int64_t max_s = (hd->V + 255) / 256;
-    if (S > max_s) S = max_s;
-    if (S < 1) S = 1;
-    p->S = (int)S;
+    p->tc = M >= kTcMinM;
     size_t off = 0;
-    p->off_count = off; off = align_up(off + 4, 256);
+    p->off_count = off; off = align_up(off + 16, 256);
     p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
-    p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 256);
-    p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 256);
+    p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 1024);
+    if (p->tc) {
+        p->grid = di.sms;
+        p->S = 1;
+        const int64_t vr = (hd->V + 255) / 256 * 256;
+        p->chunk = vr < kBwdChunk ? vr : kBwdChunk;
+        p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
+        p->off_coeff = off; off = align_up(off + 2 * (size_t)p->Mpad * p->chunk, 1024);
+        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->Mpad * hd->H, 256);
+    } else {
+        const int tb = qh::bwd_simt_tokens(hd->H);
+        const int64_t groups = (M + tb - 1) / tb;
+        const int64_t want = (int64_t)di.sms * 4;
+        int64_t S = (want + groups - 1) / groups;
+        const int64_t max_s = (hd->V + 255) / 256;
+        if (S > max_s) S = max_s;
+        if (S < 1) S = 1;
+        p->S = (int)S;
+        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 256);
+    }
     p->total = off;
     return QHEAD_OK;
 }
@@ -245,9 +264,13 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
             !qh::tmap_packed_rows(&tw, wq, head->H * head->bits / 32, head->V, words, 256))
             return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
+        qh::TcFwdArgs ta{};
+        ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H; ta.cap = head->softcap;
+        ta.count = count; ta.err = err;
+        ta.vt_begin = 0; ta.vt_end = (int)((head->V + 255) / 256);
+        ta.part = part; ta.S_out = S_dev;
         hook_before(st);
-        e = qh::launch_tc_fwd(th, tw, sc, bi, head->V, head->H, head->bits, head->softcap, count,
-                              part, S_dev, err, p.grid, st);
+        e = qh::launch_tc_fwd(th, tw, ta, head->bits, false, p.grid, st);
         hook_after(st);
         if (e) return cuda_fail(e, "tc_fwd");
     } else {
@@ -293,18 +316,65 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     const auto* bi = static_cast<const __half*>(head->biases);
     const auto* hb = static_cast<const __nv_bfloat16*>(h);
     int* count = at<int>(workspace, p.off_count);
+    int* err = count + 1;
     int* rows = at<int>(workspace, p.off_rows);
     int* pos = at<int>(workspace, p.off_pos);
     float* dhp = at<float>(workspace, p.off_dhp);
 
     cudaError_t e;
-    if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, nullptr, st)))
-        return cuda_fail(e, "compact");
-    hook_before(st);
-    e = qh::launch_bwd_simt(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb, rows,
-                            count, lse, dlogp, dhp, p.S, M, p.Mpad, st);
-    hook_after(st);
-    if (e) return cuda_fail(e, "bwd_simt");
+    if (p.tc) {
+        __half* h16 = at<__half>(workspace, p.off_h16);
+        __half* coeff = at<__half>(workspace, p.off_coeff);
+        if (M <= qh::kFusedPrologueMaxM) {
+            if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
+                                               count, h16, p.Mpad, err, st)))
+                return cuda_fail(e, "prologue");
+        } else {
+            if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
+                return cuda_fail(e, "compact");
+            if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
+                return cuda_fail(e, "convert_h");
+        }
+        CUtensorMap th, tw_logit, tcoef, tw_dh;
+        const int wpr = head->H * head->bits / 32;
+        if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
+            !qh::tmap_packed_rows(&tw_logit, wq, wpr, head->V, 64 * head->bits / 32, 256) ||
+            !qh::tmap_rows_f16_sw128(&tcoef, coeff, p.chunk, p.Mpad, 128) ||
+            !qh::tmap_packed_rows(&tw_dh, wq, wpr, head->V, qh::tc_dh_words(head->H, head->bits),
+                                  64))
+            return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
+        const int n_vt = (int)((head->V + 255) / 256);
+        const int vt_chunk = (int)(p.chunk / 256);
+        hook_before(st);
+        for (int vt0 = 0, c = 0; vt0 < n_vt; vt0 += vt_chunk, ++c) {
+            const int vt1 = vt0 + vt_chunk < n_vt ? vt0 + vt_chunk : n_vt;
+            qh::TcFwdArgs ta{};
+            ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H;
+            ta.cap = head->softcap; ta.count = count; ta.err = err;
+            ta.vt_begin = vt0; ta.vt_end = vt1;
+            ta.lse = lse; ta.rows = rows; ta.coeff = coeff; ta.coeff_ld = p.chunk;
+            ta.coeff_rows = (int)p.Mpad;
+            if ((e = qh::launch_tc_fwd(th, tw_logit, ta, head->bits, true, p.grid, st)))
+                return cuda_fail(e, "tc_coeff");
+            qh::TcDhArgs da{};
+            da.scales = sc; da.biases = bi; da.V = head->V; da.H = head->H;
+            da.count = count; da.err = err; da.rows = rows; da.dlogp = dlogp; da.dh_acc = dhp;
+            da.v_begin = (int64_t)vt0 * 256;
+            da.n_k = (vt1 - vt0) * 256 / 64;
+            da.accumulate = c > 0;
+            if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
+                return cuda_fail(e, "tc_dh");
+        }
+        hook_after(st);
+    } else {
+        if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, nullptr, st)))
+            return cuda_fail(e, "compact");
+        hook_before(st);
+        e = qh::launch_bwd_simt(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb, rows,
+                                count, lse, dlogp, dhp, p.S, M, p.Mpad, st);
+        hook_after(st);
+        if (e) return cuda_fail(e, "bwd_simt");
+    }
     if ((e = qh::launch_bwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
                                      pos, targets, dlogp, dhp, p.S, p.Mpad, dh, M, st)))
         return cuda_fail(e, "bwd_finalize");

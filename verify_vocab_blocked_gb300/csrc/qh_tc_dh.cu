@@ -1,0 +1,298 @@
+// qh_tc_dh.cu -- tensor-core backward contraction (step a10 of the hot path).
+//
+// For one vocab chunk [v_begin, v_begin + 64 * n_k):
+//     dh_acc[i, :] (+)= (-dlogp[row_i] * 2^-14) * sum_k C[i, k] * w[v_begin + k, :]
+// where C = p * sech2 * 2^14 (fp16) is the coefficient block phase 1 wrote.
+// This is phase 2 of the backward on the page "mlx-bun 0.0.4 -> 0.0.6"
+// (src/train/flash-cce.ts, BWD_STEEL_SOURCE: dh[8,H] += coeff[8,32] @ W[32,H]),
+// as a tcgen05 GEMM: M = 128 token rows, N = 256 (or 128) hidden columns,
+// K = the chunk's vocab rows.  The coefficient tile arrives by TMA (K-major,
+// 128-byte swizzle); the weight tile is dequantized from its packed rows into
+// the MN-major 128-byte-swizzled layout (hidden index contiguous), so the same
+// packed rows the forward reads serve here without a transpose.  Each output
+// tile is owned by one CTA and accumulated over the chunks in a fixed order:
+// the result is deterministic.
+#include "qh_dequant.cuh"
+#include "qh_tc.cuh"
+#include "qh_tmap.h"
+
+namespace qh {
+
+namespace {
+
+constexpr int BM = 128;   // token rows (MMA M)
+constexpr int BK = 64;    // vocab rows per stage
+constexpr int NS = 3;
+constexpr int kThreads = 320;
+
+template <int BITS, int BNH>
+struct DhLayout {
+    static constexpr int A_BYTES = BM * BK * 2;             // coeff tile, K-major SW128
+    static constexpr int B_BYTES = BNH * BK * 2;            // weight tile, MN-major SW128
+    static constexpr int P_ROW = BNH * BITS / 8;            // packed bytes per vocab row
+    static constexpr int P_BYTES = BK * P_ROW;
+    static constexpr int WORDS = BNH * BITS / 32;           // TMA box width (words)
+    static constexpr int NBLK = BNH / 64;                   // 64-column blocks along N
+    static constexpr int OFF_B = 0;                         // B first: descriptor reach stays inside
+    static constexpr int OFF_A = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_P = OFF_A + NS * A_BYTES;
+    static constexpr int OFF_BAR = OFF_P + NS * P_BYTES;
+    static constexpr int BAR_BYTES = 8 * (3 * NS + 4) + 16;
+    static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;
+    static constexpr int TMEM_COLS = 2 * BNH;
+    static constexpr uint32_t IDESC = tc::idesc_f16_f32(BM, BNH, false, true);
+};
+
+// Natural-order fp16 pairs of one 4-bit word: the dequantizer yields
+// (q0,q4), (q1,q5), (q2,q6), (q3,q7); the hidden axis is the MMA's N axis
+// here, so the pairs are regrouped to (q0,q1), (q2,q3), (q4,q5), (q6,q7).
+__device__ __forceinline__ uint4 deq4_natural(uint32_t w, __half2 s, __half2 b) {
+    uint32_t p[4];
+    deq4_word(w, s, b, p);
+    return make_uint4(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410),
+                      __byte_perm(p[0], p[1], 0x7632), __byte_perm(p[2], p[3], 0x7632));
+}
+
+template <int BITS, int BNH>
+__global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
+    const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_w,
+    const TcDhArgs a) {
+    using L = DhLayout<BITS, BNH>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+    uint64_t* dq = full + NS;
+    uint64_t* empty = dq + NS;
+    uint64_t* accf = empty + NS;
+    uint64_t* acce = accf + 2;
+    uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+    int* err = a.err;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_active = *a.count;
+    const int n_mt = (n_active + BM - 1) / BM;
+    const int n_nt = a.H / BNH;
+    const int units = n_mt * n_nt;
+    if (units == 0 || (int)blockIdx.x >= units) return;
+    const int G = a.H / 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&dq[i], 4);
+            tc::mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&accf[i], 1);
+            tc::mbar_init(&acce[i], 4);
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_tmap(&tmap_c);
+        tc::prefetch_tmap(&tmap_w);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_base_sh, L::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_sh;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                const int mt = u / n_nt, nt = u - (u / n_nt) * n_nt;
+                for (int kk = 0; kk < a.n_k; ++kk) {
+                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
+                                       tc::kErrTimeoutEmpty))
+                        goto producer_done;
+                    tc::mbar_arrive_expect_tx(&full[stage], L::A_BYTES + L::P_BYTES);
+                    tc::tma_load_2d(smem + L::OFF_A + stage * L::A_BYTES, &tmap_c, &full[stage],
+                                    kk * BK, mt * BM);
+                    tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w, &full[stage],
+                                    nt * L::WORDS, (int)(a.v_begin + kk * BK));
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
+                }
+            }
+            for (int i = 0; i < NS; ++i) {
+                if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
+                                   tc::kErrTimeoutEmpty))
+                    break;
+                if (++stage == NS) { stage = 0; phase ^= 1; }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, aphase = 0;
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
+                                   tc::kErrTimeoutAccEmpty))
+                    goto mma_done;
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BNH;
+                for (int kk = 0; kk < a.n_k; ++kk) {
+                    if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
+                        goto mma_done;
+                    if (!tc::mbar_wait(&dq[stage], phase, abort_flag, err, tc::kErrTimeoutDequant))
+                        goto mma_done;
+                    tc::tc_fence_after();
+                    const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * L::A_BYTES);
+                    const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + stage * L::B_BYTES);
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        // A: K-major, 32 bytes per 16-element K step inside the swizzle atom.
+                        const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks, 16, 1024);
+                        // B: MN-major, two 8-row K groups (2 x 1024 B) per K step;
+                        // 64-column blocks along N are BK/8 * 1024 bytes apart.
+                        const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks, (BK / 8) * 1024, 1024);
+                        tc::umma_f16(d_tmem, ad, bd, L::IDESC, (kk | ks) != 0);
+                    }
+                    tc::umma_commit(&empty[stage]);
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
+                }
+                tc::umma_commit(&accf[buf]);
+                if (++buf == 2) { buf = 0; aphase ^= 1; }
+            }
+        mma_done:;
+        }
+    } else if (warp < 6) {
+        // Dequant: thread t -> vocab row kr = t / 2 of the stage, columns
+        // [ (t & 1) * BNH/2, + BNH/2 ) of the N tile.
+        const int t = threadIdx.x - 64;
+        const int kr = t >> 1, half = t & 1;
+        constexpr int COLS = BNH / 2;
+        constexpr int NG = COLS / 64 > 0 ? COLS / 64 : 1;  // groups per thread
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int nt = u - (u / n_nt) * n_nt;
+            const int col0 = nt * BNH + half * COLS;  // first hidden column of this thread
+            for (int kk = 0; kk < a.n_k; ++kk) {
+                const int64_t v = a.v_begin + (int64_t)kk * BK + kr;
+                const bool ok = v < a.V;
+                __half sv[NG], bv[NG];
+#pragma unroll
+                for (int q = 0; q < NG; ++q) {
+                    const int gi = col0 / 64 + q;
+                    sv[q] = ok ? a.scales[v * G + gi] : __float2half(0.f);
+                    bv[q] = ok ? a.biases[v * G + gi] : __float2half(0.f);
+                }
+                if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
+                    goto dq_done;
+                const unsigned char* prow =
+                    smem + L::OFF_P + stage * L::P_BYTES + kr * L::P_ROW + half * (COLS * BITS / 8);
+                unsigned char* Bs = smem + L::OFF_B + stage * L::B_BYTES;
+                const int krow = kr & 7;
+                unsigned char* atom_base = Bs + (kr >> 3) * 1024 + krow * 128;
+#pragma unroll
+                for (int cc = 0; cc < COLS / 8; ++cc) {  // 8-column chunks of this thread
+                    const int ncol = half * COLS + cc * 8;  // column within the N tile
+                    const int nb = ncol >> 6, j = (ncol >> 3) & 7;
+                    const int q = (cc * 8) / 64;
+                    const __half2 s2 = __half2half2(sv[q]), b2 = __half2half2(bv[q]);
+                    uint4 out;
+                    if constexpr (BITS == 4) {
+                        const uint32_t w = reinterpret_cast<const uint32_t*>(prow)[cc];
+                        out = deq4_natural(w, s2, b2);
+                    } else {
+                        const uint2 w2 = reinterpret_cast<const uint2*>(prow)[cc];
+                        out = make_uint4(deq8(w2.x, 0x5140u, s2, b2), deq8(w2.x, 0x7362u, s2, b2),
+                                         deq8(w2.y, 0x5140u, s2, b2), deq8(w2.y, 0x7362u, s2, b2));
+                    }
+                    *reinterpret_cast<uint4*>(atom_base + nb * (BK / 8) * 1024 +
+                                              ((j ^ krow) << 4)) = out;
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&dq[stage]);
+                if (++stage == NS) { stage = 0; phase ^= 1; }
+            }
+        }
+    dq_done:;
+    } else {
+        const int sub = warp & 3;
+        const int row = sub * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
+        int buf = 0;
+        uint32_t aphase = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int mt = u / n_nt, nt = u - (u / n_nt) * n_nt;
+            const int i = mt * BM + row;
+            const bool row_ok = i < n_active;
+            const float scale = row_ok ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
+            if (!tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
+                goto epi_done;
+            tc::tc_fence_after();
+            float* dst = a.dh_acc + (int64_t)i * a.H + nt * BNH;
+#pragma unroll 1
+            for (int c = 0; c < BNH / 32; ++c) {
+                uint32_t r[32];
+                tc::tmem_ld32(tmem_base + lane_addr + buf * BNH + c * 32, r);
+                tc::tmem_wait_ld();
+                if (row_ok) {
+                    float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float4 v = make_float4(__uint_as_float(r[4 * q]) * scale,
+                                               __uint_as_float(r[4 * q + 1]) * scale,
+                                               __uint_as_float(r[4 * q + 2]) * scale,
+                                               __uint_as_float(r[4 * q + 3]) * scale);
+                        if (a.accumulate) {
+                            const float4 o = d4[q];
+                            v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                        }
+                        d4[q] = v;
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acce[buf]);
+            if (++buf == 2) { buf = 0; aphase ^= 1; }
+        }
+    epi_done:;
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int BITS, int BNH>
+cudaError_t launch_t(const CUtensorMap& tc_map, const CUtensorMap& tw, const TcDhArgs& a, int grid,
+                     cudaStream_t st) {
+    using L = DhLayout<BITS, BNH>;
+    cudaFuncSetAttribute(tc_dh_kernel<BITS, BNH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         L::SMEM);
+    tc_dh_kernel<BITS, BNH><<<grid, kThreads, L::SMEM, st>>>(tc_map, tw, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_dh_cols(int H) { return H % 256 == 0 ? 256 : 128; }
+
+int tc_dh_words(int H, int bits) { return tc_dh_cols(H) * bits / 32; }
+
+cudaError_t launch_tc_dh(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w, const TcDhArgs& a,
+                         int bits, int grid, cudaStream_t st) {
+    const int bnh = tc_dh_cols(a.H);
+    if (bits == 4)
+        return bnh == 256 ? launch_t<4, 256>(tmap_c, tmap_w, a, grid, st)
+                          : launch_t<4, 128>(tmap_c, tmap_w, a, grid, st);
+    return bnh == 256 ? launch_t<8, 256>(tmap_c, tmap_w, a, grid, st)
+                      : launch_t<8, 128>(tmap_c, tmap_w, a, grid, st);
+}
+
+}  // namespace qh

@@ -23,6 +23,7 @@
 
 #include "qh_dequant.cuh"
 #include "qh_tc.cuh"
+#include "qh_tmap.h"
 
 namespace qh {
 
@@ -56,10 +57,10 @@ struct Work {
     int n_mt, n_vt, n_seg, units;
 };
 
-__device__ __forceinline__ Work plan_work(int n_active, int64_t V) {
+__device__ __forceinline__ Work plan_work(int n_active, int n_vt) {
     Work w;
     w.n_mt = (n_active + BM - 1) / BM;
-    w.n_vt = (int)((V + BN - 1) / BN);
+    w.n_vt = n_vt;
     const int target = 8 * (int)gridDim.x;  // about 8 units per CTA
     int seg = w.n_mt > 0 ? (target + w.n_mt - 1) / w.n_mt : 1;
     if (seg > w.n_vt) seg = w.n_vt;
@@ -69,21 +70,30 @@ __device__ __forceinline__ Work plan_work(int n_active, int64_t V) {
     return w;
 }
 
-__device__ __forceinline__ void unit_coords(const Work& w, int u, int& mt, int& seg, int& vt0,
-                                            int& vt1) {
+__device__ __forceinline__ void unit_coords(const Work& w, int vt_begin, int u, int& mt, int& seg,
+                                            int& vt0, int& vt1) {
     seg = u / w.n_mt;
     mt = u - seg * w.n_mt;
-    vt0 = (int)((int64_t)seg * w.n_vt / w.n_seg);
-    vt1 = (int)((int64_t)(seg + 1) * w.n_vt / w.n_seg);
+    vt0 = vt_begin + (int)((int64_t)seg * w.n_vt / w.n_seg);
+    vt1 = vt_begin + (int)((int64_t)(seg + 1) * w.n_vt / w.n_seg);
 }
 
-template <int BITS>
+// EPI_SOFTMAX: per-row online softmax + argmax candidates -> partials (forward).
+// EPI_COEFF: per logit c = exp(z - lse) * sech2 * 2^14 as fp16 into a
+//            [rows x chunk] block (phase 1 of the backward).
+constexpr int EPI_SOFTMAX = 0, EPI_COEFF = 1;
+
+template <int BITS, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
-    const __half* __restrict__ scales, const __half* __restrict__ biases, int64_t V, int H,
-    float cap, const int* __restrict__ count, Partial* __restrict__ part, int* __restrict__ S_out,
-    int* __restrict__ err) {
+    const TcFwdArgs a) {
     using L = Layout<BITS>;
+    const __half* __restrict__ scales = a.scales;
+    const __half* __restrict__ biases = a.biases;
+    const int64_t V = a.V;
+    const int H = a.H;
+    const float cap = a.cap;
+    int* __restrict__ err = a.err;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -96,9 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_active = *count;
-    const Work W = plan_work(n_active, V);
-    if (blockIdx.x == 0 && threadIdx.x == 0) *S_out = W.n_seg;
+    const int n_active = *a.count;
+    const Work W = plan_work(n_active, a.vt_end - a.vt_begin);
+    if (EPI == EPI_SOFTMAX && blockIdx.x == 0 && threadIdx.x == 0) *a.S_out = W.n_seg;
     if (W.units == 0 || (int)blockIdx.x >= W.units) return;
     const int KSTEPS = H / BK;
     const int G = H / 64;
@@ -134,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             uint32_t phase = 0;
             for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
                 int mt, seg, vt0, vt1;
-                unit_coords(W, u, mt, seg, vt0, vt1);
+                unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
                 for (int vt = vt0; vt < vt1; ++vt) {
                     for (int kk = 0; kk < KSTEPS; ++kk) {
                         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
@@ -165,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             uint32_t phase = 0, aphase = 0;
             for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
                 int mt, seg, vt0, vt1;
-                unit_coords(W, u, mt, seg, vt0, vt1);
+                unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
                 for (int vt = vt0; vt < vt1; ++vt) {
                     if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
                                        tc::kErrTimeoutAccEmpty))
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
         uint32_t phase = 0;
         for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
             int mt, seg, vt0, vt1;
-            unit_coords(W, u, mt, seg, vt0, vt1);
+            unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
             for (int vt = vt0; vt < vt1; ++vt) {
                 const int64_t v0 = (int64_t)vt * BN + t, v1 = v0 + 128;
                 const bool ok0 = v0 < V, ok1 = v1 < V;
@@ -273,9 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
         uint32_t aphase = 0;
         for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
             int mt, seg, vt0, vt1;
-            unit_coords(W, u, mt, seg, vt0, vt1);
+            unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
+            const int i = mt * BM + row;  // compact row of this thread
             float m = -INFINITY, s = 0.f, v1 = -INFINITY, v2 = -INFINITY;
             int i1 = INT32_MAX, i2 = INT32_MAX;
+            // EPI_COEFF: log2(p * 2^14) = z * log2e - (lse * log2e - 14)
+            float lsb = 0.f;
+            bool row_ok = i < n_active;
+            if (EPI == EPI_COEFF && row_ok) lsb = a.lse[a.rows[i]] * kLog2e - 14.f;
             for (int vt = vt0; vt < vt1; ++vt) {
                 if (!tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
                     goto epi_done;
@@ -287,52 +302,80 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                     tc::tmem_wait_ld();
                     const int64_t col0 = (int64_t)vt * BN + c * 32;
                     const int nvalid = (int)min((int64_t)32, V - col0);
-                    if (nvalid <= 0) continue;
                     float x[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-                    float rmax = -INFINITY;
+                    if constexpr (EPI == EPI_COEFF) {
+                        // coefficient block column = col0 - first column of the chunk
+                        __half* dst = a.coeff + (int64_t)i * a.coeff_ld + (col0 - (int64_t)a.vt_begin * BN);
+                        uint32_t out[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < nvalid) rmax = fmaxf(rmax, x[j]);
-                    // argmax candidates: the two chunks with the largest raw logit
-                    const int ci = (int)col0;
-                    if (better(rmax, ci, v1, i1)) { v2 = v1; i2 = i1; v1 = rmax; i1 = ci; }
-                    else if (better(rmax, ci, v2, i2)) { v2 = rmax; i2 = ci; }
-                    // soft cap z = cap * tanh(x / cap) = cap - 2 cap / (exp(2x/cap) + 1)
-                    float zmax = rmax;
-                    if (cap > 0.f) {
+                        for (int j = 0; j < 32; j += 2) {
+                            float cj[2];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            x[j] = fmaf(-2.f * cap, tc::rcp_approx(tc::ex2_approx(x[j] * k2) + 1.f), cap);
-                        zmax = fmaf(-2.f * cap, tc::rcp_approx(tc::ex2_approx(rmax * k2) + 1.f), cap);
-                    }
-                    const float mn = fmaxf(m, zmax);
-                    const float mb = mn * kLog2e;
-                    float acc = 0.f;
-                    if (nvalid == 32) {
+                            for (int e = 0; e < 2; ++e) {
+                                const float xv = x[j + e];
+                                float lg2p, sech2 = 1.f;
+                                if (cap > 0.f) {
+                                    const float t = fmaf(-2.f, tc::rcp_approx(tc::ex2_approx(xv * k2) + 1.f), 1.f);
+                                    lg2p = fmaf(cap * t, kLog2e, -lsb);
+                                    sech2 = fmaf(-t, t, 1.f);
+                                } else {
+                                    lg2p = fmaf(xv, kLog2e, -lsb);
+                                }
+                                const bool ok = row_ok && (j + e) < nvalid;
+                                cj[e] = ok ? tc::ex2_approx(lg2p) * sech2 : 0.f;
+                            }
+                            out[j / 2] = h2_as_u32(__floats2half2_rn(cj[0], cj[1]));
+                        }
+                        if (i < a.coeff_rows) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc += tc::ex2_approx(fmaf(x[j], kLog2e, -mb));
+                            for (int q = 0; q < 4; ++q)
+                                d4[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                        }
                     } else {
+                        if (nvalid <= 0) continue;
+                        float rmax = -INFINITY;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (j < nvalid) acc += tc::ex2_approx(fmaf(x[j], kLog2e, -mb));
+                            if (j < nvalid) rmax = fmaxf(rmax, x[j]);
+                        // argmax candidates: the two chunks with the largest raw logit
+                        const int ci = (int)col0;
+                        if (better(rmax, ci, v1, i1)) { v2 = v1; i2 = i1; v1 = rmax; i1 = ci; }
+                        else if (better(rmax, ci, v2, i2)) { v2 = rmax; i2 = ci; }
+                        // soft cap z = cap * tanh(x / cap) = cap - 2 cap / (exp(2x/cap) + 1)
+                        float zmax = rmax;
+                        if (cap > 0.f) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                x[j] = fmaf(-2.f * cap, tc::rcp_approx(tc::ex2_approx(x[j] * k2) + 1.f), cap);
+                            zmax = fmaf(-2.f * cap, tc::rcp_approx(tc::ex2_approx(rmax * k2) + 1.f), cap);
+                        }
+                        const float mn = fmaxf(m, zmax);
+                        const float mb = mn * kLog2e;
+                        float acc = 0.f;
+                        if (nvalid == 32) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) acc += tc::ex2_approx(fmaf(x[j], kLog2e, -mb));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j < nvalid) acc += tc::ex2_approx(fmaf(x[j], kLog2e, -mb));
+                        }
+                        s = s * tc::ex2_approx((m - mn) * kLog2e) + acc;
+                        m = mn;
                     }
-                    s = s * tc::ex2_approx((m - mn) * kLog2e) + acc;
-                    m = mn;
                 }
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&acce[buf]);
                 if (++buf == 2) { buf = 0; aphase ^= 1; }
             }
-            {
-                const int i = mt * BM + row;
-                if (i < n_active) {
-                    Partial p;
-                    p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.pad0 = 0; p.pad1 = 0;
-                    part[(int64_t)i * W.n_seg + seg] = p;
-                }
+            if (EPI == EPI_SOFTMAX && row_ok) {
+                Partial p;
+                p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.pad0 = 0; p.pad1 = 0;
+                a.part[(int64_t)i * W.n_seg + seg] = p;
             }
         }
     epi_done:;
@@ -350,22 +393,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
 
 int tc_fwd_smem_bytes(int bits) { return bits == 4 ? Layout<4>::SMEM : Layout<8>::SMEM; }
 
-cudaError_t launch_tc_fwd(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                          const __half* scales, const __half* biases, int64_t V, int H, int bits,
-                          float cap, const int* count, Partial* part, int* S_out, int* err,
-                          int grid, cudaStream_t st) {
-    if (bits == 4) {
-        cudaFuncSetAttribute(tc_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<4>::SMEM);
-        tc_fwd_kernel<4><<<grid, kThreads, Layout<4>::SMEM, st>>>(
-            tmap_h, tmap_w, scales, biases, V, H, cap, count, part, S_out, err);
-    } else {
-        cudaFuncSetAttribute(tc_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<8>::SMEM);
-        tc_fwd_kernel<8><<<grid, kThreads, Layout<8>::SMEM, st>>>(
-            tmap_h, tmap_w, scales, biases, V, H, cap, count, part, S_out, err);
-    }
+template <int BITS, int EPI>
+static cudaError_t launch_t(const CUtensorMap& th, const CUtensorMap& tw, const TcFwdArgs& a,
+                            int grid, cudaStream_t st) {
+    cudaFuncSetAttribute(tc_fwd_kernel<BITS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Layout<BITS>::SMEM);
+    tc_fwd_kernel<BITS, EPI><<<grid, kThreads, Layout<BITS>::SMEM, st>>>(th, tw, a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_tc_fwd(const CUtensorMap& th, const CUtensorMap& tw, const TcFwdArgs& a,
+                          int bits, bool coeff_epilogue, int grid, cudaStream_t st) {
+    if (bits == 4)
+        return coeff_epilogue ? launch_t<4, EPI_COEFF>(th, tw, a, grid, st)
+                              : launch_t<4, EPI_SOFTMAX>(th, tw, a, grid, st);
+    return coeff_epilogue ? launch_t<8, EPI_COEFF>(th, tw, a, grid, st)
+                          : launch_t<8, EPI_SOFTMAX>(th, tw, a, grid, st);
 }
 
 }  // namespace qh

@@ -16,10 +16,51 @@ bool tmap_rows_f16_sw128(CUtensorMap* map, const void* base, uint64_t cols, uint
 bool tmap_packed_rows(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row, uint64_t rows,
                       uint32_t box_words, uint32_t box_rows);
 
+// Arguments of the tensor-core logit kernel (forward and backward phase 1).
+struct TcFwdArgs {
+    const __half* scales;
+    const __half* biases;
+    int64_t V;
+    int H;
+    float cap;
+    const int* count;   // active rows (device)
+    int* err;           // error word (device)
+    int vt_begin, vt_end;  // 256-row vocab tiles covered by this launch
+    // softmax epilogue (forward)
+    Partial* part;
+    int* S_out;
+    // coefficient epilogue (backward phase 1)
+    const float* lse;   // [M], original row order
+    const int* rows;    // compact -> original row
+    __half* coeff;      // [coeff_rows, coeff_ld]
+    int64_t coeff_ld;
+    int coeff_rows;
+};
+
+// Arguments of the tensor-core dh contraction (backward phase 2).
+struct TcDhArgs {
+    const __half* scales;
+    const __half* biases;
+    int64_t V;
+    int H;
+    const int* count;     // active rows (device)
+    int* err;             // error word (device)
+    const int* rows;      // compact -> original row
+    const float* dlogp;   // [M], original row order
+    float* dh_acc;        // [Mpad, H] fp32, compact rows
+    int64_t v_begin;      // first vocab row of the chunk
+    int n_k;              // 64-row vocab steps in the chunk
+    int accumulate;       // 0: write, 1: add to dh_acc
+};
+
+int tc_dh_cols(int H);          // hidden columns per output tile (256 or 128)
+int tc_dh_words(int H, int bits);
+cudaError_t launch_tc_dh(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w, const TcDhArgs& a,
+                         int bits, int grid, cudaStream_t st);
+
 int tc_fwd_smem_bytes(int bits);
 cudaError_t launch_tc_fwd(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                          const __half* scales, const __half* biases, int64_t V, int H, int bits,
-                          float cap, const int* count, Partial* part, int* S_out, int* err,
-                          int grid, cudaStream_t st);
+                          const TcFwdArgs& a, int bits, bool coeff_epilogue, int grid,
+                          cudaStream_t st);
 
 }  // namespace qh
