@@ -92,9 +92,27 @@ struct BwdPlan {
            total = 0;
 };
 
-// Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block
-// (about 94 MB at 5736 rows) stays mostly in L2 between the two phases.
-constexpr int64_t kBwdChunk = 8192;
+// Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block is
+// sized to about 96 MB (so it stays mostly in L2 between the two phases), and
+// at least 8192 rows.
+constexpr int64_t kBwdCoeffBudget = (int64_t)96 << 20;
+constexpr int64_t kBwdChunkMin = 8192;
+
+// K slices of the dh contraction: enough (m, n) tiles x slices to fill the
+// SMs in whole waves (each slice accumulates into its own buffer).
+int dh_slices(int64_t Mpad, int H, int sms, int64_t n_k_min) {
+    const int64_t tiles = (Mpad / 128) * (H / qh::tc_dh_cols(H));
+    int best = 1;
+    double best_eff = 0.0;
+    for (int ks = 1; ks <= 16 && ks <= n_k_min; ++ks) {
+        const int64_t units = tiles * ks;
+        const int64_t waves = (units + sms - 1) / sms;
+        const double eff = (double)units / (double)(waves * sms);
+        if (eff > best_eff + 0.02) { best_eff = eff; best = ks; }
+        if (eff >= 0.9 && waves >= 2) break;
+    }
+    return best;
+}
 
 int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
     DevInfo di;
@@ -144,14 +162,20 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p) {
     p->off_count = off; off = align_up(off + 16, 256);
     p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
     p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 1024);
+    // (dh_slices is declared above plan_fwd)
     if (p->tc) {
         p->grid = di.sms;
         p->S = 1;
         const int64_t vr = (hd->V + 255) / 256 * 256;
-        p->chunk = vr < kBwdChunk ? vr : kBwdChunk;
+        int64_t chunk = kBwdCoeffBudget / (2 * p->Mpad) / 256 * 256;
+        if (chunk < kBwdChunkMin) chunk = kBwdChunkMin;
+        if (chunk > vr) chunk = vr;
+        p->chunk = chunk;
+        const int64_t last = vr - (vr - 1) / chunk * chunk;  // rows of the last chunk
+        p->S = dh_slices(p->Mpad, hd->H, p->grid, (last < chunk ? last : chunk) / 64);
         p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
         p->off_coeff = off; off = align_up(off + 2 * (size_t)p->Mpad * p->chunk, 1024);
-        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->Mpad * hd->H, 256);
+        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 256);
     } else {
         const int tb = qh::bwd_simt_tokens(hd->H);
         const int64_t groups = (M + tb - 1) / tb;
@@ -359,8 +383,10 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
             qh::TcDhArgs da{};
             da.scales = sc; da.biases = bi; da.V = head->V; da.H = head->H;
             da.count = count; da.err = err; da.rows = rows; da.dlogp = dlogp; da.dh_acc = dhp;
+            da.slice_stride = p.Mpad * head->H;
             da.v_begin = (int64_t)vt0 * 256;
             da.n_k = (vt1 - vt0) * 256 / 64;
+            da.ks = p.S < da.n_k ? p.S : da.n_k;  // slices beyond a short chunk keep their sums
             da.accumulate = c > 0;
             if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
                 return cuda_fail(e, "tc_dh");

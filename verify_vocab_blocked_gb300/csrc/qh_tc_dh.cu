@@ -22,11 +22,17 @@ namespace {
 
 constexpr int BM = 128;   // token rows (MMA M)
 constexpr int BK = 64;    // vocab rows per stage
-constexpr int NS = 3;
-constexpr int kThreads = 320;
+constexpr int NB = 3;     // dequantized-tile stages
+constexpr int kDqWarps = 8;             // warps 2 .. 9 dequantize
+constexpr int kDqThreads = 32 * kDqWarps;
+constexpr int kEpiWarp0 = 2 + kDqWarps; // warps 10 .. 13 run the epilogue
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 
+// Two rings: NS stages of TMA inputs (coefficient tile + packed tile) deep
+// enough to cover HBM latency, NB stages of dequantized weight tiles.
 template <int BITS, int BNH>
 struct DhLayout {
+    static constexpr int NS = BITS == 4 ? 5 : 4;
     static constexpr int A_BYTES = BM * BK * 2;             // coeff tile, K-major SW128
     static constexpr int B_BYTES = BNH * BK * 2;            // weight tile, MN-major SW128
     static constexpr int P_ROW = BNH * BITS / 8;            // packed bytes per vocab row
@@ -34,12 +40,19 @@ struct DhLayout {
     static constexpr int WORDS = BNH * BITS / 32;           // TMA box width (words)
     static constexpr int NBLK = BNH / 64;                   // 64-column blocks along N
     static constexpr int OFF_B = 0;                         // B first: descriptor reach stays inside
-    static constexpr int OFF_A = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_A = OFF_B + NB * B_BYTES;
     static constexpr int OFF_P = OFF_A + NS * A_BYTES;
     static constexpr int OFF_BAR = OFF_P + NS * P_BYTES;
-    static constexpr int BAR_BYTES = 8 * (3 * NS + 4) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 4) + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;
     static constexpr int TMEM_COLS = 2 * BNH;
+    // Dequant work split: a packed row is PIECES 16-byte pieces; thread t takes
+    // piece t % PIECES of rows t / PIECES + RPP * pass.
+    static constexpr int PIECES = P_ROW / 16;
+    static constexpr int RPP = kDqThreads / PIECES;
+    static constexpr int PASSES = BK / RPP;
+    static constexpr int CPP = 128 / BITS;        // hidden columns per piece (32 or 16)
+    static constexpr int CHUNKS = CPP / 8;        // 16-byte output chunks per piece
     static constexpr uint32_t IDESC = tc::idesc_f16_f32(BM, BNH, false, true);
 };
 
@@ -58,13 +71,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_w,
     const TcDhArgs a) {
     using L = DhLayout<BITS, BNH>;
+    constexpr int NS = L::NS;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-    uint64_t* dq = full + NS;
-    uint64_t* empty = dq + NS;
-    uint64_t* accf = empty + NS;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);  // TMA inputs landed
+    uint64_t* empty = full + NS;  // inputs consumed (MMA commit + each dequant warp)
+    uint64_t* dq = empty + NS;    // dequantized tile written
+    uint64_t* bfree = dq + NB;    // dequantized tile consumed (MMA commit)
+    uint64_t* accf = bfree + NB;
     uint64_t* acce = accf + 2;
     uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
@@ -74,15 +89,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const int n_active = *a.count;
     const int n_mt = (n_active + BM - 1) / BM;
     const int n_nt = a.H / BNH;
-    const int units = n_mt * n_nt;
+    const int KS = a.ks;                 // K slices per output tile
+    const int units = n_mt * n_nt * KS;
     if (units == 0 || (int)blockIdx.x >= units) return;
     const int G = a.H / 64;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&dq[i], 4);
-            tc::mbar_init(&empty[i], 1);
+            tc::mbar_init(&empty[i], 1 + kDqWarps);
+        }
+        for (int i = 0; i < NB; ++i) {
+            tc::mbar_init(&dq[i], kDqWarps);
+            tc::mbar_init(&bfree[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&accf[i], 1);
@@ -107,8 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             int stage = 0;
             uint32_t phase = 0;
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
-                const int mt = u / n_nt, nt = u - (u / n_nt) * n_nt;
-                for (int kk = 0; kk < a.n_k; ++kk) {
+                const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
+                const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
+                for (int kk = k0; kk < k1; ++kk) {
                     if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
                                        tc::kErrTimeoutEmpty))
                         goto producer_done;
@@ -130,90 +150,128 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int stage = 0, buf = 0;
-            uint32_t phase = 0, aphase = 0;
+            int stage = 0, buf = 0, bs = 0;
+            uint32_t phase = 0, aphase = 0, bphase = 0;
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
+                const int ks = u % KS;
+                const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
                 if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
                                    tc::kErrTimeoutAccEmpty))
                     goto mma_done;
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BNH;
-                for (int kk = 0; kk < a.n_k; ++kk) {
+                for (int kk = k0; kk < k1; ++kk) {
                     if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                         goto mma_done;
-                    if (!tc::mbar_wait(&dq[stage], phase, abort_flag, err, tc::kErrTimeoutDequant))
+                    if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err, tc::kErrTimeoutDequant))
                         goto mma_done;
                     tc::tc_fence_after();
                     const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * L::A_BYTES);
-                    const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + stage * L::B_BYTES);
+                    const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
 #pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks) {
+                    for (int ks2 = 0; ks2 < BK / 16; ++ks2) {
                         // A: K-major, 32 bytes per 16-element K step inside the swizzle atom.
-                        const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks, 16, 1024);
+                        const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks2, 16, 1024);
                         // B: MN-major, two 8-row K groups (2 x 1024 B) per K step;
                         // 64-column blocks along N are BK/8 * 1024 bytes apart.
-                        const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks, (BK / 8) * 1024, 1024);
-                        tc::umma_f16(d_tmem, ad, bd, L::IDESC, (kk | ks) != 0);
+                        const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks2, (BK / 8) * 1024, 1024);
+                        tc::umma_f16(d_tmem, ad, bd, L::IDESC, (kk > k0 || ks2 > 0) ? 1u : 0u);
                     }
                     tc::umma_commit(&empty[stage]);
+                    tc::umma_commit(&bfree[bs]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
+                    if (++bs == NB) { bs = 0; bphase ^= 1; }
                 }
                 tc::umma_commit(&accf[buf]);
                 if (++buf == 2) { buf = 0; aphase ^= 1; }
             }
         mma_done:;
         }
-    } else if (warp < 6) {
-        // Dequant: thread t -> vocab row kr = t / 2 of the stage, columns
-        // [ (t & 1) * BNH/2, + BNH/2 ) of the N tile.
+    } else if (warp < kEpiWarp0) {
+        // Dequant.  Thread t owns 16-byte piece p = t % PIECES of packed rows
+        // t / PIECES + RPP * pass: a quarter-warp reads one contiguous 128-byte
+        // span, and the chunk order is rotated by the 64-column block so the
+        // eight 16-byte stores of a quarter-warp land in distinct bank groups.
         const int t = threadIdx.x - 64;
-        const int kr = t >> 1, half = t & 1;
-        constexpr int COLS = BNH / 2;
-        constexpr int NG = COLS / 64 > 0 ? COLS / 64 : 1;  // groups per thread
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int nt = u - (u / n_nt) * n_nt;
-            const int col0 = nt * BNH + half * COLS;  // first hidden column of this thread
-            for (int kk = 0; kk < a.n_k; ++kk) {
-                const int64_t v = a.v_begin + (int64_t)kk * BK + kr;
-                const bool ok = v < a.V;
-                __half sv[NG], bv[NG];
+        const int pc = t % L::PIECES, row0 = t / L::PIECES;
+        const int ncol_piece = pc * L::CPP;        // first column of the piece in the N tile
+        const int nb = ncol_piece >> 6;            // 64-column block
+        const int j0 = (ncol_piece & 63) >> 3;     // first 16-byte chunk in the block
+        int stage = 0, bs = 0;
+        uint32_t phase = 0, bphase = 0;
+        // (scale, bias) of each pass for the current step and the next two.
+        uint32_t sb_cur[L::PASSES], sb_n1[L::PASSES], sb_n2[L::PASSES];
+        int pf_u = blockIdx.x, pf_kk = 0, pf_k1 = 0;
+        auto pf_start = [&]() {
+            if (pf_u < units) {
+                const int ks = pf_u % KS;
+                pf_kk = ks * a.n_k / KS;
+                pf_k1 = (ks + 1) * a.n_k / KS;
+            }
+        };
+        auto pf_load = [&](uint32_t (&dst)[L::PASSES]) {
+            if (pf_u >= units) return;
+            const int nt = (pf_u / KS) % n_nt;
+            const int gi = (nt * BNH + ncol_piece) / 64;
 #pragma unroll
-                for (int q = 0; q < NG; ++q) {
-                    const int gi = col0 / 64 + q;
-                    sv[q] = ok ? a.scales[v * G + gi] : __float2half(0.f);
-                    bv[q] = ok ? a.biases[v * G + gi] : __float2half(0.f);
-                }
+            for (int ps = 0; ps < L::PASSES; ++ps) {
+                const int64_t v = a.v_begin + (int64_t)pf_kk * BK + row0 + L::RPP * ps;
+                __half sv = __float2half(0.f), bv = __float2half(0.f);
+                if (v < a.V) { sv = a.scales[v * G + gi]; bv = a.biases[v * G + gi]; }
+                dst[ps] = h2_as_u32(__halves2half2(sv, bv));
+            }
+            if (++pf_kk == pf_k1) { pf_u += gridDim.x; pf_start(); }
+        };
+        pf_start();
+        pf_load(sb_cur);
+        pf_load(sb_n1);
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int ks = u % KS;
+            const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
+            for (int kk = k0; kk < k1; ++kk) {
+                pf_load(sb_n2);
                 if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                     goto dq_done;
-                const unsigned char* prow =
-                    smem + L::OFF_P + stage * L::P_BYTES + kr * L::P_ROW + half * (COLS * BITS / 8);
-                unsigned char* Bs = smem + L::OFF_B + stage * L::B_BYTES;
-                const int krow = kr & 7;
-                unsigned char* atom_base = Bs + (kr >> 3) * 1024 + krow * 128;
+                if (!tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant))
+                    goto dq_done;
+                const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
+                unsigned char* Bs = smem + L::OFF_B + bs * L::B_BYTES + nb * (BK / 8) * 1024;
 #pragma unroll
-                for (int cc = 0; cc < COLS / 8; ++cc) {  // 8-column chunks of this thread
-                    const int ncol = half * COLS + cc * 8;  // column within the N tile
-                    const int nb = ncol >> 6, j = (ncol >> 3) & 7;
-                    const int q = (cc * 8) / 64;
-                    const __half2 s2 = __half2half2(sv[q]), b2 = __half2half2(bv[q]);
-                    uint4 out;
-                    if constexpr (BITS == 4) {
-                        const uint32_t w = reinterpret_cast<const uint32_t*>(prow)[cc];
-                        out = deq4_natural(w, s2, b2);
-                    } else {
-                        const uint2 w2 = reinterpret_cast<const uint2*>(prow)[cc];
-                        out = make_uint4(deq8(w2.x, 0x5140u, s2, b2), deq8(w2.x, 0x7362u, s2, b2),
-                                         deq8(w2.y, 0x5140u, s2, b2), deq8(w2.y, 0x7362u, s2, b2));
+                for (int ps = 0; ps < L::PASSES; ++ps) {
+                    const int kr = row0 + L::RPP * ps;
+                    const int krow = kr & 7;
+                    const uint4 wv = *reinterpret_cast<const uint4*>(P + kr * L::P_ROW + pc * 16);
+                    const __half2 sb = u32_as_h2(sb_cur[ps]);
+                    const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
+                    unsigned char* dst_row = Bs + (kr >> 3) * 1024 + krow * 128;
+                    // word i of the piece, selected without dynamic register indexing
+                    auto word = [&](int i) {
+                        return i == 0 ? wv.x : i == 1 ? wv.y : i == 2 ? wv.z : wv.w;
+                    };
+#pragma unroll
+                    for (int q = 0; q < L::CHUNKS; ++q) {
+                        const int qq = (q + nb) % L::CHUNKS;  // rotated chunk order
+                        uint4 out;
+                        if constexpr (BITS == 4) {
+                            out = deq4_natural(word(qq), s2, b2);
+                        } else {
+                            const uint32_t w0 = word(2 * qq), w1 = word(2 * qq + 1);
+                            out = make_uint4(deq8(w0, 0x5140u, s2, b2), deq8(w0, 0x7362u, s2, b2),
+                                             deq8(w1, 0x5140u, s2, b2), deq8(w1, 0x7362u, s2, b2));
+                        }
+                        *reinterpret_cast<uint4*>(dst_row + (((j0 + qq) ^ krow) << 4)) = out;
                     }
-                    *reinterpret_cast<uint4*>(atom_base + nb * (BK / 8) * 1024 +
-                                              ((j ^ krow) << 4)) = out;
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&dq[stage]);
+                if (lane == 0) {
+                    tc::mbar_arrive(&dq[bs]);
+                    tc::mbar_arrive(&empty[stage]);  // packed tile fully read
+                }
                 if (++stage == NS) { stage = 0; phase ^= 1; }
+                if (++bs == NB) { bs = 0; bphase ^= 1; }
+#pragma unroll
+                for (int ps = 0; ps < L::PASSES; ++ps) { sb_cur[ps] = sb_n1[ps]; sb_n1[ps] = sb_n2[ps]; }
             }
         }
     dq_done:;
@@ -224,14 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         int buf = 0;
         uint32_t aphase = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int mt = u / n_nt, nt = u - (u / n_nt) * n_nt;
+            const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
             const int i = mt * BM + row;
             const bool row_ok = i < n_active;
             const float scale = row_ok ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
             if (!tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
                 goto epi_done;
             tc::tc_fence_after();
-            float* dst = a.dh_acc + (int64_t)i * a.H + nt * BNH;
+            float* dst = a.dh_acc + (int64_t)ks * a.slice_stride + (int64_t)i * a.H + nt * BNH;
 #pragma unroll 1
             for (int c = 0; c < BNH / 32; ++c) {
                 uint32_t r[32];

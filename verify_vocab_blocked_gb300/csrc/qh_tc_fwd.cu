@@ -32,24 +32,29 @@ namespace {
 constexpr int BM = 128;   // token rows per tile (MMA M)
 constexpr int BN = 256;   // vocab rows per tile (MMA N)
 constexpr int BK = 64;    // K per stage (one quantization group, one swizzle atom)
-constexpr int NS = 3;     // pipeline stages
-constexpr int kThreads = 320;
+constexpr int NB = 3;     // dequantized-tile stages
+constexpr int kDqWarps = 8;             // warps 2 .. 9 dequantize
+constexpr int kEpiWarp0 = 2 + kDqWarps; // warps 10 .. 13 run the epilogue
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kTmemCols = 512;  // two 256-column fp32 accumulators
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr uint32_t kIdesc = tc::idesc_f16_f32(BM, BN, false, false);
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Two rings: NS stages of TMA inputs (h tile + packed tile, small, deep enough
+// to cover HBM latency) and NB stages of dequantized tiles (large).
 template <int BITS>
 struct Layout {
+    static constexpr int NS = BITS == 4 ? 5 : 4;
     static constexpr int P_ROW = BK * BITS / 8;  // packed bytes per row per stage
     static constexpr int P_BYTES = BN * P_ROW;
     static constexpr int WORDS = BK * BITS / 32;
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + NS * A_BYTES;
-    static constexpr int OFF_P = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_B = 0;
+    static constexpr int OFF_A = OFF_B + NB * B_BYTES;
+    static constexpr int OFF_P = OFF_A + NS * A_BYTES;
     static constexpr int OFF_BAR = OFF_P + NS * P_BYTES;
-    static constexpr int BAR_BYTES = 8 * (3 * NS + 4) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 4) + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
 };
 
@@ -88,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
     const TcFwdArgs a) {
     using L = Layout<BITS>;
+    constexpr int NS = L::NS;
     const __half* __restrict__ scales = a.scales;
     const __half* __restrict__ biases = a.biases;
     const int64_t V = a.V;
@@ -97,10 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-    uint64_t* dq = full + NS;
-    uint64_t* empty = dq + NS;
-    uint64_t* accf = empty + NS;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);  // TMA inputs landed
+    uint64_t* empty = full + NS;  // inputs consumed (MMA commit + each dequant warp)
+    uint64_t* dq = empty + NS;    // dequantized tile written
+    uint64_t* bfree = dq + NB;    // dequantized tile consumed (MMA commit)
+    uint64_t* accf = bfree + NB;
     uint64_t* acce = accf + 2;
     uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
@@ -116,8 +123,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&dq[i], 4);
-            tc::mbar_init(&empty[i], 1);
+            tc::mbar_init(&empty[i], 1 + kDqWarps);
+        }
+        for (int i = 0; i < NB; ++i) {
+            tc::mbar_init(&dq[i], kDqWarps);
+            tc::mbar_init(&bfree[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&accf[i], 1);
@@ -171,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int stage = 0, buf = 0;
-            uint32_t phase = 0, aphase = 0;
+            int stage = 0, buf = 0, bs = 0;
+            uint32_t phase = 0, aphase = 0, bphase = 0;
             for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
@@ -186,12 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                         if (!tc::mbar_wait(&full[stage], phase, abort_flag, err,
                                            tc::kErrTimeoutFull))
                             goto mma_done;
-                        if (!tc::mbar_wait(&dq[stage], phase, abort_flag, err,
+                        if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err,
                                            tc::kErrTimeoutDequant))
                             goto mma_done;
                         tc::tc_fence_after();
                         const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * A_BYTES);
-                        const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + stage * B_BYTES);
+                        const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * B_BYTES);
 #pragma unroll
                         for (int ks = 0; ks < BK / 16; ++ks) {
                             const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks, 16, 1024);
@@ -199,7 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                             tc::umma_f16(d_tmem, ad, bd, kIdesc, (kk | ks) != 0);
                         }
                         tc::umma_commit(&empty[stage]);
+                        tc::umma_commit(&bfree[bs]);
                         if (++stage == NS) { stage = 0; phase ^= 1; }
+                        if (++bs == NB) { bs = 0; bphase ^= 1; }
                     }
                     tc::umma_commit(&accf[buf]);
                     if (++buf == 2) { buf = 0; aphase ^= 1; }
@@ -207,30 +219,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             }
         mma_done:;
         }
-    } else if (warp < 6) {
+    } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ dequant warps
-        const int t = threadIdx.x - 64;  // 0..127: rows t and t + 128 of the tile
-        int stage = 0;
-        uint32_t phase = 0;
+        const int t = threadIdx.x - 64;  // 0..255: row t of the tile
+        int stage = 0, bs = 0;
+        uint32_t phase = 0, bphase = 0;
         for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
             int mt, seg, vt0, vt1;
             unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
             for (int vt = vt0; vt < vt1; ++vt) {
-                const int64_t v0 = (int64_t)vt * BN + t, v1 = v0 + 128;
-                const bool ok0 = v0 < V, ok1 = v1 < V;
+                const int64_t v0 = (int64_t)vt * BN + t;
+                const bool ok0 = v0 < V;
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const __half z = __float2half(0.f);
                     const __half s0 = ok0 ? scales[v0 * G + kk] : z, b0 = ok0 ? biases[v0 * G + kk] : z;
-                    const __half s1 = ok1 ? scales[v1 * G + kk] : z, b1 = ok1 ? biases[v1 * G + kk] : z;
                     if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                         goto dq_done;
+                    if (!tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err,
+                                       tc::kErrTimeoutDequant))
+                        goto dq_done;
                     const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
-                    unsigned char* Bs = smem + L::OFF_B + stage * B_BYTES;
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int r = t + 128 * rr;
-                        const __half2 s2 = __half2half2(rr ? s1 : s0);
-                        const __half2 b2 = __half2half2(rr ? b1 : b0);
+                    unsigned char* Bs = smem + L::OFF_B + bs * B_BYTES;
+                    {
+                        const int r = t;
+                        const __half2 s2 = __half2half2(s0);
+                        const __half2 b2 = __half2half2(b0);
                         const uint4* prow = reinterpret_cast<const uint4*>(P + r * L::P_ROW);
                         unsigned char* brow = Bs + r * 128;
                         if constexpr (BITS == 4) {
@@ -267,8 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                     }
                     tc::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&dq[stage]);
+                    if (lane == 0) {
+                        tc::mbar_arrive(&dq[bs]);
+                        tc::mbar_arrive(&empty[stage]);  // packed tile fully read
+                    }
                     if (++stage == NS) { stage = 0; phase ^= 1; }
+                    if (++bs == NB) { bs = 0; bphase ^= 1; }
                 }
             }
         }

@@ -47,9 +47,11 @@ struct TcDhArgs {
     int* err;             // error word (device)
     const int* rows;      // compact -> original row
     const float* dlogp;   // [M], original row order
-    float* dh_acc;        // [Mpad, H] fp32, compact rows
+    float* dh_acc;        // [ks][Mpad, H] fp32, compact rows, one buffer per K slice
+    int64_t slice_stride; // elements between K-slice buffers (Mpad * H)
     int64_t v_begin;      // first vocab row of the chunk
     int n_k;              // 64-row vocab steps in the chunk
+    int ks;               // K slices per output tile (each adds into its own buffer)
     int accumulate;       // 0: write, 1: add to dh_acc
 };
 
