@@ -99,6 +99,23 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Asynchronous global -> shared copy of 4 or 8 bytes; src_bytes = 0 writes zeros
+// without reading `src` (which must still be a valid address).
+template <int BYTES>
+__device__ __forceinline__ void cp_async_zfill(void* dst, const void* src, int src_bytes) {
+    static_assert(BYTES == 4 || BYTES == 8, "cp.async size");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(smem_u32(dst)), "l"(src),
+                 "n"(BYTES), "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` when all of this thread's prior cp.async copies have landed
+// (the arrival is counted in the barrier's initial count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -22,7 +22,8 @@ namespace {
 
 constexpr int BM = 128;   // token rows (MMA M)
 constexpr int BK = 64;    // vocab rows per stage
-constexpr int NB = 3;     // dequantized-tile stages
+template <int BITS>
+constexpr int dh_nb() { return BITS == 4 ? 3 : 2; }  // dequantized-tile stages
 constexpr int kDqWarps = 8;             // warps 2 .. 9 dequantize
 constexpr int kDqThreads = 32 * kDqWarps;
 constexpr int kEpiWarp0 = 2 + kDqWarps; // warps 10 .. 13 run the epilogue
@@ -33,16 +34,19 @@ constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 template <int BITS, int BNH>
 struct DhLayout {
     static constexpr int NS = BITS == 4 ? 5 : 4;
+    static constexpr int NB = dh_nb<BITS>();
     static constexpr int A_BYTES = BM * BK * 2;             // coeff tile, K-major SW128
     static constexpr int B_BYTES = BNH * BK * 2;            // weight tile, MN-major SW128
     static constexpr int P_ROW = BNH * BITS / 8;            // packed bytes per vocab row
     static constexpr int P_BYTES = BK * P_ROW;
     static constexpr int WORDS = BNH * BITS / 32;           // TMA box width (words)
-    static constexpr int NBLK = BNH / 64;                   // 64-column blocks along N
     static constexpr int OFF_B = 0;                         // B first: descriptor reach stays inside
+    static constexpr int NSB = BNH / 64;                     // groups of the N tile
+    static constexpr int SB_BYTES = 2 * BK * NSB * 2;        // scales + biases per stage
     static constexpr int OFF_A = OFF_B + NB * B_BYTES;
     static constexpr int OFF_P = OFF_A + NS * A_BYTES;
-    static constexpr int OFF_BAR = OFF_P + NS * P_BYTES;
+    static constexpr int OFF_SB = OFF_P + NS * P_BYTES;
+    static constexpr int OFF_BAR = OFF_SB + NS * SB_BYTES;
     static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 4) + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;
     static constexpr int TMEM_COLS = 2 * BNH;
@@ -72,6 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const TcDhArgs a) {
     using L = DhLayout<BITS, BNH>;
     constexpr int NS = L::NS;
+    constexpr int NB = L::NB;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&full[i], 1 + 32);  // TMA (expect_tx) + 32 cp.async arrivals
             tc::mbar_init(&empty[i], 1 + kDqWarps);
         }
         for (int i = 0; i < NB; ++i) {
@@ -122,31 +127,49 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const uint32_t tmem_base = *tmem_base_sh;
 
     if (warp == 0) {
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int u = blockIdx.x; u < units; u += gridDim.x) {
-                const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
-                const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
-                for (int kk = k0; kk < k1; ++kk) {
-                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
-                                       tc::kErrTimeoutEmpty))
-                        goto producer_done;
+        // Producer warp: lane 0 issues the TMA tiles; all 32 lanes copy the
+        // stage's scales and biases (rows lane, lane + 32; the N tile's groups)
+        // with cp.async, completing on the same barrier.
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
+            const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
+            for (int kk = k0; kk < k1; ++kk) {
+                if (lane == 0)
+                    ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
+                                       tc::kErrTimeoutEmpty);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane == 0) {
                     tc::mbar_arrive_expect_tx(&full[stage], L::A_BYTES + L::P_BYTES);
                     tc::tma_load_2d(smem + L::OFF_A + stage * L::A_BYTES, &tmap_c, &full[stage],
                                     kk * BK, mt * BM);
                     tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w, &full[stage],
                                     nt * L::WORDS, (int)(a.v_begin + kk * BK));
-                    if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
+                __half* sb = reinterpret_cast<__half*>(smem + L::OFF_SB + stage * L::SB_BYTES);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = lane + 32 * h;
+                    const int64_t v = a.v_begin + (int64_t)kk * BK + r;
+                    const int64_t gi = (v < a.V ? v : 0) * G + nt * L::NSB;
+                    const int nbytes = v < a.V ? 2 * L::NSB : 0;
+                    tc::cp_async_zfill<2 * L::NSB>(sb + r * L::NSB, a.scales + gi, nbytes);
+                    tc::cp_async_zfill<2 * L::NSB>(sb + (BK + r) * L::NSB, a.biases + gi, nbytes);
+                }
+                tc::cp_async_arrive(&full[stage]);
+                if (++stage == NS) { stage = 0; phase ^= 1; }
             }
+        }
+        if (lane == 0 && ok) {
             for (int i = 0; i < NS; ++i) {
                 if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
                                    tc::kErrTimeoutEmpty))
                     break;
                 if (++stage == NS) { stage = 0; phase ^= 1; }
             }
-        producer_done:;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -199,50 +222,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         const int j0 = (ncol_piece & 63) >> 3;     // first 16-byte chunk in the block
         int stage = 0, bs = 0;
         uint32_t phase = 0, bphase = 0;
-        // (scale, bias) of each pass for the current step and the next two.
-        uint32_t sb_cur[L::PASSES], sb_n1[L::PASSES], sb_n2[L::PASSES];
-        int pf_u = blockIdx.x, pf_kk = 0, pf_k1 = 0;
-        auto pf_start = [&]() {
-            if (pf_u < units) {
-                const int ks = pf_u % KS;
-                pf_kk = ks * a.n_k / KS;
-                pf_k1 = (ks + 1) * a.n_k / KS;
-            }
-        };
-        auto pf_load = [&](uint32_t (&dst)[L::PASSES]) {
-            if (pf_u >= units) return;
-            const int nt = (pf_u / KS) % n_nt;
-            const int gi = (nt * BNH + ncol_piece) / 64;
-#pragma unroll
-            for (int ps = 0; ps < L::PASSES; ++ps) {
-                const int64_t v = a.v_begin + (int64_t)pf_kk * BK + row0 + L::RPP * ps;
-                __half sv = __float2half(0.f), bv = __float2half(0.f);
-                if (v < a.V) { sv = a.scales[v * G + gi]; bv = a.biases[v * G + gi]; }
-                dst[ps] = h2_as_u32(__halves2half2(sv, bv));
-            }
-            if (++pf_kk == pf_k1) { pf_u += gridDim.x; pf_start(); }
-        };
-        pf_start();
-        pf_load(sb_cur);
-        pf_load(sb_n1);
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const int ks = u % KS;
             const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
             for (int kk = k0; kk < k1; ++kk) {
-                pf_load(sb_n2);
                 if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                     goto dq_done;
                 if (!tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant))
                     goto dq_done;
                 const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
+                const __half* sb = reinterpret_cast<const __half*>(smem + L::OFF_SB + stage * L::SB_BYTES);
                 unsigned char* Bs = smem + L::OFF_B + bs * L::B_BYTES + nb * (BK / 8) * 1024;
 #pragma unroll
                 for (int ps = 0; ps < L::PASSES; ++ps) {
                     const int kr = row0 + L::RPP * ps;
                     const int krow = kr & 7;
                     const uint4 wv = *reinterpret_cast<const uint4*>(P + kr * L::P_ROW + pc * 16);
-                    const __half2 sb = u32_as_h2(sb_cur[ps]);
-                    const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
+                    const __half2 s2 = __half2half2(sb[kr * L::NSB + (ncol_piece >> 6)]);
+                    const __half2 b2 = __half2half2(sb[(BK + kr) * L::NSB + (ncol_piece >> 6)]);
                     unsigned char* dst_row = Bs + (kr >> 3) * 1024 + krow * 128;
                     // word i of the piece, selected without dynamic register indexing
                     auto word = [&](int i) {
@@ -270,8 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 }
                 if (++stage == NS) { stage = 0; phase ^= 1; }
                 if (++bs == NB) { bs = 0; bphase ^= 1; }
-#pragma unroll
-                for (int ps = 0; ps < L::PASSES; ++ps) { sb_cur[ps] = sb_n1[ps]; sb_n1[ps] = sb_n2[ps]; }
             }
         }
     dq_done:;
