@@ -124,10 +124,10 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
     if (p->tc) {
         // One persistent CTA per SM; the kernel picks the number of vocab
         // segments S from the active-row count so that n_tiles * S is about
-        // 8 * grid, hence at most 128 * (8 * grid + n_tiles) records.
+        // 32 * grid, hence at most 128 * (32 * grid + n_tiles) records.
         p->grid = di.sms;
         p->cand_width = 32;
-        p->records = (size_t)128 * (8 * (size_t)p->grid + (size_t)(p->Mpad / 128));
+        p->records = (size_t)128 * (32 * (size_t)p->grid + (size_t)(p->Mpad / 128));
     } else {
         const int64_t groups = (M + qh::kTokGroup - 1) / qh::kTokGroup;
         // One full wave: every SM holds as many CTAs as fit; each split keeps at

@@ -60,14 +60,16 @@ struct DhLayout {
     static constexpr uint32_t IDESC = tc::idesc_f16_f32(BM, BNH, false, true);
 };
 
-// Natural-order fp16 pairs of one 4-bit word: the dequantizer yields
-// (q0,q4), (q1,q5), (q2,q6), (q3,q7); the hidden axis is the MMA's N axis
-// here, so the pairs are regrouped to (q0,q1), (q2,q3), (q4,q5), (q6,q7).
-__device__ __forceinline__ uint4 deq4_natural(uint32_t w, __half2 s, __half2 b) {
+// A 4-bit word dequantizes to the fp16 pairs (q0,q4), (q1,q5), (q2,q6),
+// (q3,q7) (qh_dequant.cuh).  Here the hidden axis is the MMA's N axis, so the
+// B tile keeps that order -- N position c of an 8-column block holds hidden
+// column kPerm4[c] -- and the epilogue, which holds 32 consecutive N columns
+// per thread in registers, writes column c to hidden offset kPerm4[c].  8-bit
+// words dequantize in natural order.
+__device__ __forceinline__ uint4 deq4_chunk(uint32_t w, __half2 s, __half2 b) {
     uint32_t p[4];
     deq4_word(w, s, b, p);
-    return make_uint4(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410),
-                      __byte_perm(p[0], p[1], 0x7632), __byte_perm(p[2], p[3], 0x7632));
+    return make_uint4(p[0], p[1], p[2], p[3]);
 }
 
 template <int BITS, int BNH>
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                         const int qq = (q + nb) % L::CHUNKS;  // rotated chunk order
                         uint4 out;
                         if constexpr (BITS == 4) {
-                            out = deq4_natural(word(qq), s2, b2);
+                            out = deq4_chunk(word(qq), s2, b2);
                         } else {
                             const uint32_t w0 = word(2 * qq), w1 = word(2 * qq + 1);
                             out = make_uint4(deq8(w0, 0x5140u, s2, b2), deq8(w0, 0x7362u, s2, b2),
@@ -291,18 +293,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 tc::tmem_ld32(tmem_base + lane_addr + buf * BNH + c * 32, r);
                 tc::tmem_wait_ld();
                 if (row_ok) {
+                    // N column j of this chunk is hidden offset (j & ~7) + perm[j & 7]
+                    // for 4-bit heads (perm = 0,4,1,5,2,6,3,7), natural for 8-bit.
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        constexpr int inv4[8] = {0, 2, 4, 6, 1, 3, 5, 7};  // offset -> N column
+                        const int src = BITS == 4 ? ((j & ~7) | inv4[j & 7]) : j;
+                        v[j] = __uint_as_float(r[src]) * scale;
+                    }
                     float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        float4 v = make_float4(__uint_as_float(r[4 * q]) * scale,
-                                               __uint_as_float(r[4 * q + 1]) * scale,
-                                               __uint_as_float(r[4 * q + 2]) * scale,
-                                               __uint_as_float(r[4 * q + 3]) * scale);
+                        float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                         if (a.accumulate) {
                             const float4 o = d4[q];
-                            v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                            x.x += o.x; x.y += o.y; x.z += o.z; x.w += o.w;
                         }
-                        d4[q] = v;
+                        d4[q] = x;
                     }
                 }
             }

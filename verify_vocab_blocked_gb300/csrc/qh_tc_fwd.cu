@@ -62,11 +62,15 @@ struct Work {
     int n_mt, n_vt, n_seg, units;
 };
 
+// Units (128 rows x a segment of vocab tiles) per CTA: many small units keep
+// the per-CTA totals within a few percent of each other.
+constexpr int kUnitsPerCta = 32;
+
 __device__ __forceinline__ Work plan_work(int n_active, int n_vt) {
     Work w;
     w.n_mt = (n_active + BM - 1) / BM;
     w.n_vt = n_vt;
-    const int target = 8 * (int)gridDim.x;  // about 8 units per CTA
+    const int target = kUnitsPerCta * (int)gridDim.x;
     int seg = w.n_mt > 0 ? (target + w.n_mt - 1) / w.n_mt : 1;
     if (seg > w.n_vt) seg = w.n_vt;
     if (seg < 1) seg = 1;
