@@ -134,7 +134,7 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
         // least 128 vocab rows (16 per warp).
         const int64_t want = (int64_t)di.sms * qh::stream_fwd_ctas_per_sm(hd->bits, hd->H);
         int64_t S = (want + groups - 1) / groups;
-        const int64_t max_s = (hd->V + 127) / 128;
+        const int64_t max_s = (hd->V + 127) / 128;  // at least one 128-row tile per CTA
         if (S > max_s) S = max_s;
         if (S < 1) S = 1;
         p->S = (int)S;
@@ -300,13 +300,13 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     } else {
         hook_before(st);
         e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, h16,
-                                  count, M, part, p.S, st);
+                                  count, M, part, p.S, err, st);
         hook_after(st);
         if (e) return cuda_fail(e, "stream_fwd");
     }
     if ((e = qh::launch_fwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
-                                     pos, targets, part, p.S, p.tc ? S_dev : nullptr,
-                                     p.tc ? err : nullptr, p.cand_width, logp, lse, argmax, M,
+                                     pos, targets, part, p.S, p.tc ? S_dev : nullptr, err,
+                                     p.cand_width, logp, lse, argmax, M,
                                      st)))
         return cuda_fail(e, "fwd_finalize");
     return QHEAD_OK;

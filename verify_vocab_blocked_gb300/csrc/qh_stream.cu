@@ -12,10 +12,12 @@
 //
 // How (GB300): at M = gamma+1 the cost is reading the packed head once, but
 // plain fp32 FMAs cannot keep up with HBM (10 FMA per packed byte at M = 5).
-// So each warp streams 16 vocab rows at a time straight from HBM into
-// registers, dequantizes them in registers into the A fragments of
+// A producer warp streams the CTA's vocab range through shared memory with
+// TMA (128 rows x 16 packed words per stage, 6 stages) and copies each
+// stage's scales and biases with cp.async; eight consumer warps each take 16
+// of the 128 rows, dequantize them in registers into the A fragments of
 // mma.sync.m16n8k16 (A = 16 vocab rows x 16 K, B = 16 K x 8 tokens, fp32
-// accumulate), and never stages the dequantized head anywhere.  The K axis is
+// accumulate), and never stage the dequantized head anywhere.  The K axis is
 // permuted consistently in A and B so that one packed word yields A fragments
 // with one shift + lop3 per pair of codes (4-bit), or one prmt per pair (8-bit):
 //   4-bit: word j of a row holds d = 8j .. 8j+7; lop3((w >> 4k) & 0x000F000F |
@@ -25,13 +27,20 @@
 // then w = fma(q, scale, bias) in fp16 (one rounding) after an exact
 // subtraction of 1024.  The row's logits never leave registers.
 #include "qh_dequant.cuh"
+#include "qh_tc.cuh"
+#include "qh_tmap.h"
 
 namespace qh {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kConsumers = 8;                 // consumer warps, 16 rows each
+constexpr int kThreads = 32 * (1 + kConsumers);
+constexpr int kTile = 16 * kConsumers;        // vocab rows per stage
+constexpr int kChunkWords = 16;               // packed words per row per stage
+constexpr int kPBytes = kTile * kChunkWords * 4;
+constexpr int kSBBytes = kTile * 2 * 4;       // per row: 2 scales + 2 biases (fp16)
+constexpr int kStages = 6;
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -42,28 +51,25 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ uint32_t u4_at(const uint4& v, int j) {
     return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
 // One chunk = 16 packed words of a row (128 elements at 4 bits, 64 at 8 bits).
 // Thread (g, t) owns words 4t .. 4t+3 of the chunk for rows g and g+8.
+// hblk: the chunk's block of the staged h row of token g.  For 4-bit heads the
+// staged rows are swizzled: 16-byte chunk k of each 128-element block sits at
+// position k ^ (2 * (k >> 3)), so the four threads of a quad (reading at a
+// 64-byte stride) hit distinct bank groups.
 template <int BITS>
 __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& a0, const uint4& a1,
-                                          __half2 s0, __half2 b0, __half2 s1, __half2 b1,
-                                          const __half* hb) {
+                                          uint32_t s0, uint32_t b0, uint32_t s1, uint32_t b1,
+                                          const __half* hblk, int t) {
     if constexpr (BITS == 4) {
+        const int sw = 2 * (t >> 1);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint4 bq = *reinterpret_cast<const uint4*>(hb + 8 * j);
+            const uint4 bq = *reinterpret_cast<const uint4*>(hblk + 8 * ((4 * t + j) ^ sw));
             uint32_t p0[4], p1[4];
             deq4_word(u4_at(a0, j), s0, b0, p0);
             deq4_word(u4_at(a1, j), s1, b1, p1);
@@ -74,7 +80,7 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& a0, cons
     } else {
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-            const uint4 bq = *reinterpret_cast<const uint4*>(hb + 8 * jj);
+            const uint4 bq = *reinterpret_cast<const uint4*>(hblk + 16 * t + 8 * jj);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const uint32_t w0 = u4_at(a0, 2 * jj + e), w1 = u4_at(a1, 2 * jj + e);
@@ -88,141 +94,168 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& a0, cons
     }
 }
 
-// One packed chunk of a warp's work: A words of rows g and g+8 and their
-// (scale, bias) pairs, packed as half2 (scale, bias).
-struct Item {
-    uint4 a0, a1;
-    uint32_t sb0, sb1;
+// Shared memory: [h rows: 8 x (H + 8) halves] [packed ring] [scale/bias ring] [barriers]
+struct StreamSmem {
+    int off_p, off_sb, off_bar, total;
+    __host__ __device__ StreamSmem(int H) {
+        const int hbytes = kTokGroup * (H + 8) * 2;
+        off_p = (hbytes + 127) / 128 * 128;
+        off_sb = off_p + kStages * kPBytes;
+        off_bar = off_sb + kStages * kSBBytes;
+        total = off_bar + 8 * 2 * kStages + 16;
+    }
 };
 
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 3) stream_fwd_kernel(
-    const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
+__global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
+    const __grid_constant__ CUtensorMap tmap_w, const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, float cap,
     const __half* __restrict__ h16, const int* __restrict__ count, Partial* __restrict__ part,
-    int S) {
+    int S, int* __restrict__ err) {
     const int n_active = *count;
     const int tok0 = blockIdx.x * kTokGroup;
     if (tok0 >= n_active) return;
     const int split = blockIdx.y;
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const StreamSmem L(H);
     __half* hs = reinterpret_cast<__half*>(smem_raw);
     const int hstride = H + 8;  // halves; +16 bytes per row spreads the banks
-    __shared__ Partial red[kWarps][kTokGroup];
+    unsigned char* pring = smem_raw + L.off_p;
+    unsigned char* sbring = smem_raw + L.off_sb;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.off_bar);
+    uint64_t* empty = full + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    __shared__ Partial red[kConsumers][kTokGroup];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
     const int64_t cta_v0 = V * split / S, cta_v1 = V * (split + 1) / S;
-    const int64_t len = cta_v1 - cta_v0;
-    const int64_t wv0 = cta_v0 + len * warp / kWarps, wv1 = cta_v0 + len * (warp + 1) / kWarps;
+    const int ntiles = (int)((cta_v1 - cta_v0 + kTile - 1) / kTile);
     const int wpr = H * BITS / 32;
     const int G = H / 64;
-    const int nchunks = wpr / 16;
-    const int ntiles = (int)((wv1 - wv0 + 15) / 16);
+    const int nchunks = wpr / kChunkWords;
     const int nitems = ntiles * nchunks;
 
-    // Item loader.  Rows past the warp's range are clamped to its last row (a
-    // valid address); their logits are discarded in the epilogue.  Only two
-    // row indices are kept; addresses are formed at fetch time.
-    int pf_c = 0;
-    int64_t pf_r0 = wv0 + g;
-    int rc0 = 0, rc1 = 0;
-    const int wpr4 = wpr / 4;                      // uint4 per row
-    const int go = BITS == 4 ? (t >> 1) : 0;      // group offset of this lane
-    auto set_rows = [&]() {
-        const int64_t last = wv1 - 1;
-        rc0 = (int)min(pf_r0, last);
-        rc1 = (int)min(pf_r0 + 8, last);
-    };
-    const uint4* wq4 = reinterpret_cast<const uint4*>(wq) + t;
-    auto fetch = [&](Item& it) {
-        it.a0 = ld_stream(wq4 + ((int64_t)rc0 * wpr4 + 4 * pf_c));
-        it.a1 = ld_stream(wq4 + ((int64_t)rc1 * wpr4 + 4 * pf_c));
-        const int gi = (BITS == 4 ? 2 * pf_c : pf_c) + go;
-        const int64_t o0 = (int64_t)rc0 * G + gi, o1 = (int64_t)rc1 * G + gi;
-        it.sb0 = h2_as_u32(__halves2half2(scales[o0], biases[o0]));
-        it.sb1 = h2_as_u32(__halves2half2(scales[o1], biases[o1]));
-        if (++pf_c == nchunks) {
-            pf_c = 0;
-            pf_r0 += 16;
-            set_rows();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(&full[i], 1 + 32);  // TMA (expect_tx) + 32 cp.async arrivals
+            tc::mbar_init(&empty[i], kConsumers);
         }
-    };
-
-    Item A, B, C;
-    if (nitems > 0) {
-        set_rows();
-        fetch(A);
-    }
-    if (nitems > 1) fetch(B);
-
-    // Stage the group's 8 rows of h (fp16, K-permuted for 4-bit) in shared memory.
-    const int units = H / 8;
-    for (int idx = threadIdx.x; idx < kTokGroup * units; idx += kThreads) {
-        const int r = idx / units, c = idx - r * units;
-        const uint4 v = *reinterpret_cast<const uint4*>(h16 + (int64_t)(tok0 + r) * H + 8 * c);
-        *reinterpret_cast<uint4*>(hs + r * hstride + 8 * c) = v;
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_tmap(&tmap_w);
     }
     __syncthreads();
-    const __half* hrow = hs + g * hstride + (BITS == 4 ? 32 * t : 16 * t);
-    constexpr int kChunkHalves = BITS == 4 ? 128 : 64;
 
-    RowState st[2];
-    st[0].init();
-    st[1].init();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int c = 0;
-    int64_t tile_r0 = wv0 + g;
-    auto compute = [&](const Item& it) {
-        const __half2 sb0 = u32_as_h2(it.sb0), sb1 = u32_as_h2(it.sb1);
-        chunk_mma<BITS>(acc, it.a0, it.a1, __low2half2(sb0), __high2half2(sb0), __low2half2(sb1),
-                        __high2half2(sb1), hrow + kChunkHalves * c);
-        if (++c == nchunks) {
-            // acc: (row g, tok 2t), (row g, tok 2t+1), (row g+8, tok 2t), (row g+8, tok 2t+1)
-            const int64_t r0 = tile_r0, r1 = tile_r0 + 8;
-            if (r0 < wv1) {
-                st[0].push(softcap_exact(acc[0], cap), acc[0], (int)r0);
-                st[1].push(softcap_exact(acc[1], cap), acc[1], (int)r0);
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int k = 0; k < nitems && ok; ++k) {
+            const int tile = k / nchunks, c = k - tile * nchunks;
+            const int64_t row0 = cta_v0 + (int64_t)tile * kTile;
+            if (lane == 0)
+                ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, tc::kErrTimeoutEmpty);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) {
+                tc::mbar_arrive_expect_tx(&full[stage], kPBytes);
+                tc::tma_load_2d(pring + stage * kPBytes, &tmap_w, &full[stage], kChunkWords * c,
+                                (int)row0);
             }
-            if (r1 < wv1) {
-                st[0].push(softcap_exact(acc[2], cap), acc[2], (int)r1);
-                st[1].push(softcap_exact(acc[3], cap), acc[3], (int)r1);
-            }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            c = 0;
-            tile_r0 += 16;
-        }
-    };
-    // Three-slot ring, unrolled so no slot is ever copied: item k is computed
-    // while item k+2 is in flight.
-    for (int k = 0; k < nitems; k += 3) {
-        if (k + 2 < nitems) fetch(C);
-        compute(A);
-        if (k + 1 >= nitems) break;
-        if (k + 3 < nitems) fetch(A);
-        compute(B);
-        if (k + 2 >= nitems) break;
-        if (k + 4 < nitems) fetch(B);
-        compute(C);
-    }
-
-    // Merge the 8 lanes that share t (lanes t, t+4, ..., t+28), then the warps.
+            // Scales and biases of the stage: 2 consecutive groups per row (the
+            // chunk's two groups at 4 bits; chunks c and c^1 at 8 bits).
+            const int g0 = BITS == 4 ? 2 * c : (c & ~1);
+            unsigned char* sb = sbring + stage * kSBBytes;
 #pragma unroll
-    for (int o = 4; o <= 16; o <<= 1) {
-        st[0].shfl_merge(o);
-        st[1].shfl_merge(o);
-    }
-    if (g == 0) {
-        red[warp][2 * t] = st[0].to_partial();
-        red[warp][2 * t + 1] = st[1].to_partial();
+            for (int i = 0; i < kTile / 32; ++i) {
+                const int r = lane + 32 * i;
+                const int64_t v = row0 + r;
+                const int64_t gi = (v < V ? v : 0) * G + g0;
+                const int nbytes = v < V ? 4 : 0;
+                tc::cp_async_zfill<4>(sb + 4 * r, scales + gi, nbytes);
+                tc::cp_async_zfill<4>(sb + 4 * (kTile + r), biases + gi, nbytes);
+            }
+            tc::cp_async_arrive(&full[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+    } else {
+        // ---------------------------------------------------------------- consumers
+        const int cw = warp - 1;
+        const int g = lane >> 2, t = lane & 3;
+        // Stage the group's 8 rows of h (fp16, K-permuted for 4-bit), consumers only.
+        const int units = H / 8;
+        for (int idx = threadIdx.x - 32; idx < kTokGroup * units; idx += 32 * kConsumers) {
+            const int r = idx / units, cc = idx - r * units;
+            const uint4 v = *reinterpret_cast<const uint4*>(h16 + (int64_t)(tok0 + r) * H + 8 * cc);
+            int pos = cc;
+            if (BITS == 4) {
+                const int k = cc & 15;
+                pos = (cc & ~15) | (k ^ (2 * (k >> 3)));
+            }
+            *reinterpret_cast<uint4*>(hs + r * hstride + 8 * pos) = v;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
+        const __half* hrow = hs + g * hstride;
+        constexpr int kChunkHalves = BITS == 4 ? 128 : 64;
+        const int ra = 16 * cw + g, rb = ra + 8;  // rows of this thread within a tile
+        // which of the stage's two groups this thread uses
+        const int gsel_fixed = t >> 1;
+
+        RowState st[2];
+        st[0].init();
+        st[1].init();
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = 0; tile < ntiles; ++tile) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < nchunks; ++c) {
+                if (!tc::mbar_wait_warp(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
+                    goto consumer_done;
+                const unsigned char* P = pring + stage * kPBytes;
+                const uint4 a0 = *reinterpret_cast<const uint4*>(P + ra * 64 + 16 * t);
+                const uint4 a1 = *reinterpret_cast<const uint4*>(P + rb * 64 + 16 * t);
+                const __half* sbh = reinterpret_cast<const __half*>(sbring + stage * kSBBytes);
+                const int gsel = BITS == 4 ? gsel_fixed : (c & 1);
+                const uint32_t s0 = bcast_h(sbh[2 * ra + gsel]);
+                const uint32_t s1 = bcast_h(sbh[2 * rb + gsel]);
+                const uint32_t b0 = bcast_h(sbh[2 * (kTile + ra) + gsel]);
+                const uint32_t b1 = bcast_h(sbh[2 * (kTile + rb) + gsel]);
+                chunk_mma<BITS>(acc, a0, a1, s0, b0, s1, b1, hrow + kChunkHalves * c, t);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&empty[stage]);
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+            // acc: (row ra, tok 2t), (row ra, tok 2t+1), (row rb, tok 2t), (row rb, tok 2t+1)
+            const int64_t v0 = cta_v0 + (int64_t)tile * kTile + ra, v1 = v0 + 8;
+            if (v0 < cta_v1) {
+                st[0].push(softcap_exact(acc[0], cap), acc[0], (int)v0);
+                st[1].push(softcap_exact(acc[1], cap), acc[1], (int)v0);
+            }
+            if (v1 < cta_v1) {
+                st[0].push(softcap_exact(acc[2], cap), acc[2], (int)v1);
+                st[1].push(softcap_exact(acc[3], cap), acc[3], (int)v1);
+            }
+        }
+    consumer_done:
+        // Merge the 8 lanes that share t (lanes t, t+4, ..., t+28).
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            st[0].shfl_merge(o);
+            st[1].shfl_merge(o);
+        }
+        if (g == 0) {
+            red[cw][2 * t] = st[0].to_partial();
+            red[cw][2 * t + 1] = st[1].to_partial();
+        }
     }
     __syncthreads();
     if (threadIdx.x < kTokGroup) {
         const int j = threadIdx.x;
         RowState acc;
         acc.init();
-        for (int w = 0; w < kWarps; ++w) acc.merge(red[w][j]);
+        for (int w = 0; w < kConsumers; ++w) acc.merge(red[w][j]);
         part[(int64_t)(tok0 + j) * S + split] = acc.to_partial();
     }
 }
@@ -230,14 +263,14 @@ __global__ void __launch_bounds__(kThreads, 3) stream_fwd_kernel(
 }  // namespace
 
 int stream_fwd_ctas_per_sm(int bits, int H) {
-    const size_t smem = (size_t)kTokGroup * (H + 8) * sizeof(__half);
+    const int smem = StreamSmem(H).total;
     int n = 0;
     cudaError_t e;
     if (bits == 4) {
-        cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stream_fwd_kernel<4>, kThreads, smem);
     } else {
-        cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stream_fwd_kernel<8>, kThreads, smem);
     }
     return (e == cudaSuccess && n > 0) ? n : 1;
@@ -245,20 +278,22 @@ int stream_fwd_ctas_per_sm(int bits, int H) {
 
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
                               int64_t V, int H, int bits, float cap, const __half* h16,
-                              const int* count, int64_t M, Partial* part, int S, cudaStream_t st) {
+                              const int* count, int64_t M, Partial* part, int S, int* err,
+                              cudaStream_t st) {
+    CUtensorMap tw;
+    if (!tmap_packed_rows(&tw, wq, (uint64_t)H * bits / 32, (uint64_t)V, kChunkWords, kTile))
+        return cudaErrorInvalidValue;
     const int groups = (int)((M + kTokGroup - 1) / kTokGroup);
-    const size_t smem = (size_t)kTokGroup * (H + 8) * sizeof(__half);
+    const int smem = StreamSmem(H).total;
     dim3 grid(groups, S);
     if (bits == 4) {
-        cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        stream_fwd_kernel<4><<<grid, kThreads, smem, st>>>(wq, scales, biases, V, H, cap, h16,
-                                                           count, part, S);
+        cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        stream_fwd_kernel<4><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
+                                                           count, part, S, err);
     } else {
-        cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        stream_fwd_kernel<8><<<grid, kThreads, smem, st>>>(wq, scales, biases, V, H, cap, h16,
-                                                           count, part, S);
+        cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        stream_fwd_kernel<8><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
+                                                           count, part, S, err);
     }
     return cudaGetLastError();
 }

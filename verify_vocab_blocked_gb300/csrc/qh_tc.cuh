@@ -82,6 +82,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Warp-uniform wait: every lane waits, and the warp proceeds only if all lanes
+// succeeded, so a timeout never leaves part of a warp inside a collective
+// instruction (mma.sync, tcgen05.ld, __syncwarp).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, int* err, int code) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, err, code);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ----------------------------------------------------------------------- TMA
 
 // 2D tiled load global -> shared, completion counted in bytes on `bar`.

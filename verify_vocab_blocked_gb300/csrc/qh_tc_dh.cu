@@ -66,7 +66,7 @@ struct DhLayout {
 // column kPerm4[c] -- and the epilogue, which holds 32 consecutive N columns
 // per thread in registers, writes column c to hidden offset kPerm4[c].  8-bit
 // words dequantize in natural order.
-__device__ __forceinline__ uint4 deq4_chunk(uint32_t w, __half2 s, __half2 b) {
+__device__ __forceinline__ uint4 deq4_chunk(uint32_t w, uint32_t s, uint32_t b) {
     uint32_t p[4];
     deq4_word(w, s, b, p);
     return make_uint4(p[0], p[1], p[2], p[3]);
@@ -228,9 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             const int ks = u % KS;
             const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
             for (int kk = k0; kk < k1; ++kk) {
-                if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
+                if (!tc::mbar_wait_warp(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                     goto dq_done;
-                if (!tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant))
+                if (!tc::mbar_wait_warp(&bfree[bs], bphase ^ 1, abort_flag, err,
+                                        tc::kErrTimeoutDequant))
                     goto dq_done;
                 const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
                 const __half* sb = reinterpret_cast<const __half*>(smem + L::OFF_SB + stage * L::SB_BYTES);
@@ -240,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     const int kr = row0 + L::RPP * ps;
                     const int krow = kr & 7;
                     const uint4 wv = *reinterpret_cast<const uint4*>(P + kr * L::P_ROW + pc * 16);
-                    const __half2 s2 = __half2half2(sb[kr * L::NSB + (ncol_piece >> 6)]);
-                    const __half2 b2 = __half2half2(sb[(BK + kr) * L::NSB + (ncol_piece >> 6)]);
+                    const uint32_t s2 = bcast_h(sb[kr * L::NSB + (ncol_piece >> 6)]);
+                    const uint32_t b2 = bcast_h(sb[(BK + kr) * L::NSB + (ncol_piece >> 6)]);
                     unsigned char* dst_row = Bs + (kr >> 3) * 1024 + krow * 128;
                     // word i of the piece, selected without dynamic register indexing
                     auto word = [&](int i) {
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             const int i = mt * BM + row;
             const bool row_ok = i < n_active;
             const float scale = row_ok ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
-            if (!tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
+            if (!tc::mbar_wait_warp(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
                 goto epi_done;
             tc::tc_fence_after();
             float* dst = a.dh_acc + (int64_t)ks * a.slice_stride + (int64_t)i * a.H + nt * BNH;

@@ -237,17 +237,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const __half z = __float2half(0.f);
                     const __half s0 = ok0 ? scales[v0 * G + kk] : z, b0 = ok0 ? biases[v0 * G + kk] : z;
-                    if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
+                    if (!tc::mbar_wait_warp(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                         goto dq_done;
-                    if (!tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err,
-                                       tc::kErrTimeoutDequant))
+                    if (!tc::mbar_wait_warp(&bfree[bs], bphase ^ 1, abort_flag, err,
+                                            tc::kErrTimeoutDequant))
                         goto dq_done;
                     const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
                     unsigned char* Bs = smem + L::OFF_B + bs * B_BYTES;
                     {
                         const int r = t;
-                        const __half2 s2 = __half2half2(s0);
-                        const __half2 b2 = __half2half2(b0);
+                        const uint32_t s2 = bcast_h(s0);
+                        const uint32_t b2 = bcast_h(b0);
                         const uint4* prow = reinterpret_cast<const uint4*>(P + r * L::P_ROW);
                         unsigned char* brow = Bs + r * 128;
                         if constexpr (BITS == 4) {
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             bool row_ok = i < n_active;
             if (EPI == EPI_COEFF && row_ok) lsb = a.lse[a.rows[i]] * kLog2e - 14.f;
             for (int vt = vt0; vt < vt1; ++vt) {
-                if (!tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
+                if (!tc::mbar_wait_warp(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
                     goto epi_done;
                 tc::tc_fence_after();
 #pragma unroll 1
