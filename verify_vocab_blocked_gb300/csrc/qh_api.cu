@@ -393,7 +393,7 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         }
         hook_after(st);
     } else {
-        if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, nullptr, st)))
+        if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
             return cuda_fail(e, "compact");
         hook_before(st);
         e = qh::launch_bwd_simt(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb, rows,
@@ -402,7 +402,7 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         if (e) return cuda_fail(e, "bwd_simt");
     }
     if ((e = qh::launch_bwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
-                                     pos, targets, dlogp, dhp, p.S, p.Mpad, dh, M, st)))
+                                     pos, targets, dlogp, dhp, p.S, p.Mpad, err, dh, M, st)))
         return cuda_fail(e, "bwd_finalize");
     return QHEAD_OK;
 }

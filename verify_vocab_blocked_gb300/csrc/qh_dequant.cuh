@@ -27,17 +27,13 @@ __device__ __forceinline__ uint32_t bcast_h(__half x) {
 }
 
 // (M + q_lo, M + q_hi) -> (s*q_lo + b, s*q_hi + b), fp16, one rounding: the
-// subtraction of the magic M (1024 or 64) is exact for integers q < 256.  All
-// operands are fp16x2 bit patterns in 32-bit registers (s2, b2 broadcast).
-__device__ __forceinline__ uint32_t affine(uint32_t magic_pair, uint32_t magic, uint32_t s2,
-                                           uint32_t b2) {
-    uint32_t d;
-    asm("{\n\t.reg .b32 q;\n\t"
-        "sub.f16x2 q, %1, %2;\n\t"
-        "fma.rn.f16x2 %0, q, %3, %4;\n\t}"
-        : "=r"(d)
-        : "r"(magic_pair), "r"(magic), "r"(s2), "r"(b2));
-    return d;
+// subtraction of the magic M (1024 or 64) is exact for integers q < 256.
+// The magic constant is passed as its fp16x2 bit pattern so it stays a
+// compile-time immediate (0x64006400 = (1024, 1024), 0x54005400 = (64, 64)).
+__device__ __forceinline__ uint32_t affine(uint32_t magic_pair, uint32_t magic, __half2 s,
+                                           __half2 b) {
+    const __half2 q = __hsub2(u32_as_h2(magic_pair), u32_as_h2(magic));
+    return h2_as_u32(__hfma2(q, s, b));
 }
 
 // 4-bit codes of one word as fp16 pairs (q_k, q_k+4), k = 0..3, without a
@@ -45,17 +41,26 @@ __device__ __forceinline__ uint32_t affine(uint32_t magic_pair, uint32_t magic, 
 // of 1024 + q (magic 0x6400), codes in bits 4-7 the mantissa of 64 + q (magic
 // 0x5400: exponent 2^6, mantissa step 16 -> 1).  One shift by 8 brings codes
 // 2, 3, 6, 7 down to the same two positions.
-__device__ __forceinline__ void deq4_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&p)[4]) {
+__device__ __forceinline__ void deq4_word(uint32_t w, __half2 s, __half2 b, uint32_t (&p)[4]) {
     const uint32_t w8 = w >> 8;
-    p[0] = affine(lop3_and_or(w, 0x000F000Fu, 0x64006400u), 0x64006400u, s2, b2);
-    p[1] = affine(lop3_and_or(w, 0x00F000F0u, 0x54005400u), 0x54005400u, s2, b2);
-    p[2] = affine(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), 0x64006400u, s2, b2);
-    p[3] = affine(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), 0x54005400u, s2, b2);
+    p[0] = affine(lop3_and_or(w, 0x000F000Fu, 0x64006400u), 0x64006400u, s, b);
+    p[1] = affine(lop3_and_or(w, 0x00F000F0u, 0x54005400u), 0x54005400u, s, b);
+    p[2] = affine(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), 0x64006400u, s, b);
+    p[3] = affine(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), 0x54005400u, s, b);
 }
 
 // 8-bit codes: prmt builds (1024 + q_a, 1024 + q_b) from two bytes of w.
+__device__ __forceinline__ uint32_t deq8(uint32_t w, uint32_t sel, __half2 s, __half2 b) {
+    return affine(__byte_perm(w, 0x64646464u, sel), 0x64006400u, s, b);
+}
+
+// Same, with the broadcast scale and bias held as fp16x2 bit patterns.
+__device__ __forceinline__ void deq4_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&p)[4]) {
+    deq4_word(w, u32_as_h2(s2), u32_as_h2(b2), p);
+}
+
 __device__ __forceinline__ uint32_t deq8(uint32_t w, uint32_t sel, uint32_t s2, uint32_t b2) {
-    return affine(__byte_perm(w, 0x64646464u, sel), 0x64006400u, s2, b2);
+    return deq8(w, sel, u32_as_h2(s2), u32_as_h2(b2));
 }
 
 }  // namespace qh

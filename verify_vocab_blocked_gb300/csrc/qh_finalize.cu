@@ -115,12 +115,18 @@ __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
     const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
     const int32_t* __restrict__ targets, const float* __restrict__ dlogp,
-    const float* __restrict__ dhp, int S, int64_t Mpad, float* __restrict__ dh) {
+    const float* __restrict__ dhp, int S, int64_t Mpad, const int* __restrict__ err,
+    float* __restrict__ dh) {
     const int64_t r = blockIdx.x;
     const int i = pos[r];
     float* out = dh + r * (int64_t)H;
     if (i < 0) {
         for (int d = threadIdx.x; d < H; d += kBwdFinThreads) out[d] = 0.f;
+        return;
+    }
+    if (*err != 0) {
+        // A head kernel gave up (a bounded wait expired): poison the row.
+        for (int d = threadIdx.x; d < H; d += kBwdFinThreads) out[d] = __int_as_float(0x7fc00000);
         return;
     }
     __shared__ float coef_sh;
@@ -164,11 +170,11 @@ cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const 
 cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const float* dlogp,
-                                const float* dhp, int S, int64_t Mpad, float* dh, int64_t M,
-                                cudaStream_t st) {
+                                const float* dhp, int S, int64_t Mpad, const int* err, float* dh,
+                                int64_t M, cudaStream_t st) {
     bwd_finalize_kernel<<<(unsigned)M, kBwdFinThreads, 0, st>>>(wq, scales, biases, V, H, bits,
                                                                  cap, h, pos, targets, dlogp, dhp,
-                                                                 S, Mpad, dh);
+                                                                 S, Mpad, err, dh);
     return cudaGetLastError();
 }
 

@@ -175,10 +175,10 @@ cudaError_t launch_bwd_simt(const uint32_t* wq, const __half* scales, const __ha
 cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const float* dlogp,
-                                const float* dhp, int S, int64_t Mpad, float* dh, int64_t M,
-                                cudaStream_t st);
+                                const float* dhp, int S, int64_t Mpad, const int* err, float* dh,
+                                int64_t M, cudaStream_t st);
 
-int bwd_simt_tokens(int H);
-int stream_fwd_ctas_per_sm(int bits, int H);  // occupancy of the weight-streaming kernel  // tokens per CTA of the SIMT backward
+int bwd_simt_tokens(int H);                   // tokens per CTA of the SIMT backward
+int stream_fwd_ctas_per_sm(int bits, int H);  // occupancy of the weight-streaming kernel
 
 }  // namespace qh

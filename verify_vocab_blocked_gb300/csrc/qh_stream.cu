@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         int stage = 0;
-        uint32_t phase = 0;
+        uint32_t phase = 0, fills = 0;
         bool ok = true;
         for (int k = 0; k < nitems && ok; ++k) {
             const int tile = k / nchunks, c = k - tile * nchunks;
@@ -178,8 +178,12 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
                 tc::cp_async_zfill<4>(sb + 4 * (kTile + r), biases + gi, nbytes);
             }
             tc::cp_async_arrive(&full[stage]);
+            ++fills;
             if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
+        // On the abort path the consumers stop waiting: let the copies in
+        // flight land before the CTA exits.
+        if (!ok && lane == 0) tc::drain_ring(full, kStages, fills, err);
     } else {
         // ---------------------------------------------------------------- consumers
         const int cw = warp - 1;
@@ -211,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
         for (int tile = 0; tile < ntiles; ++tile) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int c = 0; c < nchunks; ++c) {
-                if (!tc::mbar_wait_warp(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
-                    goto consumer_done;
+                // Result ignored: the warp stays converged (see the abort policy).
+                tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
                 const unsigned char* P = pring + stage * kPBytes;
                 const uint4 a0 = *reinterpret_cast<const uint4*>(P + ra * 64 + 16 * t);
                 const uint4 a1 = *reinterpret_cast<const uint4*>(P + rb * 64 + 16 * t);
@@ -238,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
                 st[1].push(softcap_exact(acc[3], cap), acc[3], (int)v1);
             }
         }
-    consumer_done:
         // Merge the 8 lanes that share t (lanes t, t+4, ..., t+28).
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {

@@ -17,7 +17,11 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 
 // Error codes written to the kernel's error word.
 constexpr int kErrTimeoutFull = 1, kErrTimeoutEmpty = 2, kErrTimeoutDequant = 3,
-              kErrTimeoutAccFull = 4, kErrTimeoutAccEmpty = 5;
+              kErrTimeoutAccFull = 4, kErrTimeoutAccEmpty = 5, kErrTimeoutDrain = 6;
+
+// Limit of a drain wait on the abort path (copies and MMAs already issued
+// always complete; this only bounds the wait if the device misbehaves).
+constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // 0.1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,13 +86,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// Warp-uniform wait: every lane waits, and the warp proceeds only if all lanes
-// succeeded, so a timeout never leaves part of a warp inside a collective
-// instruction (mma.sync, tcgen05.ld, __syncwarp).
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort_flag, int* err, int code) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, err, code);
-    return __all_sync(0xffffffffu, ok);
+// Abort-path policy.  A warp whose lanes all execute collective or .aligned
+// instructions (mma.sync, tcgen05.ld, __syncwarp, bar.sync) never leaves its
+// loop on a failed wait: it ignores the result and runs its remaining,
+// uniform iterations on whatever shared memory holds (every address stays in
+// bounds), each later wait returning at once because the abort flag is set.
+// The error word makes the host-visible results NaN.  Warps driven by one
+// thread (TMA producer, MMA issuer) do leave early, after draining their own
+// in-flight operations with the waits below.
+
+// Bounded wait that ignores the abort flag.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, int* err) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kDrainTimeoutNs) {
+            atomicCAS(err, 0, kErrTimeoutDrain);
+            return;
+        }
+    }
+}
+
+// Waits until the last min(fills, ns) fills of a ring of ns stages have landed;
+// fill i completes phase i / ns of barrier full[i % ns].
+__device__ __forceinline__ void drain_ring(uint64_t* full, int ns, uint32_t fills, int* err) {
+    const uint32_t first = fills > (uint32_t)ns ? fills - (uint32_t)ns : 0u;
+    for (uint32_t i = first; i < fills; ++i) mbar_drain(&full[i % ns], (i / ns) & 1u, err);
 }
 
 // ----------------------------------------------------------------------- TMA

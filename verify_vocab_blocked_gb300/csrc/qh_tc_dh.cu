@@ -66,7 +66,7 @@ struct DhLayout {
 // column kPerm4[c] -- and the epilogue, which holds 32 consecutive N columns
 // per thread in registers, writes column c to hidden offset kPerm4[c].  8-bit
 // words dequantize in natural order.
-__device__ __forceinline__ uint4 deq4_chunk(uint32_t w, uint32_t s, uint32_t b) {
+__device__ __forceinline__ uint4 deq4_chunk(uint32_t w, __half2 s, __half2 b) {
     uint32_t p[4];
     deq4_word(w, s, b, p);
     return make_uint4(p[0], p[1], p[2], p[3]);
@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     uint64_t* acce = accf + 2;
     uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+    uint64_t* mdrain = acce + 3;  // MMA drain on the abort path
     int* err = a.err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             tc::mbar_init(&accf[i], 1);
             tc::mbar_init(&acce[i], 4);
         }
+        tc::mbar_init(mdrain, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmap_c);
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         // stage's scales and biases (rows lane, lane + 32; the N tile's groups)
         // with cp.async, completing on the same barrier.
         int stage = 0;
-        uint32_t phase = 0;
+        uint32_t phase = 0, fills = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
@@ -162,16 +164,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     tc::cp_async_zfill<2 * L::NSB>(sb + (BK + r) * L::NSB, a.biases + gi, nbytes);
                 }
                 tc::cp_async_arrive(&full[stage]);
+                ++fills;
                 if (++stage == NS) { stage = 0; phase ^= 1; }
             }
         }
-        if (lane == 0 && ok) {
-            for (int i = 0; i < NS; ++i) {
-                if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
-                                   tc::kErrTimeoutEmpty))
-                    break;
+        if (lane == 0) {
+            // Drain: the last stages' copies landed and were consumed; on the
+            // abort path only their landing is awaited.
+            for (int i = 0; i < NS && ok; ++i) {
+                ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, tc::kErrTimeoutEmpty);
                 if (++stage == NS) { stage = 0; phase ^= 1; }
             }
+            if (!ok) tc::drain_ring(full, NS, fills, err);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -182,14 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
                 if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
                                    tc::kErrTimeoutAccEmpty))
-                    goto mma_done;
+                    goto mma_abort;
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BNH;
                 for (int kk = k0; kk < k1; ++kk) {
                     if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
-                        goto mma_done;
+                        goto mma_abort;
                     if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err, tc::kErrTimeoutDequant))
-                        goto mma_done;
+                        goto mma_abort;
                     tc::tc_fence_after();
                     const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * L::A_BYTES);
                     const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
@@ -210,6 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 tc::umma_commit(&accf[buf]);
                 if (++buf == 2) { buf = 0; aphase ^= 1; }
             }
+            goto mma_done;
+        mma_abort:
+            // Let every MMA issued so far finish before TMEM is released.
+            tc::umma_commit(mdrain);
+            tc::mbar_drain(mdrain, 0, err);
         mma_done:;
         }
     } else if (warp < kEpiWarp0) {
@@ -228,11 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             const int ks = u % KS;
             const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
             for (int kk = k0; kk < k1; ++kk) {
-                if (!tc::mbar_wait_warp(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
-                    goto dq_done;
-                if (!tc::mbar_wait_warp(&bfree[bs], bphase ^ 1, abort_flag, err,
-                                        tc::kErrTimeoutDequant))
-                    goto dq_done;
+                // Results ignored: the warp stays converged (see the abort policy).
+                tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
+                tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
                 const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
                 const __half* sb = reinterpret_cast<const __half*>(smem + L::OFF_SB + stage * L::SB_BYTES);
                 unsigned char* Bs = smem + L::OFF_B + bs * L::B_BYTES + nb * (BK / 8) * 1024;
@@ -241,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     const int kr = row0 + L::RPP * ps;
                     const int krow = kr & 7;
                     const uint4 wv = *reinterpret_cast<const uint4*>(P + kr * L::P_ROW + pc * 16);
-                    const uint32_t s2 = bcast_h(sb[kr * L::NSB + (ncol_piece >> 6)]);
-                    const uint32_t b2 = bcast_h(sb[(BK + kr) * L::NSB + (ncol_piece >> 6)]);
+                    const __half2 s2 = __half2half2(sb[kr * L::NSB + (ncol_piece >> 6)]);
+                    const __half2 b2 = __half2half2(sb[(BK + kr) * L::NSB + (ncol_piece >> 6)]);
                     unsigned char* dst_row = Bs + (kr >> 3) * 1024 + krow * 128;
                     // word i of the piece, selected without dynamic register indexing
                     auto word = [&](int i) {
@@ -272,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 if (++bs == NB) { bs = 0; bphase ^= 1; }
             }
         }
-    dq_done:;
     } else {
         const int sub = warp & 3;
         const int row = sub * 32 + lane;
@@ -284,8 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             const int i = mt * BM + row;
             const bool row_ok = i < n_active;
             const float scale = row_ok ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
-            if (!tc::mbar_wait_warp(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
-                goto epi_done;
+            tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull);
             tc::tc_fence_after();
             float* dst = a.dh_acc + (int64_t)ks * a.slice_stride + (int64_t)i * a.H + nt * BNH;
 #pragma unroll 1
@@ -320,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             if (lane == 0) tc::mbar_arrive(&acce[buf]);
             if (++buf == 2) { buf = 0; aphase ^= 1; }
         }
-    epi_done:;
     }
 
     tc::tc_fence_before();

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     uint64_t* acce = accf + 2;
     uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+    uint64_t* mdrain = acce + 3;  // MMA drain on the abort path
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_active = *a.count;
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             tc::mbar_init(&accf[i], 1);
             tc::mbar_init(&acce[i], 4);
         }
+        tc::mbar_init(mdrain, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmap_h);
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0;
+            uint32_t phase = 0, fills = 0;
             for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
@@ -163,23 +165,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                     for (int kk = 0; kk < KSTEPS; ++kk) {
                         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
                                            tc::kErrTimeoutEmpty))
-                            goto producer_done;
+                            goto producer_abort;
                         tc::mbar_arrive_expect_tx(&full[stage], A_BYTES + L::P_BYTES);
                         tc::tma_load_2d(smem + L::OFF_A + stage * A_BYTES, &tmap_h, &full[stage],
                                         kk * BK, mt * BM);
                         tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w,
                                         &full[stage], kk * L::WORDS, vt * BN);
+                        ++fills;
                         if (++stage == NS) { stage = 0; phase ^= 1; }
                     }
                 }
             }
-            // Drain: wait until the loads of the last stages have landed.
+            // Drain: wait until the loads of the last stages have landed and
+            // been consumed.
             for (int i = 0; i < NS; ++i) {
                 if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
                                    tc::kErrTimeoutEmpty))
-                    break;
+                    goto producer_abort;
                 if (++stage == NS) { stage = 0; phase ^= 1; }
             }
+            goto producer_done;
+        producer_abort:
+            tc::drain_ring(full, NS, fills, err);
         producer_done:;
         }
     } else if (warp == 1) {
@@ -193,16 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                 for (int vt = vt0; vt < vt1; ++vt) {
                     if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
                                        tc::kErrTimeoutAccEmpty))
-                        goto mma_done;
+                        goto mma_abort;
                     tc::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
                     for (int kk = 0; kk < KSTEPS; ++kk) {
                         if (!tc::mbar_wait(&full[stage], phase, abort_flag, err,
                                            tc::kErrTimeoutFull))
-                            goto mma_done;
+                            goto mma_abort;
                         if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err,
                                            tc::kErrTimeoutDequant))
-                            goto mma_done;
+                            goto mma_abort;
                         tc::tc_fence_after();
                         const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * A_BYTES);
                         const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * B_BYTES);
@@ -221,6 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                     if (++buf == 2) { buf = 0; aphase ^= 1; }
                 }
             }
+            goto mma_done;
+        mma_abort:
+            // Let every MMA issued so far finish before TMEM is released.
+            tc::umma_commit(mdrain);
+            tc::mbar_drain(mdrain, 0, err);
         mma_done:;
         }
     } else if (warp < kEpiWarp0) {
@@ -237,17 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const __half z = __float2half(0.f);
                     const __half s0 = ok0 ? scales[v0 * G + kk] : z, b0 = ok0 ? biases[v0 * G + kk] : z;
-                    if (!tc::mbar_wait_warp(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
-                        goto dq_done;
-                    if (!tc::mbar_wait_warp(&bfree[bs], bphase ^ 1, abort_flag, err,
-                                            tc::kErrTimeoutDequant))
-                        goto dq_done;
+                    // Results ignored: the warp stays converged (see the abort policy).
+                    tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
+                    tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
                     const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
                     unsigned char* Bs = smem + L::OFF_B + bs * B_BYTES;
                     {
                         const int r = t;
-                        const uint32_t s2 = bcast_h(s0);
-                        const uint32_t b2 = bcast_h(b0);
+                        const __half2 s2 = __half2half2(s0);
+                        const __half2 b2 = __half2half2(b0);
                         const uint4* prow = reinterpret_cast<const uint4*>(P + r * L::P_ROW);
                         unsigned char* brow = Bs + r * 128;
                         if constexpr (BITS == 4) {
@@ -293,7 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                 }
             }
         }
-    dq_done:;
     } else {
         // ------------------------------------------------------------ epilogue warps
         const int sub = warp & 3;  // TMEM sub-partition of this warp
@@ -313,8 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             bool row_ok = i < n_active;
             if (EPI == EPI_COEFF && row_ok) lsb = a.lse[a.rows[i]] * kLog2e - 14.f;
             for (int vt = vt0; vt < vt1; ++vt) {
-                if (!tc::mbar_wait_warp(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull))
-                    goto epi_done;
+                tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull);
                 tc::tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
@@ -399,7 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                 a.part[(int64_t)i * W.n_seg + seg] = p;
             }
         }
-    epi_done:;
     }
 
     tc::tc_fence_before();
