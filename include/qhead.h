@@ -37,6 +37,14 @@
  *     (argument errors) or a launch failed (QHEAD_ECUDA).  A message for the
  *     calling thread is available from qhead_last_error().
  *   - There is no fallback path: unsupported shapes are rejected.
+ *   - Kernel time limits: every wait inside a pipelined kernel gives up after
+ *     2 s (only a defect or a stalled device makes one that long).  The kernel
+ *     then stops waiting, lets the copies and tensor-core operations it has
+ *     issued complete, runs to its end and records the failure; qhead_fwd then
+ *     writes logp = NaN, lse = NaN and argmax = -1 for every active row, and
+ *     qhead_bwd writes NaN to every active row of dh (inactive rows keep their
+ *     defined values).  The return value cannot report this, because the call
+ *     returns before its kernels run.
  */
 #ifndef QHEAD_H
 #define QHEAD_H
@@ -180,6 +188,18 @@ const char* qhead_last_error(void);
  * cudaEvent_t handles passed as void*; passing NULL for both disarms.
  */
 void qhead_time_next_head_kernel(void* start, void* stop);
+
+/*
+ * Test instrumentation (no counterpart on the pages): arm a one-shot switch
+ * on the calling thread.  The thread's next qhead_fwd or qhead_bwd call
+ * launches its pipelined head kernel with the TMA producer issuing no loads,
+ * so the consumers' bounded waits expire and the call ends as described under
+ * "Kernel time limits" (about 2 s later, without a fault).  A qhead_bwd call
+ * on the SIMT path (fewer than 64 rows) has no pipelined kernel and ignores
+ * the switch.  armed = 0 disarms.  Exists so that the time-limit path can be
+ * tested.
+ */
+void qhead_test_stall_next_call(int armed);
 
 /* Library version string, e.g. "qhead 0.1.0 sm_103a". */
 const char* qhead_version(void);

@@ -19,6 +19,14 @@ namespace {
 
 thread_local std::string g_err;
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+thread_local bool g_stall = false;
+
+// Consumes the one-shot stall switch of qhead_test_stall_next_call.
+int take_stall() {
+    const bool s = g_stall;
+    g_stall = false;
+    return s ? 1 : 0;
+}
 
 // Records the armed "before head kernel" event (if any).
 void hook_before(cudaStream_t st) {
@@ -210,6 +218,8 @@ const char* qhead_last_error(void) { return g_err.c_str(); }
 
 const char* qhead_version(void) { return "qhead 0.1.0 sm_103a"; }
 
+void qhead_test_stall_next_call(int armed) { g_stall = armed != 0; }
+
 void qhead_time_next_head_kernel(void* start, void* stop) {
     g_ev_start = static_cast<cudaEvent_t>(start);
     g_ev_stop = static_cast<cudaEvent_t>(stop);
@@ -239,6 +249,7 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
               const uint8_t* mask, float* logp, float* lse, int32_t* argmax, void* workspace,
               size_t workspace_bytes, void* stream) {
     g_err.clear();
+    const int stall = take_stall();
     int rc = check_head(head);
     if (rc) return rc;
     if (M < 0) return fail(QHEAD_EINVAL, "M < 0");
@@ -290,7 +301,7 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
             return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
         qh::TcFwdArgs ta{};
         ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H; ta.cap = head->softcap;
-        ta.count = count; ta.err = err;
+        ta.count = count; ta.err = err; ta.stall = stall;
         ta.vt_begin = 0; ta.vt_end = (int)((head->V + 255) / 256);
         ta.part = part; ta.S_out = S_dev;
         hook_before(st);
@@ -300,7 +311,7 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     } else {
         hook_before(st);
         e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, h16,
-                                  count, M, part, p.S, err, st);
+                                  count, M, part, p.S, err, stall, st);
         hook_after(st);
         if (e) return cuda_fail(e, "stream_fwd");
     }
@@ -316,6 +327,7 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
               const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
               void* workspace, size_t workspace_bytes, void* stream) {
     g_err.clear();
+    const int stall = take_stall();
     int rc = check_head(head);
     if (rc) return rc;
     if (M < 0) return fail(QHEAD_EINVAL, "M < 0");
@@ -375,6 +387,7 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
             qh::TcFwdArgs ta{};
             ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H;
             ta.cap = head->softcap; ta.count = count; ta.err = err;
+            ta.stall = vt0 == 0 ? stall : 0;
             ta.vt_begin = vt0; ta.vt_end = vt1;
             ta.lse = lse; ta.rows = rows; ta.coeff = coeff; ta.coeff_ld = p.chunk;
             ta.coeff_rows = (int)p.Mpad;

@@ -161,7 +161,7 @@ cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bi
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
                               int64_t V, int H, int bits, float cap, const __half* h16,
                               const int* count, int64_t M, Partial* part, int S, int* err,
-                              cudaStream_t st);
+                              int stall, cudaStream_t st);
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_w, const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, float cap,
     const __half* __restrict__ h16, const int* __restrict__ count, Partial* __restrict__ part,
-    int S, int* __restrict__ err) {
+    int S, int* __restrict__ err, int stall) {
     const int n_active = *count;
     const int tok0 = blockIdx.x * kTokGroup;
     if (tok0 >= n_active) return;
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
         // ---------------------------------------------------------------- producer
         int stage = 0;
         uint32_t phase = 0, fills = 0;
-        bool ok = true;
+        bool ok = stall == 0;  // test switch: issue no loads, the consumers' waits expire
         for (int k = 0; k < nitems && ok; ++k) {
             const int tile = k / nchunks, c = k - tile * nchunks;
             const int64_t row0 = cta_v0 + (int64_t)tile * kTile;
@@ -282,7 +282,7 @@ int stream_fwd_ctas_per_sm(int bits, int H) {
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
                               int64_t V, int H, int bits, float cap, const __half* h16,
                               const int* count, int64_t M, Partial* part, int S, int* err,
-                              cudaStream_t st) {
+                              int stall, cudaStream_t st) {
     CUtensorMap tw;
     if (!tmap_packed_rows(&tw, wq, (uint64_t)H * bits / 32, (uint64_t)V, kChunkWords, kTile))
         return cudaErrorInvalidValue;
@@ -292,11 +292,11 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
     if (bits == 4) {
         cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         stream_fwd_kernel<4><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
-                                                           count, part, S, err);
+                                                           count, part, S, err, stall);
     } else {
         cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         stream_fwd_kernel<8><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
-                                                           count, part, S, err);
+                                                           count, part, S, err, stall);
     }
     return cudaGetLastError();
 }

@@ -67,8 +67,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if the
-// CTA has been told to abort or the wait ran past the time limit (then the
-// error word and the abort flag are set).
+// CTA has been told to abort, another CTA has set the kernel's error word, or
+// the wait ran past the time limit (then the error word and the abort flag
+// are set).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* err, int code) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -77,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
+        if (*abort_flag || *reinterpret_cast<volatile int*>(err) != 0) return false;
         if (globaltimer() - t0 > kWaitTimeoutNs) {
             atomicCAS(err, 0, code);
             *abort_flag = 1;

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, fills = 0;
+            if (a.stall) goto producer_abort;
             for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);

@@ -25,6 +25,7 @@ struct TcFwdArgs {
     float cap;
     const int* count;   // active rows (device)
     int* err;           // error word (device)
+    int stall;          // test switch: the producer issues no loads (waits expire)
     int vt_begin, vt_end;  // 256-row vocab tiles covered by this launch
     // softmax epilogue (forward)
     Partial* part;

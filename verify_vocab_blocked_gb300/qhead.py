@@ -21,7 +21,7 @@ QHEAD_SB_F16 = 0
 # Every symbol include/qhead.h declares.
 EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd",
            "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel",
-           "qhead_fwd_noalloc")
+           "qhead_fwd_noalloc", "qhead_test_stall_next_call")
 
 
 class CHead(ctypes.Structure):
@@ -65,10 +65,19 @@ def lib() -> ctypes.CDLL:
     L.qhead_version.restype = ctypes.c_char_p
     L.qhead_time_next_head_kernel.argtypes = [vp, vp]
     L.qhead_time_next_head_kernel.restype = None
+    L.qhead_test_stall_next_call.argtypes = [ctypes.c_int]
+    L.qhead_test_stall_next_call.restype = None
     L.qhead_fwd_noalloc.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp]
     L.qhead_fwd_noalloc.restype = ctypes.c_int
     _lib = L
     return L
+
+
+def test_stall_next_call(armed: bool = True) -> None:
+    """Arm the library's one-shot stall switch on this thread: the next fwd/bwd
+    call's pipelined head kernel gets no loads, its bounded waits expire and
+    the call's active rows come back NaN (argmax -1)."""
+    lib().qhead_test_stall_next_call(1 if armed else 0)
 
 
 def time_next_head_kernel(start: torch.cuda.Event, stop: torch.cuda.Event) -> None:
