@@ -52,22 +52,29 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def _traffic(kernel: str):
-    """ncu DRAM bytes per launch for `kernel`, if recorded for the current source."""
+def source_hash(sources) -> str | None:
+    """sha256 (16 hex digits) of the named csrc files, concatenated in order."""
+    h = hashlib.sha256()
+    for name in sources:
+        src = os.path.join(ROOT, "verify_vocab_blocked_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, workload: str):
+    """ncu DRAM bytes per launch of `kernel` on `workload`, if recorded for the
+    current sources of the kernel (its .cu and the headers it includes)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(kernel)
-    if not e:
+    e = d.get(kernel, {}).get(workload)
+    if not e or source_hash(e["sources"]) != e["sha256_16"]:
         return None
-    src = os.path.join(ROOT, "verify_vocab_blocked_gb300", "csrc", e["source"])
-    if not os.path.exists(src):
-        return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest()[:16] != e["sha256_16"]:
-            return None
     return e
 
 
@@ -184,9 +191,7 @@ class Runner:
         self.out_host = {k: torch.empty_like(v, device="cpu").pin_memory()
                          for k, v in (("lse", self.lse), ("am", self.am), ("logp", self.logp),
                                       ("dh", self.dh)) if v is not None}
-        # fwd: prologue (1 fused launch up to 256 rows, else 2) + head + finalize;
-        # bwd: compact + head + finalize
-        self.launches_per_step = (3 if M <= 256 else 4) + (3 if self.bwd else 0)
+        self.launches_per_step = None  # counted on the device by count_launches()
         self.active = int(wl.mask.sum()) if wl.mask is not None else M
 
     def _ptr(self, t):
@@ -229,6 +234,35 @@ class Runner:
                 self.out_host[k].copy_(dev, non_blocking=True)
                 n += dev.numel() * dev.element_size()
         return n
+
+
+def count_launches(R: Runner) -> tuple[int, dict]:
+    """This library's kernel launches in one step, counted by the CUDA activity
+    profiler (CUPTI) from its exported trace: returns the total and the
+    per-kernel counts."""
+    import re
+    import tempfile
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    # Kernel records appear in the trace only when CPU activity is traced too.
+    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+        R.step()
+        torch.cuda.synchronize()
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "trace.json")
+        prof.export_chrome_trace(path)
+        with open(path) as f:
+            trace = json.load(f)
+    counts: dict = {}
+    for e in trace.get("traceEvents", []):
+        name = e.get("name", "")
+        if e.get("cat") != "kernel" or ("qh::" not in name and "_ZN2qh" not in name):
+            continue
+        m = re.search(r"(\w+_kernel)", name)
+        short = m.group(1) if m else name
+        counts[short] = counts.get(short, 0) + 1
+    return sum(counts.values()), counts
 
 
 def aggregate(elapsed_ms: float, units: float, world: int, dist=None) -> tuple[float, float]:
@@ -297,6 +331,11 @@ def run_ours(args):
     for _ in range(W):
         R.step()
     torch.cuda.synchronize()
+    if args.no_launch_count:
+        n_launch, launch_list = None, {"note": "not counted (--no-launch-count)"}
+    else:
+        n_launch, launch_list = count_launches(R)
+    R.launches_per_step = n_launch
 
     # device-resident timed region
     t0, t1 = mk_ev(), mk_ev()
@@ -336,20 +375,31 @@ def run_ours(args):
 
     hbm, tf_burst, tf_sus, peak_src = _peaks()
     if R.bwd:
-        # dominant kernel: the backward contraction (recompute + dh): 4*Ma*V*H flop
-        dom = "bwd_simt_kernel"
+        # dominant work: the backward head phase (logits recomputed, 2*Ma*V*H,
+        # and the dh contraction, 2*Ma*V*H).  On the tensor-core path (M >= 64)
+        # it is a chain of two kernels per vocab chunk, timed as one region.
+        tc = R.M >= 64
+        dom = "tc_bwd_chain" if tc else "bwd_simt_kernel"
         flops = 4.0 * R.active * cfg["V"] * cfg["H"]
         kms = statistics.mean(bwd_ms)
         achieved = flops / (kms / 1e3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tf_sus,
+        roof = {"kernel": ("tc_fwd_kernel<coefficient epilogue> + tc_dh_kernel per vocab chunk"
+                           if tc else dom),
+                "bound": "tensor", "achieved": achieved, "peak": tf_sus,
                 "unit": "TFLOP/s", "frac": achieved / tf_sus,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (dense, same rate as fp16)",
-                "work_per_launch": f"{flops:.3e} flop (4*Ma*V*H)", "ms_per_launch": kms}
+                "work_per_launch": f"{flops:.3e} flop (4*Ma*V*H, Ma = active rows)",
+                "ms_per_launch": kms}
         fms = statistics.mean(fwd_ms)
         ff = 2.0 * R.active * cfg["V"] * cfg["H"]
-        roof["fwd_kernel"] = {"kernel": "tc_fwd_kernel" if R.M >= 64 else "stream_fwd_kernel",
+        roof["fwd_kernel"] = {"kernel": "tc_fwd_kernel" if tc else "stream_fwd_kernel",
                               "ms_per_launch": fms,
-                              "achieved_tflops": ff / (fms / 1e3) / 1e12}
+                              "achieved_tflops": ff / (fms / 1e3) / 1e12,
+                              "frac": ff / (fms / 1e3) / 1e12 / tf_sus}
+        step_ms = el_max / K
+        roof["step"] = {"flop": 6.0 * R.active * cfg["V"] * cfg["H"], "ms": step_ms,
+                        "achieved_tflops": 6.0 * R.active * cfg["V"] * cfg["H"] / (step_ms / 1e3) / 1e12,
+                        "frac": 6.0 * R.active * cfg["V"] * cfg["H"] / (step_ms / 1e3) / 1e12 / tf_sus}
     else:
         dom = "stream_fwd_kernel"
         nbytes = head_bytes(cfg)
@@ -359,7 +409,7 @@ def run_ours(args):
                 "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                 "work_per_launch": f"{nbytes} bytes (packed head + fp16 scales/biases)",
                 "ms_per_launch": kms}
-    tr = _traffic(dom)
+    tr = _traffic(dom, args.config)
     roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
 
     line = {
@@ -372,7 +422,8 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": units_e / (el_e_max / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": R.launches_per_step * K,
+        "gpu_launches": R.launches_per_step * K if R.launches_per_step is not None else None,
+        "launches_per_step": launch_list,
         "clocks": clk.summary(),
         "impl": "ours",
     }
@@ -444,6 +495,8 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-launch-count", action="store_true",
+                    help="skip the CUPTI launch count (for runs under a profiler)")
     args = ap.parse_args(argv)
     fwd_only = not synth.CONFIGS[args.config]["bwd"]
     if args.steps is None:

@@ -72,8 +72,8 @@ extern "C" {
  *            elements j*(32/bits) + k, k = 0 .. 32/bits - 1, element k in bits
  *            bits*k .. bits*k + bits - 1 (least-significant field first).
  *            16-byte aligned.
- *   scales   device, fp16 [V, H/group], row-major.  2-byte aligned.
- *   biases   device, fp16 [V, H/group], row-major.  2-byte aligned.
+ *   scales   device, fp16 [V, H/group], row-major.  16-byte aligned.
+ *   biases   device, fp16 [V, H/group], row-major.  16-byte aligned.
  *   V        vocab rows, 1 <= V < 2^31.
  *   H        hidden size: a multiple of 128, 128 <= H <= 8192.
  *   bits     4 or 8.

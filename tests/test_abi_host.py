@@ -72,6 +72,8 @@ def _fwd(L, head, **kw):
     (dict(V=1 << 31), qhead.QHEAD_EINVAL),
     (dict(wq=0x10004), qhead.QHEAD_EINVAL),
     (dict(scales=0x20001), qhead.QHEAD_EINVAL),
+    (dict(scales=0x20002), qhead.QHEAD_EINVAL),
+    (dict(biases=0x30008), qhead.QHEAD_EINVAL),
     (dict(wq=None), qhead.QHEAD_EINVAL),
     (dict(biases=None), qhead.QHEAD_EINVAL),
     (dict(softcap=float("nan")), qhead.QHEAD_EINVAL),

@@ -9,7 +9,10 @@
 //                    masked rows).
 #include <stdio.h>
 
+#include <map>
+#include <mutex>
 #include <string>
+#include <utility>
 
 #include "../../include/qhead.h"
 #include "qh_internal.cuh"
@@ -49,12 +52,8 @@ struct DevInfo {
 };
 
 int device_info(DevInfo* info) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(QHEAD_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
-    e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess)
-        return fail(QHEAD_ECUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    info->sms = qh::device_sms();
+    if (info->sms <= 0) return fail(QHEAD_ECUDA, "cannot query the current device's SM count");
     return QHEAD_OK;
 }
 
@@ -68,8 +67,8 @@ int check_head(const qhead_head* hd) {
         return fail(QHEAD_EUNSUPPORTED, "H must be a multiple of 128 in [128, 8192]");
     if (hd->V < 1 || hd->V >= ((int64_t)1 << 31)) return fail(QHEAD_EINVAL, "V must be in [1, 2^31)");
     if (reinterpret_cast<uintptr_t>(hd->wq) % 16) return fail(QHEAD_EINVAL, "wq must be 16-byte aligned");
-    if (reinterpret_cast<uintptr_t>(hd->scales) % 2 || reinterpret_cast<uintptr_t>(hd->biases) % 2)
-        return fail(QHEAD_EINVAL, "scales/biases must be 2-byte aligned");
+    if (reinterpret_cast<uintptr_t>(hd->scales) % 16 || reinterpret_cast<uintptr_t>(hd->biases) % 16)
+        return fail(QHEAD_EINVAL, "scales/biases must be 16-byte aligned");
     if (hd->softcap != hd->softcap) return fail(QHEAD_EINVAL, "softcap is NaN");
     return QHEAD_OK;
 }
@@ -421,3 +420,37 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
 }
 
 }  // extern "C"
+
+namespace qh {
+
+namespace {
+std::mutex g_cache_mu;
+std::map<std::pair<const void*, int>, int> g_smem_limit;  // (kernel, device) -> bytes allowed
+std::map<int, int> g_sms;                                 // device -> SM count
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void* func, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    int& allowed = g_smem_limit[{func, dev}];
+    if (allowed >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) allowed = bytes;
+    return e;
+}
+
+int device_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+    return n;
+}
+
+}  // namespace qh

@@ -148,8 +148,9 @@ cudaError_t launch_t(const uint32_t* wq, const __half* scales, const __half* bia
                      const int* count, const float* lse, const float* dlogp, float* dhp, int S,
                      int64_t M, int64_t Mpad, cudaStream_t st) {
     const size_t smem = (size_t)TB * H * 2 + (size_t)kThreads * TB * sizeof(float);
-    cudaFuncSetAttribute(bwd_simt_kernel<TB, DPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
+    if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(bwd_simt_kernel<TB, DPT>),
+                                          (int)smem))
+        return e;
     dim3 grid((unsigned)((M + TB - 1) / TB), S);
     bwd_simt_kernel<TB, DPT><<<grid, kThreads, smem, st>>>(wq, scales, biases, V, H, bits, cap, h,
                                                             rows, count, lse, dlogp, dhp, S, Mpad);

@@ -178,6 +178,13 @@ cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const 
                                 const float* dhp, int S, int64_t Mpad, const int* err, float* dh,
                                 int64_t M, cudaStream_t st);
 
+// Host-side caches (thread-safe).  ensure_smem_limit raises a kernel's dynamic
+// shared-memory limit on the current device once, skipping the runtime call
+// when the device already allows `bytes`; device_sms returns the current
+// device's SM count (0 on error).
+cudaError_t ensure_smem_limit(const void* func, int bytes);
+int device_sms();
+
 int bwd_simt_tokens(int H);                   // tokens per CTA of the SIMT backward
 int stream_fwd_ctas_per_sm(int bits, int H);  // occupancy of the weight-streaming kernel
 

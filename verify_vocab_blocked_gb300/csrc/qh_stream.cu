@@ -26,6 +26,10 @@
 //   8-bit: prmt builds (1024 + q_0, 1024 + q_1) and (1024 + q_2, 1024 + q_3).
 // then w = fma(q, scale, bias) in fp16 (one rounding) after an exact
 // subtraction of 1024.  The row's logits never leave registers.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "qh_dequant.cuh"
 #include "qh_tc.cuh"
 #include "qh_tmap.h"
@@ -266,17 +270,25 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
 }  // namespace
 
 int stream_fwd_ctas_per_sm(int bits, int H) {
-    const int smem = StreamSmem(H).total;
-    int n = 0;
-    cudaError_t e;
-    if (bits == 4) {
-        cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stream_fwd_kernel<4>, kThreads, smem);
-    } else {
-        cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stream_fwd_kernel<8>, kThreads, smem);
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, int> cache;  // (device, bits, H) -> CTAs per SM
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find({dev, bits, H});
+        if (it != cache.end()) return it->second;
     }
-    return (e == cudaSuccess && n > 0) ? n : 1;
+    const int smem = StreamSmem(H).total;
+    const void* fn = bits == 4 ? reinterpret_cast<const void*>(stream_fwd_kernel<4>)
+                               : reinterpret_cast<const void*>(stream_fwd_kernel<8>);
+    int n = 0;
+    cudaError_t e = ensure_smem_limit(fn, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem);
+    n = (e == cudaSuccess && n > 0) ? n : 1;
+    std::lock_guard<std::mutex> lock(mu);
+    cache[{dev, bits, H}] = n;
+    return n;
 }
 
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
@@ -290,11 +302,13 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
     const int smem = StreamSmem(H).total;
     dim3 grid(groups, S);
     if (bits == 4) {
-        cudaFuncSetAttribute(stream_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream_fwd_kernel<4>), smem))
+            return e;
         stream_fwd_kernel<4><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
                                                            count, part, S, err, stall);
     } else {
-        cudaFuncSetAttribute(stream_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream_fwd_kernel<8>), smem))
+            return e;
         stream_fwd_kernel<8><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
                                                            count, part, S, err, stall);
     }

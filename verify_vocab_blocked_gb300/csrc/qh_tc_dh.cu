@@ -339,8 +339,9 @@ template <int BITS, int BNH>
 cudaError_t launch_t(const CUtensorMap& tc_map, const CUtensorMap& tw, const TcDhArgs& a, int grid,
                      cudaStream_t st) {
     using L = DhLayout<BITS, BNH>;
-    cudaFuncSetAttribute(tc_dh_kernel<BITS, BNH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         L::SMEM);
+    if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_dh_kernel<BITS, BNH>),
+                                          L::SMEM))
+        return e;
     tc_dh_kernel<BITS, BNH><<<grid, kThreads, L::SMEM, st>>>(tc_map, tw, a);
     return cudaGetLastError();
 }

@@ -425,8 +425,9 @@ int tc_fwd_smem_bytes(int bits) { return bits == 4 ? Layout<4>::SMEM : Layout<8>
 template <int BITS, int EPI>
 static cudaError_t launch_t(const CUtensorMap& th, const CUtensorMap& tw, const TcFwdArgs& a,
                             int grid, cudaStream_t st) {
-    cudaFuncSetAttribute(tc_fwd_kernel<BITS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Layout<BITS>::SMEM);
+    if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_fwd_kernel<BITS, EPI>),
+                                          Layout<BITS>::SMEM))
+        return e;
     tc_fwd_kernel<BITS, EPI><<<grid, kThreads, Layout<BITS>::SMEM, st>>>(th, tw, a);
     return cudaGetLastError();
 }
