@@ -244,11 +244,18 @@ def count_launches(R: Runner) -> tuple[int, dict]:
     import tempfile
     import torch
     from torch.profiler import ProfilerActivity, profile
+    from torch.profiler import record_function
     torch.cuda.synchronize()
-    # Kernel records appear in the trace only when CPU activity is traced too.
-    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-        R.step()
+    # Kernel records appear in the trace only when CPU activity is traced too;
+    # the step itself is a CPU range so the trace has a parent for them.
+    # The first profiling session of a process records no device activity
+    # (the activity tracer attaches lazily): open and discard one first.
+    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]):
         torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+        with record_function("qhead_step"):
+            R.step()
+            torch.cuda.synchronize()
     with tempfile.TemporaryDirectory() as d:
         path = os.path.join(d, "trace.json")
         prof.export_chrome_trace(path)
@@ -262,6 +269,12 @@ def count_launches(R: Runner) -> tuple[int, dict]:
         m = re.search(r"(\w+_kernel)", name)
         short = m.group(1) if m else name
         counts[short] = counts.get(short, 0) + 1
+    if not counts:
+        cats: dict = {}
+        for e in trace.get("traceEvents", []):
+            cats[str(e.get("cat"))] = cats.get(str(e.get("cat")), 0) + 1
+        return None, {"note": "no kernel of this library in the CUDA activity trace",
+                      "trace_categories": cats}
     return sum(counts.values()), counts
 
 

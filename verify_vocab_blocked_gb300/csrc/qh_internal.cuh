@@ -155,13 +155,14 @@ cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* ro
 constexpr int64_t kFusedPrologueMaxM = 256;
 cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
                                   int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
-                                  __half* h16, int64_t nrows, int* err, cudaStream_t st);
+                                  __half* h16, int64_t nrows, int* err, float* negc, __half2* hsx,
+                                  int stat_rows, cudaStream_t st);
 cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
                              const int* count, __half* h16, cudaStream_t st);
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
                               int64_t V, int H, int bits, float cap, const __half* h16,
-                              const int* count, int64_t M, Partial* part, int S, int* err,
-                              int stall, cudaStream_t st);
+                              const int* count, const float* negc, const __half2* hsx, int64_t M,
+                              Partial* part, int S, int* err, int stall, cudaStream_t st);
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,

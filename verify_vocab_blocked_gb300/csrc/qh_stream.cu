@@ -1,5 +1,6 @@
 // qh_stream.cu -- weight-streaming forward (steps a2-a5 and a8 of the hot path
-// for small M; also the general path until the tcgen05 kernel takes large M).
+// for small M, where the tensor-core kernel's 128-row tiles would be mostly
+// empty).
 //
 // What it computes: for 8 compacted rows of h and a slice of the vocab, the
 // per-row online-softmax partial (max z, sum exp(z - max)) and the two best
@@ -10,22 +11,32 @@
 // candidates the speculative-decode verify needs (page "mlx-bun 0.0.8 ->
 // 0.0.10", src/spec/generate.ts, picksBatched).
 //
-// How (GB300): at M = gamma+1 the cost is reading the packed head once, but
-// plain fp32 FMAs cannot keep up with HBM (10 FMA per packed byte at M = 5).
+// How (GB300): at M = gamma+1 the cost is reading the packed head once, and
+// the limit is the instruction issue rate, not the arithmetic: a per-element
+// dequantization (w = s q + b) costs more issue slots than HBM leaves.  So the
+// affine map is factored out of the inner product, per 64-element group g:
+//     sum_k (s q_k + b) h_k = s (sum_k (M_k + q_k) h_k - sum_k M_k h_k) + b sum_k h_k
+// The tensor core multiplies the codes still carrying their magic-exponent
+// offset M_k (one lop3 per code pair, nothing else per element), the group's
+// fp32 accumulator starts at -sum_k M_k h_k so the offset cancels inside it,
+// one FFMA per accumulator applies s, and b sum_k h_k is a small MMA per tile
+// (fp16 biases x an fp16 hi/lo split of the group sums of h).  The group sums
+// come from the prologue, computed from the same fp16 h.  w itself is never
+// rounded to fp16.
+//
 // A producer warp streams the CTA's vocab range through shared memory with
 // TMA (128 rows x 16 packed words per stage, 6 stages) and copies each
-// stage's scales and biases with cp.async; eight consumer warps each take 16
-// of the 128 rows, dequantize them in registers into the A fragments of
-// mma.sync.m16n8k16 (A = 16 vocab rows x 16 K, B = 16 K x 8 tokens, fp32
-// accumulate), and never stage the dequantized head anywhere.  The K axis is
-// permuted consistently in A and B so that one packed word yields A fragments
-// with one shift + lop3 per pair of codes (4-bit), or one prmt per pair (8-bit):
-//   4-bit: word j of a row holds d = 8j .. 8j+7; lop3((w >> 4k) & 0x000F000F |
-//          0x64006400) = fp16 pair (1024 + q_k, 1024 + q_k+4); the staged h
-//          rows store each 8-block as (0,4,1,5,2,6,3,7).
+// stage's scales with cp.async; eight consumer warps each take 16 of the 128
+// rows as the A operand of mma.sync.m16n8k16 (A = 16 vocab rows x 16 K,
+// B = 16 K x 8 tokens, fp32 accumulate).  Every mma covers one group: a
+// thread's codes for one mma come from one packed word, and the four threads
+// of a quad take adjacent words of the same group.
+//   4-bit: word j of a row holds d = 8j .. 8j+7; lop3((w >> 8i) & 0x000F000F |
+//          0x64006400) = fp16 pair (1024 + q_k, 1024 + q_k+4) (k even) and
+//          (w >> 8i) & 0x00F000F0 | 0x54005400 = (64 + q_k, 64 + q_k+4) (k odd);
+//          the staged h rows store each 8-block as (0,4,1,5,2,6,3,7).
 //   8-bit: prmt builds (1024 + q_0, 1024 + q_1) and (1024 + q_2, 1024 + q_3).
-// then w = fma(q, scale, bias) in fp16 (one rounding) after an exact
-// subtraction of 1024.  The row's logits never leave registers.
+// The row's logits never leave registers.
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -38,14 +49,29 @@ namespace qh {
 
 namespace {
 
-constexpr int kConsumers = 8;                 // consumer warps, 16 rows each
+constexpr int kConsumers = 16;                // consumer warps, 16 rows each
 constexpr int kThreads = 32 * (1 + kConsumers);
 constexpr int kTile = 16 * kConsumers;        // vocab rows per stage
-constexpr int kChunkWords = 16;               // packed words per row per stage
-constexpr int kPBytes = kTile * kChunkWords * 4;
-constexpr int kSBBytes = kTile * 2 * 4;       // per row: 2 scales + 2 biases (fp16)
-constexpr int kStages = 6;
+constexpr int kStageWords = 32;               // packed words per row per stage (128 bytes)
+constexpr int kPBytes = kTile * kStageWords * 4;
+constexpr int kSBytes = kTile * 8;            // per row: the stage's group scales (up to 4, fp16)
+constexpr int kMaxStages = 6;
+// Dynamic shared memory of one CTA: 227 KB less the static reduction buffer.
+constexpr int kSmemLimit = 227 * 1024 - kConsumers * kTokGroup * (int)sizeof(Partial);
 
+// D = A B + C with C given separately (starts a group's accumulator).
+__device__ __forceinline__ void mma16816_init(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1, float c0,
+                                              float c1, float c2, float c3) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
+          "f"(c3));
+}
+
+// C += A B.
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -55,79 +81,85 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t u4_at(const uint4& v, int j) {
-    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+// The eight 4-bit codes of one word with their magic offsets, as fp16 pairs:
+// p[0] = (1024 + q0, 1024 + q4), p[1] = (64 + q1, 64 + q5),
+// p[2] = (1024 + q2, 1024 + q6), p[3] = (64 + q3, 64 + q7).
+__device__ __forceinline__ void codes4(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t w8 = w >> 8;
+    p[0] = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+    p[1] = lop3_and_or(w, 0x00F000F0u, 0x54005400u);
+    p[2] = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);
+    p[3] = lop3_and_or(w8, 0x00F000F0u, 0x54005400u);
 }
 
-// One chunk = 16 packed words of a row (128 elements at 4 bits, 64 at 8 bits).
-// Thread (g, t) owns words 4t .. 4t+3 of the chunk for rows g and g+8.
-// hblk: the chunk's block of the staged h row of token g.  For 4-bit heads the
-// staged rows are swizzled: 16-byte chunk k of each 128-element block sits at
-// position k ^ (2 * (k >> 3)), so the four threads of a quad (reading at a
-// 64-byte stride) hit distinct bank groups.
+// Two 8-bit codes of w with offset 1024: sel 0x5140 -> bytes 0, 1; 0x7362 -> 2, 3.
+__device__ __forceinline__ uint32_t codes8(uint32_t w, uint32_t sel) {
+    return __byte_perm(w, 0x64646464u, sel);
+}
+
+// Groups per stage, padded hidden size (whole stages; the pad is zero) and
+// padded group count of the shared-memory tables.
 template <int BITS>
-__device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& a0, const uint4& a1,
-                                          uint32_t s0, uint32_t b0, uint32_t s1, uint32_t b1,
-                                          const __half* hblk, int t) {
-    if constexpr (BITS == 4) {
-        const int sw = 2 * (t >> 1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 bq = *reinterpret_cast<const uint4*>(hblk + 8 * ((4 * t + j) ^ sw));
-            uint32_t p0[4], p1[4];
-            deq4_word(u4_at(a0, j), s0, b0, p0);
-            deq4_word(u4_at(a1, j), s1, b1, p1);
-            // step e = 0 uses pairs (0,4) and (1,5); e = 1 uses (2,6) and (3,7)
-            mma16816(acc, p0[0], p1[0], p0[1], p1[1], bq.x, bq.y);
-            mma16816(acc, p0[2], p1[2], p0[3], p1[3], bq.z, bq.w);
-        }
-    } else {
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-            const uint4 bq = *reinterpret_cast<const uint4*>(hblk + 16 * t + 8 * jj);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const uint32_t w0 = u4_at(a0, 2 * jj + e), w1 = u4_at(a1, 2 * jj + e);
-                const uint32_t A0 = deq8(w0, 0x5140u, s0, b0);
-                const uint32_t A2 = deq8(w0, 0x7362u, s0, b0);
-                const uint32_t A1 = deq8(w1, 0x5140u, s1, b1);
-                const uint32_t A3 = deq8(w1, 0x7362u, s1, b1);
-                mma16816(acc, A0, A1, A2, A3, e ? bq.z : bq.x, e ? bq.w : bq.y);
-            }
-        }
-    }
-}
+struct StreamShape {
+    static constexpr int kGroupsPerStage = kStageWords * 32 / BITS / 64;  // 4 (4-bit) or 2 (8-bit)
+    static constexpr int kStagesPerKb = 16 / kGroupsPerStage;             // stages per 16 groups
+};
 
-// Shared memory: [h rows: 8 x (H + 8) halves] [packed ring] [scale/bias ring] [barriers]
+// Shared memory (1024-byte aligned base): [packed ring: stages x 32 KB, 128B
+// swizzle] [scale ring] [h rows: 8 x (Hp + 8) halves] [negc: Gs x 8 fp32]
+// [hsum hi: 8 x gp fp16] [hsum lo: 8 x gp fp16] [barriers].  One CTA per SM:
+// the stage count is the largest that fits (more bytes in flight per SM).
 struct StreamSmem {
-    int off_p, off_sb, off_bar, total;
-    __host__ __device__ StreamSmem(int H) {
-        const int hbytes = kTokGroup * (H + 8) * 2;
-        off_p = (hbytes + 127) / 128 * 128;
-        off_sb = off_p + kStages * kPBytes;
-        off_bar = off_sb + kStages * kSBBytes;
-        total = off_bar + 8 * 2 * kStages + 16;
+    int stages, Hp, Gs, gp, off_s, off_h, off_negc, off_hs, off_bar, total;
+    __host__ __device__ StreamSmem(int H, int bits, int n_stages) {
+        const int per_stage = kStageWords * 32 / bits;      // hidden elements per stage
+        Hp = (H + per_stage - 1) / per_stage * per_stage;
+        Gs = Hp / 64;
+        gp = (H / 64 + 15) / 16 * 16;  // groups padded to whole 16-wide k-blocks
+        stages = n_stages;
+        off_s = stages * kPBytes;
+        off_h = off_s + stages * kSBytes;
+        off_negc = off_h + (kTokGroup * (Hp + 8) * 2 + 15) / 16 * 16;
+        off_hs = off_negc + Gs * kTokGroup * 4;
+        off_bar = (off_hs + 2 * kTokGroup * gp * 2 + 7) / 8 * 8;
+        total = off_bar + 8 * 2 * stages + 16 + 1024;  // + alignment slack of the base
     }
 };
 
+// The deepest ring that fits next to the staged h rows (0 if not even two).
+int stream_stages(int H, int bits) {
+    for (int s = kMaxStages; s >= 2; --s)
+        if (StreamSmem(H, bits, s).total <= kSmemLimit) return s;
+    return 0;
+}
+
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
+__global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_w, const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, float cap,
-    const __half* __restrict__ h16, const int* __restrict__ count, Partial* __restrict__ part,
-    int S, int* __restrict__ err, int stall) {
+    const __half* __restrict__ h16, const float* __restrict__ negc_g,
+    const __half2* __restrict__ hsx_g, const int* __restrict__ count, Partial* __restrict__ part,
+    int S, int* __restrict__ err, int stall, int n_stages) {
+    using Shape = StreamShape<BITS>;
     const int n_active = *count;
     const int tok0 = blockIdx.x * kTokGroup;
     if (tok0 >= n_active) return;
     const int split = blockIdx.y;
 
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    const StreamSmem L(H);
-    __half* hs = reinterpret_cast<__half*>(smem_raw);
-    const int hstride = H + 8;  // halves; +16 bytes per row spreads the banks
-    unsigned char* pring = smem_raw + L.off_p;
-    unsigned char* sbring = smem_raw + L.off_sb;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.off_bar);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    // (offsetting the shared array itself keeps the accesses in the shared
+    // address space; a round trip through an integer would make them generic)
+    const StreamSmem L(H, BITS, n_stages);
+    const int kStages = L.stages;
+    unsigned char* pring = smem;
+    unsigned char* sring = smem + L.off_s;
+    __half* hs = reinterpret_cast<__half*>(smem + L.off_h);
+    const int hstride = L.Hp + 8;  // halves; +16 bytes per row spreads the banks
+    float* negc_s = reinterpret_cast<float*>(smem + L.off_negc);
+    __half* hs_hi = reinterpret_cast<__half*>(smem + L.off_hs);
+    __half* hs_lo = hs_hi + kTokGroup * L.gp;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
     uint64_t* empty = full + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
     __shared__ Partial red[kConsumers][kTokGroup];
@@ -135,10 +167,9 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t cta_v0 = V * split / S, cta_v1 = V * (split + 1) / S;
     const int ntiles = (int)((cta_v1 - cta_v0 + kTile - 1) / kTile);
-    const int wpr = H * BITS / 32;
     const int G = H / 64;
-    const int nchunks = wpr / kChunkWords;
-    const int nitems = ntiles * nchunks;
+    const int nst = L.Gs / Shape::kGroupsPerStage;  // stages per tile
+    const int nitems = ntiles * nst;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -157,29 +188,32 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
         uint32_t phase = 0, fills = 0;
         bool ok = stall == 0;  // test switch: issue no loads, the consumers' waits expire
         for (int k = 0; k < nitems && ok; ++k) {
-            const int tile = k / nchunks, c = k - tile * nchunks;
+            const int tile = k / nst, c = k - tile * nst;
             const int64_t row0 = cta_v0 + (int64_t)tile * kTile;
             if (lane == 0)
                 ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, tc::kErrTimeoutEmpty);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) {
+                // Words past the row end (4-bit, H not a multiple of 256) read as zero.
                 tc::mbar_arrive_expect_tx(&full[stage], kPBytes);
-                tc::tma_load_2d(pring + stage * kPBytes, &tmap_w, &full[stage], kChunkWords * c,
+                tc::tma_load_2d(pring + stage * kPBytes, &tmap_w, &full[stage], kStageWords * c,
                                 (int)row0);
             }
-            // Scales and biases of the stage: 2 consecutive groups per row (the
-            // chunk's two groups at 4 bits; chunks c and c^1 at 8 bits).
-            const int g0 = BITS == 4 ? 2 * c : (c & ~1);
-            unsigned char* sb = sbring + stage * kSBBytes;
+            // The stage's scales, two groups per 4-byte copy (zeros past G or V).
+            const int g0 = Shape::kGroupsPerStage * c;
+            unsigned char* sd = sring + stage * kSBytes;
 #pragma unroll
             for (int i = 0; i < kTile / 32; ++i) {
                 const int r = lane + 32 * i;
                 const int64_t v = row0 + r;
-                const int64_t gi = (v < V ? v : 0) * G + g0;
-                const int nbytes = v < V ? 4 : 0;
-                tc::cp_async_zfill<4>(sb + 4 * r, scales + gi, nbytes);
-                tc::cp_async_zfill<4>(sb + 4 * (kTile + r), biases + gi, nbytes);
+                const int64_t vb = (v < V ? v : 0) * G;
+#pragma unroll
+                for (int q = 0; q < Shape::kGroupsPerStage / 2; ++q) {
+                    const int gq = g0 + 2 * q;
+                    tc::cp_async_zfill<4>(sd + 8 * r + 4 * q, scales + vb + (gq < G ? gq : 0),
+                                          v < V && gq < G ? 4 : 0);
+                }
             }
             tc::cp_async_arrive(&full[stage]);
             ++fills;
@@ -192,24 +226,37 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
         // ---------------------------------------------------------------- consumers
         const int cw = warp - 1;
         const int g = lane >> 2, t = lane & 3;
-        // Stage the group's 8 rows of h (fp16, K-permuted for 4-bit), consumers only.
-        const int units = H / 8;
-        for (int idx = threadIdx.x - 32; idx < kTokGroup * units; idx += 32 * kConsumers) {
+        const int ct = threadIdx.x - 32;
+        // Stage the group's 8 rows of h (fp16, K-permuted for 4-bit; zeros in
+        // [H, Hp)) and their group statistics, consumers only.
+        const int units = L.Hp / 8;
+        for (int idx = ct; idx < kTokGroup * units; idx += 32 * kConsumers) {
             const int r = idx / units, cc = idx - r * units;
-            const uint4 v = *reinterpret_cast<const uint4*>(h16 + (int64_t)(tok0 + r) * H + 8 * cc);
-            int pos = cc;
-            if (BITS == 4) {
-                const int k = cc & 15;
-                pos = (cc & ~15) | (k ^ (2 * (k >> 3)));
-            }
-            *reinterpret_cast<uint4*>(hs + r * hstride + 8 * pos) = v;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (8 * cc < H) v = *reinterpret_cast<const uint4*>(h16 + (int64_t)(tok0 + r) * H + 8 * cc);
+            *reinterpret_cast<uint4*>(hs + r * hstride + 8 * cc) = v;
+        }
+        for (int idx = ct; idx < kTokGroup * L.Gs; idx += 32 * kConsumers) {
+            const int gg = idx / kTokGroup, r = idx - gg * kTokGroup;
+            negc_s[idx] = gg < G ? negc_g[(int64_t)(tok0 + r) * G + gg] : 0.f;
+        }
+        for (int idx = ct; idx < kTokGroup * L.gp; idx += 32 * kConsumers) {
+            const int r = idx / L.gp, gg = idx - r * L.gp;
+            __half2 x = __halves2half2(__float2half(0.f), __float2half(0.f));
+            if (gg < G) x = hsx_g[(int64_t)(tok0 + r) * G + gg];
+            hs_hi[idx] = __low2half(x);
+            hs_lo[idx] = __high2half(x);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
         const __half* hrow = hs + g * hstride;
-        constexpr int kChunkHalves = BITS == 4 ? 128 : 64;
-        const int ra = 16 * cw + g, rb = ra + 8;  // rows of this thread within a tile
-        // which of the stage's two groups this thread uses
-        const int gsel_fixed = t >> 1;
+        // Physical rows of this thread's A-fragment rows g and g + 8, chosen so
+        // that the packed loads of a quarter- (8-bit) or half-warp (4-bit) hit
+        // distinct 16-byte chunks under the 128-byte swizzle.
+        const int ra = BITS == 4 ? 16 * cw + 2 * g : 16 * cw + (g >> 1) + 4 * (g & 1);
+        const int rb = BITS == 4 ? ra + 1 : ra + 8;
+        const int xa = ra & 7, xb = rb & 7;  // swizzle keys
+        const int nkb = L.gp / 16;
+        constexpr int kPer = Shape::kStagesPerKb;
 
         RowState st[2];
         st[0].init();
@@ -217,33 +264,115 @@ __global__ void __launch_bounds__(kThreads, 2) stream_fwd_kernel(
         int stage = 0;
         uint32_t phase = 0;
         for (int tile = 0; tile < ntiles; ++tile) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int c = 0; c < nchunks; ++c) {
+            const int64_t va = cta_v0 + (int64_t)tile * kTile + ra;
+            const int64_t vb = cta_v0 + (int64_t)tile * kTile + rb;
+            // tot: (row ra, tok 2t), (row ra, tok 2t+1), (row rb, tok 2t), (row rb, tok 2t+1)
+            float tot[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t bA[4] = {0u, 0u, 0u, 0u};  // biases of the pending k-block (A fragment)
+            // sum_g b[v, g] hsum[tok, g] for k-block kb: fp16 biases x (hi + lo) sums.
+            auto load_bias = [&](int kb) {
+                const int k0 = 16 * kb + 2 * t;
+                const bool oa = va < cta_v1, ob = vb < cta_v1;
+                bA[0] = oa && k0 < G ? *reinterpret_cast<const uint32_t*>(biases + va * G + k0) : 0u;
+                bA[1] = ob && k0 < G ? *reinterpret_cast<const uint32_t*>(biases + vb * G + k0) : 0u;
+                bA[2] = oa && k0 + 8 < G ? *reinterpret_cast<const uint32_t*>(biases + va * G + k0 + 8) : 0u;
+                bA[3] = ob && k0 + 8 < G ? *reinterpret_cast<const uint32_t*>(biases + vb * G + k0 + 8) : 0u;
+            };
+            auto bias_mma = [&](int kb) {
+                const int k0 = g * L.gp + 16 * kb + 2 * t;
+                mma16816(tot, bA[0], bA[1], bA[2], bA[3],
+                         *reinterpret_cast<const uint32_t*>(hs_hi + k0),
+                         *reinterpret_cast<const uint32_t*>(hs_hi + k0 + 8));
+                mma16816(tot, bA[0], bA[1], bA[2], bA[3],
+                         *reinterpret_cast<const uint32_t*>(hs_lo + k0),
+                         *reinterpret_cast<const uint32_t*>(hs_lo + k0 + 8));
+            };
+            for (int c = 0; c < nst; ++c) {
+                if (c % kPer == 0) load_bias(c / kPer);
+                if (c % kPer == kPer / 2) bias_mma(c / kPer);
                 // Result ignored: the warp stays converged (see the abort policy).
                 tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
                 const unsigned char* P = pring + stage * kPBytes;
-                const uint4 a0 = *reinterpret_cast<const uint4*>(P + ra * 64 + 16 * t);
-                const uint4 a1 = *reinterpret_cast<const uint4*>(P + rb * 64 + 16 * t);
-                const __half* sbh = reinterpret_cast<const __half*>(sbring + stage * kSBBytes);
-                const int gsel = BITS == 4 ? gsel_fixed : (c & 1);
-                const uint32_t s0 = bcast_h(sbh[2 * ra + gsel]);
-                const uint32_t s1 = bcast_h(sbh[2 * rb + gsel]);
-                const uint32_t b0 = bcast_h(sbh[2 * (kTile + ra) + gsel]);
-                const uint32_t b1 = bcast_h(sbh[2 * (kTile + rb) + gsel]);
-                chunk_mma<BITS>(acc, a0, a1, s0, b0, s1, b1, hrow + kChunkHalves * c, t);
+                const unsigned char* Sst = sring + stage * kSBytes;
+                const uint2 sa2 = *reinterpret_cast<const uint2*>(Sst + 8 * ra);
+                const uint2 sb2 = *reinterpret_cast<const uint2*>(Sst + 8 * rb);
+                const float* ncs = negc_s + Shape::kGroupsPerStage * c * kTokGroup + 2 * t;
+                if constexpr (BITS == 4) {
+                    const float2 sa01 = __half22float2(u32_as_h2(sa2.x)), sa23 = __half22float2(u32_as_h2(sa2.y));
+                    const float2 sb01 = __half22float2(u32_as_h2(sb2.x)), sb23 = __half22float2(u32_as_h2(sb2.y));
+                    const __half* hst = hrow + (kStageWords * c + 2 * t) * 8;
+#pragma unroll 2
+                    for (int gm = 0; gm < 4; ++gm) {  // the stage's four groups
+                        // words 8 gm + 2t, +1: 16-byte chunk 2 gm + (t >> 1), swizzled by row
+                        const int j = 2 * gm + (t >> 1);
+                        const uint2 wa = *reinterpret_cast<const uint2*>(
+                            P + ra * 128 + ((j ^ xa) << 4) + 8 * (t & 1));
+                        const uint2 wb = *reinterpret_cast<const uint2*>(
+                            P + rb * 128 + ((j ^ xb) << 4) + 8 * (t & 1));
+                        const float2 nc = *reinterpret_cast<const float2*>(ncs + gm * kTokGroup);
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(hst + 64 * gm);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(hst + 64 * gm + 8);
+                        uint32_t pa[4], pb[4];
+                        float acc[4];
+                        codes4(wa.x, pa);
+                        codes4(wb.x, pb);
+                        mma16816_init(acc, pa[0], pb[0], pa[1], pb[1], q0.x, q0.y, nc.x, nc.y, nc.x,
+                                      nc.y);
+                        mma16816(acc, pa[2], pb[2], pa[3], pb[3], q0.z, q0.w);
+                        codes4(wa.y, pa);
+                        codes4(wb.y, pb);
+                        mma16816(acc, pa[0], pb[0], pa[1], pb[1], q1.x, q1.y);
+                        mma16816(acc, pa[2], pb[2], pa[3], pb[3], q1.z, q1.w);
+                        const float s_a = gm == 0 ? sa01.x : gm == 1 ? sa01.y : gm == 2 ? sa23.x : sa23.y;
+                        const float s_b = gm == 0 ? sb01.x : gm == 1 ? sb01.y : gm == 2 ? sb23.x : sb23.y;
+                        tot[0] = fmaf(s_a, acc[0], tot[0]);
+                        tot[1] = fmaf(s_a, acc[1], tot[1]);
+                        tot[2] = fmaf(s_b, acc[2], tot[2]);
+                        tot[3] = fmaf(s_b, acc[3], tot[3]);
+                    }
+                } else {
+                    const float2 sa01 = __half22float2(u32_as_h2(sa2.x));
+                    const float2 sb01 = __half22float2(u32_as_h2(sb2.x));
+                    const __half* hst = hrow + (kStageWords * c) * 4 + 16 * t;
+#pragma unroll 1
+                    for (int gm = 0; gm < 2; ++gm) {  // the stage's two groups
+                        // words 16 gm + 4t .. +3: 16-byte chunk 4 gm + t, swizzled by row
+                        const int j = 4 * gm + t;
+                        const uint4 wa = *reinterpret_cast<const uint4*>(P + ra * 128 + ((j ^ xa) << 4));
+                        const uint4 wb = *reinterpret_cast<const uint4*>(P + rb * 128 + ((j ^ xb) << 4));
+                        const float2 nc = *reinterpret_cast<const float2*>(ncs + gm * kTokGroup);
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(hst + 64 * gm);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(hst + 64 * gm + 8);
+                        float acc[4];
+                        mma16816_init(acc, codes8(wa.x, 0x5140u), codes8(wb.x, 0x5140u),
+                                      codes8(wa.x, 0x7362u), codes8(wb.x, 0x7362u), q0.x, q0.y, nc.x,
+                                      nc.y, nc.x, nc.y);
+                        mma16816(acc, codes8(wa.y, 0x5140u), codes8(wb.y, 0x5140u),
+                                 codes8(wa.y, 0x7362u), codes8(wb.y, 0x7362u), q0.z, q0.w);
+                        mma16816(acc, codes8(wa.z, 0x5140u), codes8(wb.z, 0x5140u),
+                                 codes8(wa.z, 0x7362u), codes8(wb.z, 0x7362u), q1.x, q1.y);
+                        mma16816(acc, codes8(wa.w, 0x5140u), codes8(wb.w, 0x5140u),
+                                 codes8(wa.w, 0x7362u), codes8(wb.w, 0x7362u), q1.z, q1.w);
+                        const float s_a = gm ? sa01.y : sa01.x, s_b = gm ? sb01.y : sb01.x;
+                        tot[0] = fmaf(s_a, acc[0], tot[0]);
+                        tot[1] = fmaf(s_a, acc[1], tot[1]);
+                        tot[2] = fmaf(s_b, acc[2], tot[2]);
+                        tot[3] = fmaf(s_b, acc[3], tot[3]);
+                    }
+                }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&empty[stage]);
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
-            // acc: (row ra, tok 2t), (row ra, tok 2t+1), (row rb, tok 2t), (row rb, tok 2t+1)
-            const int64_t v0 = cta_v0 + (int64_t)tile * kTile + ra, v1 = v0 + 8;
-            if (v0 < cta_v1) {
-                st[0].push(softcap_exact(acc[0], cap), acc[0], (int)v0);
-                st[1].push(softcap_exact(acc[1], cap), acc[1], (int)v0);
+            // The last k-block's bias product, if its slot fell past the stages.
+            if (kPer * (nkb - 1) + kPer / 2 >= nst) bias_mma(nkb - 1);
+            if (va < cta_v1) {
+                st[0].push(softcap_exact(tot[0], cap), tot[0], (int)va);
+                st[1].push(softcap_exact(tot[1], cap), tot[1], (int)va);
             }
-            if (v1 < cta_v1) {
-                st[0].push(softcap_exact(acc[2], cap), acc[2], (int)v1);
-                st[1].push(softcap_exact(acc[3], cap), acc[3], (int)v1);
+            if (vb < cta_v1) {
+                st[0].push(softcap_exact(tot[2], cap), tot[2], (int)vb);
+                st[1].push(softcap_exact(tot[3], cap), tot[3], (int)vb);
             }
         }
         // Merge the 8 lanes that share t (lanes t, t+4, ..., t+28).
@@ -279,7 +408,7 @@ int stream_fwd_ctas_per_sm(int bits, int H) {
         auto it = cache.find({dev, bits, H});
         if (it != cache.end()) return it->second;
     }
-    const int smem = StreamSmem(H).total;
+    const int smem = StreamSmem(H, bits, stream_stages(H, bits)).total;
     const void* fn = bits == 4 ? reinterpret_cast<const void*>(stream_fwd_kernel<4>)
                                : reinterpret_cast<const void*>(stream_fwd_kernel<8>);
     int n = 0;
@@ -293,24 +422,28 @@ int stream_fwd_ctas_per_sm(int bits, int H) {
 
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
                               int64_t V, int H, int bits, float cap, const __half* h16,
-                              const int* count, int64_t M, Partial* part, int S, int* err,
-                              int stall, cudaStream_t st) {
+                              const int* count, const float* negc, const __half2* hsx, int64_t M,
+                              Partial* part, int S, int* err, int stall, cudaStream_t st) {
     CUtensorMap tw;
-    if (!tmap_packed_rows(&tw, wq, (uint64_t)H * bits / 32, (uint64_t)V, kChunkWords, kTile))
+    if (!tmap_packed_rows_sw128(&tw, wq, (uint64_t)H * bits / 32, (uint64_t)V, kTile))
         return cudaErrorInvalidValue;
     const int groups = (int)((M + kTokGroup - 1) / kTokGroup);
-    const int smem = StreamSmem(H).total;
+    const int n_stages = stream_stages(H, bits);
+    if (n_stages < 2) return cudaErrorInvalidValue;
+    const int smem = StreamSmem(H, bits, n_stages).total;
     dim3 grid(groups, S);
     if (bits == 4) {
         if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream_fwd_kernel<4>), smem))
             return e;
         stream_fwd_kernel<4><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
-                                                           count, part, S, err, stall);
+                                                           negc, hsx, count, part, S, err, stall,
+                                                           n_stages);
     } else {
         if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream_fwd_kernel<8>), smem))
             return e;
         stream_fwd_kernel<8><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
-                                                           count, part, S, err, stall);
+                                                           negc, hsx, count, part, S, err, stall,
+                                                           n_stages);
     }
     return cudaGetLastError();
 }

@@ -105,8 +105,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     const float cap = a.cap;
     int* __restrict__ err = a.err;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    // (offsetting the shared array itself keeps the accesses in the shared
+    // address space; a round trip through an integer would make them generic)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);  // TMA inputs landed
     uint64_t* empty = full + NS;  // inputs consumed (MMA commit + each dequant warp)
     uint64_t* dq = empty + NS;    // dequantized tile written

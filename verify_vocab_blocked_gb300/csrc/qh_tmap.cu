@@ -57,4 +57,10 @@ bool tmap_packed_rows(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_r
                      words_per_row * 4, box_words, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool tmap_packed_rows_sw128(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row,
+                            uint64_t rows, uint32_t box_rows) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, words_per_row, rows,
+                     words_per_row * 4, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace qh

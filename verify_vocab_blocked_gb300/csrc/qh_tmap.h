@@ -16,6 +16,12 @@ bool tmap_rows_f16_sw128(CUtensorMap* map, const void* base, uint64_t cols, uint
 bool tmap_packed_rows(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row, uint64_t rows,
                       uint32_t box_words, uint32_t box_rows);
 
+// Same with 128-byte rows in shared memory and the 128-byte swizzle: 16-byte
+// chunk j of box row r lands at chunk j ^ (r & 7) (box of 32 words x box_rows;
+// the destination must be 1024-byte aligned).
+bool tmap_packed_rows_sw128(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row,
+                            uint64_t rows, uint32_t box_rows);
+
 // Arguments of the tensor-core logit kernel (forward and backward phase 1).
 struct TcFwdArgs {
     const __half* scales;
