@@ -105,6 +105,95 @@ struct StreamShape {
     static constexpr int kStagesPerKb = 16 / kGroupsPerStage;             // stages per 16 groups
 };
 
+// Per-thread byte offsets (within a stage) of the packed words a thread reads
+// for each of the stage's groups: its A-fragment rows ra, rb, the swizzled
+// 16-byte chunk, and (4-bit) the 8-byte half of it.
+template <int BITS>
+struct StageOffsets {
+    static constexpr int NG = StreamShape<BITS>::kGroupsPerStage;
+    int a[NG], b[NG];
+    __device__ __forceinline__ StageOffsets(int ra, int rb, int t) {
+#pragma unroll
+        for (int gm = 0; gm < NG; ++gm) {
+            if constexpr (BITS == 4) {
+                // words 8 gm + 2t, +1: chunk 2 gm + (t >> 1), half t & 1
+                const int j = 2 * gm + (t >> 1);
+                a[gm] = ra * 128 + ((j ^ (ra & 7)) << 4) + 8 * (t & 1);
+                b[gm] = rb * 128 + ((j ^ (rb & 7)) << 4) + 8 * (t & 1);
+            } else {
+                // words 16 gm + 4t .. +3: chunk 4 gm + t
+                const int j = 4 * gm + t;
+                a[gm] = ra * 128 + ((j ^ (ra & 7)) << 4);
+                b[gm] = rb * 128 + ((j ^ (rb & 7)) << 4);
+            }
+        }
+    }
+};
+
+// One stage of one warp: for each group of the stage, the group-pure mma
+// chain on the magic-offset codes (accumulator started at -sum M_k h_k), then
+// tot += scale * acc.  P: the stage's packed tile; sa2 / sb2: the stage's
+// fp16 scales of rows ra / rb; ncs: negc of the stage's first group at tokens
+// 2t, 2t+1; hst: this thread's h fragment base for the stage.
+template <int BITS>
+__device__ __forceinline__ void stage_math(float (&tot)[4], const unsigned char* P,
+                                           const StageOffsets<BITS>& off, uint2 sa2, uint2 sb2,
+                                           const float* ncs, const __half* hst) {
+    if constexpr (BITS == 4) {
+        const float2 sa01 = __half22float2(u32_as_h2(sa2.x)), sa23 = __half22float2(u32_as_h2(sa2.y));
+        const float2 sb01 = __half22float2(u32_as_h2(sb2.x)), sb23 = __half22float2(u32_as_h2(sb2.y));
+#pragma unroll
+        for (int gm = 0; gm < 4; ++gm) {  // the stage's four groups
+            const uint2 wa = *reinterpret_cast<const uint2*>(P + off.a[gm]);
+            const uint2 wb = *reinterpret_cast<const uint2*>(P + off.b[gm]);
+            const float2 nc = *reinterpret_cast<const float2*>(ncs + gm * kTokGroup);
+            const uint4 q0 = *reinterpret_cast<const uint4*>(hst + 64 * gm);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(hst + 64 * gm + 8);
+            uint32_t pa[4], pb[4];
+            float acc[4];
+            codes4(wa.x, pa);
+            codes4(wb.x, pb);
+            mma16816_init(acc, pa[0], pb[0], pa[1], pb[1], q0.x, q0.y, nc.x, nc.y, nc.x, nc.y);
+            mma16816(acc, pa[2], pb[2], pa[3], pb[3], q0.z, q0.w);
+            codes4(wa.y, pa);
+            codes4(wb.y, pb);
+            mma16816(acc, pa[0], pb[0], pa[1], pb[1], q1.x, q1.y);
+            mma16816(acc, pa[2], pb[2], pa[3], pb[3], q1.z, q1.w);
+            const float s_a = gm == 0 ? sa01.x : gm == 1 ? sa01.y : gm == 2 ? sa23.x : sa23.y;
+            const float s_b = gm == 0 ? sb01.x : gm == 1 ? sb01.y : gm == 2 ? sb23.x : sb23.y;
+            tot[0] = fmaf(s_a, acc[0], tot[0]);
+            tot[1] = fmaf(s_a, acc[1], tot[1]);
+            tot[2] = fmaf(s_b, acc[2], tot[2]);
+            tot[3] = fmaf(s_b, acc[3], tot[3]);
+        }
+    } else {
+        const float2 sa01 = __half22float2(u32_as_h2(sa2.x));
+        const float2 sb01 = __half22float2(u32_as_h2(sb2.x));
+#pragma unroll 1
+        for (int gm = 0; gm < 2; ++gm) {  // the stage's two groups
+            const uint4 wa = *reinterpret_cast<const uint4*>(P + (gm ? off.a[1] : off.a[0]));
+            const uint4 wb = *reinterpret_cast<const uint4*>(P + (gm ? off.b[1] : off.b[0]));
+            const float2 nc = *reinterpret_cast<const float2*>(ncs + gm * kTokGroup);
+            const uint4 q0 = *reinterpret_cast<const uint4*>(hst + 64 * gm);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(hst + 64 * gm + 8);
+            float acc[4];
+            mma16816_init(acc, codes8(wa.x, 0x5140u), codes8(wb.x, 0x5140u), codes8(wa.x, 0x7362u),
+                          codes8(wb.x, 0x7362u), q0.x, q0.y, nc.x, nc.y, nc.x, nc.y);
+            mma16816(acc, codes8(wa.y, 0x5140u), codes8(wb.y, 0x5140u), codes8(wa.y, 0x7362u),
+                     codes8(wb.y, 0x7362u), q0.z, q0.w);
+            mma16816(acc, codes8(wa.z, 0x5140u), codes8(wb.z, 0x5140u), codes8(wa.z, 0x7362u),
+                     codes8(wb.z, 0x7362u), q1.x, q1.y);
+            mma16816(acc, codes8(wa.w, 0x5140u), codes8(wb.w, 0x5140u), codes8(wa.w, 0x7362u),
+                     codes8(wb.w, 0x7362u), q1.z, q1.w);
+            const float s_a = gm ? sa01.y : sa01.x, s_b = gm ? sb01.y : sb01.x;
+            tot[0] = fmaf(s_a, acc[0], tot[0]);
+            tot[1] = fmaf(s_a, acc[1], tot[1]);
+            tot[2] = fmaf(s_b, acc[2], tot[2]);
+            tot[3] = fmaf(s_b, acc[3], tot[3]);
+        }
+    }
+}
+
 // Shared memory (1024-byte aligned base): [packed ring: stages x 32 KB, 128B
 // swizzle] [scale ring] [h rows: 8 x (Hp + 8) halves] [negc: Gs x 8 fp32]
 // [hsum hi: 8 x gp fp16] [hsum lo: 8 x gp fp16] [barriers].  One CTA per SM:
@@ -133,7 +222,10 @@ int stream_stages(int H, int bits) {
     return 0;
 }
 
-template <int BITS>
+// NST > 0: the ring has NST stages and NST divides the stages of a tile, so
+// each round of NST stages uses compile-time ring slots (immediate shared
+// offsets); NST == 0: n_stages at run time, any shape.
+template <int BITS, int NST>
 __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_w, const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, float cap,
@@ -150,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
     unsigned char* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     // (offsetting the shared array itself keeps the accesses in the shared
     // address space; a round trip through an integer would make them generic)
-    const StreamSmem L(H, BITS, n_stages);
+    const StreamSmem L(H, BITS, NST > 0 ? NST : n_stages);
     const int kStages = L.stages;
     unsigned char* pring = smem;
     unsigned char* sring = smem + L.off_s;
@@ -254,9 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
         // distinct 16-byte chunks under the 128-byte swizzle.
         const int ra = BITS == 4 ? 16 * cw + 2 * g : 16 * cw + (g >> 1) + 4 * (g & 1);
         const int rb = BITS == 4 ? ra + 1 : ra + 8;
-        const int xa = ra & 7, xb = rb & 7;  // swizzle keys
+        const StageOffsets<BITS> off(ra, rb, t);
         const int nkb = L.gp / 16;
         constexpr int kPer = Shape::kStagesPerKb;
+        constexpr int kNG = Shape::kGroupsPerStage;
+        // This thread's h fragments of stage c start at half 32 c * (32 / BITS)
+        // + 16 t of token g's row (words 2t.. of each 4-bit group, words 4t..
+        // of each 8-bit group).
+        const __half* hbase = hrow + 16 * t;
 
         RowState st[2];
         st[0].init();
@@ -287,82 +384,45 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
                          *reinterpret_cast<const uint32_t*>(hs_lo + k0),
                          *reinterpret_cast<const uint32_t*>(hs_lo + k0 + 8));
             };
-            for (int c = 0; c < nst; ++c) {
-                if (c % kPer == 0) load_bias(c / kPer);
-                if (c % kPer == kPer / 2) bias_mma(c / kPer);
-                // Result ignored: the warp stays converged (see the abort policy).
-                tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
-                const unsigned char* P = pring + stage * kPBytes;
-                const unsigned char* Sst = sring + stage * kSBytes;
-                const uint2 sa2 = *reinterpret_cast<const uint2*>(Sst + 8 * ra);
-                const uint2 sb2 = *reinterpret_cast<const uint2*>(Sst + 8 * rb);
-                const float* ncs = negc_s + Shape::kGroupsPerStage * c * kTokGroup + 2 * t;
-                if constexpr (BITS == 4) {
-                    const float2 sa01 = __half22float2(u32_as_h2(sa2.x)), sa23 = __half22float2(u32_as_h2(sa2.y));
-                    const float2 sb01 = __half22float2(u32_as_h2(sb2.x)), sb23 = __half22float2(u32_as_h2(sb2.y));
-                    const __half* hst = hrow + (kStageWords * c + 2 * t) * 8;
-#pragma unroll 2
-                    for (int gm = 0; gm < 4; ++gm) {  // the stage's four groups
-                        // words 8 gm + 2t, +1: 16-byte chunk 2 gm + (t >> 1), swizzled by row
-                        const int j = 2 * gm + (t >> 1);
-                        const uint2 wa = *reinterpret_cast<const uint2*>(
-                            P + ra * 128 + ((j ^ xa) << 4) + 8 * (t & 1));
-                        const uint2 wb = *reinterpret_cast<const uint2*>(
-                            P + rb * 128 + ((j ^ xb) << 4) + 8 * (t & 1));
-                        const float2 nc = *reinterpret_cast<const float2*>(ncs + gm * kTokGroup);
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(hst + 64 * gm);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>(hst + 64 * gm + 8);
-                        uint32_t pa[4], pb[4];
-                        float acc[4];
-                        codes4(wa.x, pa);
-                        codes4(wb.x, pb);
-                        mma16816_init(acc, pa[0], pb[0], pa[1], pb[1], q0.x, q0.y, nc.x, nc.y, nc.x,
-                                      nc.y);
-                        mma16816(acc, pa[2], pb[2], pa[3], pb[3], q0.z, q0.w);
-                        codes4(wa.y, pa);
-                        codes4(wb.y, pb);
-                        mma16816(acc, pa[0], pb[0], pa[1], pb[1], q1.x, q1.y);
-                        mma16816(acc, pa[2], pb[2], pa[3], pb[3], q1.z, q1.w);
-                        const float s_a = gm == 0 ? sa01.x : gm == 1 ? sa01.y : gm == 2 ? sa23.x : sa23.y;
-                        const float s_b = gm == 0 ? sb01.x : gm == 1 ? sb01.y : gm == 2 ? sb23.x : sb23.y;
-                        tot[0] = fmaf(s_a, acc[0], tot[0]);
-                        tot[1] = fmaf(s_a, acc[1], tot[1]);
-                        tot[2] = fmaf(s_b, acc[2], tot[2]);
-                        tot[3] = fmaf(s_b, acc[3], tot[3]);
+            auto bias_step = [&](int c) {
+                if ((c & (kPer - 1)) == 0) load_bias(c / kPer);
+                if ((c & (kPer - 1)) == kPer / 2) bias_mma(c / kPer);
+            };
+            if constexpr (NST > 0) {
+                // Rounds of NST stages: ring slot s of every round is stage s.
+                for (int c0 = 0; c0 < nst; c0 += NST) {
+#pragma unroll
+                    for (int s = 0; s < NST; ++s) {
+                        const int c = c0 + s;
+                        bias_step(c);
+                        // Result ignored: the warp stays converged (see the abort policy).
+                        tc::mbar_wait(&full[s], phase, abort_flag, err, tc::kErrTimeoutFull);
+                        const unsigned char* Sst = sring + s * kSBytes;
+                        stage_math<BITS>(tot, pring + s * kPBytes, off,
+                                         *reinterpret_cast<const uint2*>(Sst + 8 * ra),
+                                         *reinterpret_cast<const uint2*>(Sst + 8 * rb),
+                                         negc_s + kNG * c * kTokGroup + 2 * t,
+                                         hbase + kStageWords * c * (32 / BITS));
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&empty[s]);
                     }
-                } else {
-                    const float2 sa01 = __half22float2(u32_as_h2(sa2.x));
-                    const float2 sb01 = __half22float2(u32_as_h2(sb2.x));
-                    const __half* hst = hrow + (kStageWords * c) * 4 + 16 * t;
-#pragma unroll 1
-                    for (int gm = 0; gm < 2; ++gm) {  // the stage's two groups
-                        // words 16 gm + 4t .. +3: 16-byte chunk 4 gm + t, swizzled by row
-                        const int j = 4 * gm + t;
-                        const uint4 wa = *reinterpret_cast<const uint4*>(P + ra * 128 + ((j ^ xa) << 4));
-                        const uint4 wb = *reinterpret_cast<const uint4*>(P + rb * 128 + ((j ^ xb) << 4));
-                        const float2 nc = *reinterpret_cast<const float2*>(ncs + gm * kTokGroup);
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(hst + 64 * gm);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>(hst + 64 * gm + 8);
-                        float acc[4];
-                        mma16816_init(acc, codes8(wa.x, 0x5140u), codes8(wb.x, 0x5140u),
-                                      codes8(wa.x, 0x7362u), codes8(wb.x, 0x7362u), q0.x, q0.y, nc.x,
-                                      nc.y, nc.x, nc.y);
-                        mma16816(acc, codes8(wa.y, 0x5140u), codes8(wb.y, 0x5140u),
-                                 codes8(wa.y, 0x7362u), codes8(wb.y, 0x7362u), q0.z, q0.w);
-                        mma16816(acc, codes8(wa.z, 0x5140u), codes8(wb.z, 0x5140u),
-                                 codes8(wa.z, 0x7362u), codes8(wb.z, 0x7362u), q1.x, q1.y);
-                        mma16816(acc, codes8(wa.w, 0x5140u), codes8(wb.w, 0x5140u),
-                                 codes8(wa.w, 0x7362u), codes8(wb.w, 0x7362u), q1.z, q1.w);
-                        const float s_a = gm ? sa01.y : sa01.x, s_b = gm ? sb01.y : sb01.x;
-                        tot[0] = fmaf(s_a, acc[0], tot[0]);
-                        tot[1] = fmaf(s_a, acc[1], tot[1]);
-                        tot[2] = fmaf(s_b, acc[2], tot[2]);
-                        tot[3] = fmaf(s_b, acc[3], tot[3]);
-                    }
+                    phase ^= 1;
                 }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&empty[stage]);
-                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            } else {
+                for (int c = 0; c < nst; ++c) {
+                    bias_step(c);
+                    // Result ignored: the warp stays converged (see the abort policy).
+                    tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
+                    const unsigned char* Sst = sring + stage * kSBytes;
+                    stage_math<BITS>(tot, pring + stage * kPBytes, off,
+                                     *reinterpret_cast<const uint2*>(Sst + 8 * ra),
+                                     *reinterpret_cast<const uint2*>(Sst + 8 * rb),
+                                     negc_s + kNG * c * kTokGroup + 2 * t,
+                                     hbase + kStageWords * c * (32 / BITS));
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&empty[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
             }
             // The last k-block's bias product, if its slot fell past the stages.
             if (kPer * (nkb - 1) + kPer / 2 >= nst) bias_mma(nkb - 1);
@@ -398,6 +458,38 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
 
 }  // namespace
 
+namespace {
+
+// Ring depth of the fast variant (compile-time ring slots).
+constexpr int kFastStages = 5;
+
+// Kernel variant for (bits, H): the fast one when its ring fits and divides
+// the stages of a tile, else the run-time-depth one.
+struct StreamVariant {
+    const void* fn;
+    int n_stages;
+    int smem;
+};
+
+StreamVariant stream_variant(int bits, int H) {
+    const int per_stage = kStageWords * 32 / bits;
+    const int nst = (H + per_stage - 1) / per_stage;  // stages per tile
+    StreamVariant v{};
+    if (nst % kFastStages == 0 && StreamSmem(H, bits, kFastStages).total <= kSmemLimit) {
+        v.fn = bits == 4 ? reinterpret_cast<const void*>(stream_fwd_kernel<4, kFastStages>)
+                         : reinterpret_cast<const void*>(stream_fwd_kernel<8, kFastStages>);
+        v.n_stages = kFastStages;
+    } else {
+        v.fn = bits == 4 ? reinterpret_cast<const void*>(stream_fwd_kernel<4, 0>)
+                         : reinterpret_cast<const void*>(stream_fwd_kernel<8, 0>);
+        v.n_stages = stream_stages(H, bits);
+    }
+    v.smem = v.n_stages >= 2 ? StreamSmem(H, bits, v.n_stages).total : 0;
+    return v;
+}
+
+}  // namespace
+
 int stream_fwd_ctas_per_sm(int bits, int H) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int>, int> cache;  // (device, bits, H) -> CTAs per SM
@@ -408,12 +500,10 @@ int stream_fwd_ctas_per_sm(int bits, int H) {
         auto it = cache.find({dev, bits, H});
         if (it != cache.end()) return it->second;
     }
-    const int smem = StreamSmem(H, bits, stream_stages(H, bits)).total;
-    const void* fn = bits == 4 ? reinterpret_cast<const void*>(stream_fwd_kernel<4>)
-                               : reinterpret_cast<const void*>(stream_fwd_kernel<8>);
+    const StreamVariant v = stream_variant(bits, H);
     int n = 0;
-    cudaError_t e = ensure_smem_limit(fn, smem);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem);
+    cudaError_t e = v.smem > 0 ? ensure_smem_limit(v.fn, v.smem) : cudaErrorInvalidValue;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, v.fn, kThreads, v.smem);
     n = (e == cudaSuccess && n > 0) ? n : 1;
     std::lock_guard<std::mutex> lock(mu);
     cache[{dev, bits, H}] = n;
@@ -428,24 +518,14 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
     if (!tmap_packed_rows_sw128(&tw, wq, (uint64_t)H * bits / 32, (uint64_t)V, kTile))
         return cudaErrorInvalidValue;
     const int groups = (int)((M + kTokGroup - 1) / kTokGroup);
-    const int n_stages = stream_stages(H, bits);
-    if (n_stages < 2) return cudaErrorInvalidValue;
-    const int smem = StreamSmem(H, bits, n_stages).total;
+    const StreamVariant v = stream_variant(bits, H);
+    if (v.n_stages < 2) return cudaErrorInvalidValue;
+    if (cudaError_t e = ensure_smem_limit(v.fn, v.smem)) return e;
     dim3 grid(groups, S);
-    if (bits == 4) {
-        if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream_fwd_kernel<4>), smem))
-            return e;
-        stream_fwd_kernel<4><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
-                                                           negc, hsx, count, part, S, err, stall,
-                                                           n_stages);
-    } else {
-        if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream_fwd_kernel<8>), smem))
-            return e;
-        stream_fwd_kernel<8><<<grid, kThreads, smem, st>>>(tw, scales, biases, V, H, cap, h16,
-                                                           negc, hsx, count, part, S, err, stall,
-                                                           n_stages);
-    }
-    return cudaGetLastError();
+    int n_stages = v.n_stages;
+    void* args[] = {&tw, &scales, &biases, &V, &H, &cap, &h16, &negc, &hsx, &count, &part, &S,
+                    &err, &stall, &n_stages};
+    return cudaLaunchKernel(v.fn, grid, dim3(kThreads), args, (size_t)v.smem, st);
 }
 
 }  // namespace qh
