@@ -86,9 +86,7 @@ struct FwdPlan {
     int S = 1;           // vocab splits of the partials (weight-streaming path)
     int cand_width = 1;  // argmax candidate run length
     size_t records = 0;  // partial records
-    int64_t stat_rows = 0; // rows with group statistics (weight-streaming path)
-    size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_part = 0, off_negc = 0,
-           off_hsx = 0, total = 0;
+    size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_part = 0, total = 0;
 };
 
 struct BwdPlan {
@@ -149,17 +147,14 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
         p->S = (int)S;
         p->cand_width = 1;
         p->records = (size_t)p->Mpad * p->S;
-        p->stat_rows = groups * qh::kTokGroup;
     }
     size_t off = 0;
     p->off_count = off; off = align_up(off + 16, 256);  // count, error word, segment count
     p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
     p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 256);
-    p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
+    // fp16 h for the tensor-core path; the streaming kernel converts its rows itself.
+    p->off_h16 = off;   if (p->tc) off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
     p->off_part = off;  off = align_up(off + sizeof(qh::Partial) * p->records, 256);
-    const size_t n_stat = (size_t)p->stat_rows * (hd->H / 64);
-    p->off_negc = off;  off = align_up(off + 4 * n_stat, 256);
-    p->off_hsx = off;   off = align_up(off + 4 * n_stat, 256);
     p->total = off;
     return QHEAD_OK;
 }
@@ -287,23 +282,17 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     qh::Partial* part = at<qh::Partial>(workspace, p.off_part);
 
     cudaError_t e;
-    float* negc = at<float>(workspace, p.off_negc);
-    __half2* hsx = at<__half2>(workspace, p.off_hsx);
-    static_assert(kTcMinM <= qh::kFusedPrologueMaxM,
-                  "the weight-streaming path relies on the fused prologue's group statistics");
-    if (M <= qh::kFusedPrologueMaxM) {
-        const int64_t nrows = p.tc ? p.Mpad : (M + qh::kTokGroup - 1) / qh::kTokGroup * qh::kTokGroup;
-        if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
-                                           count, h16, nrows, err, negc, hsx, (int)p.stat_rows,
-                                           st)))
-            return cuda_fail(e, "prologue");
-    } else {
-        if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
-            return cuda_fail(e, "compact");
-        if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
-            return cuda_fail(e, "convert_h");
-    }
     if (p.tc) {
+        if (M <= qh::kFusedPrologueMaxM) {
+            if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
+                                               count, h16, p.Mpad, err, st)))
+                return cuda_fail(e, "prologue");
+        } else {
+            if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
+                return cuda_fail(e, "compact");
+            if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
+                return cuda_fail(e, "convert_h");
+        }
         CUtensorMap th, tw;
         const int words = 64 * head->bits / 32;
         if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
@@ -320,8 +309,9 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         if (e) return cuda_fail(e, "tc_fwd");
     } else {
         hook_before(st);
-        e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, h16,
-                                  count, negc, hsx, M, part, p.S, err, stall, st);
+        // Compaction, fp16 conversion and group sums happen inside this kernel.
+        e = qh::launch_stream_fwd(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+                                  mask, M, rows, pos, count, part, p.S, err, stall, st);
         hook_after(st);
         if (e) return cuda_fail(e, "stream_fwd");
     }
@@ -373,8 +363,7 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         __half* coeff = at<__half>(workspace, p.off_coeff);
         if (M <= qh::kFusedPrologueMaxM) {
             if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
-                                               count, h16, p.Mpad, err, nullptr, nullptr, 0,
-                                               st)))
+                                               count, h16, p.Mpad, err, st)))
                 return cuda_fail(e, "prologue");
         } else {
             if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
 
     RowState st;
     st.init();
+    int bad = 0;  // some CTA that wrote a partial of this row gave up
     // Up to 4 partials per thread per round, loads issued before the merges.
     const Partial* prow = part + (int64_t)i * S;
     for (int s0 = threadIdx.x; s0 < S; s0 += 4 * kFinThreads) {
@@ -67,7 +68,18 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
             if (s0 + k * kFinThreads < S) buf[k] = prow[s0 + k * kFinThreads];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            if (s0 + k * kFinThreads < S) st.merge(buf[k]);
+            if (s0 + k * kFinThreads < S) {
+                st.merge(buf[k]);
+                bad |= buf[k].status;
+            }
+    }
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) {
+            if (logp) logp[r] = __int_as_float(0x7fc00000);
+            if (lse) lse[r] = __int_as_float(0x7fc00000);
+            if (argmax) argmax[r] = -1;
+        }
+        return;
     }
 #pragma unroll
     for (int o = 1; o <= 16; o <<= 1) st.shfl_merge(o);

@@ -18,9 +18,12 @@ void set_error(const std::string& msg);
 // split's vocab rows (m = max z, s = sum exp(z - m)) and the split's two best
 // raw logits with their vocab indices (i = start of a candidate run of
 // `cand_width` indices; empty entries hold v = -inf, i = INT32_MAX).
+// Per-(row, vocab segment) partial of the forward.  status: 0, or the code of
+// a bounded wait that expired in the CTA that wrote the record (the finalize
+// then poisons the row).
 struct __align__(32) Partial {
     float m, s, v1, v2;
-    int i1, i2, pad0, pad1;
+    int i1, i2, status, pad1;
 };
 
 constexpr int kTokGroup = 8;      // tokens per weight-streaming CTA (mma n = 8)
@@ -78,7 +81,7 @@ struct RowState {
         else { merge(o); }
     }
     __device__ __forceinline__ Partial to_partial() const {
-        Partial p; p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.pad0 = 0; p.pad1 = 0;
+        Partial p; p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.status = 0; p.pad1 = 0;
         return p;
     }
 };
@@ -155,13 +158,12 @@ cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* ro
 constexpr int64_t kFusedPrologueMaxM = 256;
 cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
                                   int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
-                                  __half* h16, int64_t nrows, int* err, float* negc, __half2* hsx,
-                                  int stat_rows, cudaStream_t st);
+                                  __half* h16, int64_t nrows, int* err, cudaStream_t st);
 cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
                              const int* count, __half* h16, cudaStream_t st);
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
-                              int64_t V, int H, int bits, float cap, const __half* h16,
-                              const int* count, const float* negc, const __half2* hsx, int64_t M,
+                              int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                              const uint8_t* mask, int64_t M, int* rows, int* pos, int* count,
                               Partial* part, int S, int* err, int stall, cudaStream_t st);
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,

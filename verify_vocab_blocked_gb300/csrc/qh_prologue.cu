@@ -65,10 +65,9 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
 
 // h16[i, :] = fp16(h[rows[i], :]) for i < count, zeros for count <= i < Mpad.
 // For 4-bit heads every 8-element block is stored in the order
-// (0,4,1,5,2,6,3,7): the order in which the weight-streaming kernel's
-// dequantizer yields (q_k, q_k+4) pairs out of one packed word, so the B
-// operand of every mma sees the same permutation of the K axis as the A
-// operand.  8-bit heads keep the natural order.
+// (0,4,1,5,2,6,3,7): the order in which the tensor-core kernels' dequantizer
+// yields (q_k, q_k+4) pairs out of one packed word, so both mma operands see
+// the same permutation of the K axis.  8-bit heads keep the natural order.
 __device__ __forceinline__ uint4 convert_unit(const __nv_bfloat16* __restrict__ src, int bits) {
     const uint4 in = *reinterpret_cast<const uint4*>(src);
     const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&in);
@@ -95,84 +94,13 @@ __global__ void convert_h_kernel(const __nv_bfloat16* __restrict__ h, int H, int
     *reinterpret_cast<uint4*>(h16 + i * H + 8 * u) = out;
 }
 
-// Error-free sum: s + e == a + b exactly (Knuth's TwoSum).
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-    s = a + b;
-    const float bb = s - a;
-    e = (a - (s - bb)) + (b - bb);
-}
-
-// Compensated accumulation of x into (s, c).
-__device__ __forceinline__ void acc2(float& s, float& c, float x) {
-    float e;
-    two_sum(s, x, s, e);
-    c += e;
-}
-
-// Per (row, 64-element group) statistics of the fp16 h the weight-streaming
-// kernel multiplies: hsum = sum_k h_k and negc = -sum_k M_k h_k, where M_k is
-// the magic offset its dequantizer leaves in code k (4-bit: 1024 for even k,
-// 64 for odd k; 8-bit: 1024).  That kernel feeds 1024 + q (or 64 + q) to the
-// tensor core and removes sum_k M_k h_k per group, so
-//   sum_k (s q_k + b) h_k = s (sum_k (M_k + q_k) h_k - sum_k M_k h_k) + b hsum.
-// Eight lanes share one (row, group): each sums 8 elements with compensation,
-// then the lanes combine their (sum, error) pairs exactly.  hsum is stored as
-// an fp16 (hi, lo) pair, hi + lo = hsum to about 2^-22 relative.
-__device__ void group_stats(const __nv_bfloat16* __restrict__ h, const int* __restrict__ rows,
-                            int n, int H, int bits, int stat_rows, float* __restrict__ negc,
-                            __half2* __restrict__ hsx) {
-    const int G = H / 64;
-    const int64_t ntask = (int64_t)stat_rows * G * 8;
-    const int64_t nloop = (ntask + 1023) / 1024 * 1024;  // whole passes: the shuffles below are warp-wide
-    for (int64_t task = threadIdx.x; task < nloop; task += 1024) {
-        const bool valid = task < ntask;
-        const int64_t pair = task >> 3;
-        const int sub = (int)(task & 7);
-        const int64_t i = valid ? pair / G : 0;
-        const int g = valid ? (int)(pair - i * G) : 0;
-        float es = 0.f, ec = 0.f, os = 0.f, oc = 0.f;  // even / odd element sums + errors
-        if (valid && i < n) {
-            const uint4 in =
-                *reinterpret_cast<const uint4*>(h + (int64_t)rows[i] * H + 64 * g + 8 * sub);
-            const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&in);
-#pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-                acc2(es, ec, __half2float(__float2half_rn(__bfloat162float(x[k]))));
-                acc2(os, oc, __half2float(__float2half_rn(__bfloat162float(x[k + 1]))));
-            }
-        }
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-            const float es2 = __shfl_xor_sync(0xffffffffu, es, o);
-            const float ec2 = __shfl_xor_sync(0xffffffffu, ec, o);
-            const float os2 = __shfl_xor_sync(0xffffffffu, os, o);
-            const float oc2 = __shfl_xor_sync(0xffffffffu, oc, o);
-            float e;
-            two_sum(es, es2, es, e);
-            ec += ec2 + e;
-            two_sum(os, os2, os, e);
-            oc += oc2 + e;
-        }
-        if (valid && sub == 0) {
-            const float me = 1024.f, mo = bits == 4 ? 64.f : 1024.f;
-            negc[pair] = -((me * es + mo * os) + (me * ec + mo * oc));
-            const float hs = (es + os) + (ec + oc);
-            const __half hi = __float2half_rn(hs);
-            const __half lo = __float2half_rn(hs - __half2float(hi));
-            hsx[pair] = __halves2half2(hi, lo);
-        }
-    }
-}
-
 // Small M: one CTA compacts, then converts rows [0, nrows) (zeros past the
 // active count): groups of 8 for the weight-streaming kernel, whole 128-row
-// tiles for the tensor-core kernel.  With stat_rows > 0 it also writes the
-// group statistics of rows [0, stat_rows) (zeros past the active count).
+// tiles for the tensor-core kernel.
 __global__ void __launch_bounds__(1024) prologue_fused_kernel(
     const uint8_t* __restrict__ mask, const __nv_bfloat16* __restrict__ h, int64_t M, int64_t Mpad,
     int H, int bits, int* __restrict__ rows, int* __restrict__ pos, int* __restrict__ count,
-    __half* __restrict__ h16, int64_t nrows, int* __restrict__ err, float* __restrict__ negc,
-    __half2* __restrict__ hsx, int stat_rows) {
+    __half* __restrict__ h16, int64_t nrows, int* __restrict__ err) {
     if (err && threadIdx.x == 0) *err = 0;
     const int n = compact_rows(mask, M, Mpad, rows, pos, count);
     __syncthreads();  // rows[] written by other threads
@@ -184,15 +112,13 @@ __global__ void __launch_bounds__(1024) prologue_fused_kernel(
         if (i < n) out = convert_unit(h + (int64_t)rows[i] * H + 8 * u, bits);
         *reinterpret_cast<uint4*>(h16 + i * H + 8 * u) = out;
     }
-    if (stat_rows > 0) group_stats(h, rows, n, H, bits, stat_rows, negc, hsx);
 }
 
 cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
                                   int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
-                                  __half* h16, int64_t nrows, int* err, float* negc, __half2* hsx,
-                                  int stat_rows, cudaStream_t st) {
+                                  __half* h16, int64_t nrows, int* err, cudaStream_t st) {
     prologue_fused_kernel<<<1, 1024, 0, st>>>(mask, h, M, Mpad, H, bits, rows, pos, count, h16,
-                                              nrows, err, negc, hsx, stat_rows);
+                                              nrows, err);
     return cudaGetLastError();
 }
 

@@ -20,8 +20,10 @@
 // offset M_k (one lop3 per code pair, nothing else per element), the group's
 // fp32 accumulator starts at -sum_k M_k h_k so the offset cancels inside it,
 // one FFMA per accumulator applies s, and b sum_k h_k is a small MMA per tile
-// (fp16 biases x an fp16 hi/lo split of the group sums of h).  The group sums
-// come from the prologue, computed from the same fp16 h.  w itself is never
+// (fp16 biases x an fp16 hi/lo split of the group sums of h).  Each CTA
+// compacts the mask, converts its 8 rows of h to fp16 in shared memory and
+// takes the group sums from those values while the first stages load, so the
+// verify call needs no separate prologue kernel.  w itself is never
 // rounded to fp16.
 //
 // A producer warp streams the CTA's vocab range through shared memory with
@@ -135,17 +137,20 @@ struct StageOffsets {
 // tot += scale * acc.  P: the stage's packed tile; sa2 / sb2: the stage's
 // fp16 scales of rows ra / rb; ncs: negc of the stage's first group at tokens
 // 2t, 2t+1; hst: this thread's h fragment base for the stage.
-template <int BITS>
+template <int BITS, int UNROLL4>
 __device__ __forceinline__ void stage_math(float (&tot)[4], const unsigned char* P,
                                            const StageOffsets<BITS>& off, uint2 sa2, uint2 sb2,
                                            const float* ncs, const __half* hst) {
     if constexpr (BITS == 4) {
         const float2 sa01 = __half22float2(u32_as_h2(sa2.x)), sa23 = __half22float2(u32_as_h2(sa2.y));
         const float2 sb01 = __half22float2(u32_as_h2(sb2.x)), sb23 = __half22float2(u32_as_h2(sb2.y));
-#pragma unroll
+#pragma unroll UNROLL4
         for (int gm = 0; gm < 4; ++gm) {  // the stage's four groups
-            const uint2 wa = *reinterpret_cast<const uint2*>(P + off.a[gm]);
-            const uint2 wb = *reinterpret_cast<const uint2*>(P + off.b[gm]);
+            // (select chains: a run-time index into off.a would put it in local memory)
+            const int oa = gm == 0 ? off.a[0] : gm == 1 ? off.a[1] : gm == 2 ? off.a[2] : off.a[3];
+            const int ob = gm == 0 ? off.b[0] : gm == 1 ? off.b[1] : gm == 2 ? off.b[2] : off.b[3];
+            const uint2 wa = *reinterpret_cast<const uint2*>(P + oa);
+            const uint2 wb = *reinterpret_cast<const uint2*>(P + ob);
             const float2 nc = *reinterpret_cast<const float2*>(ncs + gm * kTokGroup);
             const uint4 q0 = *reinterpret_cast<const uint4*>(hst + 64 * gm);
             const uint4 q1 = *reinterpret_cast<const uint4*>(hst + 64 * gm + 8);
@@ -229,11 +234,35 @@ template <int BITS, int NST>
 __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_w, const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, float cap,
-    const __half* __restrict__ h16, const float* __restrict__ negc_g,
-    const __half2* __restrict__ hsx_g, const int* __restrict__ count, Partial* __restrict__ part,
-    int S, int* __restrict__ err, int stall, int n_stages) {
+    const __nv_bfloat16* __restrict__ h, const uint8_t* __restrict__ mask, int M,
+    int* __restrict__ rows, int* __restrict__ pos, int* __restrict__ count,
+    Partial* __restrict__ part, int S, int* __restrict__ err, int stall, int n_stages) {
     using Shape = StreamShape<BITS>;
-    const int n_active = *count;
+    // Compaction of the (at most 63) rows, by every warp for itself: bit j of
+    // (act1:act0) marks row j active; compact index = rank among active rows.
+    const int lane_c = threadIdx.x & 31;
+    const unsigned act0 =
+        __ballot_sync(0xffffffffu, lane_c < M && (mask == nullptr || mask[lane_c] != 0));
+    const unsigned act1 =
+        __ballot_sync(0xffffffffu, lane_c + 32 < M && (mask == nullptr || mask[lane_c + 32] != 0));
+    const int n_active = __popc(act0) + __popc(act1);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
+        // One CTA publishes the maps and clears the error word for the finalize.
+        for (int r = lane_c; r < kRowPad; r += 32) {
+            if (r < M) {
+                const bool a = r < 32 ? (act0 >> r) & 1u : (act1 >> (r - 32)) & 1u;
+                const int idx = r < 32 ? __popc(act0 & ((1u << r) - 1u))
+                                       : __popc(act0) + __popc(act1 & ((1u << (r - 32)) - 1u));
+                pos[r] = a ? idx : -1;
+                if (a) rows[idx] = r;
+            }
+            if (r >= n_active) rows[r] = -1;
+        }
+        if (lane_c == 0) {
+            *count = n_active;
+            *err = 0;
+        }
+    }
     const int tok0 = blockIdx.x * kTokGroup;
     if (tok0 >= n_active) return;
     const int split = blockIdx.y;
@@ -283,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
             const int tile = k / nst, c = k - tile * nst;
             const int64_t row0 = cta_v0 + (int64_t)tile * kTile;
             if (lane == 0)
-                ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, tc::kErrTimeoutEmpty);
+                ok = tc::mbar_wait_cta(&empty[stage], phase ^ 1, abort_flag, err, tc::kErrTimeoutEmpty);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) {
@@ -319,25 +348,86 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
         const int cw = warp - 1;
         const int g = lane >> 2, t = lane & 3;
         const int ct = threadIdx.x - 32;
-        // Stage the group's 8 rows of h (fp16, K-permuted for 4-bit; zeros in
-        // [H, Hp)) and their group statistics, consumers only.
+        // Stage the group's 8 rows of h as fp16 (8-element blocks in the order
+        // (0,4,1,5,2,6,3,7) for 4-bit heads, matching the pairs codes4 yields;
+        // zeros past the active rows and in [H, Hp)), consumers only.
+        __shared__ int orig_s[kTokGroup];
+        if (ct < kTokGroup) {
+            int row = -1, k = tok0 + ct;  // compact index -> original row
+            if (k < n_active) {
+                for (int r = 0; r < M; ++r) {
+                    const bool a = r < 32 ? (act0 >> r) & 1u : (act1 >> (r - 32)) & 1u;
+                    if (a && k-- == 0) { row = r; break; }
+                }
+            }
+            orig_s[ct] = row;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
         const int units = L.Hp / 8;
         for (int idx = ct; idx < kTokGroup * units; idx += 32 * kConsumers) {
             const int r = idx / units, cc = idx - r * units;
+            const int row = orig_s[r];
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (8 * cc < H) v = *reinterpret_cast<const uint4*>(h16 + (int64_t)(tok0 + r) * H + 8 * cc);
+            if (row >= 0 && 8 * cc < H) {
+                const uint4 in = *reinterpret_cast<const uint4*>(h + (int64_t)row * H + 8 * cc);
+                const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&in);
+                __half y[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    y[k] = __float2half_rn(__bfloat162float(x[BITS == 4 ? ((k & 1) * 4 + (k >> 1)) : k]));
+                v = *reinterpret_cast<const uint4*>(y);
+            }
             *reinterpret_cast<uint4*>(hs + r * hstride + 8 * cc) = v;
         }
-        for (int idx = ct; idx < kTokGroup * L.Gs; idx += 32 * kConsumers) {
-            const int gg = idx / kTokGroup, r = idx - gg * kTokGroup;
-            negc_s[idx] = gg < G ? negc_g[(int64_t)(tok0 + r) * G + gg] : 0.f;
-        }
-        for (int idx = ct; idx < kTokGroup * L.gp; idx += 32 * kConsumers) {
-            const int r = idx / L.gp, gg = idx - r * L.gp;
-            __half2 x = __halves2half2(__float2half(0.f), __float2half(0.f));
-            if (gg < G) x = hsx_g[(int64_t)(tok0 + r) * G + gg];
-            hs_hi[idx] = __low2half(x);
-            hs_lo[idx] = __high2half(x);
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
+        // Group statistics of the staged fp16 rows (exactly what the mma sees):
+        // negc = -sum_k M_k h_k (M_k = 1024 for even k, 64 for odd k at 4 bits,
+        // 1024 at 8 bits) and hsum = sum_k h_k as an fp16 (hi, lo) pair.  Eight
+        // lanes per (row, group), one 8-element block each, compensated sums
+        // combined exactly across the lanes.
+        {
+            const int npair = kTokGroup * L.gp;
+            const int ntask = npair * 8;
+            for (int task0 = 0; task0 < ntask; task0 += 32 * kConsumers) {  // uniform trip count
+                const int task = task0 + ct;
+                const int pr = task >> 3, sub = task & 7;
+                const int r = pr / L.gp, gg = pr - r * L.gp;
+                float es = 0.f, ec = 0.f, os = 0.f, oc = 0.f;
+                if (task < ntask && gg < L.Gs) {
+                    const uint4 in = *reinterpret_cast<const uint4*>(hs + r * hstride + 64 * gg + 8 * sub);
+                    const __half* y = reinterpret_cast<const __half*>(&in);
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) {
+                        // natural element index parity of staged position p
+                        const bool even = BITS == 4 ? (p & 2) == 0 : (p & 1) == 0;
+                        const float xv = __half2float(y[p]);
+                        float e, sum;
+                        if (even) { sum = es + xv; const float bb = sum - es; e = (es - (sum - bb)) + (xv - bb); es = sum; ec += e; }
+                        else      { sum = os + xv; const float bb = sum - os; e = (os - (sum - bb)) + (xv - bb); os = sum; oc += e; }
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    const float es2 = __shfl_xor_sync(0xffffffffu, es, o);
+                    const float ec2 = __shfl_xor_sync(0xffffffffu, ec, o);
+                    const float os2 = __shfl_xor_sync(0xffffffffu, os, o);
+                    const float oc2 = __shfl_xor_sync(0xffffffffu, oc, o);
+                    float sum = es + es2, bb = sum - es;
+                    ec += ec2 + ((es - (sum - bb)) + (es2 - bb));
+                    es = sum;
+                    sum = os + os2; bb = sum - os;
+                    oc += oc2 + ((os - (sum - bb)) + (os2 - bb));
+                    os = sum;
+                }
+                if (task < ntask && sub == 0) {
+                    const float me = 1024.f, mo = BITS == 4 ? 64.f : 1024.f;
+                    if (gg < L.Gs) negc_s[gg * kTokGroup + r] = -((me * es + mo * os) + (me * ec + mo * oc));
+                    const float hsv = gg < G ? (es + os) + (ec + oc) : 0.f;
+                    const __half hi = __float2half_rn(hsv);
+                    hs_hi[pr] = hi;
+                    hs_lo[pr] = __float2half_rn(hsv - __half2float(hi));
+                }
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
         const __half* hrow = hs + g * hstride;
@@ -396,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
                         const int c = c0 + s;
                         bias_step(c);
                         // Result ignored: the warp stays converged (see the abort policy).
-                        tc::mbar_wait(&full[s], phase, abort_flag, err, tc::kErrTimeoutFull);
+                        tc::mbar_wait_cta(&full[s], phase, abort_flag, err, tc::kErrTimeoutFull);
                         const unsigned char* Sst = sring + s * kSBytes;
-                        stage_math<BITS>(tot, pring + s * kPBytes, off,
+                        stage_math<BITS, 4>(tot, pring + s * kPBytes, off,
                                          *reinterpret_cast<const uint2*>(Sst + 8 * ra),
                                          *reinterpret_cast<const uint2*>(Sst + 8 * rb),
                                          negc_s + kNG * c * kTokGroup + 2 * t,
@@ -412,9 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
                 for (int c = 0; c < nst; ++c) {
                     bias_step(c);
                     // Result ignored: the warp stays converged (see the abort policy).
-                    tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
+                    tc::mbar_wait_cta(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
                     const unsigned char* Sst = sring + stage * kSBytes;
-                    stage_math<BITS>(tot, pring + stage * kPBytes, off,
+                    stage_math<BITS, 2>(tot, pring + stage * kPBytes, off,
                                      *reinterpret_cast<const uint2*>(Sst + 8 * ra),
                                      *reinterpret_cast<const uint2*>(Sst + 8 * rb),
                                      negc_s + kNG * c * kTokGroup + 2 * t,
@@ -452,7 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
         RowState acc;
         acc.init();
         for (int w = 0; w < kConsumers; ++w) acc.merge(red[w][j]);
-        part[(int64_t)(tok0 + j) * S + split] = acc.to_partial();
+        Partial p = acc.to_partial();
+        p.status = *abort_flag;
+        part[(int64_t)(tok0 + j) * S + split] = p;
     }
 }
 
@@ -511,9 +603,10 @@ int stream_fwd_ctas_per_sm(int bits, int H) {
 }
 
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
-                              int64_t V, int H, int bits, float cap, const __half* h16,
-                              const int* count, const float* negc, const __half2* hsx, int64_t M,
+                              int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                              const uint8_t* mask, int64_t M, int* rows, int* pos, int* count,
                               Partial* part, int S, int* err, int stall, cudaStream_t st) {
+    if (M >= 64) return cudaErrorInvalidValue;  // the in-kernel compaction covers 64 rows
     CUtensorMap tw;
     if (!tmap_packed_rows_sw128(&tw, wq, (uint64_t)H * bits / 32, (uint64_t)V, kTile))
         return cudaErrorInvalidValue;
@@ -523,8 +616,9 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
     if (cudaError_t e = ensure_smem_limit(v.fn, v.smem)) return e;
     dim3 grid(groups, S);
     int n_stages = v.n_stages;
-    void* args[] = {&tw, &scales, &biases, &V, &H, &cap, &h16, &negc, &hsx, &count, &part, &S,
-                    &err, &stall, &n_stages};
+    int m32 = (int)M;
+    void* args[] = {&tw,   &scales, &biases, &V,    &H, &cap, &h,     &mask,    &m32,
+                    &rows, &pos,    &count,  &part, &S, &err, &stall, &n_stages};
     return cudaLaunchKernel(v.fn, grid, dim3(kThreads), args, (size_t)v.smem, st);
 }
 

@@ -87,6 +87,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// As mbar_wait, but only this CTA's abort flag ends the wait early: for a
+// kernel that clears the error word itself, whose other CTAs must not read a
+// value left there by an earlier call.
+__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag, int* err, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitTimeoutNs) {
+            atomicCAS(err, 0, code);
+            *abort_flag = code;
+            return false;
+        }
+    }
+}
+
 // Abort-path policy.  A warp whose lanes all execute collective or .aligned
 // instructions (mma.sync, tcgen05.ld, __syncwarp, bar.sync) never leaves its
 // loop on a failed wait: it ignores the result and runs its remaining,

@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             }
             if (EPI == EPI_SOFTMAX && row_ok) {
                 Partial p;
-                p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.pad0 = 0; p.pad1 = 0;
+                p.m = m; p.s = s; p.v1 = v1; p.v2 = v2; p.i1 = i1; p.i2 = i2; p.status = *abort_flag; p.pad1 = 0;
                 a.part[(int64_t)i * W.n_seg + seg] = p;
             }
         }
