@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     } else if (warp < kEpiWarp0) {
         // Dequant.  Thread t owns 16-byte piece p = t % PIECES of packed rows
         // t / PIECES + RPP * pass: a quarter-warp reads one contiguous 128-byte
-        // span, and the chunk order is rotated by the 64-column block so the
-        // eight 16-byte stores of a quarter-warp land in distinct bank groups.
+        // span.  Its stores of one chunk index go to four 64-column blocks at
+        // the same bank offset (4-way conflict); rotating the chunk order per
+        // block avoids that but costs more in run-time selects than it saves.
         const int t = threadIdx.x - 64;
         const int pc = t % L::PIECES, row0 = t / L::PIECES;
         const int ncol_piece = pc * L::CPP;        // first column of the piece in the N tile
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     };
 #pragma unroll
                     for (int q = 0; q < L::CHUNKS; ++q) {
-                        const int qq = (q + nb) % L::CHUNKS;  // rotated chunk order
+                        const int qq = q;
                         uint4 out;
                         if constexpr (BITS == 4) {
                             out = deq4_chunk(word(qq), s2, b2);
