@@ -108,7 +108,7 @@ constexpr int64_t kBwdChunkMin = 8192;
 // K slices of the dh contraction: enough (m, n) tiles x slices to fill the
 // SMs in whole waves (each slice accumulates into its own buffer).
 int dh_slices(int64_t Mpad, int H, int sms, int64_t n_k_min) {
-    const int64_t tiles = (Mpad / 128) * (H / qh::tc_dh_cols(H));
+    const int64_t tiles = ((Mpad + 255) / 256) * (H / qh::tc_dh_cols(H));  // 256-row units
     int best = 1;
     double best_eff = 0.0;
     for (int ks = 1; ks <= 16 && ks <= n_k_min; ++ks) {

@@ -20,7 +20,8 @@ namespace qh {
 
 namespace {
 
-constexpr int BM = 128;   // token rows (MMA M)
+constexpr int BM = 128;   // token rows per MMA (M); a unit covers two halves
+constexpr int BMU = 2 * BM;
 constexpr int BK = 64;    // vocab rows per stage
 template <int BITS>
 constexpr int dh_nb() { return BITS == 4 ? 3 : 2; }  // dequantized-tile stages
@@ -29,13 +30,16 @@ constexpr int kDqThreads = 32 * kDqWarps;
 constexpr int kEpiWarp0 = 2 + kDqWarps; // warps 10 .. 13 run the epilogue
 constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 
-// Two rings: NS stages of TMA inputs (coefficient tile + packed tile) deep
-// enough to cover HBM latency, NB stages of dequantized weight tiles.
+// Two rings: NS stages of TMA inputs (two 128-row coefficient tiles + packed
+// tile), NB stages of dequantized weight tiles.  Each dequantized tile feeds
+// the MMAs of both 128-row halves of the unit, so a weight tile is
+// dequantized once per 256 token rows.
 template <int BITS, int BNH>
 struct DhLayout {
-    static constexpr int NS = BITS == 4 ? 5 : 4;
+    static constexpr int NS = BNH == 256 ? 3 : 4;
     static constexpr int NB = dh_nb<BITS>();
-    static constexpr int A_BYTES = BM * BK * 2;             // coeff tile, K-major SW128
+    static constexpr int A_BYTES = 2 * BM * BK * 2;         // coeff tiles of both halves, K-major SW128
+    static constexpr int A_HALF = BM * BK * 2;
     static constexpr int B_BYTES = BNH * BK * 2;            // weight tile, MN-major SW128
     static constexpr int P_ROW = BNH * BITS / 8;            // packed bytes per vocab row
     static constexpr int P_BYTES = BK * P_ROW;
@@ -49,7 +53,7 @@ struct DhLayout {
     static constexpr int OFF_BAR = OFF_SB + NS * SB_BYTES;
     static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 4) + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;
-    static constexpr int TMEM_COLS = 2 * BNH;
+    static constexpr int TMEM_COLS = 2 * BNH;               // the two halves' accumulators
     // Dequant work split: a packed row is PIECES 16-byte pieces; thread t takes
     // piece t % PIECES of rows t / PIECES + RPP * pass.
     static constexpr int PIECES = P_ROW / 16;
@@ -87,8 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     uint64_t* empty = full + NS;  // inputs consumed (MMA commit + each dequant warp)
     uint64_t* dq = empty + NS;    // dequantized tile written
     uint64_t* bfree = dq + NB;    // dequantized tile consumed (MMA commit)
-    uint64_t* accf = bfree + NB;
-    uint64_t* acce = accf + 2;
+    uint64_t* accf = bfree + NB;  // [0]: the unit's accumulators are complete (MMA commit)
+    uint64_t* acce = accf + 2;    // [h]: half h has been read out (epilogue warps)
     uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
     uint64_t* mdrain = acce + 3;  // MMA drain on the abort path
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_active = *a.count;
-    const int n_mt = (n_active + BM - 1) / BM;
+    const int n_mt = (n_active + BMU - 1) / BMU;
     const int n_nt = a.H / BNH;
     const int KS = a.ks;                 // K slices per output tile
     const int units = n_mt * n_nt * KS;
@@ -149,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 if (!ok) break;
                 if (lane == 0) {
                     tc::mbar_arrive_expect_tx(&full[stage], L::A_BYTES + L::P_BYTES);
-                    tc::tma_load_2d(smem + L::OFF_A + stage * L::A_BYTES, &tmap_c, &full[stage],
-                                    kk * BK, mt * BM);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)  // rows past the block read as zero
+                        tc::tma_load_2d(smem + L::OFF_A + stage * L::A_BYTES + hh * L::A_HALF,
+                                        &tmap_c, &full[stage], kk * BK, mt * BMU + hh * BM);
                     tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w, &full[stage],
                                     nt * L::WORDS, (int)(a.v_begin + kk * BK));
                 }
@@ -180,16 +186,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int stage = 0, buf = 0, bs = 0;
+            int stage = 0, bs = 0;
             uint32_t phase = 0, aphase = 0, bphase = 0;
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
                 const int ks = u % KS;
                 const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
-                if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
-                                   tc::kErrTimeoutAccEmpty))
+                // Half h's accumulator may be overwritten once the epilogue has
+                // read it out: half 0 before the unit starts, half 1 before its
+                // first MMA (so reading out half 1 overlaps the next unit).
+                if (!tc::mbar_wait(&acce[0], aphase ^ 1, abort_flag, err, tc::kErrTimeoutAccEmpty))
                     goto mma_abort;
                 tc::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * BNH;
                 for (int kk = k0; kk < k1; ++kk) {
                     if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                         goto mma_abort;
@@ -199,21 +206,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * L::A_BYTES);
                     const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
 #pragma unroll
-                    for (int ks2 = 0; ks2 < BK / 16; ++ks2) {
-                        // A: K-major, 32 bytes per 16-element K step inside the swizzle atom.
-                        const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks2, 16, 1024);
-                        // B: MN-major, two 8-row K groups (2 x 1024 B) per K step;
-                        // 64-column blocks along N are BK/8 * 1024 bytes apart.
-                        const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks2, (BK / 8) * 1024, 1024);
-                        tc::umma_f16(d_tmem, ad, bd, L::IDESC, (kk > k0 || ks2 > 0) ? 1u : 0u);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh == 1 && kk == k0) {
+                            if (!tc::mbar_wait(&acce[1], aphase ^ 1, abort_flag, err,
+                                               tc::kErrTimeoutAccEmpty))
+                                goto mma_abort;
+                            tc::tc_fence_after();
+                        }
+#pragma unroll
+                        for (int ks2 = 0; ks2 < BK / 16; ++ks2) {
+                            // A: K-major, 32 bytes per 16-element K step inside the swizzle atom.
+                            const uint64_t ad = tc::sdesc_sw128(a0 + hh * L::A_HALF + 32 * ks2, 16, 1024);
+                            // B: MN-major, two 8-row K groups (2 x 1024 B) per K step;
+                            // 64-column blocks along N are BK/8 * 1024 bytes apart.
+                            const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks2, (BK / 8) * 1024, 1024);
+                            tc::umma_f16(tmem_base + hh * BNH, ad, bd, L::IDESC,
+                                         (kk > k0 || ks2 > 0) ? 1u : 0u);
+                        }
                     }
                     tc::umma_commit(&empty[stage]);
                     tc::umma_commit(&bfree[bs]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                     if (++bs == NB) { bs = 0; bphase ^= 1; }
                 }
-                tc::umma_commit(&accf[buf]);
-                if (++buf == 2) { buf = 0; aphase ^= 1; }
+                tc::umma_commit(&accf[0]);
+                aphase ^= 1;
             }
             goto mma_done;
         mma_abort:
@@ -285,47 +302,50 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         const int sub = warp & 3;
         const int row = sub * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
-        int buf = 0;
         uint32_t aphase = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
-            const int i = mt * BM + row;
-            const bool row_ok = i < n_active;
-            const float scale = row_ok ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
-            tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull);
+            // Result ignored: the warp stays converged (see the abort policy).
+            tc::mbar_wait(&accf[0], aphase, abort_flag, err, tc::kErrTimeoutAccFull);
             tc::tc_fence_after();
-            float* dst = a.dh_acc + (int64_t)ks * a.slice_stride + (int64_t)i * a.H + nt * BNH;
 #pragma unroll 1
-            for (int c = 0; c < BNH / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32(tmem_base + lane_addr + buf * BNH + c * 32, r);
-                tc::tmem_wait_ld();
-                if (row_ok) {
-                    // N column j of this chunk is hidden offset (j & ~7) + perm[j & 7]
-                    // for 4-bit heads (perm = 0,4,1,5,2,6,3,7), natural for 8-bit.
-                    float v[32];
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = mt * BMU + hh * BM + row;
+                const bool row_ok = i < n_active;
+                const float scale = row_ok ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
+                float* dst = a.dh_acc + (int64_t)ks * a.slice_stride + (int64_t)i * a.H + nt * BNH;
+#pragma unroll 1
+                for (int c = 0; c < BNH / 32; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tmem_base + lane_addr + hh * BNH + c * 32, r);
+                    tc::tmem_wait_ld();
+                    if (row_ok) {
+                        // N column j of this chunk is hidden offset (j & ~7) + perm[j & 7]
+                        // for 4-bit heads (perm = 0,4,1,5,2,6,3,7), natural for 8-bit.
+                        float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        constexpr int inv4[8] = {0, 2, 4, 6, 1, 3, 5, 7};  // offset -> N column
-                        const int src = BITS == 4 ? ((j & ~7) | inv4[j & 7]) : j;
-                        v[j] = __uint_as_float(r[src]) * scale;
-                    }
-                    float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                        if (a.accumulate) {
-                            const float4 o = d4[q];
-                            x.x += o.x; x.y += o.y; x.z += o.z; x.w += o.w;
+                        for (int j = 0; j < 32; ++j) {
+                            constexpr int inv4[8] = {0, 2, 4, 6, 1, 3, 5, 7};  // offset -> N column
+                            const int src = BITS == 4 ? ((j & ~7) | inv4[j & 7]) : j;
+                            v[j] = __uint_as_float(r[src]) * scale;
                         }
-                        d4[q] = x;
+                        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            if (a.accumulate) {
+                                const float4 o = d4[q];
+                                x.x += o.x; x.y += o.y; x.z += o.z; x.w += o.w;
+                            }
+                            d4[q] = x;
+                        }
                     }
                 }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&acce[hh]);
             }
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&acce[buf]);
-            if (++buf == 2) { buf = 0; aphase ^= 1; }
+            aphase ^= 1;
         }
     }
 
