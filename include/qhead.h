@@ -130,6 +130,31 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
               size_t workspace_bytes, void* stream);
 
 /*
+ * Speculative-decode verify with the accept step fused on the device.
+ * Definition: page "mlx-bun 0.0.8 -> 0.0.10" (src/spec/generate.ts): one head
+ * pass over the gamma + 1 window, the argmax of every position (picksBatched),
+ * then the longest prefix of the draft that the argmax reproduces.
+ *   h         device, bf16 [B * W, H]: B windows of W = gamma + 1 rows each.
+ *   B, W      B >= 0 windows (B == 0 returns QHEAD_OK), W in [1, 2^20].
+ *   draft     device, int32 [B, W - 1]: the drafted tokens; required if W > 1.
+ *   mask      as for qhead_fwd ([B * W] or NULL); a masked row's argmax is -1,
+ *             so a draft token never matches it.
+ *   lse       device, float [B * W], or NULL.
+ *   argmax    device, int32 [B * W] (required): as for qhead_fwd.
+ *   n_accept  device, int32 [B] (required): for window b, the first k < W - 1
+ *             with draft[b, k] != argmax[b, k], or W - 1 if every draft token
+ *             is accepted.
+ *   next_token device, int32 [B], or NULL: argmax[b, n_accept[b]], the token
+ *             the target model emits after the accepted prefix.
+ *   workspace as for qhead_fwd with M = B * W (qhead_fwd_workspace(head, B * W)).
+ * Outputs may not alias inputs or each other.
+ */
+int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,
+                 const int32_t* draft, const uint8_t* mask, float* lse, int32_t* argmax,
+                 int32_t* n_accept, int32_t* next_token, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/*
  * Backward of the frozen head: dh = d(sum_m dlogp[m] * logp[m]) / dh.
  * Definition: flashCceBackward on the page "mlx-bun 0.0.4 -> 0.0.6"
  * (src/train/flash-cce.ts: logits recomputed per vocab tile, coefficient
@@ -165,7 +190,9 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
  *     before any stream capture on the device.
  *   - M rows whose workspace (qhead_fwd_workspace) exceeds the scratch size
  *     are rejected with QHEAD_EINVAL and a message; nothing is launched.
- *     With H = 2560 that is roughly M > 1500.
+ *     In practice the scratch holds the weight-streaming path (M < 64, a few
+ *     hundred KB at H = 2560); the tensor-core path (M >= 64) needs tens of
+ *     MB of per-segment partials and is rejected.
  *   - Every call shares the one array.  No byte of it needs to start at zero
  *     (a call writes all scratch it reads), but calls whose kernels may
  *     overlap on the GPU (e.g. issued on different streams without ordering)

@@ -15,6 +15,10 @@ them (page "mlx-bun 0.0.4 -> 0.0.6", src/train/flash-cce.ts):
 4. lse = logsumexp_v z;  logp = z[target] - lse;  argmax = first argmax of raw
 5. dh = sum_v dlogp*(onehot - exp(z - lse))*sech2 * w[v,:]
 
+and the speculative-decode accept step (page "mlx-bun 0.0.8 -> 0.0.10",
+src/spec/generate.ts): per window of gamma + 1 positions, the longest prefix of
+the draft that the argmax reproduces, and the token after it.
+
 Masked rows (mask == 0) are skipped: logp = lse = 0, argmax = -1, dh = 0.
 """
 from __future__ import annotations
@@ -267,3 +271,25 @@ def backward(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
     _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
                       _ptr(b, _f64p), _ptr(raw, _f64p), _ptr(dh, _f64p), threads)
     return dh
+
+
+# ------------------------------------------------------------ verify accept
+
+def accept_prefix(argmax: np.ndarray, draft: np.ndarray, W: int):
+    """Per window b of W = gamma + 1 rows: the number of leading draft tokens
+    equal to the argmax at their positions (stop at the first mismatch, at
+    most gamma), and argmax at that position -- the accept loop of the
+    speculative decoder (page "mlx-bun 0.0.8 -> 0.0.10", src/spec/generate.ts),
+    written as the plain loop."""
+    argmax = np.asarray(argmax).reshape(-1, W)
+    gamma = W - 1
+    draft = np.asarray(draft).reshape(argmax.shape[0], gamma)
+    n_accept = np.empty(argmax.shape[0], np.int64)
+    nxt = np.empty(argmax.shape[0], np.int64)
+    for b in range(argmax.shape[0]):
+        k = 0
+        while k < gamma and draft[b, k] == argmax[b, k]:
+            k += 1
+        n_accept[b] = k
+        nxt[b] = argmax[b, k]
+    return n_accept, nxt

@@ -118,3 +118,31 @@ def test_error_message_is_per_call(L):
     assert "bits" in L.qhead_last_error().decode()
     assert _fwd(L, _head(), M=0) == 0
     assert L.qhead_last_error().decode() == ""
+
+
+def _verify(L, **kw):
+    a = dict(head=_head(), h=0x40000, B=2, W=5, draft=0x41000, mask=None, lse=None,
+             argmax=0x42000, n_accept=0x43000, next_token=None, ws=0x60000, ws_bytes=1 << 20)
+    a.update(kw)
+    return L.qhead_verify(ctypes.byref(a["head"]), a["h"], a["B"], a["W"], a["draft"], a["mask"],
+                          a["lse"], a["argmax"], a["n_accept"], a["next_token"], a["ws"],
+                          a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), qhead.QHEAD_EINVAL),
+    (dict(W=0), qhead.QHEAD_EINVAL),
+    (dict(W=(1 << 20) + 1), qhead.QHEAD_EINVAL),
+    (dict(B=1 << 40), qhead.QHEAD_EINVAL),
+    (dict(argmax=None), qhead.QHEAD_EINVAL),
+    (dict(n_accept=None), qhead.QHEAD_EINVAL),
+    (dict(draft=None), qhead.QHEAD_EINVAL),
+    (dict(head=_head(bits=3)), qhead.QHEAD_EUNSUPPORTED),
+])
+def test_bad_verify_args(L, kw, code):
+    assert _verify(L, **kw) == code
+    assert L.qhead_last_error().decode() != ""
+
+
+def test_verify_zero_windows_is_a_no_op(L):
+    assert _verify(L, B=0, ws=None, ws_bytes=0) == qhead.QHEAD_OK

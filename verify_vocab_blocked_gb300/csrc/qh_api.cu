@@ -174,7 +174,11 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p) {
     if (p->tc) {
         p->grid = di.sms;
         p->S = 1;
-        const int64_t vr = (hd->V + 255) / 256 * 256;
+        // Vocab rows rounded to the logit kernel's tiles; the slice count S is
+        // kept within the K steps of the shortest (last) chunk, so every chunk
+        // writes or adds every slice.
+        const int64_t tr = qh::kTcFwdTileRows;
+        const int64_t vr = (hd->V + tr - 1) / tr * tr;
         int64_t chunk = kBwdCoeffBudget / (2 * p->Mpad) / 256 * 256;
         if (chunk < kBwdChunkMin) chunk = kBwdChunkMin;
         if (chunk > vr) chunk = vr;
@@ -296,12 +300,13 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         CUtensorMap th, tw;
         const int words = 64 * head->bits / 32;
         if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
-            !qh::tmap_packed_rows(&tw, wq, head->H * head->bits / 32, head->V, words, 256))
+            !qh::tmap_packed_rows(&tw, wq, head->H * head->bits / 32, head->V, words,
+                                  qh::kTcFwdTileRows))
             return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
         qh::TcFwdArgs ta{};
         ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H; ta.cap = head->softcap;
         ta.count = count; ta.err = err; ta.stall = stall;
-        ta.vt_begin = 0; ta.vt_end = (int)((head->V + 255) / 256);
+        ta.vt_begin = 0; ta.vt_end = (int)((head->V + qh::kTcFwdTileRows - 1) / qh::kTcFwdTileRows);
         ta.part = part; ta.S_out = S_dev;
         hook_before(st);
         e = qh::launch_tc_fwd(th, tw, ta, head->bits, false, p.grid, st);
@@ -374,13 +379,15 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         CUtensorMap th, tw_logit, tcoef, tw_dh;
         const int wpr = head->H * head->bits / 32;
         if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
-            !qh::tmap_packed_rows(&tw_logit, wq, wpr, head->V, 64 * head->bits / 32, 256) ||
+            !qh::tmap_packed_rows(&tw_logit, wq, wpr, head->V, 64 * head->bits / 32,
+                                  qh::kTcFwdTileRows) ||
             !qh::tmap_rows_f16_sw128(&tcoef, coeff, p.chunk, p.Mpad, 128) ||
             !qh::tmap_packed_rows(&tw_dh, wq, wpr, head->V, qh::tc_dh_words(head->H, head->bits),
                                   64))
             return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
-        const int n_vt = (int)((head->V + 255) / 256);
-        const int vt_chunk = (int)(p.chunk / 256);
+        const int tr = qh::kTcFwdTileRows;
+        const int n_vt = (int)((head->V + tr - 1) / tr);
+        const int vt_chunk = (int)(p.chunk / tr);
         hook_before(st);
         for (int vt0 = 0, c = 0; vt0 < n_vt; vt0 += vt_chunk, ++c) {
             const int vt1 = vt0 + vt_chunk < n_vt ? vt0 + vt_chunk : n_vt;
@@ -397,9 +404,9 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
             da.scales = sc; da.biases = bi; da.V = head->V; da.H = head->H;
             da.count = count; da.err = err; da.rows = rows; da.dlogp = dlogp; da.dh_acc = dhp;
             da.slice_stride = p.Mpad * head->H;
-            da.v_begin = (int64_t)vt0 * 256;
-            da.n_k = (vt1 - vt0) * 256 / 64;
-            da.ks = p.S < da.n_k ? p.S : da.n_k;  // slices beyond a short chunk keep their sums
+            da.v_begin = (int64_t)vt0 * tr;
+            da.n_k = (vt1 - vt0) * tr / 64;
+            da.ks = p.S;  // <= the K steps of every chunk (plan_bwd)
             da.accumulate = c > 0;
             if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
                 return cuda_fail(e, "tc_dh");
@@ -417,6 +424,27 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     if ((e = qh::launch_bwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
                                      pos, targets, dlogp, dhp, p.S, p.Mpad, err, dh, M, st)))
         return cuda_fail(e, "bwd_finalize");
+    return QHEAD_OK;
+}
+
+int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,
+                 const int32_t* draft, const uint8_t* mask, float* lse, int32_t* argmax,
+                 int32_t* n_accept, int32_t* next_token, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+    g_err.clear();
+    if (B < 0) return fail(QHEAD_EINVAL, "B < 0");
+    if (W < 1 || W > (int64_t)1 << 20) return fail(QHEAD_EINVAL, "W must be in [1, 2^20]");
+    if (B > 0 && B > (((int64_t)1 << 31) - qh::kRowPad) / W)
+        return fail(QHEAD_EINVAL, "B * W too large");
+    if (B == 0) return QHEAD_OK;
+    if (!argmax || !n_accept) return fail(QHEAD_EINVAL, "argmax and n_accept are required");
+    if (W > 1 && !draft) return fail(QHEAD_EINVAL, "draft is required when W > 1");
+    const int rc = qhead_fwd(head, h, B * W, nullptr, mask, nullptr, lse, argmax, workspace,
+                             workspace_bytes, stream);
+    if (rc) return rc;
+    cudaError_t e = qh::launch_accept_prefix(argmax, draft, B, (int)W, n_accept, next_token,
+                                             static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, "accept_prefix");
     return QHEAD_OK;
 }
 

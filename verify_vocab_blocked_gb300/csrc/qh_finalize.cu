@@ -179,6 +179,46 @@ cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const 
     return cudaGetLastError();
 }
 
+// Longest accepted draft prefix per verify window (page "mlx-bun 0.0.8 ->
+// 0.0.10", src/spec/generate.ts: the accept loop that follows picksBatched).
+// Window b holds W = gamma + 1 consecutive rows of the forward's argmax;
+// n_accept[b] = the first k < gamma with draft[b, k] != argmax[b, k] (gamma if
+// there is none) and next_token[b] = argmax[b, n_accept[b]]: the target's own
+// token at the first rejected position, or the bonus token after a fully
+// accepted draft.  One warp per window.
+__global__ void accept_prefix_kernel(const int32_t* __restrict__ argmax,
+                                     const int32_t* __restrict__ draft, int64_t B, int W,
+                                     int32_t* __restrict__ n_accept,
+                                     int32_t* __restrict__ next_token) {
+    const int64_t b = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (b >= B) return;
+    const int gamma = W - 1;
+    int n = gamma;
+    for (int k0 = 0; k0 < gamma; k0 += 32) {
+        const int k = k0 + lane;
+        const bool miss = k < gamma && draft[b * gamma + k] != argmax[b * W + k];
+        const unsigned bal = __ballot_sync(0xffffffffu, miss);
+        if (bal) {  // the same for every lane
+            n = k0 + __ffs(bal) - 1;
+            break;
+        }
+    }
+    if (lane == 0) {
+        n_accept[b] = n;
+        if (next_token) next_token[b] = argmax[b * W + n];
+    }
+}
+
+cudaError_t launch_accept_prefix(const int32_t* argmax, const int32_t* draft, int64_t B, int W,
+                                 int32_t* n_accept, int32_t* next_token, cudaStream_t st) {
+    constexpr int kWarpsPerCta = 8;
+    const unsigned grid = (unsigned)((B + kWarpsPerCta - 1) / kWarpsPerCta);
+    accept_prefix_kernel<<<grid, 32 * kWarpsPerCta, 0, st>>>(argmax, draft, B, W, n_accept,
+                                                             next_token);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const float* dlogp,

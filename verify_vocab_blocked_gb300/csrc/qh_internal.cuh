@@ -188,6 +188,9 @@ cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const 
 cudaError_t ensure_smem_limit(const void* func, int bytes);
 int device_sms();
 
+cudaError_t launch_accept_prefix(const int32_t* argmax, const int32_t* draft, int64_t B, int W,
+                                 int32_t* n_accept, int32_t* next_token, cudaStream_t st);
+
 int bwd_simt_tokens(int H);                   // tokens per CTA of the SIMT backward
 int stream_fwd_ctas_per_sm(int bits, int H);  // occupancy of the weight-streaming kernel
 

@@ -30,7 +30,7 @@ namespace qh {
 namespace {
 
 constexpr int BM = 128;   // token rows per tile (MMA M)
-constexpr int BN = 256;   // vocab rows per tile (MMA N)
+constexpr int BN = kTcFwdTileRows;  // vocab rows per tile (MMA N)
 constexpr int BK = 64;    // K per stage (one quantization group, one swizzle atom)
 constexpr int NB = 3;     // dequantized-tile stages
 constexpr int kDqWarps = 8;             // warps 2 .. 9 dequantize

@@ -22,6 +22,10 @@ bool tmap_packed_rows(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_r
 bool tmap_packed_rows_sw128(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row,
                             uint64_t rows, uint32_t box_rows);
 
+// Vocab rows per tile of the tensor-core logit kernel (its MMA N); vocab
+// ranges handed to it are counted in these tiles.
+constexpr int kTcFwdTileRows = 256;
+
 // Arguments of the tensor-core logit kernel (forward and backward phase 1).
 struct TcFwdArgs {
     const __half* scales;
@@ -32,7 +36,7 @@ struct TcFwdArgs {
     const int* count;   // active rows (device)
     int* err;           // error word (device)
     int stall;          // test switch: the producer issues no loads (waits expire)
-    int vt_begin, vt_end;  // 256-row vocab tiles covered by this launch
+    int vt_begin, vt_end;  // vocab tiles (kTcFwdTileRows rows) covered by this launch
     // softmax epilogue (forward)
     Partial* part;
     int* S_out;

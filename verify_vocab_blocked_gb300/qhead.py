@@ -21,7 +21,7 @@ QHEAD_SB_F16 = 0
 # Every symbol include/qhead.h declares.
 EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd",
            "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel",
-           "qhead_fwd_noalloc", "qhead_test_stall_next_call")
+           "qhead_fwd_noalloc", "qhead_test_stall_next_call", "qhead_verify")
 
 
 class CHead(ctypes.Structure):
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
     L.qhead_fwd.restype = ctypes.c_int
     L.qhead_bwd.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_bwd.restype = ctypes.c_int
+    L.qhead_verify.argtypes = [hp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.qhead_verify.restype = ctypes.c_int
     L.qhead_last_error.argtypes = []
     L.qhead_last_error.restype = ctypes.c_char_p
     L.qhead_version.argtypes = []
@@ -195,3 +197,32 @@ def bwd(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
                            lse.data_ptr(), dlogp.data_ptr(), dh.data_ptr(), workspace.data_ptr(),
                            workspace.numel(), _stream(stream)))
     return dh
+
+
+def verify(head: Head, h: torch.Tensor, W: int, draft: torch.Tensor | None,
+           mask: torch.Tensor | None = None, *, want_lse: bool = False,
+           workspace: torch.Tensor | None = None, stream=None):
+    """Verify B = h.shape[0] / W windows of W = gamma + 1 rows against their
+    drafts (int32 [B, W - 1]).  Returns (n_accept [B], next_token [B],
+    argmax [B * W], lse [B * W] or None), all on the device."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous bf16 [B * W, H] tensor")
+    M = h.shape[0]
+    if W < 1 or M % W:
+        raise ValueError("the row count must be a multiple of W >= 1")
+    B = M // W
+    if draft is not None and (draft.dtype != torch.int32 or not draft.is_contiguous()
+                              or draft.numel() != B * (W - 1)):
+        raise ValueError("draft must be a contiguous int32 [B, W - 1] tensor")
+    dev = h.device
+    am = torch.empty(M, dtype=torch.int32, device=dev)
+    lse = torch.empty(M, dtype=torch.float32, device=dev) if want_lse else None
+    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(fwd_workspace(head, M), dev)
+    _check(lib().qhead_verify(ctypes.byref(head.c()), h.data_ptr(), B, W, _ptr(draft),
+                              _ptr(mask), _ptr(lse), am.data_ptr(), n_acc.data_ptr(),
+                              nxt.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                              _stream(stream)))
+    return n_acc, nxt, am, lse
