@@ -33,9 +33,16 @@ constexpr int BM = 128;   // token rows per tile (MMA M)
 constexpr int BN = kTcFwdTileRows;  // vocab rows per tile (MMA N)
 constexpr int BK = 64;    // K per stage (one quantization group, one swizzle atom)
 constexpr int NB = 3;     // dequantized-tile stages
-constexpr int kDqWarps = 8;             // warps 2 .. 9 dequantize
-constexpr int kEpiWarp0 = 2 + kDqWarps; // warps 10 .. 13 run the epilogue
-constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+// Warp roles: 0 TMA, 1 MMA, 2 .. 2 + dequant warps - 1 dequantize, then four
+// epilogue warps.  Dequant warps: one thread per vocab row at 4 bits; two per
+// row at 8 bits (twice the words per row; measured faster).
+template <int BITS>
+struct Warps {
+    static constexpr int kDq = BITS == 4 ? 8 : 16;
+    static constexpr int kTpr = kDq * 32 / 256;  // dequant threads per vocab row
+    static constexpr int kEpi0 = 2 + kDq;        // first epilogue warp
+    static constexpr int kThreads = 32 * (kEpi0 + 4);
+};
 constexpr int kTmemCols = 512;  // two 256-column fp32 accumulators
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
@@ -93,10 +100,11 @@ __device__ __forceinline__ void unit_coords(const Work& w, int vt_begin, int u, 
 constexpr int EPI_SOFTMAX = 0, EPI_COEFF = 1;
 
 template <int BITS, int EPI>
-__global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
+__global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
     const TcFwdArgs a) {
     using L = Layout<BITS>;
+    using WR = Warps<BITS>;
     constexpr int NS = L::NS;
     const __half* __restrict__ scales = a.scales;
     const __half* __restrict__ biases = a.biases;
@@ -129,10 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], 1 + kDqWarps);
+            tc::mbar_init(&empty[i], 1 + WR::kDq);
         }
         for (int i = 0; i < NB; ++i) {
-            tc::mbar_init(&dq[i], kDqWarps);
+            tc::mbar_init(&dq[i], WR::kDq);
             tc::mbar_init(&bfree[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -237,9 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
             tc::mbar_drain(mdrain, 0, err);
         mma_done:;
         }
-    } else if (warp < kEpiWarp0) {
+    } else if (warp < WR::kEpi0) {
         // ------------------------------------------------------------ dequant warps
-        const int t = threadIdx.x - 64;  // 0..255: row t of the tile
+        // Thread: part `pt` of vocab row t of the tile (kTpr parts per row).
+        const int t = (threadIdx.x - 64) / WR::kTpr, pt = (threadIdx.x - 64) % WR::kTpr;
         int stage = 0, bs = 0;
         uint32_t phase = 0, bphase = 0;
         for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
@@ -263,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                         const uint4* prow = reinterpret_cast<const uint4*>(P + r * L::P_ROW);
                         unsigned char* brow = Bs + r * 128;
                         if constexpr (BITS == 4) {
+                            static_assert(WR::kTpr == 1, "4-bit rows: one thread per row");
 #pragma unroll
                             for (int hq = 0; hq < 2; ++hq) {
                                 const uint4 wv = prow[hq];
@@ -278,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(
                             }
                         } else {
 #pragma unroll
-                            for (int hq = 0; hq < 4; ++hq) {
+                            for (int hq0 = 0; hq0 < 4 / WR::kTpr; ++hq0) {
+                                const int hq = pt * (4 / WR::kTpr) + hq0;  // this thread's 16-byte parts
                                 const uint4 wv = prow[hq];
                                 const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
@@ -429,7 +440,7 @@ static cudaError_t launch_t(const CUtensorMap& th, const CUtensorMap& tw, const 
     if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_fwd_kernel<BITS, EPI>),
                                           Layout<BITS>::SMEM))
         return e;
-    tc_fwd_kernel<BITS, EPI><<<grid, kThreads, Layout<BITS>::SMEM, st>>>(th, tw, a);
+    tc_fwd_kernel<BITS, EPI><<<grid, Warps<BITS>::kThreads, Layout<BITS>::SMEM, st>>>(th, tw, a);
     return cudaGetLastError();
 }
 
