@@ -84,7 +84,6 @@ struct FwdPlan {
     bool tc = false;     // tensor-core path
     int grid = 0;        // persistent CTAs of the tensor-core kernel
     int S = 1;           // vocab splits of the partials (weight-streaming path)
-    int cand_width = 1;  // argmax candidate run length
     size_t records = 0;  // partial records
     size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_part = 0, total = 0;
 };
@@ -133,7 +132,6 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
         // segments S from the active-row count so that n_tiles * S is about
         // 32 * grid, hence at most 128 * (32 * grid + n_tiles) records.
         p->grid = di.sms;
-        p->cand_width = 32;
         p->records = (size_t)128 * (32 * (size_t)p->grid + (size_t)(p->Mpad / 128));
     } else {
         const int64_t groups = (M + qh::kTokGroup - 1) / qh::kTokGroup;
@@ -145,7 +143,6 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
         if (S > max_s) S = max_s;
         if (S < 1) S = 1;
         p->S = (int)S;
-        p->cand_width = 1;
         p->records = (size_t)p->Mpad * p->S;
     }
     size_t off = 0;
@@ -322,8 +319,7 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     }
     if ((e = qh::launch_fwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
                                      pos, targets, part, p.S, p.tc ? S_dev : nullptr, err,
-                                     p.cand_width, logp, lse, argmax, M,
-                                     st)))
+                                     logp, lse, argmax, M, st)))
         return cuda_fail(e, "fwd_finalize");
     return QHEAD_OK;
 }

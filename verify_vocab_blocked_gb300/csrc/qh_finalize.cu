@@ -8,9 +8,8 @@
 //   * the target logit is recomputed exactly in fp32 (h widened from bf16,
 //     w = fmaf(scale, q, bias)), so logp = softcap(raw_target) - lse carries
 //     no fp16 operand rounding;
-//   * the argmax candidates (the two best raw logits over all splits, as runs
-//     of `cand_width` indices) are recomputed the same way and the best exact
-//     value wins, lowest index on ties (argmax over the raw logits, which
+//   * the two argmax candidates (the best two raw logits over all splits)
+//     are recomputed the same way and the better exact value wins, lowest index on ties (argmax over the raw logits, which
 //     picksBatched on the page "mlx-bun 0.0.8 -> 0.0.10" notes is the argmax of
 //     the capped, lse-shifted log-probs too);
 //   * masked rows get logp = 0, lse = 0, argmax = -1.
@@ -30,7 +29,7 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
     const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
     const int32_t* __restrict__ targets, const Partial* __restrict__ part, int S,
-    const int* __restrict__ S_dev, const int* __restrict__ err, int cand_width,
+    const int* __restrict__ S_dev, const int* __restrict__ err,
     float* __restrict__ logp, float* __restrict__ lse, int32_t* __restrict__ argmax) {
     const int64_t r = blockIdx.x;
     const int i = pos[r];
@@ -92,14 +91,14 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
     const __nv_bfloat16* hrow = h + r * (int64_t)H;
     const int32_t t = targets ? targets[r] : -1;
     const bool t_ok = t >= 0 && (int64_t)t < V;
-    // Work items: candidate indices of run 1, run 2, then the target.
-    const int n1 = fin.i1 == INT32_MAX ? 0 : (int)min((int64_t)cand_width, V - fin.i1);
-    const int n2 = fin.i2 == INT32_MAX ? 0 : (int)min((int64_t)cand_width, V - fin.i2);
+    // Work items: candidate 1, candidate 2 (if any), then the target.
+    const int n1 = fin.i1 < V ? 1 : 0;  // (an empty slot holds INT32_MAX)
+    const int n2 = fin.i2 < V ? 1 : 0;
     const int nitems = n1 + n2 + 1;
     for (int it = warp; it < nitems; it += kFinThreads / 32) {
         int64_t v;
-        if (it < n1) v = fin.i1 + it;
-        else if (it < n1 + n2) v = fin.i2 + (it - n1);
+        if (it < n1) v = fin.i1;
+        else if (it < n1 + n2) v = fin.i2;
         else v = t_ok ? t : -1;
         float x = 0.f;
         if (v >= 0) x = warp_exact_logit(hrow, wq, scales, biases, v, H, bits);
@@ -111,7 +110,7 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
         float best = -INFINITY;
         int bi = INT32_MAX;
         for (int it = 0; it < n1 + n2; ++it) {
-            const int v = it < n1 ? fin.i1 + it : fin.i2 + (it - n1);
+            const int v = it < n1 ? fin.i1 : fin.i2;
             if (better(exact[it], v, best, bi)) { best = exact[it]; bi = v; }
         }
         if (lse) lse[r] = l;
@@ -171,11 +170,11 @@ __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
-                                const int* S_dev, const int* err, int cand_width, float* logp,
+                                const int* S_dev, const int* err, float* logp,
                                 float* lse, int32_t* argmax, int64_t M, cudaStream_t st) {
     fwd_finalize_kernel<<<(unsigned)M, kFinThreads, 0, st>>>(wq, scales, biases, V, H, bits, cap,
                                                               h, pos, targets, part, S, S_dev, err,
-                                                              cand_width, logp, lse, argmax);
+                                                              logp, lse, argmax);
     return cudaGetLastError();
 }
 

@@ -15,12 +15,11 @@ namespace qh {
 void set_error(const std::string& msg);
 
 // Per-(row, vocab split) partial of the forward: online-softmax state over the
-// split's vocab rows (m = max z, s = sum exp(z - m)) and the split's two best
-// raw logits with their vocab indices (i = start of a candidate run of
-// `cand_width` indices; empty entries hold v = -inf, i = INT32_MAX).
-// Per-(row, vocab segment) partial of the forward.  status: 0, or the code of
-// a bounded wait that expired in the CTA that wrote the record (the finalize
-// then poisons the row).
+// split's vocab rows (m = max z, s = sum exp(z - m)) and two argmax candidates
+// with their vocab indices (the split's two best raw logits; the tensor-core
+// kernel's are the maxima of its two best 32-column slices; empty entries hold
+// v = -inf, i = INT32_MAX).  status: 0, or the code of a bounded wait that
+// expired in the CTA that wrote the record (the finalize then poisons the row).
 struct __align__(32) Partial {
     float m, s, v1, v2;
     int i1, i2, status, pad1;
@@ -168,7 +167,7 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
-                                const int* S_dev, const int* err, int cand_width, float* logp,
+                                const int* S_dev, const int* err, float* logp,
                                 float* lse, int32_t* argmax, int64_t M, cudaStream_t st);
 cudaError_t launch_bwd_simt(const uint32_t* wq, const __half* scales, const __half* biases,
                             int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,

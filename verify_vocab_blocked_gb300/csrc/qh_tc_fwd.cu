@@ -10,14 +10,16 @@
 //     256-row vocab tiles), chosen on the device from the active-row count;
 //   * a TMA warp streams the fp16 h tile (128 x 64, 128-byte swizzle) and the
 //     packed weight tile (256 rows x 64 codes) into a 3-stage ring;
-//   * four dequant warps turn the packed tile into fp16 in the tensor core's
-//     K-major 128-byte-swizzled layout (w = fma(q, scale, bias), one rounding);
+//   * eight (4-bit heads) or sixteen (8-bit heads) dequant warps turn the
+//     packed tile into fp16 in the tensor core's K-major 128-byte-swizzled
+//     layout (w = fma(q, scale, bias), one rounding);
 //   * one thread issues tcgen05.mma (M=128, N=256, K=16, fp32 accumulate) into
 //     one of two 256-column TMEM accumulators;
 //   * four epilogue warps read the accumulator with tcgen05.ld (one row per
 //     thread), apply the soft cap, update the row's online softmax and track
-//     the two 32-column chunks with the largest raw logit (argmax candidates,
-//     rechecked exactly by the finalize kernel).
+//     the maxima of the two 32-column slices with the largest raw logit, each
+//     with the lowest column holding it (argmax candidates, rechecked exactly
+//     by the finalize kernel).
 // The [M,V] logits and the dequantized head never leave the SM.
 #include <stdio.h>
 
@@ -379,11 +381,24 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                     } else {
                         if (nvalid <= 0) continue;
                         float rmax = -INFINITY;
+                        if (nvalid == 32) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < nvalid) rmax = fmaxf(rmax, x[j]);
-                        // argmax candidates: the two chunks with the largest raw logit
-                        const int ci = (int)col0;
+                            for (int j = 0; j < 32; ++j) rmax = fmaxf(rmax, x[j]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j < nvalid) rmax = fmaxf(rmax, x[j]);
+                        }
+                        // Lowest column of the slice holding its maximum.  No
+                        // guard is needed: the column that set rmax is valid and
+                        // lies below every padding column.
+                        int jb = 31;
+#pragma unroll
+                        for (int j = 30; j >= 0; --j) jb = x[j] == rmax ? j : jb;
+                        jb = min(jb, nvalid - 1);  // (no match at all: NaN logits)
+                        // argmax candidates: the maxima of the two slices with the
+                        // largest raw logit
+                        const int ci = (int)col0 + jb;
                         if (better(rmax, ci, v1, i1)) { v2 = v1; i2 = i1; v1 = rmax; i1 = ci; }
                         else if (better(rmax, ci, v2, i2)) { v2 = rmax; i2 = ci; }
                         // soft cap z = cap * tanh(x / cap) = cap - 2 cap / (exp(2x/cap) + 1)
