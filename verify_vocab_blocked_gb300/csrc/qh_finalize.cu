@@ -17,6 +17,7 @@
 // term dlogp * sech2(raw_target) * w[target, :] added exactly in fp32; masked
 // rows are written as exact zeros.
 #include "qh_internal.cuh"
+#include "qh_tc.cuh"
 
 namespace qh {
 
@@ -31,6 +32,8 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
     const int32_t* __restrict__ targets, const Partial* __restrict__ part, int S,
     const int* __restrict__ S_dev, const int* __restrict__ err,
     float* __restrict__ logp, float* __restrict__ lse, int32_t* __restrict__ argmax) {
+    tc::grid_dep_wait();  // the head kernel's partials (programmatic dependent launch)
+    tc::grid_dep_trigger();
     const int64_t r = blockIdx.x;
     const int i = pos[r];
     if (S_dev) S = *S_dev;
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
         else if (it < n1 + n2) v = fin.i2;
         else v = t_ok ? t : -1;
         float x = 0.f;
-        if (v >= 0) x = warp_exact_logit(hrow, wq, scales, biases, v, H, bits);
+        if (v >= 0) x = warp_exact_logit<10>(hrow, wq, scales, biases, v, H, bits);
         if (lane == 0) exact[it] = x;
     }
     __syncthreads();
@@ -172,10 +175,10 @@ cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const 
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
                                 const int* S_dev, const int* err, float* logp,
                                 float* lse, int32_t* argmax, int64_t M, cudaStream_t st) {
-    fwd_finalize_kernel<<<(unsigned)M, kFinThreads, 0, st>>>(wq, scales, biases, V, H, bits, cap,
-                                                              h, pos, targets, part, S, S_dev, err,
-                                                              logp, lse, argmax);
-    return cudaGetLastError();
+    void* args[] = {&wq, &scales, &biases, &V,     &H,   &bits,  &cap,   &h,      &pos,
+                    &targets, &part, &S, &S_dev, &err, &logp, &lse, &argmax};
+    return launch_dependent(reinterpret_cast<const void*>(fwd_finalize_kernel), dim3((unsigned)M),
+                            dim3(kFinThreads), 0, st, args);
 }
 
 // Longest accepted draft prefix per verify window (page "mlx-bun 0.0.8 ->

@@ -87,7 +87,9 @@ struct RowState {
 
 // Exact fp32 logit of one (row of h, vocab row) pair, computed by one warp:
 // h widened from bf16 exactly, w = fmaf(scale, q, bias) in fp32.  Every lane
-// returns the same value (fixed butterfly order).
+// returns the same value (fixed butterfly order).  U: 8-element units per lane
+// whose loads are issued together (one round trip per round).
+template <int U = 4>
 __device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restrict__ hrow,
                                                   const uint32_t* __restrict__ wq,
                                                   const __half* __restrict__ scales,
@@ -100,14 +102,14 @@ __device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restric
     const __half* srow = scales + v * (int64_t)G;
     const __half* brow = biases + v * (int64_t)G;
     float acc = 0.f;
-    // Units of 8 consecutive elements, 4 per lane per round, loads of a round
+    // Units of 8 consecutive elements, U per lane per round, loads of a round
     // issued together.
-    for (int u0 = lane; u0 < H / 8; u0 += 4 * 32) {
-        uint4 hv[4];
-        uint32_t w0[4], w1[4];
-        float s[4], b[4];
+    for (int u0 = lane; u0 < H / 8; u0 += U * 32) {
+        uint4 hv[U];
+        uint32_t w0[U], w1[U];
+        float s[U], b[U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < U; ++i) {
             const int u = u0 + 32 * i;
             if (u < H / 8) {
                 hv[i] = *reinterpret_cast<const uint4*>(hrow + 8 * u);
@@ -118,7 +120,7 @@ __device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restric
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < U; ++i) {
             if (u0 + 32 * i < H / 8) {
                 const __nv_bfloat16* hp = reinterpret_cast<const __nv_bfloat16*>(&hv[i]);
 #pragma unroll
@@ -160,6 +162,11 @@ cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, i
                                   __half* h16, int64_t nrows, int* err, cudaStream_t st);
 cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
                              const int* count, __half* h16, cudaStream_t st);
+// Launches `fn` with programmatic stream serialization: its CTAs may start
+// while the preceding kernel on `st` finishes, and wait for it with
+// tc::grid_dep_wait() before touching memory that kernel may write.
+cudaError_t launch_dependent(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             void** args);
 cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __half* biases,
                               int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                               const uint8_t* mask, int64_t M, int* rows, int* pos, int* count,

@@ -238,6 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
     int* __restrict__ rows, int* __restrict__ pos, int* __restrict__ count,
     Partial* __restrict__ part, int S, int* __restrict__ err, int stall, int n_stages) {
     using Shape = StreamShape<BITS>;
+    // Launched as a programmatic dependent: nothing in global memory is
+    // touched before the preceding grid on the stream has completed; the
+    // finalize that follows may then start its CTAs (they wait for this grid).
+    tc::grid_dep_wait();
+    tc::grid_dep_trigger();
     // Compaction of the (at most 63) rows, by every warp for itself: bit j of
     // (act1:act0) marks row j active; compact index = rank among active rows.
     const int lane_c = threadIdx.x & 31;
@@ -619,7 +624,7 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
     int m32 = (int)M;
     void* args[] = {&tw,   &scales, &biases, &V,    &H, &cap, &h,     &mask,    &m32,
                     &rows, &pos,    &count,  &part, &S, &err, &stall, &n_stages};
-    return cudaLaunchKernel(v.fn, grid, dim3(kThreads), args, (size_t)v.smem, st);
+    return launch_dependent(v.fn, grid, dim3(kThreads), (size_t)v.smem, st, args);
 }
 
 }  // namespace qh

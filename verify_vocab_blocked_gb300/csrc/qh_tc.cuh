@@ -40,6 +40,16 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                  : "memory");
 }
 
+// Programmatic dependent launch.  grid_dep_wait: block until the grids this
+// launch depends on have completed and their writes are visible (returns at
+// once for a launch without programmatic dependencies).  grid_dep_trigger:
+// allow the next programmatically dependent launch on the stream to start
+// (its CTAs run up to their own grid_dep_wait).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
