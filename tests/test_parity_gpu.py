@@ -92,6 +92,23 @@ TC_SHAPES = [
 ]
 
 
+# Shapes on the weight-streaming forward (M < 64) whose tiles span 5 or 20
+# stages and whose scale table has 8k groups: the variant with compile-time
+# ring slots and TMA-staged scales (4 and 8 bits, vocab sizes off the 256-row
+# tile, one to five token groups); H = 1280 (20 groups) takes the other one.
+STREAM_SHAPES = [
+    (5, 2560, 3001, 4, 30.0),
+    (13, 2560, 2000, 8, 0.0),
+    (40, 2560, 1500, 4, 0.0),
+    (6, 1280, 2500, 4, 30.0),
+]
+
+
+@pytest.mark.parametrize("M,H,V,bits,cap", STREAM_SHAPES)
+def test_stream_forward_shapes(M, H, V, bits, cap):
+    _run_all(_custom(M, H, V, bits, cap, seed=M * 11 + V))
+
+
 @pytest.mark.parametrize("M,H,V,bits,cap", TC_SHAPES)
 def test_tensor_core_forward_shapes(M, H, V, bits, cap):
     _run_all(_custom(M, H, V, bits, cap, seed=M * 7 + V))

@@ -53,7 +53,8 @@ def _assert_poisoned_fwd(wl, logp, lse, am):
 
 
 @pytest.mark.parametrize("M,H,V,bits,cap,masked", [
-    (5, 256, 3000, 4, 30.0, False),    # weight-streaming kernel
+    (5, 256, 3000, 4, 30.0, False),    # weight-streaming kernel (scales by cp.async)
+    (5, 2560, 1200, 4, 30.0, False),   # weight-streaming kernel, TMA-staged scales
     (200, 256, 2000, 8, 0.0, True),    # tensor-core kernel, some rows inactive
 ])
 def test_forward_wait_expires_then_recovers(M, H, V, bits, cap, masked):

@@ -107,6 +107,18 @@ struct StreamShape {
     static constexpr int kStagesPerKb = 16 / kGroupsPerStage;             // stages per 16 groups
 };
 
+// TMA-staged scales (fast variant): one box of kSBoxGroups groups x 256 rows
+// (16-byte rows, the TMA minimum) holds the scales of kPer consecutive stages
+// of a tile; kSlots such boxes are in flight (at least the 5 stages of the
+// packed ring, whatever the tile's remainder).
+constexpr int kSBoxGroups = 8;
+constexpr int kSSlotBytes = kTile * kSBoxGroups * 2;
+template <int BITS>
+struct ScaleRing {
+    static constexpr int kPer = kSBoxGroups / StreamShape<BITS>::kGroupsPerStage;  // 2 or 4
+    static constexpr int kSlots = BITS == 4 ? 3 : 2;
+};
+
 // Per-thread byte offsets (within a stage) of the packed words a thread reads
 // for each of the stage's groups: its A-fragment rows ra, rb, the swizzled
 // 16-byte chunk, and (4-bit) the 8-byte half of it.
@@ -200,39 +212,44 @@ __device__ __forceinline__ void stage_math(float (&tot)[4], const unsigned char*
 }
 
 // Shared memory (1024-byte aligned base): [packed ring: stages x 32 KB, 128B
-// swizzle] [scale ring] [h rows: 8 x (Hp + 8) halves] [negc: Gs x 8 fp32]
-// [hsum hi: 8 x gp fp16] [hsum lo: 8 x gp fp16] [barriers].  One CTA per SM:
-// the stage count is the largest that fits (more bytes in flight per SM).
+// swizzle] [scale ring: per stage 256 x 8 bytes, or with TMA-staged scales
+// kSlots boxes of 256 x 16 bytes] [h rows: 8 x (Hp + 8) halves] [negc: Gs x 8
+// fp32] [hsum hi: 8 x gp fp16] [hsum lo: 8 x gp fp16] [barriers].  One CTA
+// per SM: the stage count is the largest that fits (more bytes in flight).
 struct StreamSmem {
-    int stages, Hp, Gs, gp, off_s, off_h, off_negc, off_hs, off_bar, total;
-    __host__ __device__ StreamSmem(int H, int bits, int n_stages) {
+    int stages, sslots, Hp, Gs, gp, off_s, off_h, off_negc, off_hs, off_bar, total;
+    __host__ __device__ StreamSmem(int H, int bits, int n_stages, bool tma_scales) {
         const int per_stage = kStageWords * 32 / bits;      // hidden elements per stage
         Hp = (H + per_stage - 1) / per_stage * per_stage;
         Gs = Hp / 64;
         gp = (H / 64 + 15) / 16 * 16;  // groups padded to whole 16-wide k-blocks
         stages = n_stages;
+        sslots = tma_scales ? (bits == 4 ? ScaleRing<4>::kSlots : ScaleRing<8>::kSlots) : 0;
         off_s = stages * kPBytes;
-        off_h = off_s + stages * kSBytes;
+        off_h = off_s + (tma_scales ? sslots * kSSlotBytes : stages * kSBytes);
         off_negc = off_h + (kTokGroup * (Hp + 8) * 2 + 15) / 16 * 16;
         off_hs = off_negc + Gs * kTokGroup * 4;
         off_bar = (off_hs + 2 * kTokGroup * gp * 2 + 7) / 8 * 8;
-        total = off_bar + 8 * 2 * stages + 16 + 1024;  // + alignment slack of the base
+        total = off_bar + 8 * 2 * (stages + sslots) + 16 + 1024;  // + alignment slack of the base
     }
 };
 
 // The deepest ring that fits next to the staged h rows (0 if not even two).
 int stream_stages(int H, int bits) {
     for (int s = kMaxStages; s >= 2; --s)
-        if (StreamSmem(H, bits, s).total <= kSmemLimit) return s;
+        if (StreamSmem(H, bits, s, false).total <= kSmemLimit) return s;
     return 0;
 }
 
 // NST > 0: the ring has NST stages and NST divides the stages of a tile, so
 // each round of NST stages uses compile-time ring slots (immediate shared
-// offsets); NST == 0: n_stages at run time, any shape.
+// offsets), and the scales arrive by TMA (tmap_s; the group count is a
+// multiple of 8); NST == 0: n_stages at run time, any shape, scales copied
+// with cp.async (tmap_s unused).
 template <int BITS, int NST>
 __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
-    const __grid_constant__ CUtensorMap tmap_w, const __half* __restrict__ scales,
+    const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
+    const __half* __restrict__ scales,
     const __half* __restrict__ biases, int64_t V, int H, float cap,
     const __nv_bfloat16* __restrict__ h, const uint8_t* __restrict__ mask, int M,
     int* __restrict__ rows, int* __restrict__ pos, int* __restrict__ count,
@@ -276,7 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
     unsigned char* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     // (offsetting the shared array itself keeps the accesses in the shared
     // address space; a round trip through an integer would make them generic)
-    const StreamSmem L(H, BITS, NST > 0 ? NST : n_stages);
+    constexpr bool kTmaScales = NST > 0;
+    constexpr int kSPer = ScaleRing<BITS>::kPer;
+    constexpr int kSSlots = kTmaScales ? ScaleRing<BITS>::kSlots : 0;
+    const StreamSmem L(H, BITS, NST > 0 ? NST : n_stages, kTmaScales);
     const int kStages = L.stages;
     unsigned char* pring = smem;
     unsigned char* sring = smem + L.off_s;
@@ -287,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
     __half* hs_lo = hs_hi + kTokGroup * L.gp;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
     uint64_t* empty = full + kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    uint64_t* sfull = empty + kStages;  // TMA-staged scales: box landed
+    uint64_t* sempty = sfull + kSSlots;  // box consumed by every consumer warp
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sempty + kSSlots);
     __shared__ Partial red[kConsumers][kTokGroup];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -299,25 +321,44 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            tc::mbar_init(&full[i], 1 + 32);  // TMA (expect_tx) + 32 cp.async arrivals
+            // TMA (expect_tx), plus 32 cp.async arrivals when the scales ride along
+            tc::mbar_init(&full[i], kTmaScales ? 1 : 1 + 32);
             tc::mbar_init(&empty[i], kConsumers);
+        }
+        for (int i = 0; i < kSSlots; ++i) {
+            tc::mbar_init(&sfull[i], 1);
+            tc::mbar_init(&sempty[i], kConsumers);
         }
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmap_w);
+        if (kTmaScales) tc::prefetch_tmap(&tmap_s);
     }
     __syncthreads();
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        int stage = 0;
-        uint32_t phase = 0, fills = 0;
+        int stage = 0, sslot = 0;
+        uint32_t phase = 0, fills = 0, sphase = 0, sfills = 0;
         bool ok = stall == 0;  // test switch: issue no loads, the consumers' waits expire
         for (int k = 0; k < nitems && ok; ++k) {
             const int tile = k / nst, c = k - tile * nst;
             const int64_t row0 = cta_v0 + (int64_t)tile * kTile;
             if (lane == 0)
                 ok = tc::mbar_wait_cta(&empty[stage], phase ^ 1, abort_flag, err, tc::kErrTimeoutEmpty);
+            if (kTmaScales && lane == 0 && ok && c % kSPer == 0) {
+                // The scales of stages c .. c + kSPer - 1: groups kSBoxGroups * (c / kSPer)
+                // onward of the tile's 256 rows (rows past V read as zero).
+                ok = tc::mbar_wait_cta(&sempty[sslot], sphase ^ 1, abort_flag, err,
+                                       tc::kErrTimeoutEmpty);
+                if (ok) {
+                    tc::mbar_arrive_expect_tx(&sfull[sslot], kSSlotBytes);
+                    tc::tma_load_2d(sring + sslot * kSSlotBytes, &tmap_s, &sfull[sslot],
+                                    kSBoxGroups * (c / kSPer), (int)row0);
+                    ++sfills;
+                    if (++sslot == kSSlots) { sslot = 0; sphase ^= 1; }
+                }
+            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) {
@@ -326,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
                 tc::tma_load_2d(pring + stage * kPBytes, &tmap_w, &full[stage], kStageWords * c,
                                 (int)row0);
             }
+            if constexpr (!kTmaScales) {
             // The stage's scales, two groups per 4-byte copy (zeros past G or V).
             const int g0 = Shape::kGroupsPerStage * c;
             unsigned char* sd = sring + stage * kSBytes;
@@ -342,12 +384,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
                 }
             }
             tc::cp_async_arrive(&full[stage]);
+            }
             ++fills;
             if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         // On the abort path the consumers stop waiting: let the copies in
         // flight land before the CTA exits.
-        if (!ok && lane == 0) tc::drain_ring(full, kStages, fills, err);
+        if (!ok && lane == 0) {
+            tc::drain_ring(full, kStages, fills, err);
+            if (kTmaScales) tc::drain_ring(sfull, kSSlots, sfills, err);
+        }
     } else {
         // ---------------------------------------------------------------- consumers
         const int cw = warp - 1;
@@ -453,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
         RowState st[2];
         st[0].init();
         st[1].init();
-        int stage = 0;
-        uint32_t phase = 0;
+        int stage = 0, cs = 0;  // packed ring slot; scale box slot (fast variant)
+        uint32_t phase = 0, csphase = 0;
         for (int tile = 0; tile < ntiles; ++tile) {
             const int64_t va = cta_v0 + (int64_t)tile * kTile + ra;
             const int64_t vb = cta_v0 + (int64_t)tile * kTile + rb;
@@ -490,16 +536,30 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
                     for (int s = 0; s < NST; ++s) {
                         const int c = c0 + s;
                         bias_step(c);
-                        // Result ignored: the warp stays converged (see the abort policy).
+                        const int cq = c % kSPer;  // this stage's part of the scale box
+                        // Results ignored: the warp stays converged (see the abort policy).
+                        if (cq == 0)
+                            tc::mbar_wait_cta(&sfull[cs], csphase, abort_flag, err, tc::kErrTimeoutFull);
                         tc::mbar_wait_cta(&full[s], phase, abort_flag, err, tc::kErrTimeoutFull);
-                        const unsigned char* Sst = sring + s * kSBytes;
-                        stage_math<BITS, 4>(tot, pring + s * kPBytes, off,
-                                         *reinterpret_cast<const uint2*>(Sst + 8 * ra),
-                                         *reinterpret_cast<const uint2*>(Sst + 8 * rb),
+                        // Box row r: kSBoxGroups scales; this stage's kNG start at group kNG * cq.
+                        const unsigned char* Sb = sring + cs * kSSlotBytes + 2 * kNG * cq;
+                        uint2 sa, sb;
+                        if constexpr (BITS == 4) {
+                            sa = *reinterpret_cast<const uint2*>(Sb + 16 * ra);
+                            sb = *reinterpret_cast<const uint2*>(Sb + 16 * rb);
+                        } else {
+                            sa = make_uint2(*reinterpret_cast<const uint32_t*>(Sb + 16 * ra), 0u);
+                            sb = make_uint2(*reinterpret_cast<const uint32_t*>(Sb + 16 * rb), 0u);
+                        }
+                        stage_math<BITS, 4>(tot, pring + s * kPBytes, off, sa, sb,
                                          negc_s + kNG * c * kTokGroup + 2 * t,
                                          hbase + kStageWords * c * (32 / BITS));
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&empty[s]);
+                        if (cq == kSPer - 1 || c == nst - 1) {
+                            if (lane == 0) tc::mbar_arrive(&sempty[cs]);
+                            if (++cs == kSSlots) { cs = 0; csphase ^= 1; }
+                        }
                     }
                     phase ^= 1;
                 }
@@ -565,6 +625,7 @@ constexpr int kFastStages = 5;
 struct StreamVariant {
     const void* fn;
     int n_stages;
+    bool tma_scales;
     int smem;
 };
 
@@ -572,16 +633,20 @@ StreamVariant stream_variant(int bits, int H) {
     const int per_stage = kStageWords * 32 / bits;
     const int nst = (H + per_stage - 1) / per_stage;  // stages per tile
     StreamVariant v{};
-    if (nst % kFastStages == 0 && StreamSmem(H, bits, kFastStages).total <= kSmemLimit) {
+    // The fast variant stages the scales by TMA: 16-byte rows of the scale
+    // table (groups a multiple of 8).
+    if (nst % kFastStages == 0 && (H / 64) % kSBoxGroups == 0 &&
+        StreamSmem(H, bits, kFastStages, true).total <= kSmemLimit) {
         v.fn = bits == 4 ? reinterpret_cast<const void*>(stream_fwd_kernel<4, kFastStages>)
                          : reinterpret_cast<const void*>(stream_fwd_kernel<8, kFastStages>);
         v.n_stages = kFastStages;
+        v.tma_scales = true;
     } else {
         v.fn = bits == 4 ? reinterpret_cast<const void*>(stream_fwd_kernel<4, 0>)
                          : reinterpret_cast<const void*>(stream_fwd_kernel<8, 0>);
         v.n_stages = stream_stages(H, bits);
     }
-    v.smem = v.n_stages >= 2 ? StreamSmem(H, bits, v.n_stages).total : 0;
+    v.smem = v.n_stages >= 2 ? StreamSmem(H, bits, v.n_stages, v.tma_scales).total : 0;
     return v;
 }
 
@@ -618,12 +683,16 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
     const int groups = (int)((M + kTokGroup - 1) / kTokGroup);
     const StreamVariant v = stream_variant(bits, H);
     if (v.n_stages < 2) return cudaErrorInvalidValue;
+    CUtensorMap ts{};  // unused by the run-time-depth variant
+    if (v.tma_scales &&
+        !tmap_group_rows(&ts, scales, (uint64_t)H / 64, (uint64_t)V, kSBoxGroups, kTile))
+        return cudaErrorInvalidValue;
     if (cudaError_t e = ensure_smem_limit(v.fn, v.smem)) return e;
     dim3 grid(groups, S);
     int n_stages = v.n_stages;
     int m32 = (int)M;
-    void* args[] = {&tw,   &scales, &biases, &V,    &H, &cap, &h,     &mask,    &m32,
-                    &rows, &pos,    &count,  &part, &S, &err, &stall, &n_stages};
+    void* args[] = {&tw,  &ts,   &scales, &biases, &V, &H,   &cap,   &h,       &mask,
+                    &m32, &rows, &pos,    &count,  &part, &S, &err, &stall, &n_stages};
     return launch_dependent(v.fn, grid, dim3(kThreads), (size_t)v.smem, st, args);
 }
 

@@ -63,4 +63,10 @@ bool tmap_packed_rows_sw128(CUtensorMap* map, const uint32_t* wq, uint64_t words
                      words_per_row * 4, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool tmap_group_rows(CUtensorMap* map, const void* scales, uint64_t groups, uint64_t rows,
+                     uint32_t box_groups, uint32_t box_rows) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, groups, rows, groups * 2,
+                     box_groups, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 }  // namespace qh

@@ -22,6 +22,12 @@ bool tmap_packed_rows(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_r
 bool tmap_packed_rows_sw128(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row,
                             uint64_t rows, uint32_t box_rows);
 
+// Per-group fp16 table [rows, groups] (scales or biases), box of box_groups x
+// box_rows, no swizzle.  The row pitch (groups * 2 bytes) must be a multiple
+// of 16 bytes and box_groups a multiple of 8; false otherwise.
+bool tmap_group_rows(CUtensorMap* map, const void* scales, uint64_t groups, uint64_t rows,
+                     uint32_t box_groups, uint32_t box_rows);
+
 // Vocab rows per tile of the tensor-core logit kernel (its MMA N); vocab
 // ranges handed to it are counted in these tiles.
 constexpr int kTcFwdTileRows = 256;
