@@ -50,6 +50,15 @@ __device__ __forceinline__ void grid_dep_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// *p += v, four fp32 lanes, performed at L2 (fire-and-forget: no value comes
+// back, so no round trip).  Each lane is one fp32 addition rounded to
+// nearest; subnormal inputs and results are flushed to zero.
+__device__ __forceinline__ void red_add_v4(float* p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -330,14 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                             v[j] = __uint_as_float(r[src]) * scale;
                         }
                         float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+                        // Later chunks add at L2 (one addition per element per
+                        // launch, launches in chunk order: the sums of a
+                        // read-modify-write in the same fixed order, subnormals
+                        // flushed, without its round trip on the accumulators'
+                        // critical path).
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
-                            float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                            if (a.accumulate) {
-                                const float4 o = d4[q];
-                                x.x += o.x; x.y += o.y; x.z += o.z; x.w += o.w;
-                            }
-                            d4[q] = x;
+                            const float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            if (a.accumulate) tc::red_add_v4(reinterpret_cast<float*>(d4 + q), x);
+                            else d4[q] = x;
                         }
                     }
                 }
