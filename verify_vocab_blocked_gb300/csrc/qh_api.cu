@@ -378,8 +378,10 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
             !qh::tmap_packed_rows(&tw_logit, wq, wpr, head->V, 64 * head->bits / 32,
                                   qh::kTcFwdTileRows) ||
             !qh::tmap_rows_f16_sw128(&tcoef, coeff, p.chunk, p.Mpad, 128) ||
-            !qh::tmap_packed_rows(&tw_dh, wq, wpr, head->V, qh::tc_dh_words(head->H, head->bits),
-                                  64))
+            !(qh::tc_dh_swizzled(head->H, head->bits)
+                  ? qh::tmap_packed_rows_sw128(&tw_dh, wq, wpr, head->V, 64)
+                  : qh::tmap_packed_rows(&tw_dh, wq, wpr, head->V,
+                                         qh::tc_dh_words(head->H, head->bits), 64)))
             return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
         const int tr = qh::kTcFwdTileRows;
         const int n_vt = (int)((head->V + tr - 1) / tr);

@@ -61,6 +61,14 @@ struct DhLayout {
     static constexpr int PASSES = BK / RPP;
     static constexpr int CPP = 128 / BITS;        // hidden columns per piece (32 or 16)
     static constexpr int CHUNKS = CPP / 8;        // 16-byte output chunks per piece
+    // Packed rows of 128 or 256 bytes arrive as 128-byte-swizzled halves
+    // [half][64 rows][128 B] (chunk j of row r at j ^ (r & 7)), and each 8-lane
+    // phase of a dequant warp takes 8 consecutive vocab rows of one piece, so
+    // that its 16-byte loads and its stores into the swizzled B tile hit 8
+    // distinct bank groups; 64-byte rows keep the unswizzled layout with the
+    // 8 pieces of one row per phase.
+    static constexpr bool SWZ = P_ROW >= 128;
+    static constexpr int HALVES = P_ROW / 128;
     static constexpr uint32_t IDESC = tc::idesc_f16_f32(BM, BNH, false, true);
 };
 
@@ -157,8 +165,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     for (int hh = 0; hh < 2; ++hh)  // rows past the block read as zero
                         tc::tma_load_2d(smem + L::OFF_A + stage * L::A_BYTES + hh * L::A_HALF,
                                         &tmap_c, &full[stage], kk * BK, mt * BMU + hh * BM);
-                    tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w, &full[stage],
-                                    nt * L::WORDS, (int)(a.v_begin + kk * BK));
+                    if constexpr (L::SWZ) {
+#pragma unroll
+                        for (int hf = 0; hf < L::HALVES; ++hf)
+                            tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES + hf * (BK * 128),
+                                            &tmap_w, &full[stage], nt * L::WORDS + 32 * hf,
+                                            (int)(a.v_begin + kk * BK));
+                    } else {
+                        tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w, &full[stage],
+                                        nt * L::WORDS, (int)(a.v_begin + kk * BK));
+                    }
                 }
                 __half* sb = reinterpret_cast<__half*>(smem + L::OFF_SB + stage * L::SB_BYTES);
 #pragma unroll
@@ -240,16 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         mma_done:;
         }
     } else if (warp < kEpiWarp0) {
-        // Dequant.  Thread t owns 16-byte piece p = t % PIECES of packed rows
-        // t / PIECES + RPP * pass: a quarter-warp reads one contiguous 128-byte
-        // span.  Its stores of one chunk index go to four 64-column blocks at
-        // the same bank offset (4-way conflict); rotating the chunk order per
-        // block avoids that but costs more in run-time selects than it saves.
+        // Dequant.  Swizzled rows (SWZ): in pass ps, dequant warp dw's lane
+        // 8 a + b takes row 32 (ps & 1) + 8 (dw & 3) + b, piece
+        // 8 (ps >> 1) + 4 (dw >> 2) + a.  Otherwise thread t takes piece
+        // t % PIECES of rows t / PIECES + RPP * ps (a phase reads one 128-byte
+        // span; its stores go to four 64-column blocks at one bank offset).
         const int t = threadIdx.x - 64;
-        const int pc = t % L::PIECES, row0 = t / L::PIECES;
-        const int ncol_piece = pc * L::CPP;        // first column of the piece in the N tile
-        const int nb = ncol_piece >> 6;            // 64-column block
-        const int j0 = (ncol_piece & 63) >> 3;     // first 16-byte chunk in the block
+        const int dw = t >> 5, qa = (t >> 3) & 3, qb = t & 7;
         int stage = 0, bs = 0;
         uint32_t phase = 0, bphase = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -261,15 +274,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
                 const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
                 const __half* sb = reinterpret_cast<const __half*>(smem + L::OFF_SB + stage * L::SB_BYTES);
-                unsigned char* Bs = smem + L::OFF_B + bs * L::B_BYTES + nb * (BK / 8) * 1024;
+                unsigned char* Bs = smem + L::OFF_B + bs * L::B_BYTES;
 #pragma unroll
                 for (int ps = 0; ps < L::PASSES; ++ps) {
-                    const int kr = row0 + L::RPP * ps;
+                    const int kr = L::SWZ ? 32 * (ps & 1) + 8 * (dw & 3) + qb
+                                          : t / L::PIECES + L::RPP * ps;
+                    const int pc = L::SWZ ? 8 * (ps >> 1) + 4 * (dw >> 2) + qa : t % L::PIECES;
                     const int krow = kr & 7;
-                    const uint4 wv = *reinterpret_cast<const uint4*>(P + kr * L::P_ROW + pc * 16);
-                    const __half2 s2 = __half2half2(sb[kr * L::NSB + (ncol_piece >> 6)]);
-                    const __half2 b2 = __half2half2(sb[(BK + kr) * L::NSB + (ncol_piece >> 6)]);
-                    unsigned char* dst_row = Bs + (kr >> 3) * 1024 + krow * 128;
+                    const int ncol_piece = pc * L::CPP;     // first column of the piece in the N tile
+                    const int nb = ncol_piece >> 6;         // 64-column block
+                    const int j0 = (ncol_piece & 63) >> 3;  // first 16-byte chunk in the block
+                    const uint4 wv = *reinterpret_cast<const uint4*>(
+                        L::SWZ ? P + (pc >> 3) * (BK * 128) + kr * 128 + (((pc & 7) ^ krow) << 4)
+                               : P + kr * L::P_ROW + pc * 16);
+                    const __half2 s2 = __half2half2(sb[kr * L::NSB + nb]);
+                    const __half2 b2 = __half2half2(sb[(BK + kr) * L::NSB + nb]);
+                    unsigned char* dst_row = Bs + nb * (BK / 8) * 1024 + (kr >> 3) * 1024 + krow * 128;
                     // word i of the piece, selected without dynamic register indexing
                     auto word = [&](int i) {
                         return i == 0 ? wv.x : i == 1 ? wv.y : i == 2 ? wv.z : wv.w;
@@ -375,6 +395,8 @@ cudaError_t launch_t(const CUtensorMap& tc_map, const CUtensorMap& tw, const TcD
 int tc_dh_cols(int H) { return H % 256 == 0 ? 256 : 128; }
 
 int tc_dh_words(int H, int bits) { return tc_dh_cols(H) * bits / 32; }
+
+bool tc_dh_swizzled(int H, int bits) { return tc_dh_cols(H) * bits / 8 >= 128; }
 
 cudaError_t launch_tc_dh(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w, const TcDhArgs& a,
                          int bits, int grid, cudaStream_t st) {

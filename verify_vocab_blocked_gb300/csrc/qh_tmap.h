@@ -74,6 +74,10 @@ struct TcDhArgs {
 
 int tc_dh_cols(int H);          // hidden columns per output tile (256 or 128)
 int tc_dh_words(int H, int bits);
+// True when the dh kernel takes its packed tile as 128-byte-swizzled halves
+// (tensor map: tmap_packed_rows_sw128 with 64-row boxes); false: unswizzled
+// boxes of tc_dh_words words (tmap_packed_rows).
+bool tc_dh_swizzled(int H, int bits);
 cudaError_t launch_tc_dh(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w, const TcDhArgs& a,
                          int bits, int grid, cudaStream_t st);
 
