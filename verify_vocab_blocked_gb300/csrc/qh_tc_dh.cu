@@ -325,6 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         uint32_t aphase = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
+            // The rows' cotangents, fetched before the wait (a dependent pair
+            // of global loads off the accumulators' critical path).
+            float scale2[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = mt * BMU + hh * BM + row;
+                scale2[hh] = i < n_active ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
+            }
             // Result ignored: the warp stays converged (see the abort policy).
             tc::mbar_wait(&accf[0], aphase, abort_flag, err, tc::kErrTimeoutAccFull);
             tc::tc_fence_after();
@@ -332,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             for (int hh = 0; hh < 2; ++hh) {
                 const int i = mt * BMU + hh * BM + row;
                 const bool row_ok = i < n_active;
-                const float scale = row_ok ? -a.dlogp[a.rows[i]] * (1.f / 16384.f) : 0.f;
+                const float scale = hh ? scale2[1] : scale2[0];
                 float* dst = a.dh_acc + (int64_t)ks * a.slice_stride + (int64_t)i * a.H + nt * BNH;
 #pragma unroll 1
                 for (int c = 0; c < BNH / 32; ++c) {

@@ -373,10 +373,9 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                             out[j / 2] = h2_as_u32(__floats2half2_rn(cj[0], cj[1]));
                         }
                         if (i < a.coeff_rows) {
-                            uint4* d4 = reinterpret_cast<uint4*>(dst);
+                            // 32-byte stores: every store fills whole sectors.
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                d4[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                            for (int q = 0; q < 2; ++q) tc::st_global_v8(dst + 16 * q, out + 8 * q);
                         }
                     } else {
                         if (nvalid <= 0) continue;
