@@ -271,13 +271,18 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                         const int r = t;
                         const __half2 s2 = __half2half2(s0);
                         const __half2 b2 = __half2half2(b0);
-                        const uint4* prow = reinterpret_cast<const uint4*>(P + r * L::P_ROW);
+                        // 8-bit packed tiles arrive with the 64-byte swizzle (16-byte
+                        // part q of row r at q ^ ((r >> 1) & 3)), so an 8-lane phase
+                        // of part loads hits 8 bank groups (measured -1.5 % at 8 bits;
+                        // the 32-byte swizzle of 4-bit tiles was not faster).
+                        const unsigned char* prow = P + r * L::P_ROW;
+                        const int pswz = BITS == 8 ? (r >> 1) & 3 : 0;
                         unsigned char* brow = Bs + r * 128;
                         if constexpr (BITS == 4) {
                             static_assert(WR::kTpr == 1, "4-bit rows: one thread per row");
 #pragma unroll
                             for (int hq = 0; hq < 2; ++hq) {
-                                const uint4 wv = prow[hq];
+                                const uint4 wv = *reinterpret_cast<const uint4*>(prow + ((hq ^ pswz) << 4));
                                 const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
 #pragma unroll
                             for (int hq0 = 0; hq0 < 4 / WR::kTpr; ++hq0) {
                                 const int hq = pt * (4 / WR::kTpr) + hq0;  // this thread's 16-byte parts
-                                const uint4 wv = prow[hq];
+                                const uint4 wv = *reinterpret_cast<const uint4*>(prow + ((hq ^ pswz) << 4));
                                 const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                                 for (int j = 0; j < 2; ++j) {

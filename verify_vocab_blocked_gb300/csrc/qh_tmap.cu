@@ -63,6 +63,17 @@ bool tmap_packed_rows_sw128(CUtensorMap* map, const uint32_t* wq, uint64_t words
                      words_per_row * 4, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool tmap_packed_rows_swz(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row,
+                          uint64_t rows, uint32_t box_words, uint32_t box_rows) {
+    const CUtensorMapSwizzle swz = box_words * 4 == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
+                                   : box_words * 4 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                   : box_words * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                          : CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (swz == CU_TENSOR_MAP_SWIZZLE_NONE) return false;
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, words_per_row, rows,
+                     words_per_row * 4, box_words, box_rows, swz);
+}
+
 bool tmap_group_rows(CUtensorMap* map, const void* scales, uint64_t groups, uint64_t rows,
                      uint32_t box_groups, uint32_t box_rows) {
     return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, groups, rows, groups * 2,

@@ -22,6 +22,14 @@ bool tmap_packed_rows(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_r
 bool tmap_packed_rows_sw128(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row,
                             uint64_t rows, uint32_t box_rows);
 
+// Packed uint32 head, box of box_words (8, 16 or 32) x box_rows, rows of
+// 32, 64 or 128 bytes in shared memory with the swizzle of the same span:
+// 16-byte chunk c of box row r lands at c ^ ((r >> 2) & 1) (32 B),
+// c ^ ((r >> 1) & 3) (64 B) or c ^ (r & 7) (128 B); the destination must be
+// aligned to 256, 512 or 1024 bytes respectively.
+bool tmap_packed_rows_swz(CUtensorMap* map, const uint32_t* wq, uint64_t words_per_row,
+                          uint64_t rows, uint32_t box_words, uint32_t box_rows);
+
 // Per-group fp16 table [rows, groups] (scales or biases), box of box_groups x
 // box_rows, no swizzle.  The row pitch (groups * 2 bytes) must be a multiple
 // of 16 bytes and box_groups a multiple of 8; false otherwise.
