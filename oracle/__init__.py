@@ -14,6 +14,8 @@ them (page "mlx-bun 0.0.4 -> 0.0.6", src/train/flash-cce.ts):
 3. z = cap*tanh(raw/cap) if cap > 0 else raw
 4. lse = logsumexp_v z;  logp = z[target] - lse;  argmax = first argmax of raw
 5. dh = sum_v dlogp*(onehot - exp(z - lse))*sech2 * w[v,:]
+6. (the head gradient, a variant the pages leave out because their head is
+   frozen) dW[v,:] = sum_m dlogp*(onehot - exp(z - lse))*sech2 * h[m,:]
 
 and the speculative-decode accept step (page "mlx-bun 0.0.8 -> 0.0.10",
 src/spec/generate.ts): per window of gamma + 1 positions, the longest prefix of
@@ -76,6 +78,7 @@ def _load():
                                  _f64p, _int]
     lib.oracle_dh.argtypes = [_i64, _i64, _i64, _int, _int, _u32p, _f64p, _f64p, _f64p,
                               _f64p, _int]
+    lib.oracle_dw.argtypes = [_i64, _i64, _i64, _f64p, _f64p, _f64p, _int]
     lib.oracle_num_threads.argtypes = [_int]
     lib.oracle_num_threads.restype = _int
     _lib = lib
@@ -243,11 +246,9 @@ def forward(h: np.ndarray, head: Head, targets=None, mask=None, threads: int = 0
     return Forward(logp, lse, am, gap, zmax, raw if keep_raw else None)
 
 
-def backward(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
-             threads: int = 0) -> np.ndarray:
-    """dh = d(sum_m dlogp[m] * logp[m]) / dh  (fp64 [M,H]).  When ``lse`` is None
-    it is recomputed by the forward definition (the same value the forward
-    returns)."""
+def _coeff(h: np.ndarray, head: Head, targets, dlogp, mask, lse, threads: int):
+    """coeff[m,v] = dlogp[m] (1[v = t_m] - p[m,v]) sech2[m,v]  (fp64 [M,V]; 0 on
+    masked rows), the factor both gradients share."""
     raw = logits(h, head, threads)
     M, V = raw.shape
     t = _targets(targets, M)
@@ -265,12 +266,36 @@ def backward(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
     g = np.ascontiguousarray(np.broadcast_to(np.asarray(dlogp, dtype=np.float64), (M,)))
     _load().oracle_coeff(M, V, float(head.softcap), _ptr(raw, _f64p), _ptr(lse, _f64p),
                          _ptr(t, _i32p), _ptr(mk, _u8p), _ptr(g, _f64p), threads)
+    return raw
+
+
+def backward(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
+             threads: int = 0) -> np.ndarray:
+    """dh = d(sum_m dlogp[m] * logp[m]) / dh  (fp64 [M,H]).  When ``lse`` is None
+    it is recomputed by the forward definition (the same value the forward
+    returns)."""
+    raw = _coeff(h, head, targets, dlogp, mask, lse, threads)
+    M, V = raw.shape
     wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
     s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
     dh = np.empty((M, head.H), dtype=np.float64)
     _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
                       _ptr(b, _f64p), _ptr(raw, _f64p), _ptr(dh, _f64p), threads)
     return dh
+
+
+def grad_head(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
+              threads: int = 0) -> np.ndarray:
+    """dW = d(sum_m dlogp[m] * logp[m]) / dW  (fp64 [V,H]) with respect to the
+    dequantized head w[v,d] = s q + b: sum_m coeff[m,v] h[m,d], the classifier
+    gradient of the Apple CCE reference (the pages' head is frozen and
+    computes none).  Masked rows contribute nothing."""
+    raw = _coeff(h, head, targets, dlogp, mask, lse, threads)
+    M, V = raw.shape
+    hf = _as_f64_h(h)
+    dw = np.empty((V, head.H), dtype=np.float64)
+    _load().oracle_dw(M, head.H, V, _ptr(raw, _f64p), _ptr(hf, _f64p), _ptr(dw, _f64p), threads)
+    return dw
 
 
 # ------------------------------------------------------------ verify accept

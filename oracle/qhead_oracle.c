@@ -223,6 +223,27 @@ void oracle_coeff(int64_t M, int64_t V, double softcap, double *raw, const doubl
     }
 }
 
+/* dW[v,d] = sum_m coeff[m,v] * h[m,d]: the gradient of sum_m dlogp[m] * logp[m]
+ * with respect to the dequantized head (the classifier gradient of the
+ * Apple CCE reference, which the pages leave out because their head is
+ * frozen).  Each output row is owned by one thread and summed over m in
+ * ascending order, so the result does not depend on the thread count. */
+void oracle_dw(int64_t M, int64_t H, int64_t V, const double *coeff, const double *h, double *dw,
+               int nthreads) {
+    const int nt = pick_threads(nthreads);
+#pragma omp parallel for schedule(static) num_threads(nt)
+    for (int64_t v = 0; v < V; ++v) {
+        double *o = dw + v * H;
+        for (int64_t d = 0; d < H; ++d) o[d] = 0.0;
+        for (int64_t m = 0; m < M; ++m) {
+            const double c = coeff[m * V + v];
+            if (c == 0.0) continue;
+            const double *hm = h + m * H;
+            for (int64_t d = 0; d < H; ++d) o[d] += c * hm[d];
+        }
+    }
+}
+
 /* dh[m,d] = sum_v coeff[m,v] * w[v,d]; each output column is owned by one
  * thread and summed over v in ascending order, so the result does not depend
  * on the thread count. */

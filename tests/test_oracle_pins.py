@@ -11,7 +11,10 @@
   autograd's dh on an independently unpacked head;
 * finite differences of sum_m dlogp_m * logp_m against dh;
 * invariants: logp <= 0, max z <= lse <= max z + ln V, z at the argmax is the
-  row maximum.
+  row maximum;
+* the head gradient dW: torch fp64 autograd with respect to the dense head,
+  finite differences with respect to a group's bias and scale, a two-row
+  closed form, vanishing column sums without the cap, V = 1 and masking.
 """
 import math
 import os
@@ -302,3 +305,121 @@ def test_invariants(name):
         assert abs(z[m, f.argmax[m]] - f.zmax[m]) <= 1e-12
         assert f.argmax[m] == int(np.argmax(f.raw[m]))
     assert (f.argmax[~act] == -1).all() and (f.logp[~act] == 0).all()
+
+
+# ------------------------------------------------- head gradient (dW) pins
+
+def _torch_dw(h64, head: oracle.Head, targets, dlogp, mask=None):
+    """torch fp64 autograd with respect to the dense head (independent unpack)."""
+    q = torch.from_numpy(_unpack_independent(head.wq, head.bits)).double()
+    s = torch.from_numpy(np.asarray(head.scales, dtype=np.float64))
+    b = torch.from_numpy(np.asarray(head.biases, dtype=np.float64))
+    w = (q * s.repeat_interleave(head.group, 1) + b.repeat_interleave(head.group, 1))
+    w = w.clone().requires_grad_(True)
+    h = torch.from_numpy(h64)
+    raw = h @ w.T
+    z = head.softcap * torch.tanh(raw / head.softcap) if head.softcap > 0 else raw
+    lp = torch.log_softmax(z, dim=1)
+    t = torch.from_numpy(np.asarray(targets, dtype=np.int64))
+    logp = lp.gather(1, t[:, None])[:, 0]
+    g = torch.from_numpy(np.asarray(dlogp, dtype=np.float64))
+    if mask is not None:
+        g = g * torch.from_numpy(np.asarray(mask, dtype=np.float64))
+    (g * logp).sum().backward()
+    return w.grad.numpy()
+
+
+@pytest.mark.parametrize("bits,cap", [(4, 30.0), (8, 0.0), (4, 2.0)])
+def test_dw_against_torch_autograd(bits, cap):
+    V, H, M = 700, 128, 9
+    head = synth.make_head(V, H, bits, softcap=cap, seed=21)
+    ohead = oracle.Head(head.wq, head.scales, head.biases, bits, 64, cap)
+    h = synth.make_hidden(M, H, seed=21)
+    t = synth.make_targets(M, V, seed=21)
+    t[4] = t[1]  # two rows share a target
+    g = synth.make_dlogp(M, seed=21).astype(np.float64)
+    mask = np.array([1, 1, 0, 1, 1, 1, 0, 1, 1], dtype=np.uint8)
+    dw = oracle.grad_head(h, ohead, t, g, mask=mask)
+    ohead64 = oracle.Head(head.wq, oracle.widen_f16(head.scales).reshape(head.scales.shape),
+                          oracle.widen_f16(head.biases).reshape(head.biases.shape), bits, 64, cap)
+    ref = _torch_dw(oracle.widen_bf16(h), ohead64, t, g, mask)
+    assert np.abs(dw - ref).max() <= 1e-10 * max(1.0, np.abs(ref).max())
+
+
+def test_dw_finite_differences_of_group_bias_and_scale():
+    # A group's bias moves every element of the group: d/db = sum_d dW[v,d];
+    # its scale moves element d by q[v,d]: d/ds = sum_d q[v,d] dW[v,d].
+    V, H, M, cap = 200, 128, 5, 3.0
+    head = synth.make_head(V, H, 4, softcap=cap, seed=22)
+    s = oracle.widen_f16(head.scales).reshape(head.scales.shape)
+    b = oracle.widen_f16(head.biases).reshape(head.biases.shape)
+    h = oracle.widen_bf16(synth.make_hidden(M, H, seed=22)) * 2.0
+    t = synth.make_targets(M, V, seed=22)
+    g = synth.make_dlogp(M, seed=22).astype(np.float64)
+    dw = oracle.grad_head(h, oracle.Head(head.wq, s, b, 4, 64, cap), t, g)
+    q = oracle.codes(head.wq, H, 4).astype(np.float64)
+
+    def loss(ss, bb):
+        return float((g * oracle.forward(h, oracle.Head(head.wq, ss, bb, 4, 64, cap), t).logp).sum())
+
+    eps = 1e-6
+    for v, grp in [(int(t[0]), 0), (int(t[2]), 1), (17, 1), (150, 0)]:
+        sl = slice(64 * grp, 64 * grp + 64)
+        db = b.copy(); db[v, grp] += eps
+        bm = b.copy(); bm[v, grp] -= eps
+        fd_b = (loss(s, db) - loss(s, bm)) / (2 * eps)
+        assert abs(fd_b - dw[v, sl].sum()) <= 1e-6 * max(1.0, abs(fd_b)), (v, grp)
+        ds = s.copy(); ds[v, grp] += eps
+        sm = s.copy(); sm[v, grp] -= eps
+        fd_s = (loss(ds, b) - loss(sm, b)) / (2 * eps)
+        an_s = (q[v, sl] * dw[v, sl]).sum()
+        assert abs(fd_s - an_s) <= 1e-6 * max(1.0, abs(fd_s)), (v, grp)
+
+
+def test_dw_worked_example_two_rows():
+    # One token, two vocab rows, no cap: raw = (a, b), p = softmax(raw),
+    # target 0: dW[0] = g (1 - p0) h, dW[1] = -g p1 h.
+    wq = np.zeros((2, 16), dtype=np.uint32)
+    wq[0, :] = 0x11111111        # codes 1
+    wq[1, :] = 0x22222222        # codes 2
+    s = np.array([[0.01, 0.01], [0.01, 0.01]])
+    b = np.zeros((2, 2))
+    head = oracle.Head(wq, s, b, 4, 64, 0.0)
+    h = np.linspace(-1.0, 1.0, 128)[None, :]
+    hs = h.sum()
+    a0, a1 = 0.01 * hs, 0.02 * hs
+    p0 = 1.0 / (1.0 + math.exp(a1 - a0))
+    g = 0.75
+    dw = oracle.grad_head(h, head, [0], g)
+    assert np.allclose(dw[0], g * (1 - p0) * h[0], atol=1e-14)
+    assert np.allclose(dw[1], -g * (1 - p0) * h[0], atol=1e-14)
+
+
+def test_dw_column_sums_vanish_without_cap():
+    # No cap: sum_v (1[v = t] - p_v) = 0 for every row, so sum_v dW[v, :] = 0.
+    wl = synth.make_workload("tiny")
+    head = oracle.Head(wl.head.wq, wl.head.scales, wl.head.biases, 4, 64, 0.0)
+    g = synth.make_dlogp(wl.M, seed=23)
+    dw = oracle.grad_head(wl.h, head, wl.targets, g)
+    assert np.abs(dw.sum(axis=0)).max() <= 1e-12 * max(1.0, np.abs(dw).max())
+    # ...and a soft cap breaks it (the sech2 factors differ per vocab row)
+    capped = oracle.Head(wl.head.wq, wl.head.scales, wl.head.biases, 4, 64, 2.0)
+    assert np.abs(oracle.grad_head(wl.h, capped, wl.targets, g).sum(axis=0)).max() > 1e-6
+
+
+def test_dw_single_vocab_row_and_mask():
+    head = synth.make_head(1, 128, 4, seed=24)
+    oh = oracle.Head(head.wq, head.scales, head.biases, 4, 64, 30.0)
+    h = synth.make_hidden(3, 128, seed=24)
+    assert np.abs(oracle.grad_head(h, oh, [0, 0, 0], 1.0)).max() < 1e-13
+    # masked rows contribute nothing: equal to the gradient of the active rows alone
+    head = synth.make_head(300, 128, 8, seed=25)
+    oh = oracle.Head(head.wq, head.scales, head.biases, 8, 64, 0.0)
+    h = synth.make_hidden(6, 128, seed=25)
+    t = synth.make_targets(6, 300, seed=25)
+    g = synth.make_dlogp(6, seed=25)
+    mask = np.array([0, 1, 1, 0, 1, 0], dtype=np.uint8)
+    act = mask == 1
+    a = oracle.grad_head(h, oh, t, g, mask=mask)
+    b = oracle.grad_head(h[act], oh, t[act], g[act])
+    assert np.allclose(a, b, atol=1e-13, rtol=0)
