@@ -167,11 +167,44 @@ int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,
  *   dh        device, float [M, H] row-major, 16-byte aligned.  Every row is
  *             written; inactive rows are exactly 0.
  *   workspace device, >= qhead_bwd_workspace(head, M) bytes, 256-byte aligned.
- * The result is deterministic: fixed-order reductions, no float atomics.
+ * The result is deterministic: fixed-order reductions; where vocab chunks add
+ * into a partial buffer, each element receives one addition per chunk, in
+ * chunk order.
  */
 int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
               const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes qhead_bwd_dw needs for M rows with this head ((size_t)-1 on
+ * invalid arguments).
+ */
+size_t qhead_bwd_dw_workspace(const qhead_head* head, int64_t M);
+
+/*
+ * Backward with the head gradient: dw = d(sum_m dlogp[m] * logp[m]) / dW with
+ * respect to the dequantized head W[v, d] = scale * q + bias, and optionally
+ * dh as qhead_bwd computes it, from one pass of logit recomputation.
+ * Definition: the classifier gradient (dC) of the Apple CCE reference that
+ * the page "mlx-bun 0.0.4 -> 0.0.6" (src/train/flash-cce.ts) cites; the pages
+ * compute none because their head is frozen:
+ *     dw[v, :] = sum_m dlogp[m] * (1[v == target_m] - softmax[m, v]) * sech2[m, v] * h[m, :].
+ * From it, d/dscale[v, g] = sum_{d in g} q[v, d] * dw[v, d] and
+ * d/dbias[v, g] = sum_{d in g} dw[v, d] (the codes are not differentiable).
+ *   h, M, targets, mask, lse, dlogp  as for qhead_bwd.
+ *   dh        device, float [M, H], 16-byte aligned, or NULL (not computed).
+ *   dw        device, float [V, H] row-major, 32-byte aligned; every element is
+ *             written (M == 0 or no active row: all zeros).
+ *   workspace device, >= qhead_bwd_dw_workspace(head, M) bytes, 256-byte aligned.
+ * Every M takes the tensor-core path (dw reuses its per-chunk coefficient
+ * blocks).  A row whose target lies outside [0, V) contributes its softmax
+ * term but no one-hot term.  If a kernel wait expires, every element of dw is
+ * NaN.  The result is deterministic: each dw element is written once, and the
+ * rows that share a target are summed in row order.
+ */
+int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                 const uint8_t* mask, const float* lse, const float* dlogp, float* dh, float* dw,
+                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Forward without a workspace argument, for callers that cannot allocate

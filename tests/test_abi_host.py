@@ -146,3 +146,17 @@ def test_bad_verify_args(L, kw, code):
 
 def test_verify_zero_windows_is_a_no_op(L):
     assert _verify(L, B=0, ws=None, ws_bytes=0) == qhead.QHEAD_OK
+
+
+def test_bad_bwd_dw_args(L):
+    a = dict(h=0x40000, targets=0x41000, lse=0x42000, dlogp=0x43000, dh=None, dw=0x44000)
+    fn = L.qhead_bwd_dw
+    assert fn(ctypes.byref(_head()), a["h"], 4, a["targets"], None, a["lse"], a["dlogp"], None,
+              None, 0x60000, 1 << 20, None) == qhead.QHEAD_EINVAL       # no dw
+    assert fn(ctypes.byref(_head()), a["h"], 4, a["targets"], None, a["lse"], a["dlogp"], None,
+              0x44010, 0x60000, 1 << 20, None) == qhead.QHEAD_EINVAL    # dw not 32-byte aligned
+    assert "32-byte" in L.qhead_last_error().decode()
+    assert fn(ctypes.byref(_head()), None, 4, a["targets"], None, a["lse"], a["dlogp"], None,
+              a["dw"], 0x60000, 1 << 20, None) == qhead.QHEAD_EINVAL    # no h
+    assert L.qhead_bwd_dw_workspace(ctypes.byref(_head()), 100) >= \
+        L.qhead_bwd_workspace(ctypes.byref(_head()), 100)

@@ -97,3 +97,18 @@ def test_disarmed_switch_has_no_effect():
     head, h, t, mk, _ = to_dev(wl)
     logp, lse, am = gpu_fwd(head, h, t, mk)
     check_fwd(wl, np.arange(wl.M), logp, lse, am)
+
+
+def test_head_gradient_wait_expires_then_recovers():
+    M = 150
+    mask = synth.make_mask(M, 16, 0.3)
+    wl = _workload(M, 256, 2200, 4, 30.0, seed=43, mask=mask)
+    head, h, t, mk, g = to_dev(wl)
+    lse = qhead.fwd(head, h, t, mk)[1]
+    qhead.test_stall_next_call(True)
+    _, dw = qhead.bwd_dw(head, h, t, lse, g, mk)
+    torch.cuda.synchronize()
+    assert torch.isnan(dw).all()
+    _, dw = qhead.bwd_dw(head, h, t, lse, g, mk)
+    torch.cuda.synchronize()
+    assert torch.isfinite(dw).all()

@@ -94,8 +94,10 @@ struct BwdPlan {
     int grid = 0;
     int S = 1;               // vocab splits of the CUDA-core path
     int64_t chunk = 0;       // vocab rows per coefficient block (tensor-core path)
+    bool dw = false;         // head gradient requested: the regions below are planned
     size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_coeff = 0, off_dhp = 0,
-           total = 0;
+           off_hp = 0, off_g = 0, off_dmax = 0, off_cnt = 0, off_offs = 0, off_cursor = 0,
+           off_idx = 0, total = 0;
 };
 
 // Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block is
@@ -159,13 +161,16 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
     return QHEAD_OK;
 }
 
-int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p) {
+// with_dw: the head gradient is requested too; it reuses the tensor-core
+// path's coefficient blocks, so that path is taken for every M.
+int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false) {
     DevInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    p->tc = M >= kTcMinM;
+    p->tc = M >= kTcMinM || with_dw;
+    p->dw = with_dw;
     size_t off = 0;
     p->off_count = off; off = align_up(off + 16, 256);
     p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
@@ -187,7 +192,16 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p) {
         p->S = dh_slices(p->Mpad, hd->H, p->grid, (last < chunk ? last : chunk) / 64);
         p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
         p->off_coeff = off; off = align_up(off + 2 * (size_t)p->Mpad * p->chunk, 1024);
-        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 256);
+        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 1024);
+        if (with_dw) {
+            p->off_hp = off;     off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
+            p->off_g = off;      off = align_up(off + 4 * (size_t)p->Mpad, 256);
+            p->off_dmax = off;   off = align_up(off + 16, 256);
+            p->off_cnt = off;    off = align_up(off + 4 * (size_t)hd->V, 256);
+            p->off_offs = off;   off = align_up(off + 4 * ((size_t)hd->V + 1), 256);
+            p->off_cursor = off; off = align_up(off + 4 * (size_t)hd->V, 256);
+            p->off_idx = off;    off = align_up(off + 4 * (size_t)p->Mpad, 256);
+        }
     } else {
         const int tb = qh::bwd_simt_tokens(hd->H);
         const int64_t groups = (M + tb - 1) / tb;
@@ -327,25 +341,46 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     return QHEAD_OK;
 }
 
-int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
-              const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
-              void* workspace, size_t workspace_bytes, void* stream) {
+size_t qhead_bwd_dw_workspace(const qhead_head* head, int64_t M) {
+    g_err.clear();
+    if (check_head(head)) return (size_t)-1;
+    if (M < 0) { fail(QHEAD_EINVAL, "M < 0"); return (size_t)-1; }
+    if (M == 0) return 0;
+    BwdPlan p;
+    if (plan_bwd(head, M, &p, true)) return (size_t)-1;
+    return p.total;
+}
+
+// The backward chain: dh (if dh != NULL) and the head gradient (if dw != NULL).
+static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                    const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
+                    float* dw, void* workspace, size_t workspace_bytes, void* stream) {
     g_err.clear();
     const int stall = take_stall();
     int rc = check_head(head);
     if (rc) return rc;
     if (M < 0) return fail(QHEAD_EINVAL, "M < 0");
     if (M >= ((int64_t)1 << 31) - qh::kRowPad) return fail(QHEAD_EINVAL, "M too large");
-    if (M == 0) return QHEAD_OK;
-    if (!h || !targets || !lse || !dlogp || !dh)
-        return fail(QHEAD_EINVAL, "h, targets, lse, dlogp and dh are required");
+    if (M == 0 && !dw) return QHEAD_OK;
+    if (!dh && !dw) return fail(QHEAD_EINVAL, "dh (or, in qhead_bwd_dw, dw) is required");
+    if (dw && reinterpret_cast<uintptr_t>(dw) % 32)
+        return fail(QHEAD_EINVAL, "dw must be 32-byte aligned");
+    if (M == 0) {  // no rows: nothing for dh; the head gradient is zero
+        if (!dw) return QHEAD_OK;
+        cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)head->V * head->H,
+                                        static_cast<cudaStream_t>(stream));
+        return e ? cuda_fail(e, "dw zero") : QHEAD_OK;
+    }
+    if (!h || !targets || !lse || !dlogp)
+        return fail(QHEAD_EINVAL, "h, targets, lse and dlogp are required");
     if (reinterpret_cast<uintptr_t>(h) % 16) return fail(QHEAD_EINVAL, "h must be 16-byte aligned");
-    if (reinterpret_cast<uintptr_t>(dh) % 16) return fail(QHEAD_EINVAL, "dh must be 16-byte aligned");
+    if (dh && reinterpret_cast<uintptr_t>(dh) % 16)
+        return fail(QHEAD_EINVAL, "dh must be 16-byte aligned");
     if (!workspace) return fail(QHEAD_EINVAL, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(workspace) % 256)
         return fail(QHEAD_EINVAL, "workspace must be 256-byte aligned");
     BwdPlan p;
-    rc = plan_bwd(head, M, &p);
+    rc = plan_bwd(head, M, &p, dw != nullptr);
     if (rc) return rc;
     if (workspace_bytes < p.total)
         return fail(QHEAD_EINVAL, "workspace too small: need " + std::to_string(p.total) + " bytes");
@@ -375,7 +410,24 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
             if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
                 return cuda_fail(e, "convert_h");
         }
-        CUtensorMap th, tw_logit, tcoef, tw_dh;
+        // Head gradient: max |dlogp|, the scaled fp16 h', the one-hot terms and
+        // the per-target row lists, once per call.
+        __half* hp = p.dw ? at<__half>(workspace, p.off_hp) : nullptr;
+        float* g = p.dw ? at<float>(workspace, p.off_g) : nullptr;
+        float* dmax = p.dw ? at<float>(workspace, p.off_dmax) : nullptr;
+        int* offs = p.dw ? at<int>(workspace, p.off_offs) : nullptr;
+        int* idx = p.dw ? at<int>(workspace, p.off_idx) : nullptr;
+        if (p.dw &&
+            (e = qh::launch_dw_prep(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+                                    rows, count, targets, dlogp, p.Mpad, dmax, hp, g,
+                                    at<int>(workspace, p.off_cnt), offs,
+                                    at<int>(workspace, p.off_cursor), idx, st)))
+            return cuda_fail(e, "dw_prep");
+        CUtensorMap th, tw_logit, tcoef, tw_dh, tcoef_t{}, thp{};
+        if (p.dw && (!qh::tmap_rows_f16_sw128(&tcoef_t, at<__half>(workspace, p.off_coeff),
+                                               p.chunk, p.Mpad, 64) ||
+                     !qh::tmap_rows_f16_sw128(&thp, hp, head->H, p.Mpad, 64)))
+            return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
         const int wpr = head->H * head->bits / 32;
         if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
             !(head->bits == 8 ? qh::tmap_packed_rows_swz : qh::tmap_packed_rows)(
@@ -402,18 +454,32 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
             ta.coeff_rows = (int)p.Mpad;
             if ((e = qh::launch_tc_fwd(th, tw_logit, ta, head->bits, true, p.grid, st)))
                 return cuda_fail(e, "tc_coeff");
-            qh::TcDhArgs da{};
-            da.scales = sc; da.biases = bi; da.V = head->V; da.H = head->H;
-            da.count = count; da.err = err; da.rows = rows; da.dlogp = dlogp; da.dh_acc = dhp;
-            da.slice_stride = p.Mpad * head->H;
-            da.v_begin = (int64_t)vt0 * tr;
-            da.n_k = (vt1 - vt0) * tr / 64;
-            da.ks = p.S;  // <= the K steps of every chunk (plan_bwd)
-            da.accumulate = c > 0;
-            if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
-                return cuda_fail(e, "tc_dh");
+            if (dh) {
+                qh::TcDhArgs da{};
+                da.scales = sc; da.biases = bi; da.V = head->V; da.H = head->H;
+                da.count = count; da.err = err; da.rows = rows; da.dlogp = dlogp; da.dh_acc = dhp;
+                da.slice_stride = p.Mpad * head->H;
+                da.v_begin = (int64_t)vt0 * tr;
+                da.n_k = (vt1 - vt0) * tr / 64;
+                da.ks = p.S;  // <= the K steps of every chunk (plan_bwd)
+                da.accumulate = c > 0;
+                if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
+                    return cuda_fail(e, "tc_dh");
+            }
+            if (dw) {
+                qh::TcDwArgs wa{};
+                wa.V = head->V; wa.H = head->H; wa.count = count; wa.err = err;
+                wa.v_begin = (int64_t)vt0 * tr;
+                wa.chunk_rows = (vt1 - vt0) * tr;
+                wa.dmax = dmax; wa.offs = offs; wa.idx = idx; wa.g = g; wa.rows = rows;
+                wa.h = hb; wa.dw = dw;
+                if ((e = qh::launch_tc_dw(tcoef_t, thp, wa, p.grid, st)))
+                    return cuda_fail(e, "tc_dw");
+            }
         }
         hook_after(st);
+        if (dw && (e = qh::launch_dw_poison(err, dw, head->V * (int64_t)head->H, st)))
+            return cuda_fail(e, "dw_poison");
     } else {
         if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
             return cuda_fail(e, "compact");
@@ -423,10 +489,29 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         hook_after(st);
         if (e) return cuda_fail(e, "bwd_simt");
     }
-    if ((e = qh::launch_bwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+    if (dh &&
+        (e = qh::launch_bwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
                                      pos, targets, dlogp, dhp, p.S, p.Mpad, err, dh, M, st)))
         return cuda_fail(e, "bwd_finalize");
     return QHEAD_OK;
+}
+
+int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+              const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
+              void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, workspace,
+                    workspace_bytes, stream);
+}
+
+int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                 const uint8_t* mask, const float* lse, const float* dlogp, float* dh, float* dw,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (!dw) {
+        g_err.clear();
+        return fail(QHEAD_EINVAL, "dw is required (qhead_bwd computes dh alone)");
+    }
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, dw, workspace, workspace_bytes,
+                    stream);
 }
 
 int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,

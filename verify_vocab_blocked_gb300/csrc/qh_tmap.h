@@ -80,6 +80,24 @@ struct TcDhArgs {
     int accumulate;       // 0: write, 1: add to dh_acc
 };
 
+// Arguments of the head-gradient contraction (one vocab chunk).
+struct TcDwArgs {
+    int64_t V;
+    int H;
+    const int* count;          // active rows (device)
+    int* err;                  // error word (device)
+    int stall;                 // test switch: the producer issues no loads (waits expire)
+    int64_t v_begin;           // first vocab row of the chunk
+    int chunk_rows;            // vocab rows of the chunk (<= the coefficient block's columns)
+    const float* dmax;         // max |dlogp| over the active rows (device scalar)
+    const int* offs;           // [V + 1] one-hot list offsets
+    const int* idx;            // one-hot lists: compact rows, ascending per target
+    const float* g;            // [Mpad] dlogp * sech2(target logit) per compact row
+    const int* rows;           // compact -> original row
+    const __nv_bfloat16* h;    // [M, H] original hidden states
+    float* dw;                 // [V, H] output, 32-byte aligned
+};
+
 int tc_dh_cols(int H);          // hidden columns per output tile (256 or 128)
 int tc_dh_words(int H, int bits);
 // True when the dh kernel takes its packed tile as 128-byte-swizzled halves
@@ -90,6 +108,18 @@ cudaError_t launch_tc_dh(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w, c
                          int bits, int grid, cudaStream_t st);
 
 int tc_fwd_smem_bytes(int bits);
+int tc_dw_smem_bytes(int H);
+// max |dlogp|, the scaled fp16 copy h' and the one-hot terms g, and the
+// per-target row lists (counting sort, stable in row order).
+cudaError_t launch_dw_prep(const uint32_t* wq, const __half* scales, const __half* biases,
+                           int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
+                           const int* rows, const int* count, const int32_t* targets,
+                           const float* dlogp, int64_t Mpad, float* dmax, __half* hp, float* g,
+                           int* cnt, int* offs, int* cursor, int* idx, cudaStream_t st);
+cudaError_t launch_tc_dw(const CUtensorMap& tmap_c, const CUtensorMap& tmap_hp, const TcDwArgs& a,
+                         int grid, cudaStream_t st);
+// Writes NaN to all of dw [V, H] if the error word is set (a wait expired).
+cudaError_t launch_dw_poison(const int* err, float* dw, int64_t n, cudaStream_t st);
 cudaError_t launch_tc_fwd(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
                           const TcFwdArgs& a, int bits, bool coeff_epilogue, int grid,
                           cudaStream_t st);

@@ -21,7 +21,8 @@ QHEAD_SB_F16 = 0
 # Every symbol include/qhead.h declares.
 EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd",
            "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel",
-           "qhead_fwd_noalloc", "qhead_test_stall_next_call", "qhead_verify")
+           "qhead_fwd_noalloc", "qhead_test_stall_next_call", "qhead_verify",
+           "qhead_bwd_dw_workspace", "qhead_bwd_dw")
 
 
 class CHead(ctypes.Structure):
@@ -55,10 +56,14 @@ def lib() -> ctypes.CDLL:
     L.qhead_fwd_workspace.restype = sz
     L.qhead_bwd_workspace.argtypes = [hp, i64]
     L.qhead_bwd_workspace.restype = sz
+    L.qhead_bwd_dw_workspace.argtypes = [hp, i64]
+    L.qhead_bwd_dw_workspace.restype = sz
     L.qhead_fwd.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_fwd.restype = ctypes.c_int
     L.qhead_bwd.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_bwd.restype = ctypes.c_int
+    L.qhead_bwd_dw.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.qhead_bwd_dw.restype = ctypes.c_int
     L.qhead_verify.argtypes = [hp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_verify.restype = ctypes.c_int
     L.qhead_last_error.argtypes = []
@@ -157,6 +162,13 @@ def bwd_workspace(head: Head, M: int) -> int:
     return int(n)
 
 
+def bwd_dw_workspace(head: Head, M: int) -> int:
+    n = lib().qhead_bwd_dw_workspace(ctypes.byref(head.c()), M)
+    if n == ctypes.c_size_t(-1).value:
+        raise QheadError(QHEAD_EINVAL, last_error())
+    return int(n)
+
+
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
     """A 256-byte aligned device buffer of at least nbytes (torch allocations are)."""
     return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
@@ -197,6 +209,26 @@ def bwd(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
                            lse.data_ptr(), dlogp.data_ptr(), dh.data_ptr(), workspace.data_ptr(),
                            workspace.numel(), _stream(stream)))
     return dh
+
+
+def bwd_dw(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+           dlogp: torch.Tensor, mask: torch.Tensor | None = None, *, want_dh: bool = False,
+           workspace: torch.Tensor | None = None, stream=None):
+    """(dh [M, H] float32 or None, dw [V, H] float32): the gradients of
+    sum_m dlogp[m] * logp[m] with respect to h and to the dequantized head."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
+    M = h.shape[0]
+    dev = h.device
+    dh = torch.empty(M, head.H, dtype=torch.float32, device=dev) if want_dh else None
+    dw = torch.empty(head.V, head.H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(bwd_dw_workspace(head, M), dev)
+    _check(lib().qhead_bwd_dw(ctypes.byref(head.c()), h.data_ptr(), M, targets.data_ptr(),
+                              _ptr(mask), lse.data_ptr(), dlogp.data_ptr(), _ptr(dh),
+                              dw.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                              _stream(stream)))
+    return dh, dw
 
 
 def verify(head: Head, h: torch.Tensor, W: int, draft: torch.Tensor | None,
