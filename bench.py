@@ -156,7 +156,7 @@ class ClockSampler:
 class Runner:
     """Device buffers for one workload and the C-ABI calls of one step."""
 
-    def __init__(self, wl: synth.Workload, device):
+    def __init__(self, wl: synth.Workload, device, with_dw: bool = False):
         import torch
         from verify_vocab_blocked_gb300 import qhead
         self.torch, self.q = torch, qhead
@@ -170,6 +170,7 @@ class Runner:
         self.h_host = torch.from_numpy(wl.h.astype(np.int16)).view(torch.bfloat16).pin_memory()
         self.h = self.h_host.to(device)
         self.bwd = bool(wl.cfg["bwd"])
+        self.with_dw = with_dw and self.bwd  # the backward also returns the head gradient
         self.t_host = (torch.from_numpy(wl.targets).pin_memory()
                        if wl.targets is not None else None)
         self.t = self.t_host.to(device) if self.t_host is not None else None
@@ -182,16 +183,19 @@ class Runner:
         self.lse = torch.empty(M, dtype=f32, device=device)
         self.am = torch.empty(M, dtype=i32, device=device)
         self.dh = torch.empty(M, wl.head.H, dtype=f32, device=device) if self.bwd else None
+        self.dw = (torch.empty(wl.head.V, wl.head.H, dtype=f32, device=device)
+                   if self.with_dw else None)
         n = qhead.fwd_workspace(self.head, M)
         if self.bwd:
-            n = max(n, qhead.bwd_workspace(self.head, M))
+            n = max(n, qhead.bwd_dw_workspace(self.head, M) if self.with_dw
+                    else qhead.bwd_workspace(self.head, M))
         self.ws = qhead.alloc_workspace(n, device)
         self.chead = self.head.c()
         self.stream = torch.cuda.current_stream(device)
         # pinned outputs for the end-to-end leg
         self.out_host = {k: torch.empty_like(v, device="cpu").pin_memory()
                          for k, v in (("lse", self.lse), ("am", self.am), ("logp", self.logp),
-                                      ("dh", self.dh)) if v is not None}
+                                      ("dh", self.dh), ("dw", self.dw)) if v is not None}
         self.launches_per_step = None  # counted on the device by count_launches()
         self.active = int(wl.mask.sum()) if wl.mask is not None else M
 
@@ -212,10 +216,16 @@ class Runner:
         if self.bwd:
             if ev_bwd is not None:
                 L.qhead_time_next_head_kernel(ev_bwd[0].cuda_event, ev_bwd[1].cuda_event)
-            rc = L.qhead_bwd(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
-                             self.t.data_ptr(), self._ptr(self.mk), self.lse.data_ptr(),
-                             self.g.data_ptr(), self.dh.data_ptr(), self.ws.data_ptr(),
-                             self.ws.numel(), self.stream.cuda_stream)
+            if self.with_dw:
+                rc = L.qhead_bwd_dw(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
+                                    self.t.data_ptr(), self._ptr(self.mk), self.lse.data_ptr(),
+                                    self.g.data_ptr(), self.dh.data_ptr(), self.dw.data_ptr(),
+                                    self.ws.data_ptr(), self.ws.numel(), self.stream.cuda_stream)
+            else:
+                rc = L.qhead_bwd(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
+                                 self.t.data_ptr(), self._ptr(self.mk), self.lse.data_ptr(),
+                                 self.g.data_ptr(), self.dh.data_ptr(), self.ws.data_ptr(),
+                                 self.ws.numel(), self.stream.cuda_stream)
             if rc:
                 raise RuntimeError(self.q.last_error())
 
@@ -230,7 +240,8 @@ class Runner:
 
     def d2h(self):
         n = 0
-        for k, dev in (("lse", self.lse), ("am", self.am), ("logp", self.logp), ("dh", self.dh)):
+        for k, dev in (("lse", self.lse), ("am", self.am), ("logp", self.logp), ("dh", self.dh),
+                       ("dw", self.dw)):
             if dev is not None:
                 self.out_host[k].copy_(dev, non_blocking=True)
                 n += dev.numel() * dev.element_size()
@@ -293,10 +304,11 @@ def aggregate(elapsed_ms: float, units: float, world: int, dist=None) -> tuple[f
     return elapsed_ms, units
 
 
-def cpu_baseline(wl: synth.Workload, budget_s: float = 12.0, max_reps: int = 64) -> dict:
+def cpu_baseline(wl: synth.Workload, budget_s: float = 12.0, max_reps: int = 64,
+                 with_dw: bool = False) -> dict:
     """The fp64 oracle, as it stands, on a bounded sample: one row of the
-    workload (full vocab), forward (+ backward for training configs), repeated
-    until the budget is spent."""
+    workload (full vocab), forward (+ backward, and the head gradient with
+    with_dw, for training configs), repeated until the budget is spent."""
     import oracle
     oh = oracle.Head(wl.head.wq, wl.head.scales, wl.head.biases, wl.head.bits, wl.head.group,
                      wl.head.softcap)
@@ -310,13 +322,16 @@ def cpu_baseline(wl: synth.Workload, budget_s: float = 12.0, max_reps: int = 64)
         f = oracle.forward(wl.h[r], oh, tg)
         if bwd:
             oracle.backward(wl.h[r], oh, tg, wl.dlogp[r].astype(np.float64), lse=f.lse)
+            if with_dw:
+                oracle.grad_head(wl.h[r], oh, tg, wl.dlogp[r].astype(np.float64), lse=f.lse)
         reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
     return {"value": reps / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{reps} x 1 row of the workload (full V={wl.head.V}), "
-                      f"{'fwd+bwd' if bwd else 'fwd'}, fp64, {el:.1f} s"}
+                      f"{('fwd+bwd+dW' if with_dw else 'fwd+bwd') if bwd else 'fwd'}, fp64, "
+                      f"{el:.1f} s"}
 
 
 def run_ours(args):
@@ -332,7 +347,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = synth.CONFIGS[args.config]
     wl = synth.make_workload(args.config, seed=0)
-    R = Runner(wl, dev)
+    R = Runner(wl, dev, with_dw=args.with_dw)
     K, W = args.steps, args.warmup
 
     # warm-up (also creates the timing events)
@@ -398,17 +413,22 @@ def run_ours(args):
         # dominant work: the backward head phase (logits recomputed, 2*Ma*V*H,
         # and the dh contraction, 2*Ma*V*H).  On the tensor-core path (M >= 64)
         # it is a chain of two kernels per vocab chunk, timed as one region.
-        tc = R.M >= 64
-        dom = "tc_bwd_chain" if tc else "bwd_simt_kernel"
-        flops = 4.0 * R.active * cfg["V"] * cfg["H"]
+        # With the head gradient (--with-dw) a third contraction per chunk,
+        # 2*Ma*V*H more, joins the chain (which then runs for every M).
+        tc = R.M >= 64 or R.with_dw
+        dom = ("tc_bwd_chain_dw" if R.with_dw else "tc_bwd_chain") if tc else "bwd_simt_kernel"
+        nmul = 6.0 if R.with_dw else 4.0
+        flops = nmul * R.active * cfg["V"] * cfg["H"]
         kms = statistics.mean(bwd_ms)
         achieved = flops / (kms / 1e3) / 1e12
-        roof = {"kernel": ("tc_fwd_kernel<coefficient epilogue> + tc_dh_kernel per vocab chunk"
-                           if tc else dom),
+        kname = "tc_fwd_kernel<coefficient epilogue> + tc_dh_kernel"
+        if R.with_dw:
+            kname += " + tc_dw_kernel"
+        roof = {"kernel": (kname + " per vocab chunk" if tc else dom),
                 "bound": "tensor", "achieved": achieved, "peak": tf_sus,
                 "unit": "TFLOP/s", "frac": achieved / tf_sus,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (dense, same rate as fp16)",
-                "work_per_launch": f"{flops:.3e} flop (4*Ma*V*H, Ma = active rows)",
+                "work_per_launch": f"{flops:.3e} flop ({int(nmul)}*Ma*V*H, Ma = active rows)",
                 "ms_per_launch": kms}
         fms = statistics.mean(fwd_ms)
         ff = 2.0 * R.active * cfg["V"] * cfg["H"]
@@ -417,9 +437,10 @@ def run_ours(args):
                               "achieved_tflops": ff / (fms / 1e3) / 1e12,
                               "frac": ff / (fms / 1e3) / 1e12 / tf_sus}
         step_ms = el_max / K
-        roof["step"] = {"flop": 6.0 * R.active * cfg["V"] * cfg["H"], "ms": step_ms,
-                        "achieved_tflops": 6.0 * R.active * cfg["V"] * cfg["H"] / (step_ms / 1e3) / 1e12,
-                        "frac": 6.0 * R.active * cfg["V"] * cfg["H"] / (step_ms / 1e3) / 1e12 / tf_sus}
+        sf = (nmul + 2.0) * R.active * cfg["V"] * cfg["H"]
+        roof["step"] = {"flop": sf, "ms": step_ms,
+                        "achieved_tflops": sf / (step_ms / 1e3) / 1e12,
+                        "frac": sf / (step_ms / 1e3) / 1e12 / tf_sus}
     else:
         dom = "stream_fwd_kernel"
         nbytes = head_bytes(cfg)
@@ -439,6 +460,7 @@ def run_ours(args):
                         if args.config in PAGES_TOKENS_PER_S else None),
         "dtype": "f16", "data": "synthetic (seeded; no real weights or data)",
         "config": dict(workload_desc(args.config, cfg),
+                       **({"pass": "fwd+bwd (dh and dW)"} if R.with_dw else {}),
                        kernel_timing="CUDA events around the head kernel on every "
                                      + (f"{stride}th timed step" if stride > 1 else "timed step")),
         "roofline": roof,
@@ -450,7 +472,7 @@ def run_ours(args):
         "impl": "ours",
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, with_dw=R.with_dw)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -478,6 +500,8 @@ def run_reference(args):
         f = oracle.forward(wl.h[r], oh, tg)
         if bwd:
             oracle.backward(wl.h[r], oh, tg, wl.dlogp[r].astype(np.float64), lse=f.lse)
+            if args.with_dw:
+                oracle.grad_head(wl.h[r], oh, tg, wl.dlogp[r].astype(np.float64), lse=f.lse)
 
     cap_s = 180.0
     w0 = time.perf_counter()
@@ -495,7 +519,8 @@ def run_reference(args):
     el = time.perf_counter() - t0
     value = done / el
     sample = (f"{done} of {args.steps} steps (time cap {cap_s:.0f} s), each 1 row of the workload "
-              f"(full V={cfg['V']}), {'fwd+bwd' if bwd else 'fwd'}, fp64")
+              f"(full V={cfg['V']}), "
+              f"{('fwd+bwd+dW' if args.with_dw else 'fwd+bwd') if bwd else 'fwd'}, fp64")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", 1)),
         "steps": done, "warmup": args.warmup, "ms_per_step": el / max(done, 1) * 1e3,
@@ -517,6 +542,9 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--with-dw", action="store_true",
+                    help="training configs: the backward also returns the head gradient dW "
+                         "(qhead_bwd_dw)")
     ap.add_argument("--no-launch-count", action="store_true",
                     help="skip the CUPTI launch count (for runs under a profiler)")
     args = ap.parse_args(argv)
