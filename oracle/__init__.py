@@ -16,6 +16,9 @@ them (page "mlx-bun 0.0.4 -> 0.0.6", src/train/flash-cce.ts):
 5. dh = sum_v dlogp*(onehot - exp(z - lse))*sech2 * w[v,:]
 6. (the head gradient, a variant the pages leave out because their head is
    frozen) dW[v,:] = sum_m dlogp*(onehot - exp(z - lse))*sech2 * h[m,:]
+7. (the approximate blockMax early exit) per-vocab-tile maxima of z, and dh
+   with the (row tile, vocab tile) blocks whose rows all lie below
+   lse + ln(eps) and hold no target dropped
 
 and the speculative-decode accept step (page "mlx-bun 0.0.8 -> 0.0.10",
 src/spec/generate.ts): per window of gamma + 1 positions, the longest prefix of
@@ -296,6 +299,57 @@ def grad_head(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
     dw = np.empty((V, head.H), dtype=np.float64)
     _load().oracle_dw(M, head.H, V, _ptr(raw, _f64p), _ptr(hf, _f64p), _ptr(dw, _f64p), threads)
     return dw
+
+
+# ------------------------------------------------- blockMax early exit (approximate)
+
+def block_max(h: np.ndarray, head: Head, mask=None, tile: int = 256, threads: int = 0) -> np.ndarray:
+    """bm[m, k] = max of the capped logits z[m, v] over vocab tile k (rows
+    k*tile .. k*tile + tile - 1), -inf on masked rows: the per-block maxima the
+    vocab-parallel forward hands to its backward (page "mlx-bun 0.0.4 ->
+    0.0.6", src/train/flash-cce.ts, blockMax), over fixed vocab tiles."""
+    raw = logits(h, head, threads)
+    M, V = raw.shape
+    z = head.softcap * np.tanh(raw / head.softcap) if head.softcap > 0 else raw
+    nt = (V + tile - 1) // tile
+    zp = np.full((M, nt * tile), -np.inf)
+    zp[:, :V] = z
+    bm = zp.reshape(M, nt, tile).max(axis=2)
+    mk = _mask(mask, M)
+    if mk is not None:
+        bm[mk == 0] = -np.inf
+    return bm
+
+
+def backward_blockskip(h: np.ndarray, head: Head, targets, dlogp, lse, bm, eps: float,
+                       mask=None, tile_rows: int = 128, tile: int = 256,
+                       threads: int = 0) -> np.ndarray:
+    """The approximate dh of the blockMax early exit (same page, the
+    backward's block skip): the active rows, in ascending order, form tiles
+    of tile_rows; a (row tile, vocab tile) block is dropped -- its
+    coefficients left out of dh = coeff . W -- when every row of the tile has
+    exp(bm[m, k] - lse[m]) < eps and no row's target lies in vocab tile k.
+    The decision uses the given bm and lse (those the caller's forward
+    returned)."""
+    coeff = _coeff(h, head, targets, dlogp, mask, lse, threads)
+    M, V = coeff.shape
+    t = np.asarray(targets, dtype=np.int64)
+    act = np.arange(M) if mask is None else np.nonzero(np.asarray(mask))[0]
+    lse = np.asarray(lse, dtype=np.float64)
+    bm = np.asarray(bm, dtype=np.float64)
+    for j0 in range(0, len(act), tile_rows):
+        rows = act[j0:j0 + tile_rows]
+        below = np.exp(bm[rows] - lse[rows, None]) < eps        # [rows, tiles]
+        drop = below.all(axis=0)
+        drop[t[rows] // tile] = False
+        for k in np.nonzero(drop)[0]:
+            coeff[rows, k * tile:(k + 1) * tile] = 0.0
+    wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
+    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    dh = np.empty((M, head.H), dtype=np.float64)
+    _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
+                      _ptr(b, _f64p), _ptr(coeff, _f64p), _ptr(dh, _f64p), threads)
+    return dh
 
 
 # ------------------------------------------------------------ verify accept

@@ -14,7 +14,11 @@
   row maximum;
 * the head gradient dW: torch fp64 autograd with respect to the dense head,
   finite differences with respect to a group's bias and scale, a two-row
-  closed form, vanishing column sums without the cap, V = 1 and masking.
+  closed form, vanishing column sums without the cap, V = 1 and masking;
+* the blockMax early exit: tile maxima against the row maxima of the C row
+  statistics and a hand example, the approximate dh equal to the exact one at
+  eps = 0 and within |dlogp| eps sum_v |w_v| of it otherwise, and a hand
+  derivation of a row whose tile keeps only its own target's vocab tile.
 """
 import math
 import os
@@ -423,3 +427,83 @@ def test_dw_single_vocab_row_and_mask():
     a = oracle.grad_head(h, oh, t, g, mask=mask)
     b = oracle.grad_head(h[act], oh, t[act], g[act])
     assert np.allclose(a, b, atol=1e-13, rtol=0)
+
+
+# ------------------------------------------- blockMax early exit (approximate)
+
+def test_block_max_pins():
+    # The maximum over a row's tiles is the row's maximum capped logit (from
+    # the C row statistics), every tile maximum lies below lse, and a hand
+    # example: V = 3 rows in one tile of 2 and one of 1.
+    head = synth.make_head(700, 128, 4, softcap=30.0, seed=26)
+    oh = oracle.Head(head.wq, head.scales, head.biases, 4, 64, 30.0)
+    h = synth.make_hidden(6, 128, seed=26)
+    mask = np.array([1, 1, 0, 1, 1, 1], np.uint8)
+    bm = oracle.block_max(h, oh, mask=mask)
+    f = oracle.forward(h, oh, mask=mask)
+    act = mask == 1
+    assert bm.shape == (6, 3)
+    assert np.allclose(bm[act].max(axis=1), f.zmax[act], atol=1e-13)
+    assert (bm[act] <= f.lse[act, None]).all()
+    assert np.isneginf(bm[~act]).all()
+    wq = np.zeros((3, 16), np.uint32)
+    wq[1, :] = 0x11111111
+    wq[2, :] = 0x33333333
+    small = oracle.Head(wq, np.full((3, 2), 0.01), np.zeros((3, 2)), 4, 64, 0.0)
+    x = np.ones((1, 128))
+    assert np.allclose(oracle.block_max(x, small, tile=2)[0], [1.28, 3.84], atol=1e-12)
+
+
+def test_blockskip_reduces_to_exact_and_obeys_its_bound():
+    # one row tile of 40 rows over 32 vocab tiles: most tiles hold no target
+    V = 8192
+    head, hot = synth.make_peaked_head(V, 128, 4, n_hot=4, bias_shift=0.3, softcap=30.0,
+                                       seed=27)
+    oh = oracle.Head(head.wq, head.scales, head.biases, 4, 64, 30.0)
+    M = 40
+    h = synth.make_hidden(M, 128, seed=27, mean=0.5)
+    t = synth.make_targets(M, V, seed=27)
+    g = synth.make_dlogp(M, seed=27).astype(np.float64)
+    mask = synth.make_mask(M, 20, 0.2)
+    f = oracle.forward(h, oh, t, mask=mask)
+    bm = oracle.block_max(h, oh, mask=mask)
+    exact = oracle.backward(h, oh, t, g, mask=mask)
+    # eps = 0 drops nothing
+    assert np.array_equal(oracle.backward_blockskip(h, oh, t, g, f.lse, bm, 0.0, mask=mask), exact)
+    # eps > 0 drops blocks: every dropped coefficient is below |dlogp| eps (sech2 <= 1),
+    # so per row the change is at most |dlogp| eps sum_v |w_v|
+    eps = 1e-4
+    approx = oracle.backward_blockskip(h, oh, t, g, f.lse, bm, eps, mask=mask)
+    wnorm = np.linalg.norm(oracle.dequant(oh), axis=1).sum()
+    act = mask == 1
+    diff = np.linalg.norm(approx - exact, axis=1)
+    assert (diff[act] <= np.abs(g[act]) * eps * wnorm + 1e-12).all()
+    assert diff[act].max() > 0.0           # something was dropped...
+    assert (approx[~act] == 0.0).all()      # ...and masked rows stay exact zeros
+
+
+def test_blockskip_keeps_target_tiles_and_decides_per_row_tile():
+    # 129 active rows: two row tiles (128 + 1).  With an enormous eps every
+    # vocab tile is below it, so only the tiles holding one of the row tile's
+    # targets survive: row 128 (alone in its tile) keeps exactly its own
+    # target's tile.
+    head = synth.make_head(1024, 128, 4, seed=28)
+    oh = oracle.Head(head.wq, head.scales, head.biases, 4, 64, 0.0)
+    M = 129
+    h = synth.make_hidden(M, 128, seed=28)
+    t = synth.make_targets(M, 1024, seed=28)
+    t[128] = 700                                  # tile 2
+    t[:128] = np.where(t[:128] // 256 == 2, 5, t[:128])  # no other row targets tile 2
+    g = np.ones(M)
+    f = oracle.forward(h, oh, t)
+    bm = oracle.block_max(h, oh)
+    approx = oracle.backward_blockskip(h, oh, t, g, f.lse, bm, 1e300)
+    # row 128: dh = (onehot - p) sech2 . W restricted to vocab tile 2
+    raw = oracle.logits(h[128:], oh)[0]
+    p = np.exp(raw - f.lse[128])
+    c = -p
+    c[700] += 1.0
+    c[:512] = 0.0
+    c[768:] = 0.0
+    w = oracle.dequant(oh)
+    assert np.allclose(approx[128], c @ w, atol=1e-12)

@@ -48,7 +48,7 @@ CONFIGS: dict[str, dict] = {
                                 "(8 x 1024-token sequences), H=2560, V=262144, 4-bit, cap 30"),
 }
 
-_STREAMS = {"wq": 1, "scales": 2, "bias_noise": 3, "h": 4, "targets": 5, "dlogp": 6}
+_STREAMS = {"wq": 1, "scales": 2, "bias_noise": 3, "h": 4, "targets": 5, "dlogp": 6, "hot": 7}
 
 
 def _rng(seed: int, stream: str) -> np.random.Generator:
@@ -106,10 +106,27 @@ def make_head(V: int, H: int, bits: int, group: int = 64, softcap: float = 0.0,
                      float(softcap))
 
 
-def make_hidden(M: int, H: int, seed: int = 0) -> np.ndarray:
-    """bf16 bit patterns (uint16 [M,H]) of N(0,1) draws."""
+def make_hidden(M: int, H: int, seed: int = 0, mean: float = 0.0) -> np.ndarray:
+    """bf16 bit patterns (uint16 [M,H]) of N(mean,1) draws."""
     x = _rng(seed, "h").standard_normal(size=(M, H), dtype=np.float32)
+    if mean:
+        x = x + np.float32(mean)
     return f32_to_bf16_bits(x)
+
+
+def make_peaked_head(V: int, H: int, bits: int, n_hot: int, bias_shift: float,
+                     softcap: float = 0.0, seed: int = 0) -> tuple[SynthHead, np.ndarray]:
+    """A head as make_head draws it, with every group bias of n_hot vocab rows
+    (drawn uniformly without replacement) raised by bias_shift (rounded to
+    fp16).  With hidden states of positive mean (make_hidden(mean=...)), those
+    rows dominate every token's softmax: a peaked distribution, where most
+    vocab tiles carry negligible probability.  Returns (head, hot rows)."""
+    head = make_head(V, H, bits, softcap=softcap, seed=seed)
+    hot = np.sort(_rng(seed, "hot").choice(V, size=n_hot, replace=False))
+    b = head.biases.astype(np.float32)
+    b[hot] += np.float32(bias_shift)
+    head.biases = b.astype(np.float16)
+    return head, hot
 
 
 def make_targets(M: int, V: int, seed: int = 0) -> np.ndarray:
