@@ -176,6 +176,39 @@ int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The blockMax early exit (an approximate backward; page "mlx-bun 0.0.4 ->
+ * 0.0.6", src/train/flash-cce.ts: the forward hands per-block logit maxima to
+ * the backward, which skips a (token block, vocab block) program when every
+ * token has exp(blockMax - lse) < eps and no target lies in the block).
+ *
+ * qhead_fwd_blockmax: qhead_fwd plus
+ *   block_max device, float [M, ceil(V / 256)] row-major, 4-byte aligned: the
+ *             maximum capped logit z of each active row over each 256-row
+ *             vocab tile (rows with mask 0 are not written).
+ *   workspace >= qhead_fwd_blockmax_workspace(head, M) bytes (every M takes
+ *             the tensor-core path).
+ *
+ * qhead_bwd_blockskip: qhead_bwd, except that the (128 consecutive active
+ * rows, 256-row vocab tile) blocks in which every row has
+ * exp(block_max - lse) < eps and no row's target lies are left out of both
+ * backward phases (their coefficients count as 0): dh then differs from the
+ * exact one by at most |dlogp| * eps * sum_v |w_v| per row, and the skipped
+ * blocks cost nothing.
+ *   block_max the forward's block_max for the same h / head / mask.
+ *   eps       in [0, 1]; 0 skips nothing (the exact backward).
+ *   workspace >= qhead_bwd_blockskip_workspace(head, M) bytes.
+ */
+size_t qhead_fwd_blockmax_workspace(const qhead_head* head, int64_t M);
+int qhead_fwd_blockmax(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                       const uint8_t* mask, float* logp, float* lse, int32_t* argmax,
+                       float* block_max, void* workspace, size_t workspace_bytes, void* stream);
+size_t qhead_bwd_blockskip_workspace(const qhead_head* head, int64_t M);
+int qhead_bwd_blockskip(const qhead_head* head, const void* h, int64_t M,
+                        const int32_t* targets, const uint8_t* mask, const float* lse,
+                        const float* dlogp, const float* block_max, float eps, float* dh,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Workspace bytes qhead_bwd_dw needs for M rows with this head ((size_t)-1 on
  * invalid arguments).
  */

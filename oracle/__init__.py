@@ -321,21 +321,28 @@ def block_max(h: np.ndarray, head: Head, mask=None, tile: int = 256, threads: in
     return bm
 
 
-def backward_blockskip(h: np.ndarray, head: Head, targets, dlogp, lse, bm, eps: float,
-                       mask=None, tile_rows: int = 128, tile: int = 256,
-                       threads: int = 0) -> np.ndarray:
+def backward_blockskip(h: np.ndarray, head: Head, targets, dlogp, bm, eps: float,
+                       mask=None, lse=None, lse_decide=None, tile_rows: int = 128,
+                       tile: int = 256, threads: int = 0) -> np.ndarray:
     """The approximate dh of the blockMax early exit (same page, the
     backward's block skip): the active rows, in ascending order, form tiles
     of tile_rows; a (row tile, vocab tile) block is dropped -- its
     coefficients left out of dh = coeff . W -- when every row of the tile has
-    exp(bm[m, k] - lse[m]) < eps and no row's target lies in vocab tile k.
-    The decision uses the given bm and lse (those the caller's forward
-    returned)."""
+    exp(bm[m, k] - lse_decide[m]) < eps and no row's target lies in vocab
+    tile k.  The coefficients use ``lse`` (None: recomputed, the forward
+    definition); the decision uses the given bm and ``lse_decide`` (default:
+    that lse) -- those the caller's forward returned, so that both sides
+    drop the same blocks."""
     coeff = _coeff(h, head, targets, dlogp, mask, lse, threads)
     M, V = coeff.shape
     t = np.asarray(targets, dtype=np.int64)
     act = np.arange(M) if mask is None else np.nonzero(np.asarray(mask))[0]
-    lse = np.asarray(lse, dtype=np.float64)
+    if lse_decide is None:
+        if lse is None:
+            lse_decide = forward(h, head, mask=mask, threads=threads).lse
+        else:
+            lse_decide = lse
+    lse = np.asarray(lse_decide, dtype=np.float64)
     bm = np.asarray(bm, dtype=np.float64)
     for j0 in range(0, len(act), tile_rows):
         rows = act[j0:j0 + tile_rows]

@@ -469,11 +469,12 @@ def test_blockskip_reduces_to_exact_and_obeys_its_bound():
     bm = oracle.block_max(h, oh, mask=mask)
     exact = oracle.backward(h, oh, t, g, mask=mask)
     # eps = 0 drops nothing
-    assert np.array_equal(oracle.backward_blockskip(h, oh, t, g, f.lse, bm, 0.0, mask=mask), exact)
+    assert np.array_equal(oracle.backward_blockskip(h, oh, t, g, bm, 0.0, mask=mask, lse=f.lse),
+                          exact)
     # eps > 0 drops blocks: every dropped coefficient is below |dlogp| eps (sech2 <= 1),
     # so per row the change is at most |dlogp| eps sum_v |w_v|
     eps = 1e-4
-    approx = oracle.backward_blockskip(h, oh, t, g, f.lse, bm, eps, mask=mask)
+    approx = oracle.backward_blockskip(h, oh, t, g, bm, eps, mask=mask, lse=f.lse)
     wnorm = np.linalg.norm(oracle.dequant(oh), axis=1).sum()
     act = mask == 1
     diff = np.linalg.norm(approx - exact, axis=1)
@@ -497,7 +498,7 @@ def test_blockskip_keeps_target_tiles_and_decides_per_row_tile():
     g = np.ones(M)
     f = oracle.forward(h, oh, t)
     bm = oracle.block_max(h, oh)
-    approx = oracle.backward_blockskip(h, oh, t, g, f.lse, bm, 1e300)
+    approx = oracle.backward_blockskip(h, oh, t, g, bm, 1e300, lse=f.lse)
     # row 128: dh = (onehot - p) sech2 . W restricted to vocab tile 2
     raw = oracle.logits(h[128:], oh)[0]
     p = np.exp(raw - f.lse[128])

@@ -95,9 +95,11 @@ struct BwdPlan {
     int S = 1;               // vocab splits of the CUDA-core path
     int64_t chunk = 0;       // vocab rows per coefficient block (tensor-core path)
     bool dw = false;         // head gradient requested: the regions below are planned
+    bool skip = false;       // blockMax early exit: the skip map is planned
+    int64_t n_vt = 0;        // vocab tiles of 256 rows
     size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_coeff = 0, off_dhp = 0,
            off_hp = 0, off_g = 0, off_dmax = 0, off_cnt = 0, off_offs = 0, off_cursor = 0,
-           off_idx = 0, total = 0;
+           off_idx = 0, off_skip = 0, total = 0;
 };
 
 // Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block is
@@ -125,13 +127,15 @@ int dh_slices(int64_t Mpad, int H, int sms, int64_t n_k_min) {
     return best;
 }
 
-int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
+// force_tc: the tensor-core path for every M (the per-tile maxima of the
+// blockMax early exit come from its epilogue).
+int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p, bool force_tc = false) {
     DevInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    p->tc = M >= kTcMinM;
+    p->tc = M >= kTcMinM || force_tc;
     if (p->tc) {
         // One persistent CTA per SM; the kernel picks the number of vocab
         // segments S from the active-row count so that n_tiles * S is about
@@ -162,15 +166,19 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p) {
 }
 
 // with_dw: the head gradient is requested too; it reuses the tensor-core
-// path's coefficient blocks, so that path is taken for every M.
-int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false) {
+// path's coefficient blocks.  with_skip: the blockMax early exit, whose skip
+// map is in the tensor-core kernels' tiles.  Either takes that path for every M.
+int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false,
+             bool with_skip = false) {
     DevInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    p->tc = M >= kTcMinM || with_dw;
+    p->tc = M >= kTcMinM || with_dw || with_skip;
     p->dw = with_dw;
+    p->skip = with_skip;
+    p->n_vt = (hd->V + qh::kTcFwdTileRows - 1) / qh::kTcFwdTileRows;
     size_t off = 0;
     p->off_count = off; off = align_up(off + 16, 256);
     p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
@@ -201,6 +209,9 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false) 
             p->off_offs = off;   off = align_up(off + 4 * ((size_t)hd->V + 1), 256);
             p->off_cursor = off; off = align_up(off + 4 * (size_t)hd->V, 256);
             p->off_idx = off;    off = align_up(off + 4 * (size_t)p->Mpad, 256);
+        }
+        if (with_skip) {
+            p->off_skip = off;   off = align_up(off + (size_t)(p->Mpad / 128) * p->n_vt, 256);
         }
     } else {
         const int tb = qh::bwd_simt_tokens(hd->H);
@@ -263,9 +274,21 @@ size_t qhead_bwd_workspace(const qhead_head* head, int64_t M) {
     return p.total;
 }
 
-int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
-              const uint8_t* mask, float* logp, float* lse, int32_t* argmax, void* workspace,
-              size_t workspace_bytes, void* stream) {
+size_t qhead_fwd_blockmax_workspace(const qhead_head* head, int64_t M) {
+    g_err.clear();
+    if (check_head(head)) return (size_t)-1;
+    if (M < 0) { fail(QHEAD_EINVAL, "M < 0"); return (size_t)-1; }
+    if (M == 0) return 0;
+    FwdPlan p;
+    if (plan_fwd(head, M, &p, true)) return (size_t)-1;
+    return p.total;
+}
+
+// The forward; bmax != NULL also writes the per-tile maxima of z (and takes
+// the tensor-core path).
+static int fwd_impl(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                    const uint8_t* mask, float* logp, float* lse, int32_t* argmax, float* bmax,
+                    void* workspace, size_t workspace_bytes, void* stream) {
     g_err.clear();
     const int stall = take_stall();
     int rc = check_head(head);
@@ -276,12 +299,14 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
     if (!h) return fail(QHEAD_EINVAL, "h is NULL");
     if (reinterpret_cast<uintptr_t>(h) % 16) return fail(QHEAD_EINVAL, "h must be 16-byte aligned");
     if (logp && !targets) return fail(QHEAD_EINVAL, "logp requested without targets");
-    if (!logp && !lse && !argmax) return fail(QHEAD_EINVAL, "no output requested");
+    if (!logp && !lse && !argmax && !bmax) return fail(QHEAD_EINVAL, "no output requested");
     if (!workspace) return fail(QHEAD_EINVAL, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(workspace) % 256)
         return fail(QHEAD_EINVAL, "workspace must be 256-byte aligned");
+    if (bmax && reinterpret_cast<uintptr_t>(bmax) % 4)
+        return fail(QHEAD_EINVAL, "block_max must be 4-byte aligned");
     FwdPlan p;
-    rc = plan_fwd(head, M, &p);
+    rc = plan_fwd(head, M, &p, bmax != nullptr);
     if (rc) return rc;
     if (workspace_bytes < p.total)
         return fail(QHEAD_EINVAL, "workspace too small: need " + std::to_string(p.total) + " bytes");
@@ -322,6 +347,11 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
         ta.count = count; ta.err = err; ta.stall = stall;
         ta.vt_begin = 0; ta.vt_end = (int)((head->V + qh::kTcFwdTileRows - 1) / qh::kTcFwdTileRows);
         ta.part = part; ta.S_out = S_dev;
+        if (bmax) {
+            ta.bmax = bmax;
+            ta.bmax_ld = ta.vt_end;  // vocab tiles of 256 rows
+            ta.rows = rows;
+        }
         hook_before(st);
         e = qh::launch_tc_fwd(th, tw, ta, head->bits, false, p.grid, st);
         hook_after(st);
@@ -354,7 +384,8 @@ size_t qhead_bwd_dw_workspace(const qhead_head* head, int64_t M) {
 // The backward chain: dh (if dh != NULL) and the head gradient (if dw != NULL).
 static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
                     const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
-                    float* dw, void* workspace, size_t workspace_bytes, void* stream) {
+                    float* dw, const float* bmax, float eps, void* workspace,
+                    size_t workspace_bytes, void* stream) {
     g_err.clear();
     const int stall = take_stall();
     int rc = check_head(head);
@@ -380,7 +411,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
     if (reinterpret_cast<uintptr_t>(workspace) % 256)
         return fail(QHEAD_EINVAL, "workspace must be 256-byte aligned");
     BwdPlan p;
-    rc = plan_bwd(head, M, &p, dw != nullptr);
+    rc = plan_bwd(head, M, &p, dw != nullptr, bmax != nullptr);
     if (rc) return rc;
     if (workspace_bytes < p.total)
         return fail(QHEAD_EINVAL, "workspace too small: need " + std::to_string(p.total) + " bytes");
@@ -410,6 +441,11 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
             if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
                 return cuda_fail(e, "convert_h");
         }
+        // blockMax early exit: the (row tile, vocab tile) pairs both phases skip.
+        uint8_t* skip = p.skip ? at<uint8_t>(workspace, p.off_skip) : nullptr;
+        if (skip && (e = qh::launch_skip_map(bmax, p.n_vt, lse, targets, rows, count, p.Mpad / 128,
+                                             p.n_vt, eps, skip, st)))
+            return cuda_fail(e, "skip_map");
         // Head gradient: max |dlogp|, the scaled fp16 h', the one-hot terms and
         // the per-target row lists, once per call.
         __half* hp = p.dw ? at<__half>(workspace, p.off_hp) : nullptr;
@@ -452,6 +488,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
             ta.vt_begin = vt0; ta.vt_end = vt1;
             ta.lse = lse; ta.rows = rows; ta.coeff = coeff; ta.coeff_ld = p.chunk;
             ta.coeff_rows = (int)p.Mpad;
+            ta.skip = skip; ta.skip_ld = p.n_vt;
             if ((e = qh::launch_tc_fwd(th, tw_logit, ta, head->bits, true, p.grid, st)))
                 return cuda_fail(e, "tc_coeff");
             if (dh) {
@@ -463,6 +500,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
                 da.n_k = (vt1 - vt0) * tr / 64;
                 da.ks = p.S;  // <= the K steps of every chunk (plan_bwd)
                 da.accumulate = c > 0;
+                da.skip = skip; da.skip_ld = p.n_vt; da.skip_rows = (int)(p.Mpad / 128);
                 if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
                     return cuda_fail(e, "tc_dh");
             }
@@ -499,7 +537,25 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
 int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
               const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
               void* workspace, size_t workspace_bytes, void* stream) {
-    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, workspace,
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, nullptr, 0.f, workspace,
+                    workspace_bytes, stream);
+}
+
+int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+              const uint8_t* mask, float* logp, float* lse, int32_t* argmax, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    return fwd_impl(head, h, M, targets, mask, logp, lse, argmax, nullptr, workspace,
+                    workspace_bytes, stream);
+}
+
+int qhead_fwd_blockmax(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                       const uint8_t* mask, float* logp, float* lse, int32_t* argmax,
+                       float* block_max, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!block_max && M > 0) {
+        g_err.clear();
+        return fail(QHEAD_EINVAL, "block_max is required");
+    }
+    return fwd_impl(head, h, M, targets, mask, logp, lse, argmax, block_max, workspace,
                     workspace_bytes, stream);
 }
 
@@ -510,8 +566,34 @@ int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t
         g_err.clear();
         return fail(QHEAD_EINVAL, "dw is required (qhead_bwd computes dh alone)");
     }
-    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, dw, workspace, workspace_bytes,
-                    stream);
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, dw, nullptr, 0.f, workspace,
+                    workspace_bytes, stream);
+}
+
+size_t qhead_bwd_blockskip_workspace(const qhead_head* head, int64_t M) {
+    g_err.clear();
+    if (check_head(head)) return (size_t)-1;
+    if (M < 0) { fail(QHEAD_EINVAL, "M < 0"); return (size_t)-1; }
+    if (M == 0) return 0;
+    BwdPlan p;
+    if (plan_bwd(head, M, &p, false, true)) return (size_t)-1;
+    return p.total;
+}
+
+int qhead_bwd_blockskip(const qhead_head* head, const void* h, int64_t M,
+                        const int32_t* targets, const uint8_t* mask, const float* lse,
+                        const float* dlogp, const float* block_max, float eps, float* dh,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (M > 0 && !block_max) {
+        g_err.clear();
+        return fail(QHEAD_EINVAL, "block_max is required");
+    }
+    if (!(eps >= 0.f) || eps > 1.f) {
+        g_err.clear();
+        return fail(QHEAD_EINVAL, "eps must lie in [0, 1]");
+    }
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, block_max, eps, workspace,
+                    workspace_bytes, stream);
 }
 
 int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,

@@ -171,6 +171,13 @@ cudaError_t launch_stream_fwd(const uint32_t* wq, const __half* scales, const __
                               int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                               const uint8_t* mask, int64_t M, int* rows, int* pos, int* count,
                               Partial* part, int S, int* err, int stall, cudaStream_t st);
+// Skip map of the blockMax early exit: skip[mt * n_vt + vt] = 1 when every
+// active row of 128-row tile mt has bmax - lse < ln(eps) on vocab tile vt and
+// none of them targets it.
+cudaError_t launch_skip_map(const float* bmax, int64_t ld, const float* lse,
+                            const int32_t* targets, const int* rows, const int* count,
+                            int64_t n_mt, int64_t n_vt, float eps, uint8_t* skip,
+                            cudaStream_t st);
 cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,

@@ -114,6 +114,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const int units = n_mt * n_nt * KS;
     if (units == 0 || (int)blockIdx.x >= units) return;
     const int G = a.H / 64;
+    // blockMax early exit: K step kk of 256-row unit mt is skipped when both
+    // 128-row tiles skip its vocab tile.  Every role evaluates the same map.
+    auto kskip = [&](int mt, int kk) {
+        if (a.skip == nullptr) return false;
+        const int64_t vt = (a.v_begin + (int64_t)kk * BK) >> 8;
+        const int t0 = 2 * mt, t1 = 2 * mt + 1;
+        return a.skip[(int64_t)t0 * a.skip_ld + vt] != 0 &&
+               (t1 >= a.skip_rows || a.skip[(int64_t)t1 * a.skip_ld + vt] != 0);
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -154,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
             const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
             for (int kk = k0; kk < k1; ++kk) {
+                if (kskip(mt, kk)) continue;
                 if (lane == 0)
                     ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
                                        tc::kErrTimeoutEmpty);
@@ -205,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             int stage = 0, bs = 0;
             uint32_t phase = 0, aphase = 0, bphase = 0;
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
-                const int ks = u % KS;
+                const int mt = u / (n_nt * KS), ks = u % KS;
                 const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
                 // Half h's accumulator may be overwritten once the epilogue has
                 // read it out: half 0 before the unit starts, half 1 before its
@@ -213,7 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 if (!tc::mbar_wait(&acce[0], aphase ^ 1, abort_flag, err, tc::kErrTimeoutAccEmpty))
                     goto mma_abort;
                 tc::tc_fence_after();
+                bool first = true;  // no K step of this unit issued yet
                 for (int kk = k0; kk < k1; ++kk) {
+                    if (kskip(mt, kk)) continue;
                     if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                         goto mma_abort;
                     if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err, tc::kErrTimeoutDequant))
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        if (hh == 1 && kk == k0) {
+                        if (hh == 1 && first) {
                             if (!tc::mbar_wait(&acce[1], aphase ^ 1, abort_flag, err,
                                                tc::kErrTimeoutAccEmpty))
                                 goto mma_abort;
@@ -237,13 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                             // 64-column blocks along N are BK/8 * 1024 bytes apart.
                             const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks2, (BK / 8) * 1024, 1024);
                             tc::umma_f16(tmem_base + hh * BNH, ad, bd, L::IDESC,
-                                         (kk > k0 || ks2 > 0) ? 1u : 0u);
+                                         (!first || ks2 > 0) ? 1u : 0u);
                         }
                     }
                     tc::umma_commit(&empty[stage]);
                     tc::umma_commit(&bfree[bs]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                     if (++bs == NB) { bs = 0; bphase ^= 1; }
+                    first = false;
                 }
                 tc::umma_commit(&accf[0]);
                 aphase ^= 1;
@@ -266,9 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         int stage = 0, bs = 0;
         uint32_t phase = 0, bphase = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int ks = u % KS;
+            const int mt = u / (n_nt * KS), ks = u % KS;
             const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
             for (int kk = k0; kk < k1; ++kk) {
+                if (kskip(mt, kk)) continue;
                 // Results ignored: the warp stays converged (see the abort policy).
                 tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
                 tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
@@ -325,6 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         uint32_t aphase = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
+            // Whether any K step of the unit was issued (blockMax early exit:
+            // otherwise the accumulators hold no sum of this unit).
+            bool any_k = a.skip == nullptr;
+            if (!any_k) {
+                const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
+                for (int kk = k0; kk < k1 && !any_k; ++kk) any_k = !kskip(mt, kk);
+            }
             // The rows' cotangents, fetched before the wait (a dependent pair
             // of global loads off the accumulators' critical path).
             float scale2[2];
@@ -347,7 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     uint32_t r[32];
                     tc::tmem_ld32(tmem_base + lane_addr + hh * BNH + c * 32, r);
                     tc::tmem_wait_ld();
-                    if (row_ok) {
+                    if (!any_k) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;  // an empty sum
+                    }
+                    if (row_ok && (any_k || !a.accumulate)) {
                         // N column j of this chunk is hidden offset (j & ~7) + perm[j & 7]
                         // for 4-bit heads (perm = 0,4,1,5,2,6,3,7), natural for 8-bit.
                         float v[32];

@@ -135,6 +135,12 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     if (W.units == 0 || (int)blockIdx.x >= W.units) return;
     const int KSTEPS = H / BK;
     const int G = H / 64;
+    // Backward with the blockMax early exit: every role skips the same
+    // (row tile, vocab tile) pairs (no loads, dequantization or MMAs; the
+    // epilogue writes the tile's coefficients as zeros).
+    auto skipped = [&](int mt, int vt) {
+        return EPI == EPI_COEFF && a.skip != nullptr && a.skip[(int64_t)mt * a.skip_ld + vt] != 0;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -174,6 +180,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
                 for (int vt = vt0; vt < vt1; ++vt) {
+                    if (skipped(mt, vt)) continue;
                     for (int kk = 0; kk < KSTEPS; ++kk) {
                         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
                                            tc::kErrTimeoutEmpty))
@@ -210,6 +217,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
                 for (int vt = vt0; vt < vt1; ++vt) {
+                    if (skipped(mt, vt)) continue;
                     if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
                                        tc::kErrTimeoutAccEmpty))
                         goto mma_abort;
@@ -257,6 +265,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
             int mt, seg, vt0, vt1;
             unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
             for (int vt = vt0; vt < vt1; ++vt) {
+                if (skipped(mt, vt)) continue;
                 const int64_t v0 = (int64_t)vt * BN + t;
                 const bool ok0 = v0 < V;
                 for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -342,8 +351,20 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
             bool row_ok = i < n_active;
             if (EPI == EPI_COEFF && row_ok) lsb = a.lse[a.rows[i]] * kLog2e - 14.f;
             for (int vt = vt0; vt < vt1; ++vt) {
+                if (skipped(mt, vt)) {
+                    // The tile's coefficients of this row are written as zeros.
+                    if (EPI == EPI_COEFF && i < a.coeff_rows) {
+                        __half* dst = a.coeff + (int64_t)i * a.coeff_ld +
+                                      (int64_t)(vt - a.vt_begin) * BN;
+                        const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll 1
+                        for (int q = 0; q < BN / 16; ++q) tc::st_global_v8(dst + 16 * q, zero);
+                    }
+                    continue;
+                }
                 tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull);
                 tc::tc_fence_after();
+                float tz = -INFINITY;  // the tile's maximum of z (blockMax)
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -426,8 +447,11 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                         }
                         s = s * tc::ex2_approx((m - mn) * kLog2e) + acc;
                         m = mn;
+                        tz = fmaxf(tz, zmax);
                     }
                 }
+                if (EPI == EPI_SOFTMAX && a.bmax != nullptr && row_ok)
+                    a.bmax[(int64_t)a.rows[i] * a.bmax_ld + vt] = tz;
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&acce[buf]);

@@ -56,10 +56,17 @@ struct TcFwdArgs {
     int* S_out;
     // coefficient epilogue (backward phase 1)
     const float* lse;   // [M], original row order
-    const int* rows;    // compact -> original row
+    const int* rows;    // compact -> original row (also for bmax)
     __half* coeff;      // [coeff_rows, coeff_ld]
     int64_t coeff_ld;
     int coeff_rows;
+    // blockMax early exit: the forward's per-tile maxima of z (softmax
+    // epilogue; [M, bmax_ld], original row order) and the backward's skip map
+    // (coefficient epilogue; [128-row tile, skip_ld], 1 = skip the vocab tile)
+    float* bmax;
+    int64_t bmax_ld;
+    const uint8_t* skip;
+    int64_t skip_ld;
 };
 
 // Arguments of the tensor-core dh contraction (backward phase 2).
@@ -78,6 +85,12 @@ struct TcDhArgs {
     int n_k;              // 64-row vocab steps in the chunk
     int ks;               // K slices per output tile (each adds into its own buffer)
     int accumulate;       // 0: write, 1: add to dh_acc
+    // blockMax early exit: skip map [skip_rows 128-row tiles, skip_ld vocab
+    // tiles of 256 rows]; a K step is skipped when both 128-row tiles of the
+    // unit skip its vocab tile (NULL: no skipping)
+    const uint8_t* skip;
+    int64_t skip_ld;
+    int skip_rows;
 };
 
 // Arguments of the head-gradient contraction (one vocab chunk).

@@ -22,7 +22,8 @@ QHEAD_SB_F16 = 0
 EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd",
            "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel",
            "qhead_fwd_noalloc", "qhead_test_stall_next_call", "qhead_verify",
-           "qhead_bwd_dw_workspace", "qhead_bwd_dw")
+           "qhead_bwd_dw_workspace", "qhead_bwd_dw", "qhead_fwd_blockmax_workspace",
+           "qhead_fwd_blockmax", "qhead_bwd_blockskip_workspace", "qhead_bwd_blockskip")
 
 
 class CHead(ctypes.Structure):
@@ -64,6 +65,14 @@ def lib() -> ctypes.CDLL:
     L.qhead_bwd.restype = ctypes.c_int
     L.qhead_bwd_dw.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_bwd_dw.restype = ctypes.c_int
+    for name in ("qhead_fwd_blockmax_workspace", "qhead_bwd_blockskip_workspace"):
+        getattr(L, name).argtypes = [hp, i64]
+        getattr(L, name).restype = sz
+    L.qhead_fwd_blockmax.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.qhead_fwd_blockmax.restype = ctypes.c_int
+    L.qhead_bwd_blockskip.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                      sz, vp]
+    L.qhead_bwd_blockskip.restype = ctypes.c_int
     L.qhead_verify.argtypes = [hp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_verify.restype = ctypes.c_int
     L.qhead_last_error.argtypes = []
@@ -229,6 +238,55 @@ def bwd_dw(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor
                               dw.data_ptr(), workspace.data_ptr(), workspace.numel(),
                               _stream(stream)))
     return dh, dw
+
+
+def _ws_size(fn_name: str, head: Head, M: int) -> int:
+    n = getattr(lib(), fn_name)(ctypes.byref(head.c()), M)
+    if n == ctypes.c_size_t(-1).value:
+        raise QheadError(QHEAD_EINVAL, last_error())
+    return int(n)
+
+
+def fwd_blockmax(head: Head, h: torch.Tensor, targets: torch.Tensor | None = None,
+                 mask: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None,
+                 stream=None):
+    """(logp or None, lse, argmax, block_max [M, ceil(V / 256)]): the forward
+    plus each row's maximum capped logit per 256-row vocab tile."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
+    M = h.shape[0]
+    dev = h.device
+    logp = torch.empty(M, dtype=torch.float32, device=dev) if targets is not None else None
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    am = torch.empty(M, dtype=torch.int32, device=dev)
+    bm = torch.full((M, (head.V + 255) // 256), float("-inf"), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(_ws_size("qhead_fwd_blockmax_workspace", head, M), dev)
+    _check(lib().qhead_fwd_blockmax(ctypes.byref(head.c()), h.data_ptr(), M, _ptr(targets),
+                                    _ptr(mask), _ptr(logp), lse.data_ptr(), am.data_ptr(),
+                                    bm.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                    _stream(stream)))
+    return logp, lse, am, bm
+
+
+def bwd_blockskip(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+                  dlogp: torch.Tensor, block_max: torch.Tensor, eps: float,
+                  mask: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Approximate dh [M, H] float32: the blocks below eps (see
+    qhead_bwd_blockskip) are left out of both backward phases."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
+    M = h.shape[0]
+    dev = h.device
+    dh = torch.empty(M, head.H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(_ws_size("qhead_bwd_blockskip_workspace", head, M), dev)
+    _check(lib().qhead_bwd_blockskip(ctypes.byref(head.c()), h.data_ptr(), M, targets.data_ptr(),
+                                     _ptr(mask), lse.data_ptr(), dlogp.data_ptr(),
+                                     block_max.data_ptr(), float(eps), dh.data_ptr(),
+                                     workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return dh
 
 
 def verify(head: Head, h: torch.Tensor, W: int, draft: torch.Tensor | None,
