@@ -488,7 +488,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
             ta.vt_begin = vt0; ta.vt_end = vt1;
             ta.lse = lse; ta.rows = rows; ta.coeff = coeff; ta.coeff_ld = p.chunk;
             ta.coeff_rows = (int)p.Mpad;
-            ta.skip = skip; ta.skip_ld = p.n_vt;
+            ta.skip = skip; ta.skip_ld = p.n_vt; ta.skip_rows = (int)(p.Mpad / 128);
             if ((e = qh::launch_tc_fwd(th, tw_logit, ta, head->bits, true, p.grid, st)))
                 return cuda_fail(e, "tc_coeff");
             if (dh) {

@@ -352,8 +352,13 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
             if (EPI == EPI_COEFF && row_ok) lsb = a.lse[a.rows[i]] * kLog2e - 14.f;
             for (int vt = vt0; vt < vt1; ++vt) {
                 if (skipped(mt, vt)) {
-                    // The tile's coefficients of this row are written as zeros.
-                    if (EPI == EPI_COEFF && i < a.coeff_rows) {
+                    // The tile's coefficients of this row are written as zeros
+                    // where the dh contraction reads them: when the other
+                    // 128-row tile of its 256-row unit keeps the vocab tile.
+                    const int pm = mt ^ 1;
+                    const bool partner_skips =
+                        pm >= a.skip_rows || a.skip[(int64_t)pm * a.skip_ld + vt] != 0;
+                    if (EPI == EPI_COEFF && !partner_skips && i < a.coeff_rows) {
                         __half* dst = a.coeff + (int64_t)i * a.coeff_ld +
                                       (int64_t)(vt - a.vt_begin) * BN;
                         const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};

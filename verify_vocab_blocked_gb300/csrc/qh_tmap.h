@@ -67,6 +67,7 @@ struct TcFwdArgs {
     int64_t bmax_ld;
     const uint8_t* skip;
     int64_t skip_ld;
+    int skip_rows;      // 128-row tiles in the skip map
 };
 
 // Arguments of the tensor-core dh contraction (backward phase 2).

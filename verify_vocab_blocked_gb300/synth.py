@@ -46,9 +46,20 @@ CONFIGS: dict[str, dict] = {
                            mask=(1024, 0.3), bwd=True,
                            desc="Gemma-class head, M=8192 with 30% masked prompt spans "
                                 "(8 x 1024-token sequences), H=2560, V=262144, 4-bit, cap 30"),
+    # A peaked softmax for the approximate blockMax early exit (not one of the
+    # five parity workloads): 64 hot vocab rows with every group bias raised
+    # by 0.03, hidden states of mean 0.5 (so the hot logits sit ~38 above the
+    # rest before the cap), 90% of the targets hot.
+    "gemma8k_peaked": dict(M=8192, H=2560, V=262144, bits=4, group=64, softcap=30.0,
+                           mask=(1024, 0.3), bwd=True,
+                           peaked=dict(n_hot=64, bias_shift=0.03, h_mean=0.5, hot_frac=0.9),
+                           desc="Gemma-class head with a peaked softmax (64 hot vocab rows, "
+                                "90% hot targets), M=8192 with 30% masked prompt spans, "
+                                "H=2560, V=262144, 4-bit, cap 30"),
 }
 
-_STREAMS = {"wq": 1, "scales": 2, "bias_noise": 3, "h": 4, "targets": 5, "dlogp": 6, "hot": 7}
+_STREAMS = {"wq": 1, "scales": 2, "bias_noise": 3, "h": 4, "targets": 5, "dlogp": 6, "hot": 7,
+            "hot_targets": 8}
 
 
 def _rng(seed: int, stream: str) -> np.random.Generator:
@@ -165,9 +176,19 @@ class Workload:
 def make_workload(name: str, seed: int = 0, M: int | None = None) -> Workload:
     cfg = dict(CONFIGS[name])
     M = cfg["M"] if M is None else M
-    head = make_head(cfg["V"], cfg["H"], cfg["bits"], cfg["group"], cfg["softcap"], seed)
-    h = make_hidden(M, cfg["H"], seed)
+    pk = cfg.get("peaked")
+    if pk:
+        head, hot = make_peaked_head(cfg["V"], cfg["H"], cfg["bits"], pk["n_hot"],
+                                     pk["bias_shift"], cfg["softcap"], seed)
+        h = make_hidden(M, cfg["H"], seed, mean=pk["h_mean"])
+    else:
+        head = make_head(cfg["V"], cfg["H"], cfg["bits"], cfg["group"], cfg["softcap"], seed)
+        h = make_hidden(M, cfg["H"], seed)
     targets = make_targets(M, cfg["V"], seed) if cfg.get("targets", True) else None
+    if pk and targets is not None:
+        rt = _rng(seed, "hot_targets")
+        pick = rt.random(M) < pk["hot_frac"]
+        targets[pick] = hot[rt.integers(0, len(hot), size=int(pick.sum()))].astype(np.int32)
     mask = make_mask(M, cfg["mask"][0], cfg["mask"][1]) if cfg["mask"] else None
     dlogp = np.ones(M, dtype=np.float32)
     return Workload(name, head, h, targets, mask, dlogp, cfg)
