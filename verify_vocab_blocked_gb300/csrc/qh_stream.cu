@@ -241,6 +241,30 @@ int stream_stages(int H, int bits) {
     return 0;
 }
 
+// The per-tile push of a consumer thread's four logits: the soft cap and the
+// online-softmax update in their approximate forms (ex2.approx, rcp.approx;
+// relative error ~1e-7, far inside the lse tolerance), ~50 fewer instructions
+// per push than tanhf / expf (the kernel is issue-bound: 80.0 -> 75.0 us per
+// verify window).  The finalize recomputes the target logit and rechecks the
+// argmax candidates with the accurate forms.
+__device__ __forceinline__ float softcap_fast(float raw, float cap2l, float cap) {
+    // cap * tanh(raw / cap) = cap - 2 cap / (exp(2 raw / cap) + 1)
+    return cap > 0.f ? fmaf(-2.f * cap, tc::rcp_approx(tc::ex2_approx(raw * cap2l) + 1.f), cap)
+                     : raw;
+}
+
+__device__ __forceinline__ void push_fast(RowState& st, float z, float raw, int idx) {
+    constexpr float kL2e = 1.4426950408889634f;
+    if (z > st.m) {
+        st.s = fmaf(st.s, tc::ex2_approx((st.m - z) * kL2e), 1.f);
+        st.m = z;
+    } else {
+        st.s += tc::ex2_approx((z - st.m) * kL2e);
+    }
+    if (better(raw, idx, st.v1, st.i1)) { st.v2 = st.v1; st.i2 = st.i1; st.v1 = raw; st.i1 = idx; }
+    else if (better(raw, idx, st.v2, st.i2)) { st.v2 = raw; st.i2 = idx; }
+}
+
 // NST > 0: the ring has NST stages and NST divides the stages of a tile, so
 // each round of NST stages uses compile-time ring slots (immediate shared
 // offsets), and the scales arrive by TMA (tmap_s; the group count is a
@@ -581,13 +605,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_fwd_kernel(
             }
             // The last k-block's bias product, if its slot fell past the stages.
             if (kPer * (nkb - 1) + kPer / 2 >= nst) bias_mma(nkb - 1);
+            // (computed here, not held across the tile loop: one register fewer)
+            const float cap2l = cap > 0.f ? 2.f * 1.4426950408889634f / cap : 0.f;
             if (va < cta_v1) {
-                st[0].push(softcap_exact(tot[0], cap), tot[0], (int)va);
-                st[1].push(softcap_exact(tot[1], cap), tot[1], (int)va);
+                push_fast(st[0], softcap_fast(tot[0], cap2l, cap), tot[0], (int)va);
+                push_fast(st[1], softcap_fast(tot[1], cap2l, cap), tot[1], (int)va);
             }
             if (vb < cta_v1) {
-                st[0].push(softcap_exact(tot[2], cap), tot[2], (int)vb);
-                st[1].push(softcap_exact(tot[3], cap), tot[3], (int)vb);
+                push_fast(st[0], softcap_fast(tot[2], cap2l, cap), tot[2], (int)vb);
+                push_fast(st[1], softcap_fast(tot[3], cap2l, cap), tot[3], (int)vb);
             }
         }
         // Merge the 8 lanes that share t (lanes t, t+4, ..., t+28).
