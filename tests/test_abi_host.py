@@ -160,3 +160,27 @@ def test_bad_bwd_dw_args(L):
               a["dw"], 0x60000, 1 << 20, None) == qhead.QHEAD_EINVAL    # no h
     assert L.qhead_bwd_dw_workspace(ctypes.byref(_head()), 100) >= \
         L.qhead_bwd_workspace(ctypes.byref(_head()), 100)
+
+
+def test_bad_blockmax_and_blockskip_args(L):
+    hd = ctypes.byref(_head())
+    # the forward with tile maxima needs the block_max output
+    assert L.qhead_fwd_blockmax(hd, 0x40000, 4, None, None, None, 0x42000, None, None,
+                                0x60000, 1 << 20, None) == qhead.QHEAD_EINVAL
+    assert "block_max" in L.qhead_last_error().decode()
+    # the skipping backward needs block_max and an eps in [0, 1]
+    args = (0x40000, 4, 0x41000, None, 0x42000, 0x43000)
+    assert L.qhead_bwd_blockskip(hd, *args, None, ctypes.c_float(1e-5), 0x44000, 0x60000,
+                                 1 << 20, None) == qhead.QHEAD_EINVAL
+    for bad in (-1.0, 2.0, float("nan")):
+        assert L.qhead_bwd_blockskip(hd, *args, 0x45000, ctypes.c_float(bad), 0x44000, 0x60000,
+                                     1 << 20, None) == qhead.QHEAD_EINVAL
+        assert "eps" in L.qhead_last_error().decode()
+    # M = 0 is a no-op for both
+    assert L.qhead_fwd_blockmax(hd, None, 0, None, None, None, None, None, None, None, 0,
+                                None) == qhead.QHEAD_OK
+    assert L.qhead_bwd_blockskip(hd, None, 0, None, None, None, None, None, ctypes.c_float(0.0),
+                                 None, None, 0, None) == qhead.QHEAD_OK
+    # their workspaces cover the tensor-core path for every M
+    assert L.qhead_fwd_blockmax_workspace(hd, 8) >= L.qhead_fwd_workspace(hd, 8)
+    assert L.qhead_bwd_blockskip_workspace(hd, 8) > 0
