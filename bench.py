@@ -156,7 +156,10 @@ class ClockSampler:
 class Runner:
     """Device buffers for one workload and the C-ABI calls of one step."""
 
-    def __init__(self, wl: synth.Workload, device, with_dw: bool = False):
+    def __init__(self, wl: synth.Workload, device, with_dw: bool = False,
+                 blockskip: float | None = None):
+        import ctypes
+
         import torch
         from verify_vocab_blocked_gb300 import qhead
         self.torch, self.q = torch, qhead
@@ -171,6 +174,8 @@ class Runner:
         self.h = self.h_host.to(device)
         self.bwd = bool(wl.cfg["bwd"])
         self.with_dw = with_dw and self.bwd  # the backward also returns the head gradient
+        # approximate backward: the blockMax early exit with this eps
+        self.blockskip = blockskip if self.bwd else None
         self.t_host = (torch.from_numpy(wl.targets).pin_memory()
                        if wl.targets is not None else None)
         self.t = self.t_host.to(device) if self.t_host is not None else None
@@ -189,6 +194,13 @@ class Runner:
         if self.bwd:
             n = max(n, qhead.bwd_dw_workspace(self.head, M) if self.with_dw
                     else qhead.bwd_workspace(self.head, M))
+        self.bm = None
+        if self.blockskip is not None:
+            self.bm = torch.full((M, (wl.head.V + 255) // 256), float("-inf"), dtype=f32,
+                                 device=device)
+            L0 = qhead.lib()
+            n = max(n, L0.qhead_fwd_blockmax_workspace(ctypes.byref(self.head.c()), M),
+                    L0.qhead_bwd_blockskip_workspace(ctypes.byref(self.head.c()), M))
         self.ws = qhead.alloc_workspace(n, device)
         self.chead = self.head.c()
         self.stream = torch.cuda.current_stream(device)
@@ -207,16 +219,29 @@ class Runner:
         L = self.q.lib()
         if ev_fwd is not None:
             L.qhead_time_next_head_kernel(ev_fwd[0].cuda_event, ev_fwd[1].cuda_event)
-        rc = L.qhead_fwd(ctypes.byref(self.chead), self.h.data_ptr(), self.M, self._ptr(self.t),
-                         self._ptr(self.mk), self._ptr(self.logp), self.lse.data_ptr(),
-                         self.am.data_ptr(), self.ws.data_ptr(), self.ws.numel(),
-                         self.stream.cuda_stream)
+        if self.bm is not None:
+            rc = L.qhead_fwd_blockmax(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
+                                      self._ptr(self.t), self._ptr(self.mk), self._ptr(self.logp),
+                                      self.lse.data_ptr(), self.am.data_ptr(), self.bm.data_ptr(),
+                                      self.ws.data_ptr(), self.ws.numel(), self.stream.cuda_stream)
+        else:
+            rc = L.qhead_fwd(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
+                             self._ptr(self.t), self._ptr(self.mk), self._ptr(self.logp),
+                             self.lse.data_ptr(), self.am.data_ptr(), self.ws.data_ptr(),
+                             self.ws.numel(), self.stream.cuda_stream)
         if rc:
             raise RuntimeError(self.q.last_error())
         if self.bwd:
             if ev_bwd is not None:
                 L.qhead_time_next_head_kernel(ev_bwd[0].cuda_event, ev_bwd[1].cuda_event)
-            if self.with_dw:
+            if self.bm is not None:
+                rc = L.qhead_bwd_blockskip(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
+                                           self.t.data_ptr(), self._ptr(self.mk),
+                                           self.lse.data_ptr(), self.g.data_ptr(),
+                                           self.bm.data_ptr(), float(self.blockskip),
+                                           self.dh.data_ptr(), self.ws.data_ptr(),
+                                           self.ws.numel(), self.stream.cuda_stream)
+            elif self.with_dw:
                 rc = L.qhead_bwd_dw(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
                                     self.t.data_ptr(), self._ptr(self.mk), self.lse.data_ptr(),
                                     self.g.data_ptr(), self.dh.data_ptr(), self.dw.data_ptr(),
@@ -347,7 +372,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = synth.CONFIGS[args.config]
     wl = synth.make_workload(args.config, seed=0)
-    R = Runner(wl, dev, with_dw=args.with_dw)
+    R = Runner(wl, dev, with_dw=args.with_dw, blockskip=args.blockskip)
     K, W = args.steps, args.warmup
 
     # warm-up (also creates the timing events)
@@ -415,7 +440,7 @@ def run_ours(args):
         # it is a chain of two kernels per vocab chunk, timed as one region.
         # With the head gradient (--with-dw) a third contraction per chunk,
         # 2*Ma*V*H more, joins the chain (which then runs for every M).
-        tc = R.M >= 64 or R.with_dw
+        tc = R.M >= 64 or R.with_dw or R.blockskip is not None
         dom = ("tc_bwd_chain_dw" if R.with_dw else "tc_bwd_chain") if tc else "bwd_simt_kernel"
         nmul = 6.0 if R.with_dw else 4.0
         flops = nmul * R.active * cfg["V"] * cfg["H"]
@@ -424,6 +449,8 @@ def run_ours(args):
         kname = "tc_fwd_kernel<coefficient epilogue> + tc_dh_kernel"
         if R.with_dw:
             kname += " + tc_dw_kernel"
+        if R.blockskip is not None:
+            dom = "tc_bwd_chain_blockskip"
         roof = {"kernel": (kname + " per vocab chunk" if tc else dom),
                 "bound": "tensor", "achieved": achieved, "peak": tf_sus,
                 "unit": "TFLOP/s", "frac": achieved / tf_sus,
@@ -461,6 +488,11 @@ def run_ours(args):
         "dtype": "f16", "data": "synthetic (seeded; no real weights or data)",
         "config": dict(workload_desc(args.config, cfg),
                        **({"pass": "fwd+bwd (dh and dW)"} if R.with_dw else {}),
+                       **({"pass": "fwd+bwd, approximate: blockMax early exit",
+                           "blockskip_eps": R.blockskip,
+                           "flop_accounting": "exact-equivalent (skipped blocks counted as "
+                                              "done): an effective rate"}
+                          if R.blockskip is not None else {}),
                        kernel_timing="CUDA events around the head kernel on every "
                                      + (f"{stride}th timed step" if stride > 1 else "timed step")),
         "roofline": roof,
@@ -542,6 +574,9 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--blockskip", type=float, default=None, metavar="EPS",
+                    help="training configs: the approximate backward (blockMax early exit "
+                         "with this eps; e.g. with --config gemma8k_peaked)")
     ap.add_argument("--with-dw", action="store_true",
                     help="training configs: the backward also returns the head gradient dW "
                          "(qhead_bwd_dw)")
