@@ -359,6 +359,72 @@ def backward_blockskip(h: np.ndarray, head: Head, targets, dlogp, bm, eps: float
     return dh
 
 
+# ------------------------------------------- coefficient filter (approximate)
+
+class FilterDecision:
+    """Blocks of the coefficient filter: ``cold[j, k]`` for the block of active
+    rows 32j .. 32j + 31 (ascending order) and vocab rows 32k .. 32k + 31;
+    ``cmax[j, k]`` the block's largest softmax term |dlogp| p sech2 (over
+    columns that hold no row's target); ``has_target[j, k]`` whether a row's
+    target lies in the block's vocab range."""
+
+    def __init__(self, cold, cmax, has_target):
+        self.cold, self.cmax, self.has_target = cold, cmax, has_target
+
+
+def filter_blocks(coeff: np.ndarray, targets, eps: float, mask=None, rows_per_block: int = 32,
+                  cols_per_block: int = 32) -> FilterDecision:
+    """The coefficient filter's decisions (page "mlx-bun 0.0.4 -> 0.0.6",
+    src/train/flash-cce.ts, the backward's near-zero coefficient filter:
+    phase 2 skips a coefficient tile whose largest |coeff| is below eps).
+    Here a block is cold when no row's target lies in its vocab range and
+    every coefficient in it, |dlogp (0 - p) sech2|, is below eps; a block
+    that holds a target is always warm, because its one-hot term is carried
+    whole (reading of the pages: they test the combined coefficient)."""
+    M, V = coeff.shape
+    t = np.asarray(targets, dtype=np.int64)
+    act = np.arange(M) if mask is None else np.nonzero(np.asarray(mask))[0]
+    nrb = (len(act) + rows_per_block - 1) // rows_per_block
+    nvb = (V + cols_per_block - 1) // cols_per_block
+    cmax = np.zeros((nrb, nvb))
+    has_t = np.zeros((nrb, nvb), dtype=bool)
+    for j in range(nrb):
+        rows = act[j * rows_per_block:(j + 1) * rows_per_block]
+        a = np.abs(coeff[rows])
+        for r, m in enumerate(rows):
+            if 0 <= t[m] < V:
+                a[r, t[m]] = 0.0  # the target column holds the one-hot term
+                has_t[j, t[m] // cols_per_block] = True
+        pad = np.zeros((len(rows), nvb * cols_per_block))
+        pad[:, :V] = a
+        cmax[j] = pad.reshape(len(rows), nvb, cols_per_block).max(axis=(0, 2))
+    cold = (cmax < eps) & ~has_t
+    return FilterDecision(cold, cmax, has_t)
+
+
+def backward_filter(h: np.ndarray, head: Head, targets, dlogp, eps: float, mask=None, lse=None,
+                    cold=None, threads: int = 0):
+    """The approximate dh of the coefficient filter: dh = coeff . W with the
+    coefficients of every cold block (``filter_blocks``) set to 0.  ``cold``
+    (bool [row blocks, vocab blocks]) overrides the decisions, so that a
+    caller can apply the ones another implementation took.  Returns
+    (dh, FilterDecision)."""
+    coeff = _coeff(h, head, targets, dlogp, mask, lse, threads)
+    M, V = coeff.shape
+    dec = filter_blocks(coeff, targets, eps, mask)
+    drop = dec.cold if cold is None else np.asarray(cold, dtype=bool)
+    act = np.arange(M) if mask is None else np.nonzero(np.asarray(mask))[0]
+    for j, k in zip(*np.nonzero(drop)):
+        rows = act[32 * j:32 * (j + 1)]
+        coeff[rows, 32 * k:32 * (k + 1)] = 0.0
+    wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
+    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    dh = np.empty((M, head.H), dtype=np.float64)
+    _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
+                      _ptr(b, _f64p), _ptr(coeff, _f64p), _ptr(dh, _f64p), threads)
+    return dh, dec
+
+
 # ------------------------------------------------------------ verify accept
 
 def accept_prefix(argmax: np.ndarray, draft: np.ndarray, W: int):

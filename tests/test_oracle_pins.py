@@ -18,7 +18,12 @@
 * the blockMax early exit: tile maxima against the row maxima of the C row
   statistics and a hand example, the approximate dh equal to the exact one at
   eps = 0 and within |dlogp| eps sum_v |w_v| of it otherwise, and a hand
-  derivation of a row whose tile keeps only its own target's vocab tile.
+  derivation of a row whose tile keeps only its own target's vocab tile;
+* the coefficient filter: block decisions and block maxima against plain
+  loops over torch's softmax terms, the approximate dh against autograd's
+  exact dh plus the dropped terms, equality with the exact dh at eps = 0, the
+  eps sum_v |w_v| bound, and a hand derivation of a row whose block keeps
+  only its own target's 32 vocab rows.
 """
 import math
 import os
@@ -508,3 +513,136 @@ def test_blockskip_keeps_target_tiles_and_decides_per_row_tile():
     c[768:] = 0.0
     w = oracle.dequant(oh)
     assert np.allclose(approx[128], c @ w, atol=1e-12)
+
+
+# ---------------------------------------------- coefficient filter (approximate)
+
+def _torch_softmax_terms(h64, head: oracle.Head):
+    """torch fp64 on the independently unpacked dense head: p[m, v] and
+    sech2[m, v] (1 without a cap), and the dense head itself."""
+    q = torch.from_numpy(_unpack_independent(head.wq, head.bits)).double()
+    s = torch.from_numpy(head.scales.astype(np.float64))
+    b = torch.from_numpy(head.biases.astype(np.float64))
+    w = q * s.repeat_interleave(head.group, 1) + b.repeat_interleave(head.group, 1)
+    raw = torch.from_numpy(h64) @ w.T
+    if head.softcap > 0:
+        th = torch.tanh(raw / head.softcap)
+        z, sech2 = head.softcap * th, 1.0 - th * th
+    else:
+        z, sech2 = raw, torch.ones_like(raw)
+    return torch.softmax(z, dim=1).numpy(), sech2.numpy(), w.numpy()
+
+
+def _filter_case(seed=41):
+    # 52 of 70 rows active: row blocks of 32 and 20; V = 640: 20 vocab blocks;
+    # peaked logits so that some blocks are cold and others warm
+    V, H, M = 640, 128, 70
+    head, hot = synth.make_peaked_head(V, H, 4, n_hot=6, bias_shift=0.3, softcap=30.0, seed=seed)
+    oh = oracle.Head(head.wq, head.scales, head.biases, 4, 64, 30.0)
+    h = synth.make_hidden(M, H, seed=seed, mean=0.5)
+    t = synth.make_targets(M, V, seed=seed)
+    g = synth.make_dlogp(M, seed=seed).astype(np.float64)
+    mask = np.ones(M, np.uint8)
+    mask[[0, 3, 4, 9, 17, 18, 19, 25, 33, 40, 41, 44, 50, 51, 60, 61, 62, 69]] = 0
+    return oh, h, t, g, mask
+
+
+def _brute_decisions(oh, h, t, g, mask, eps):
+    """Block decisions by plain loops over torch's softmax terms."""
+    p, sech2, _ = _torch_softmax_terms(oracle._as_f64_h(h), oh)
+    act = [m for m in range(len(mask)) if mask[m]]
+    V = p.shape[1]
+    nrb, nvb = (len(act) + 31) // 32, (V + 31) // 32
+    cold = np.zeros((nrb, nvb), bool)
+    cmax = np.zeros((nrb, nvb))
+    for j in range(nrb):
+        rows = act[32 * j:32 * j + 32]
+        for k in range(nvb):
+            best, target_here = 0.0, False
+            for m in rows:
+                for v in range(32 * k, min(32 * k + 32, V)):
+                    if v == t[m]:
+                        target_here = True
+                        continue
+                    best = max(best, abs(g[m]) * p[m, v] * sech2[m, v])
+            cmax[j, k] = best
+            cold[j, k] = best < eps and not target_here
+    return cold, cmax, p, sech2, act
+
+
+def test_filter_decisions_match_brute_force():
+    oh, h, t, g, mask = _filter_case()
+    dec0 = oracle.filter_blocks(np.zeros((70, 640)), t, 1.0, mask)  # shape only
+    assert dec0.cold.shape == (2, 20)
+    _, dec = oracle.backward_filter(h, oh, t, g, 0.0, mask=mask)
+    eps = float(np.median(dec.cmax))
+    cold_b, cmax_b, *_ = _brute_decisions(oh, h, t, g, mask, eps)
+    _, dec = oracle.backward_filter(h, oh, t, g, eps, mask=mask)
+    assert np.allclose(dec.cmax, cmax_b, rtol=1e-10, atol=1e-300)
+    assert np.array_equal(dec.cold, cold_b)
+    assert 0 < dec.cold.sum() < dec.cold.size  # both kinds of block occur
+
+
+def test_filter_dh_against_torch_autograd():
+    # dh with the filter = the exact autograd dh plus the dropped softmax terms
+    # (a dropped coefficient is -dlogp p sech2, so dropping it adds
+    # dlogp p sech2 w_v back), with the brute-force decisions
+    oh, h, t, g, mask = _filter_case(seed=42)
+    _, dec = oracle.backward_filter(h, oh, t, g, 0.0, mask=mask)
+    eps = float(np.quantile(dec.cmax, 0.6))
+    cold_b, _, p, sech2, act = _brute_decisions(oh, h, t, g, mask, eps)
+    h64 = oracle._as_f64_h(h)
+    act_idx = np.array(act)
+    *_, dh_exact = _torch_reference(h64[act_idx], oh, t[act_idx], g[act_idx])
+    _, _, w = _torch_softmax_terms(h64, oh)
+    want = np.zeros((70, 128))
+    want[act_idx] = dh_exact
+    for j, k in zip(*np.nonzero(cold_b)):
+        for m in act[32 * j:32 * j + 32]:
+            cols = slice(32 * k, 32 * k + 32)
+            want[m] += (g[m] * p[m, cols] * sech2[m, cols]) @ w[cols]
+    got, dec = oracle.backward_filter(h, oh, t, g, eps, mask=mask)
+    assert np.array_equal(dec.cold, cold_b)
+    assert np.allclose(got, want, rtol=0, atol=1e-10)
+
+
+def test_filter_reduces_to_exact_and_obeys_its_bound():
+    oh, h, t, g, mask = _filter_case(seed=43)
+    exact = oracle.backward(h, oh, t, g, mask=mask)
+    got0, dec0 = oracle.backward_filter(h, oh, t, g, 0.0, mask=mask)
+    assert not dec0.cold.any()
+    assert np.array_equal(got0, exact)
+    eps = float(np.quantile(dec0.cmax, 0.5))
+    got, dec = oracle.backward_filter(h, oh, t, g, eps, mask=mask)
+    # every dropped coefficient is below eps, so per row the change is at
+    # most eps sum_v |w_v|
+    wnorm = np.linalg.norm(oracle.dequant(oh), axis=1).sum()
+    diff = np.linalg.norm(got - exact, axis=1)
+    act = mask == 1
+    assert (diff <= eps * wnorm + 1e-12).all()
+    assert diff[act].max() > 0.0
+    assert (got[~act] == 0.0).all()
+
+
+def test_filter_keeps_target_blocks():
+    # With an enormous eps every block is cold except those holding a target:
+    # the 33rd active row, alone in its row block, keeps exactly its own
+    # target's 32 vocab rows.
+    head = synth.make_head(256, 128, 4, softcap=30.0, seed=44)
+    oh = oracle.Head(head.wq, head.scales, head.biases, 4, 64, 30.0)
+    M = 33
+    h = synth.make_hidden(M, 128, seed=44)
+    t = synth.make_targets(M, 256, seed=44)
+    t[32] = 77                                       # vocab block 2
+    g = np.full(M, -1.5)
+    got, dec = oracle.backward_filter(h, oh, t, g, 1e300)
+    assert dec.cold[1].sum() == 7 and not dec.cold[1, 2]
+    f = oracle.forward(h[32:], oh)
+    raw = oracle.logits(h[32:], oh)[0]
+    th = np.tanh(raw / 30.0)
+    p = np.exp(30.0 * th - f.lse[0])
+    onehot = (np.arange(256) == 77).astype(np.float64)
+    c = -1.5 * (onehot - p) * (1.0 - th * th)
+    c[:64] = 0.0
+    c[96:] = 0.0
+    assert np.allclose(got[32], c @ oracle.dequant(oh), atol=1e-12)
