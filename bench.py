@@ -157,7 +157,7 @@ class Runner:
     """Device buffers for one workload and the C-ABI calls of one step."""
 
     def __init__(self, wl: synth.Workload, device, with_dw: bool = False,
-                 blockskip: float | None = None):
+                 blockskip: float | None = None, filter_eps: float | None = None):
         import ctypes
 
         import torch
@@ -176,6 +176,8 @@ class Runner:
         self.with_dw = with_dw and self.bwd  # the backward also returns the head gradient
         # approximate backward: the blockMax early exit with this eps
         self.blockskip = blockskip if self.bwd else None
+        # approximate backward: the coefficient filter with this eps
+        self.filter_eps = filter_eps if self.bwd and blockskip is None else None
         self.t_host = (torch.from_numpy(wl.targets).pin_memory()
                        if wl.targets is not None else None)
         self.t = self.t_host.to(device) if self.t_host is not None else None
@@ -201,6 +203,9 @@ class Runner:
             L0 = qhead.lib()
             n = max(n, L0.qhead_fwd_blockmax_workspace(ctypes.byref(self.head.c()), M),
                     L0.qhead_bwd_blockskip_workspace(ctypes.byref(self.head.c()), M))
+        if self.filter_eps is not None:
+            L0 = qhead.lib()
+            n = max(n, L0.qhead_bwd_filter_workspace(ctypes.byref(self.head.c()), M))
         self.ws = qhead.alloc_workspace(n, device)
         self.chead = self.head.c()
         self.stream = torch.cuda.current_stream(device)
@@ -241,6 +246,13 @@ class Runner:
                                            self.bm.data_ptr(), float(self.blockskip),
                                            self.dh.data_ptr(), self.ws.data_ptr(),
                                            self.ws.numel(), self.stream.cuda_stream)
+            elif self.filter_eps is not None:
+                rc = L.qhead_bwd_filter(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
+                                        self.t.data_ptr(), self._ptr(self.mk),
+                                        self.lse.data_ptr(), self.g.data_ptr(),
+                                        ctypes.c_float(self.filter_eps), self.dh.data_ptr(),
+                                        None, self.ws.data_ptr(), self.ws.numel(),
+                                        self.stream.cuda_stream)
             elif self.with_dw:
                 rc = L.qhead_bwd_dw(ctypes.byref(self.chead), self.h.data_ptr(), self.M,
                                     self.t.data_ptr(), self._ptr(self.mk), self.lse.data_ptr(),
@@ -372,7 +384,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     cfg = synth.CONFIGS[args.config]
     wl = synth.make_workload(args.config, seed=0)
-    R = Runner(wl, dev, with_dw=args.with_dw, blockskip=args.blockskip)
+    R = Runner(wl, dev, with_dw=args.with_dw, blockskip=args.blockskip,
+               filter_eps=args.filter)
     K, W = args.steps, args.warmup
 
     # warm-up (also creates the timing events)
@@ -440,7 +453,7 @@ def run_ours(args):
         # it is a chain of two kernels per vocab chunk, timed as one region.
         # With the head gradient (--with-dw) a third contraction per chunk,
         # 2*Ma*V*H more, joins the chain (which then runs for every M).
-        tc = R.M >= 64 or R.with_dw or R.blockskip is not None
+        tc = R.M >= 64 or R.with_dw or R.blockskip is not None or R.filter_eps is not None
         dom = ("tc_bwd_chain_dw" if R.with_dw else "tc_bwd_chain") if tc else "bwd_simt_kernel"
         nmul = 6.0 if R.with_dw else 4.0
         flops = nmul * R.active * cfg["V"] * cfg["H"]
@@ -451,6 +464,8 @@ def run_ours(args):
             kname += " + tc_dw_kernel"
         if R.blockskip is not None:
             dom = "tc_bwd_chain_blockskip"
+        if R.filter_eps is not None:
+            dom = "tc_bwd_chain_filter"
         roof = {"kernel": (kname + " per vocab chunk" if tc else dom),
                 "bound": "tensor", "achieved": achieved, "peak": tf_sus,
                 "unit": "TFLOP/s", "frac": achieved / tf_sus,
@@ -493,6 +508,11 @@ def run_ours(args):
                            "flop_accounting": "exact-equivalent (skipped blocks counted as "
                                               "done): an effective rate"}
                           if R.blockskip is not None else {}),
+                       **({"pass": "fwd+bwd, approximate: coefficient filter",
+                           "filter_eps": R.filter_eps,
+                           "flop_accounting": "exact-equivalent (skipped dh steps counted as "
+                                              "done): an effective rate"}
+                          if R.filter_eps is not None else {}),
                        kernel_timing="CUDA events around the head kernel on every "
                                      + (f"{stride}th timed step" if stride > 1 else "timed step")),
         "roofline": roof,
@@ -577,12 +597,18 @@ def main(argv=None):
     ap.add_argument("--blockskip", type=float, default=None, metavar="EPS",
                     help="training configs: the approximate backward (blockMax early exit "
                          "with this eps; e.g. with --config gemma8k_peaked)")
+    ap.add_argument("--filter", type=float, default=None, metavar="EPS",
+                    help="training configs: the approximate backward (coefficient filter "
+                         "with this eps; e.g. with --config gemma8k_peaked)")
     ap.add_argument("--with-dw", action="store_true",
                     help="training configs: the backward also returns the head gradient dW "
                          "(qhead_bwd_dw)")
     ap.add_argument("--no-launch-count", action="store_true",
                     help="skip the CUPTI launch count (for runs under a profiler)")
     args = ap.parse_args(argv)
+    if (args.blockskip is not None) + (args.filter is not None) + args.with_dw > 1:
+        ap.error("--blockskip, --filter and --with-dw select different backward entry points: "
+                 "give at most one")
     fwd_only = not synth.CONFIGS[args.config]["bwd"]
     if args.steps is None:
         args.steps = 3000 if fwd_only else 5

@@ -209,6 +209,36 @@ int qhead_bwd_blockskip(const qhead_head* head, const void* h, int64_t M,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The coefficient filter (an approximate backward; page "mlx-bun 0.0.4 ->
+ * 0.0.6", src/train/flash-cce.ts: the backward's near-zero coefficient filter
+ * skips the dh contraction of a coefficient tile whose largest |coeff| is
+ * below eps, since the softmax mass concentrates on a few vocab rows).
+ *
+ * qhead_bwd_filter: qhead_bwd, except that the blocks of 32 consecutive
+ * active rows x 32 vocab rows (rows 32k .. 32k + 31) in which no row's target
+ * lies and every softmax term |dlogp[m]| * softmax[m, v] * sech2[m, v] is
+ * below eps are cold: their coefficients count as 0, and a dh step whose
+ * blocks are all cold is skipped.  Blocks holding a target always stay warm
+ * (the one-hot term is added whole).  dh then differs from the exact one by at
+ * most eps * sum_v |w_v| per row.  The decision is taken in fp32 on the
+ * kernel's logits, so a block whose largest term lies within a small relative
+ * distance of eps may go either way.
+ *   eps       >= 0 (+inf allowed); 0 makes nothing cold (the exact backward).
+ *             NaN or a negative value is rejected (QHEAD_EINVAL).
+ *   cold      device, uint8 [ceil(M / 32), ceil(V / 32)] row-major, or NULL:
+ *             1 where the block of active rows 32j .. 32j + 31 (ascending
+ *             order of the active rows) and vocab rows 32k .. 32k + 31 is
+ *             cold, else 0; row blocks past the active rows are 1.
+ *   workspace >= qhead_bwd_filter_workspace(head, M) bytes (every M takes
+ *             the tensor-core path).
+ */
+size_t qhead_bwd_filter_workspace(const qhead_head* head, int64_t M);
+int qhead_bwd_filter(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                     const uint8_t* mask, const float* lse, const float* dlogp, float eps,
+                     float* dh, uint8_t* cold, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/*
  * Workspace bytes qhead_bwd_dw needs for M rows with this head ((size_t)-1 on
  * invalid arguments).
  */

@@ -184,3 +184,19 @@ def test_bad_blockmax_and_blockskip_args(L):
     # their workspaces cover the tensor-core path for every M
     assert L.qhead_fwd_blockmax_workspace(hd, 8) >= L.qhead_fwd_workspace(hd, 8)
     assert L.qhead_bwd_blockskip_workspace(hd, 8) > 0
+
+
+def test_bad_filter_args(L):
+    hd = ctypes.byref(_head())
+    args = (0x40000, 4, 0x41000, None, 0x42000, 0x43000)
+    # eps must be a number >= 0 (+inf allowed: every block without a target is cold)
+    for bad in (-1.0, -1e-30, float("nan")):
+        assert L.qhead_bwd_filter(hd, *args, ctypes.c_float(bad), 0x44000, None, 0x60000,
+                                  1 << 20, None) == qhead.QHEAD_EINVAL
+        assert "eps" in L.qhead_last_error().decode()
+    # dh is required; M = 0 is a no-op
+    assert L.qhead_bwd_filter(hd, *args, ctypes.c_float(1e-5), None, None, 0x60000, 1 << 20,
+                              None) == qhead.QHEAD_EINVAL
+    assert L.qhead_bwd_filter(hd, None, 0, None, None, None, None, ctypes.c_float(1e-5), None,
+                              None, None, 0, None) == qhead.QHEAD_OK
+    # workspace sizes need the device's SM count: checked in the GPU tests

@@ -96,10 +96,12 @@ struct BwdPlan {
     int64_t chunk = 0;       // vocab rows per coefficient block (tensor-core path)
     bool dw = false;         // head gradient requested: the regions below are planned
     bool skip = false;       // blockMax early exit: the skip map is planned
+    bool filter = false;     // coefficient filter: the dh step bits are planned
     int64_t n_vt = 0;        // vocab tiles of 256 rows
+    int64_t kbits_ld = 0;    // filter: 64-bit words of vocab-step bits per 256-row unit
     size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_coeff = 0, off_dhp = 0,
            off_hp = 0, off_g = 0, off_dmax = 0, off_cnt = 0, off_offs = 0, off_cursor = 0,
-           off_idx = 0, off_skip = 0, total = 0;
+           off_idx = 0, off_skip = 0, off_kbits = 0, total = 0;
 };
 
 // Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block is
@@ -168,17 +170,20 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p, bool force_tc = false)
 
 // with_dw: the head gradient is requested too; it reuses the tensor-core
 // path's coefficient blocks.  with_skip: the blockMax early exit, whose skip
-// map is in the tensor-core kernels' tiles.  Either takes that path for every M.
+// map is in the tensor-core kernels' tiles.  with_filter: the coefficient
+// filter, decided in the tensor-core coefficient epilogue.  Each takes that
+// path for every M.
 int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false,
-             bool with_skip = false) {
+             bool with_skip = false, bool with_filter = false) {
     DevInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    p->tc = M >= kTcMinM || with_dw || with_skip;
+    p->tc = M >= kTcMinM || with_dw || with_skip || with_filter;
     p->dw = with_dw;
     p->skip = with_skip;
+    p->filter = with_filter;
     p->n_vt = (hd->V + qh::kTcFwdTileRows - 1) / qh::kTcFwdTileRows;
     size_t off = 0;
     p->off_count = off; off = align_up(off + 16, 256);
@@ -217,6 +222,12 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false,
         }
         if (with_skip) {
             p->off_skip = off;   off = align_up(off + (size_t)(p->Mpad / 128) * p->n_vt, 256);
+        }
+        if (with_filter) {
+            // one bit per (256-row dh unit, 64-row vocab step of the head)
+            p->kbits_ld = (p->n_vt * 4 + 63) / 64;
+            p->off_kbits = off;
+            off = align_up(off + 8 * (size_t)((p->Mpad + 255) / 256) * p->kbits_ld, 256);
         }
     } else {
         const int tb = qh::bwd_simt_tokens(hd->H);
@@ -389,8 +400,8 @@ size_t qhead_bwd_dw_workspace(const qhead_head* head, int64_t M) {
 // The backward chain: dh (if dh != NULL) and the head gradient (if dw != NULL).
 static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
                     const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
-                    float* dw, const float* bmax, float eps, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+                    float* dw, const float* bmax, float eps, bool filter, uint8_t* cold_out,
+                    void* workspace, size_t workspace_bytes, void* stream) {
     g_err.clear();
     const int stall = take_stall();
     int rc = check_head(head);
@@ -416,7 +427,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
     if (reinterpret_cast<uintptr_t>(workspace) % 256)
         return fail(QHEAD_EINVAL, "workspace must be 256-byte aligned");
     BwdPlan p;
-    rc = plan_bwd(head, M, &p, dw != nullptr, bmax != nullptr);
+    rc = plan_bwd(head, M, &p, dw != nullptr, bmax != nullptr, filter);
     if (rc) return rc;
     if (workspace_bytes < p.total)
         return fail(QHEAD_EINVAL, "workspace too small: need " + std::to_string(p.total) + " bytes");
@@ -451,6 +462,16 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
         if (skip && (e = qh::launch_skip_map(bmax, p.n_vt, lse, targets, rows, count, p.Mpad / 128,
                                              p.n_vt, eps, skip, st)))
             return cuda_fail(e, "skip_map");
+        // Coefficient filter: every dh step starts skipped and every block cold
+        // (rows past the active ones stay so); the coefficient pass clears the
+        // bits of the steps that hold a warm block.
+        auto* kbits = p.filter ? at<unsigned long long>(workspace, p.off_kbits) : nullptr;
+        const int64_t n_vb = (head->V + 31) / 32, n_rb = (M + 31) / 32;
+        if (kbits && (e = cudaMemsetAsync(kbits, 0xff,
+                                          8 * (size_t)((p.Mpad + 255) / 256) * p.kbits_ld, st)))
+            return cuda_fail(e, "filter bits");
+        if (kbits && cold_out && (e = cudaMemsetAsync(cold_out, 1, (size_t)(n_rb * n_vb), st)))
+            return cuda_fail(e, "cold output");
         // Head gradient: max |dlogp|, the scaled fp16 h', the one-hot terms and
         // the per-target row lists, once per call.
         __half* hp = p.dw ? at<__half>(workspace, p.off_hp) : nullptr;
@@ -494,6 +515,9 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
             ta.lse = lse; ta.rows = rows; ta.coeff = coeff; ta.coeff_ld = p.chunk;
             ta.coeff_rows = (int)p.Mpad;
             ta.skip = skip; ta.skip_ld = p.n_vt; ta.skip_rows = (int)(p.Mpad / 128);
+            ta.dlogp = dlogp; ta.targets = targets; ta.filter_eps = eps;
+            ta.kbits = kbits; ta.kbits_ld = p.kbits_ld;
+            ta.cold_out = cold_out; ta.cold_out_ld = n_vb; ta.cold_out_rows = n_rb;
             if ((e = qh::launch_tc_fwd(th, tw_logit, ta, head->bits, true, p.grid, st)))
                 return cuda_fail(e, "tc_coeff");
             if (dh) {
@@ -506,6 +530,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
                 da.ks = p.S;  // <= the K steps of every chunk (plan_bwd)
                 da.accumulate = c > 0;
                 da.skip = skip; da.skip_ld = p.n_vt; da.skip_rows = (int)(p.Mpad / 128);
+                da.kbits = kbits; da.kbits_ld = p.kbits_ld;
                 if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
                     return cuda_fail(e, "tc_dh");
             }
@@ -542,7 +567,8 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
 int qhead_bwd(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
               const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
               void* workspace, size_t workspace_bytes, void* stream) {
-    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, nullptr, 0.f, workspace,
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, nullptr, 0.f, false,
+                    nullptr, workspace,
                     workspace_bytes, stream);
 }
 
@@ -571,7 +597,8 @@ int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t
         g_err.clear();
         return fail(QHEAD_EINVAL, "dw is required (qhead_bwd computes dh alone)");
     }
-    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, dw, nullptr, 0.f, workspace,
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, dw, nullptr, 0.f, false, nullptr,
+                    workspace,
                     workspace_bytes, stream);
 }
 
@@ -597,8 +624,31 @@ int qhead_bwd_blockskip(const qhead_head* head, const void* h, int64_t M,
         g_err.clear();
         return fail(QHEAD_EINVAL, "eps must lie in [0, 1]");
     }
-    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, block_max, eps, workspace,
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, block_max, eps, false,
+                    nullptr, workspace,
                     workspace_bytes, stream);
+}
+
+size_t qhead_bwd_filter_workspace(const qhead_head* head, int64_t M) {
+    g_err.clear();
+    if (check_head(head)) return (size_t)-1;
+    if (M < 0) { fail(QHEAD_EINVAL, "M < 0"); return (size_t)-1; }
+    if (M == 0) return 0;
+    BwdPlan p;
+    if (plan_bwd(head, M, &p, false, false, true)) return (size_t)-1;
+    return p.total;
+}
+
+int qhead_bwd_filter(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
+                     const uint8_t* mask, const float* lse, const float* dlogp, float eps,
+                     float* dh, uint8_t* cold, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+    if (!(eps >= 0.f)) {
+        g_err.clear();
+        return fail(QHEAD_EINVAL, "eps must be >= 0");
+    }
+    return bwd_impl(head, h, M, targets, mask, lse, dlogp, dh, nullptr, nullptr, eps, true, cold,
+                    workspace, workspace_bytes, stream);
 }
 
 int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,

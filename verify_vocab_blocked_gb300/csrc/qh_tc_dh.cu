@@ -84,7 +84,9 @@ __device__ __forceinline__ uint4 deq4_chunk(uint32_t w, __half2 s, __half2 b) {
     return make_uint4(p[0], p[1], p[2], p[3]);
 }
 
-template <int BITS, int BNH>
+// SKIP: the launch carries a skip map (blockMax early exit or coefficient
+// filter); without one the kernel has no skip logic at all.
+template <int BITS, int BNH, bool SKIP>
 __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_w,
     const TcDhArgs a) {
@@ -116,7 +118,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const int G = a.H / 64;
     // blockMax early exit: K step kk of 256-row unit mt is skipped when both
     // 128-row tiles skip its vocab tile.  Every role evaluates the same map.
+    // Coefficient filter: K step kk is skipped when its bit is set (64 steps
+    // share a word, so consecutive checks hit L1).
     auto kskip = [&](int mt, int kk) {
+        if constexpr (!SKIP) return false;
+        if (a.kbits != nullptr) {
+            const int64_t k = (a.v_begin >> 6) + kk;
+            return ((__ldg(a.kbits + mt * a.kbits_ld + (k >> 6)) >> (k & 63)) & 1ull) != 0;
+        }
         if (a.skip == nullptr) return false;
         const int64_t vt = (a.v_begin + (int64_t)kk * BK) >> 8;
         const int t0 = 2 * mt, t1 = 2 * mt + 1;
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
             // Whether any K step of the unit was issued (blockMax early exit:
             // otherwise the accumulators hold no sum of this unit).
-            bool any_k = a.skip == nullptr;
+            bool any_k = !SKIP;
             if (!any_k) {
                 const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
                 for (int kk = k0; kk < k1 && !any_k; ++kk) any_k = !kskip(mt, kk);
@@ -412,14 +421,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     }
 }
 
-template <int BITS, int BNH>
+template <int BITS, int BNH, bool SKIP>
 cudaError_t launch_t(const CUtensorMap& tc_map, const CUtensorMap& tw, const TcDhArgs& a, int grid,
                      cudaStream_t st) {
     using L = DhLayout<BITS, BNH>;
-    if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_dh_kernel<BITS, BNH>),
+    if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_dh_kernel<BITS, BNH, SKIP>),
                                           L::SMEM))
         return e;
-    tc_dh_kernel<BITS, BNH><<<grid, kThreads, L::SMEM, st>>>(tc_map, tw, a);
+    tc_dh_kernel<BITS, BNH, SKIP><<<grid, kThreads, L::SMEM, st>>>(tc_map, tw, a);
     return cudaGetLastError();
 }
 
@@ -434,11 +443,16 @@ bool tc_dh_swizzled(int H, int bits) { return tc_dh_cols(H) * bits / 8 >= 128; }
 cudaError_t launch_tc_dh(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w, const TcDhArgs& a,
                          int bits, int grid, cudaStream_t st) {
     const int bnh = tc_dh_cols(a.H);
+    const bool skip = a.skip != nullptr || a.kbits != nullptr;
     if (bits == 4)
-        return bnh == 256 ? launch_t<4, 256>(tmap_c, tmap_w, a, grid, st)
-                          : launch_t<4, 128>(tmap_c, tmap_w, a, grid, st);
-    return bnh == 256 ? launch_t<8, 256>(tmap_c, tmap_w, a, grid, st)
-                      : launch_t<8, 128>(tmap_c, tmap_w, a, grid, st);
+        return bnh == 256 ? (skip ? launch_t<4, 256, true>(tmap_c, tmap_w, a, grid, st)
+                                  : launch_t<4, 256, false>(tmap_c, tmap_w, a, grid, st))
+                          : (skip ? launch_t<4, 128, true>(tmap_c, tmap_w, a, grid, st)
+                                  : launch_t<4, 128, false>(tmap_c, tmap_w, a, grid, st));
+    return bnh == 256 ? (skip ? launch_t<8, 256, true>(tmap_c, tmap_w, a, grid, st)
+                              : launch_t<8, 256, false>(tmap_c, tmap_w, a, grid, st))
+                      : (skip ? launch_t<8, 128, true>(tmap_c, tmap_w, a, grid, st)
+                              : launch_t<8, 128, false>(tmap_c, tmap_w, a, grid, st));
 }
 
 }  // namespace qh

@@ -99,7 +99,9 @@ __device__ __forceinline__ void unit_coords(const Work& w, int vt_begin, int u, 
 // EPI_SOFTMAX: per-row online softmax + argmax candidates -> partials (forward).
 // EPI_COEFF: per logit c = exp(z - lse) * sech2 * 2^14 as fp16 into a
 //            [rows x chunk] block (phase 1 of the backward).
-constexpr int EPI_SOFTMAX = 0, EPI_COEFF = 1;
+// EPI_FILTER: EPI_COEFF plus the coefficient filter (blocks of 32 rows x 32
+//             vocab rows below filter_eps are written as zeros; a.kbits).
+constexpr int EPI_SOFTMAX = 0, EPI_COEFF = 1, EPI_FILTER = 2;
 
 template <int BITS, int EPI>
 __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     // (row tile, vocab tile) pairs (no loads, dequantization or MMAs; the
     // epilogue writes the tile's coefficients as zeros).
     auto skipped = [&](int mt, int vt) {
-        return EPI == EPI_COEFF && a.skip != nullptr && a.skip[(int64_t)mt * a.skip_ld + vt] != 0;
+        return EPI != EPI_SOFTMAX && a.skip != nullptr && a.skip[(int64_t)mt * a.skip_ld + vt] != 0;
     };
 
     if (threadIdx.x == 0) {
@@ -349,7 +351,16 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
             // EPI_COEFF: log2(p * 2^14) = z * log2e - (lse * log2e - 14)
             float lsb = 0.f;
             bool row_ok = i < n_active;
-            if (EPI == EPI_COEFF && row_ok) lsb = a.lse[a.rows[i]] * kLog2e - 14.f;
+            if (EPI != EPI_SOFTMAX && row_ok) lsb = a.lse[a.rows[i]] * kLog2e - 14.f;
+            // Coefficient filter: |dlogp| and the valid target of this row.
+            float fg = 0.f;
+            int64_t ftgt = -1;
+            if (EPI == EPI_FILTER && row_ok) {
+                const int r = a.rows[i];
+                fg = fabsf(a.dlogp[r]);
+                const int32_t tg = a.targets[r];
+                ftgt = tg >= 0 && (int64_t)tg < V ? (int64_t)tg : -1;
+            }
             for (int vt = vt0; vt < vt1; ++vt) {
                 if (skipped(mt, vt)) {
                     // The tile's coefficients of this row are written as zeros
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                     const int pm = mt ^ 1;
                     const bool partner_skips =
                         pm >= a.skip_rows || a.skip[(int64_t)pm * a.skip_ld + vt] != 0;
-                    if (EPI == EPI_COEFF && !partner_skips && i < a.coeff_rows) {
+                    if (EPI != EPI_SOFTMAX && !partner_skips && i < a.coeff_rows) {
                         __half* dst = a.coeff + (int64_t)i * a.coeff_ld +
                                       (int64_t)(vt - a.vt_begin) * BN;
                         const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
@@ -380,10 +391,11 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                     float x[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-                    if constexpr (EPI == EPI_COEFF) {
+                    if constexpr (EPI != EPI_SOFTMAX) {
                         // coefficient block column = col0 - first column of the chunk
                         __half* dst = a.coeff + (int64_t)i * a.coeff_ld + (col0 - (int64_t)a.vt_begin * BN);
                         uint32_t out[16];
+                        float cmax = 0.f;  // the chunk's largest p * sech2 * 2^14 of this row
 #pragma unroll
                         for (int j = 0; j < 32; j += 2) {
                             float cj[2];
@@ -402,6 +414,27 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                                 cj[e] = ok ? tc::ex2_approx(lg2p) * sech2 : 0.f;
                             }
                             out[j / 2] = h2_as_u32(__floats2half2_rn(cj[0], cj[1]));
+                            if constexpr (EPI == EPI_FILTER) cmax = fmaxf(cmax, fmaxf(cj[0], cj[1]));
+                        }
+                        if constexpr (EPI == EPI_FILTER) {
+                            // The block of this warp's 32 rows x these 32 vocab rows is
+                            // warm when a row has |dlogp| p sech2 >= eps there (both
+                            // sides scaled by 2^14) or its target lies there.
+                            const bool warm_row = row_ok && (fg * cmax >= a.filter_eps * 16384.f ||
+                                                             (ftgt >> 5) == (col0 >> 5));
+                            const bool warm = __any_sync(0xffffffffu, warm_row);
+                            if (!warm) {
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) out[q] = 0u;
+                            }
+                            if (lane == 0) {
+                                const int64_t vc = col0 >> 5, rg = i >> 5, k = vc >> 1;
+                                if (warm)  // the dh step of these rows is needed
+                                    atomicAnd(a.kbits + (rg >> 3) * a.kbits_ld + (k >> 6),
+                                              ~(1ull << (k & 63)));
+                                if (a.cold_out != nullptr && rg < a.cold_out_rows && vc < a.cold_out_ld)
+                                    a.cold_out[rg * a.cold_out_ld + vc] = warm ? 0 : 1;
+                            }
                         }
                         if (i < a.coeff_rows) {
                             // 32-byte stores: every store fills whole sectors.
@@ -495,10 +528,12 @@ static cudaError_t launch_t(const CUtensorMap& th, const CUtensorMap& tw, const 
 cudaError_t launch_tc_fwd(const CUtensorMap& th, const CUtensorMap& tw, const TcFwdArgs& a,
                           int bits, bool coeff_epilogue, int grid, cudaStream_t st) {
     if (bits == 4)
-        return coeff_epilogue ? launch_t<4, EPI_COEFF>(th, tw, a, grid, st)
-                              : launch_t<4, EPI_SOFTMAX>(th, tw, a, grid, st);
-    return coeff_epilogue ? launch_t<8, EPI_COEFF>(th, tw, a, grid, st)
-                          : launch_t<8, EPI_SOFTMAX>(th, tw, a, grid, st);
+        return !coeff_epilogue ? launch_t<4, EPI_SOFTMAX>(th, tw, a, grid, st)
+               : a.kbits != nullptr ? launch_t<4, EPI_FILTER>(th, tw, a, grid, st)
+                                    : launch_t<4, EPI_COEFF>(th, tw, a, grid, st);
+    return !coeff_epilogue ? launch_t<8, EPI_SOFTMAX>(th, tw, a, grid, st)
+           : a.kbits != nullptr ? launch_t<8, EPI_FILTER>(th, tw, a, grid, st)
+                                : launch_t<8, EPI_COEFF>(th, tw, a, grid, st);
 }
 
 }  // namespace qh

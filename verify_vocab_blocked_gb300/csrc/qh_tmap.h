@@ -68,6 +68,21 @@ struct TcFwdArgs {
     const uint8_t* skip;
     int64_t skip_ld;
     int skip_rows;      // 128-row tiles in the skip map
+    // Coefficient filter (EPI_FILTER epilogue): a block of 32 compact rows x
+    // 32 vocab rows is cold when no row's target lies in it and every
+    // p * sech2 * |dlogp| < filter_eps; its coefficients are written as
+    // zeros.  A warm block clears bit k & 63 of kbits[u * kbits_ld + k / 64]
+    // (256-row dh unit u, 64-row vocab step k of the head); cold_out, when
+    // set, gets cold_out[rg * cold_out_ld + vc] = 1 for a cold block (row
+    // block rg, vocab block vc < cold_out_ld), 0 for a warm one.
+    const float* dlogp;     // [M], original row order
+    const int32_t* targets; // [M], original row order
+    float filter_eps;
+    unsigned long long* kbits;
+    int64_t kbits_ld;
+    uint8_t* cold_out;
+    int64_t cold_out_ld;
+    int64_t cold_out_rows;
 };
 
 // Arguments of the tensor-core dh contraction (backward phase 2).
@@ -92,6 +107,11 @@ struct TcDhArgs {
     const uint8_t* skip;
     int64_t skip_ld;
     int skip_rows;
+    // Coefficient filter: bit k & 63 of kbits[unit * kbits_ld + k / 64] set =
+    // the unit's 64-row vocab step k of the head (counted from row 0) holds
+    // only cold blocks and is skipped (NULL: no skipping)
+    const unsigned long long* kbits;
+    int64_t kbits_ld;
 };
 
 // Arguments of the head-gradient contraction (one vocab chunk).

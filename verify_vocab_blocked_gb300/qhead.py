@@ -23,7 +23,8 @@ EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd
            "qhead_last_error", "qhead_version", "qhead_time_next_head_kernel",
            "qhead_fwd_noalloc", "qhead_test_stall_next_call", "qhead_verify",
            "qhead_bwd_dw_workspace", "qhead_bwd_dw", "qhead_fwd_blockmax_workspace",
-           "qhead_fwd_blockmax", "qhead_bwd_blockskip_workspace", "qhead_bwd_blockskip")
+           "qhead_fwd_blockmax", "qhead_bwd_blockskip_workspace", "qhead_bwd_blockskip",
+           "qhead_bwd_filter_workspace", "qhead_bwd_filter")
 
 
 class CHead(ctypes.Structure):
@@ -65,7 +66,8 @@ def lib() -> ctypes.CDLL:
     L.qhead_bwd.restype = ctypes.c_int
     L.qhead_bwd_dw.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_bwd_dw.restype = ctypes.c_int
-    for name in ("qhead_fwd_blockmax_workspace", "qhead_bwd_blockskip_workspace"):
+    for name in ("qhead_fwd_blockmax_workspace", "qhead_bwd_blockskip_workspace",
+                 "qhead_bwd_filter_workspace"):
         getattr(L, name).argtypes = [hp, i64]
         getattr(L, name).restype = sz
     L.qhead_fwd_blockmax.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -73,6 +75,9 @@ def lib() -> ctypes.CDLL:
     L.qhead_bwd_blockskip.argtypes = [hp, vp, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
                                       sz, vp]
     L.qhead_bwd_blockskip.restype = ctypes.c_int
+    L.qhead_bwd_filter.argtypes = [hp, vp, i64, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz,
+                                   vp]
+    L.qhead_bwd_filter.restype = ctypes.c_int
     L.qhead_verify.argtypes = [hp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.qhead_verify.restype = ctypes.c_int
     L.qhead_last_error.argtypes = []
@@ -287,6 +292,28 @@ def bwd_blockskip(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch
                                      block_max.data_ptr(), float(eps), dh.data_ptr(),
                                      workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return dh
+
+
+def bwd_filter(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+               dlogp: torch.Tensor, eps: float, mask: torch.Tensor | None = None, *,
+               want_cold: bool = False, workspace: torch.Tensor | None = None, stream=None):
+    """(dh [M, H] float32, cold or None): the approximate dh of the
+    coefficient filter (see qhead_bwd_filter) and, when asked for, its block
+    decisions uint8 [ceil(M / 32), ceil(V / 32)] (1 = cold)."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
+    M = h.shape[0]
+    dev = h.device
+    dh = torch.empty(M, head.H, dtype=torch.float32, device=dev)
+    cold = (torch.empty(((M + 31) // 32, (head.V + 31) // 32), dtype=torch.uint8, device=dev)
+            if want_cold else None)
+    if workspace is None:
+        workspace = alloc_workspace(_ws_size("qhead_bwd_filter_workspace", head, M), dev)
+    _check(lib().qhead_bwd_filter(ctypes.byref(head.c()), h.data_ptr(), M, targets.data_ptr(),
+                                  _ptr(mask), lse.data_ptr(), dlogp.data_ptr(), float(eps),
+                                  dh.data_ptr(), _ptr(cold), workspace.data_ptr(),
+                                  workspace.numel(), _stream(stream)))
+    return dh, cold
 
 
 def verify(head: Head, h: torch.Tensor, W: int, draft: torch.Tensor | None,
