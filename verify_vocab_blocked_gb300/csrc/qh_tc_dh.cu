@@ -12,6 +12,8 @@
 // packed rows the forward reads serve here without a transpose.  Each output
 // tile is owned by one CTA and accumulated over the chunks in a fixed order:
 // the result is deterministic.
+#include <type_traits>
+
 #include "qh_dequant.cuh"
 #include "qh_tc.cuh"
 #include "qh_tmap.h"
@@ -84,9 +86,11 @@ __device__ __forceinline__ uint4 deq4_chunk(uint32_t w, __half2 s, __half2 b) {
     return make_uint4(p[0], p[1], p[2], p[3]);
 }
 
-// SKIP: the launch carries a skip map (blockMax early exit or coefficient
-// filter); without one the kernel has no skip logic at all.
-template <int BITS, int BNH, bool SKIP>
+// SKIP: kSkipNone (no skip logic at all), kSkipTiles (the blockMax early
+// exit's map of 128-row tiles x vocab tiles) or kSkipSteps (the coefficient
+// filter's bits per 256-row unit and 64-row vocab step).
+constexpr int kSkipNone = 0, kSkipTiles = 1, kSkipSteps = 2;
+template <int BITS, int BNH, int SKIP>
 __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_w,
     const TcDhArgs a) {
@@ -121,12 +125,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     // Coefficient filter: K step kk is skipped when its bit is set (64 steps
     // share a word, so consecutive checks hit L1).
     auto kskip = [&](int mt, int kk) {
-        if constexpr (!SKIP) return false;
-        if (a.kbits != nullptr) {
+        if constexpr (SKIP == kSkipNone) return false;
+        if constexpr (SKIP == kSkipSteps) {
             const int64_t k = (a.v_begin >> 6) + kk;
             return ((__ldg(a.kbits + mt * a.kbits_ld + (k >> 6)) >> (k & 63)) & 1ull) != 0;
         }
-        if (a.skip == nullptr) return false;
         const int64_t vt = (a.v_begin + (int64_t)kk * BK) >> 8;
         const int t0 = 2 * mt, t1 = 2 * mt + 1;
         return a.skip[(int64_t)t0 * a.skip_ld + vt] != 0 &&
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
             const int mt = u / (n_nt * KS), nt = (u / KS) % n_nt, ks = u % KS;
             // Whether any K step of the unit was issued (blockMax early exit:
             // otherwise the accumulators hold no sum of this unit).
-            bool any_k = !SKIP;
+            bool any_k = SKIP == kSkipNone;
             if (!any_k) {
                 const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
                 for (int kk = k0; kk < k1 && !any_k; ++kk) any_k = !kskip(mt, kk);
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
     }
 }
 
-template <int BITS, int BNH, bool SKIP>
+template <int BITS, int BNH, int SKIP>
 cudaError_t launch_t(const CUtensorMap& tc_map, const CUtensorMap& tw, const TcDhArgs& a, int grid,
                      cudaStream_t st) {
     using L = DhLayout<BITS, BNH>;
@@ -443,16 +446,20 @@ bool tc_dh_swizzled(int H, int bits) { return tc_dh_cols(H) * bits / 8 >= 128; }
 cudaError_t launch_tc_dh(const CUtensorMap& tmap_c, const CUtensorMap& tmap_w, const TcDhArgs& a,
                          int bits, int grid, cudaStream_t st) {
     const int bnh = tc_dh_cols(a.H);
-    const bool skip = a.skip != nullptr || a.kbits != nullptr;
-    if (bits == 4)
-        return bnh == 256 ? (skip ? launch_t<4, 256, true>(tmap_c, tmap_w, a, grid, st)
-                                  : launch_t<4, 256, false>(tmap_c, tmap_w, a, grid, st))
-                          : (skip ? launch_t<4, 128, true>(tmap_c, tmap_w, a, grid, st)
-                                  : launch_t<4, 128, false>(tmap_c, tmap_w, a, grid, st));
-    return bnh == 256 ? (skip ? launch_t<8, 256, true>(tmap_c, tmap_w, a, grid, st)
-                              : launch_t<8, 256, false>(tmap_c, tmap_w, a, grid, st))
-                      : (skip ? launch_t<8, 128, true>(tmap_c, tmap_w, a, grid, st)
-                              : launch_t<8, 128, false>(tmap_c, tmap_w, a, grid, st));
+    const int skip = a.kbits != nullptr ? kSkipSteps : a.skip != nullptr ? kSkipTiles : kSkipNone;
+    // One instantiation per (bits, columns, skip kind).
+    auto go = [&](auto bits_c, auto bnh_c) {
+        constexpr int B = decltype(bits_c)::value, N = decltype(bnh_c)::value;
+        return skip == kSkipSteps   ? launch_t<B, N, kSkipSteps>(tmap_c, tmap_w, a, grid, st)
+               : skip == kSkipTiles ? launch_t<B, N, kSkipTiles>(tmap_c, tmap_w, a, grid, st)
+                                    : launch_t<B, N, kSkipNone>(tmap_c, tmap_w, a, grid, st);
+    };
+    using I4 = std::integral_constant<int, 4>;
+    using I8 = std::integral_constant<int, 8>;
+    using C256 = std::integral_constant<int, 256>;
+    using C128 = std::integral_constant<int, 128>;
+    if (bits == 4) return bnh == 256 ? go(I4{}, C256{}) : go(I4{}, C128{});
+    return bnh == 256 ? go(I8{}, C256{}) : go(I8{}, C128{});
 }
 
 }  // namespace qh
