@@ -186,9 +186,12 @@ class Runner:
         self.g_host = torch.from_numpy(wl.dlogp).pin_memory()
         self.g = self.g_host.to(device)
         f32, i32 = torch.float32, torch.int32
-        self.logp = torch.empty(M, dtype=f32, device=device) if self.t is not None else None
-        self.lse = torch.empty(M, dtype=f32, device=device)
-        self.am = torch.empty(M, dtype=i32, device=device)
+        # The per-row results (logp, lse, argmax) share one device buffer, so
+        # the end-to-end leg reads them back with a single copy.
+        self.rows_out = torch.empty(3, M, dtype=i32, device=device)
+        self.logp = self.rows_out[0].view(f32) if self.t is not None else None
+        self.lse = self.rows_out[1].view(f32)
+        self.am = self.rows_out[2]
         self.dh = torch.empty(M, wl.head.H, dtype=f32, device=device) if self.bwd else None
         self.dw = (torch.empty(wl.head.V, wl.head.H, dtype=f32, device=device)
                    if self.with_dw else None)
@@ -211,8 +214,8 @@ class Runner:
         self.stream = torch.cuda.current_stream(device)
         # pinned outputs for the end-to-end leg
         self.out_host = {k: torch.empty_like(v, device="cpu").pin_memory()
-                         for k, v in (("lse", self.lse), ("am", self.am), ("logp", self.logp),
-                                      ("dh", self.dh), ("dw", self.dw)) if v is not None}
+                         for k, v in (("rows", self.rows_out), ("dh", self.dh), ("dw", self.dw))
+                         if v is not None}
         self.launches_per_step = None  # counted on the device by count_launches()
         self.active = int(wl.mask.sum()) if wl.mask is not None else M
 
@@ -277,10 +280,12 @@ class Runner:
 
     def d2h(self):
         n = 0
-        for k, dev in (("lse", self.lse), ("am", self.am), ("logp", self.logp), ("dh", self.dh),
-                       ("dw", self.dw)):
+        # logp (when targets are given), lse and argmax in one copy; dh and dW
+        for k, dev in (("rows", self.rows_out if self.t is not None else self.rows_out[1:]),
+                       ("dh", self.dh), ("dw", self.dw)):
             if dev is not None:
-                self.out_host[k].copy_(dev, non_blocking=True)
+                dst = self.out_host[k] if k != "rows" or self.t is not None else self.out_host[k][1:]
+                dst.copy_(dev, non_blocking=True)
                 n += dev.numel() * dev.element_size()
         return n
 
