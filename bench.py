@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -53,15 +54,24 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def code_of(text: str) -> str:
+    """C/CUDA source with comments removed and whitespace collapsed: what a
+    recorded measurement depends on (edits to comments keep it valid)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(sources) -> str | None:
-    """sha256 (16 hex digits) of the named csrc files, concatenated in order."""
+    """sha256 (16 hex digits) of the code of the named csrc files (comments
+    and whitespace left out), concatenated in order."""
     h = hashlib.sha256()
     for name in sources:
         src = os.path.join(ROOT, "verify_vocab_blocked_gb300", "csrc", name)
         if not os.path.exists(src):
             return None
-        with open(src, "rb") as f:
-            h.update(f.read())
+        with open(src, encoding="utf-8") as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

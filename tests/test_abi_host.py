@@ -158,8 +158,7 @@ def test_bad_bwd_dw_args(L):
     assert "32-byte" in L.qhead_last_error().decode()
     assert fn(ctypes.byref(_head()), None, 4, a["targets"], None, a["lse"], a["dlogp"], None,
               a["dw"], 0x60000, 1 << 20, None) == qhead.QHEAD_EINVAL    # no h
-    assert L.qhead_bwd_dw_workspace(ctypes.byref(_head()), 100) >= \
-        L.qhead_bwd_workspace(ctypes.byref(_head()), 100)
+    # (workspace sizes need the device's SM count: checked in the GPU tests)
 
 
 def test_bad_blockmax_and_blockskip_args(L):
@@ -181,9 +180,8 @@ def test_bad_blockmax_and_blockskip_args(L):
                                 None) == qhead.QHEAD_OK
     assert L.qhead_bwd_blockskip(hd, None, 0, None, None, None, None, None, ctypes.c_float(0.0),
                                  None, None, 0, None) == qhead.QHEAD_OK
-    # their workspaces cover the tensor-core path for every M
-    assert L.qhead_fwd_blockmax_workspace(hd, 8) >= L.qhead_fwd_workspace(hd, 8)
-    assert L.qhead_bwd_blockskip_workspace(hd, 8) > 0
+    # (their workspace sizes, which need the device's SM count, are checked in
+    # the GPU tests)
 
 
 def test_bad_filter_args(L):

@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py: the replica aggregation over ranks (gloo,
-world size 2), the algorithmic byte count and the reference arm's JSON line."""
+world size 2), the algorithmic byte count, the reference arm's JSON line and
+the code hash that keys recorded DRAM traffic."""
 import json
 import os
 import subprocess
@@ -56,3 +57,18 @@ def test_reference_arm_line():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_recorded_traffic_is_keyed_by_code_not_comments():
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* no\n overflow check */ }\n"
+    b = "/* header */\nint f(int x) {\n    return 2 * x;\n}\n// end\n"
+    c = "int f(int x) { return 3 * x; }\n"
+    assert bench.code_of(a) == bench.code_of(b) == "int f(int x) { return 2 * x; }"
+    assert bench.code_of(c) != bench.code_of(a)
+    # every recorded figure names sources that exist (a figure whose code has
+    # changed since is reported as null by the bench, not failed here)
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        d = json.load(f)
+    for kernel, per in d.items():
+        for workload, e in per.items():
+            assert bench.source_hash(e["sources"]) is not None, (kernel, workload)

@@ -4,6 +4,8 @@ Small cases are compared on every row; the full-size workloads on sampled rows
 (rows are independent, so a sampled row is an exact check of that row) plus
 properties that hold on every row.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -193,6 +195,28 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(qhead.QheadError) as e:
         qhead.fwd(head, h, t, mk, workspace=ws)
     assert e.value.code == qhead.QHEAD_EINVAL
+
+
+def test_workspace_sizes_of_the_variants():
+    # Each variant's workspace covers its plan: the tensor-core plan for every
+    # M where the variant needs it (tile maxima, skip maps, dW), a superset of
+    # the exact backward's at M >= 64.
+    wl = _custom(100, 256, 3000, 4, 30.0, seed=14)
+    head = to_dev(wl)[0]
+    c = ctypes.byref(head.c())
+    L = qhead.lib()
+    bad = ctypes.c_size_t(-1).value
+    for m in (8, 100):
+        f, b = L.qhead_fwd_workspace(c, m), L.qhead_bwd_workspace(c, m)
+        for name in ("qhead_fwd_blockmax_workspace", "qhead_bwd_blockskip_workspace",
+                     "qhead_bwd_filter_workspace", "qhead_bwd_dw_workspace"):
+            assert getattr(L, name)(c, m) not in (0, bad), name
+        assert f not in (0, bad) and b not in (0, bad)
+        assert L.qhead_fwd_blockmax_workspace(c, m) >= f
+    for name in ("qhead_bwd_blockskip_workspace", "qhead_bwd_filter_workspace",
+                 "qhead_bwd_dw_workspace"):
+        assert getattr(L, name)(c, 100) >= L.qhead_bwd_workspace(c, 100), name
+        assert getattr(L, name)(c, 0) == 0, name
 
 
 # ------------------------------------------------------------ full-size configs

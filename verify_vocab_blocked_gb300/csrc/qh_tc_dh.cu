@@ -12,6 +12,12 @@
 // packed rows the forward reads serve here without a transpose.  Each output
 // tile is owned by one CTA and accumulated over the chunks in a fixed order:
 // the result is deterministic.
+//
+// The approximate backwards skip K steps (64 vocab rows) whose coefficients
+// all count as zero: by the blockMax early exit's map of (128-row tile, vocab
+// tile) pairs, or by the coefficient filter's bits per (256-row unit, step)
+// that phase 1 leaves set (the skip kind is a template parameter, so the
+// exact backward carries no skip logic).
 #include <type_traits>
 
 #include "qh_dequant.cuh"

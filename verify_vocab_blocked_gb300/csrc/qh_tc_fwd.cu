@@ -21,6 +21,13 @@
 //     with the lowest column holding it (argmax candidates, rechecked exactly
 //     by the finalize kernel).
 // The [M,V] logits and the dequantized head never leave the SM.
+//
+// The same kernel is phase 1 of the backward: its coefficient epilogue writes
+// p * sech2 * 2^14 as fp16 per logit into the chunk's [rows x chunk] block;
+// with the coefficient filter (a separate instantiation) each warp also votes
+// per 32 x 32 block whether any term reaches eps, writes a cold block as
+// zeros and clears, for a warm one, the dh step's bit in the filter's map
+// (the backward's near-zero coefficient filter on the same page).
 #include <stdio.h>
 
 #include "qh_dequant.cuh"
