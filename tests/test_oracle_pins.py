@@ -7,6 +7,8 @@
   with and without the soft cap);
 * special cases: V = 1, identical vocab rows, a very large cap equals no cap,
   a shared bias shift leaves logp / argmax / dh unchanged;
+* a naive second fp64 path on the tiny shapes (codes by integer division,
+  unshifted log-sum-exp, a scanned first maximum, dh from its definition);
 * a library cross-check: torch fp64 log_softmax / logsumexp / argmax and
   autograd's dh on an independently unpacked head;
 * finite differences of sum_m dlogp_m * logp_m against dh;
@@ -223,6 +225,60 @@ def test_shared_bias_shift_invariance():
     da = oracle.backward(wl.h, ha, wl.targets, g)
     db = oracle.backward(wl.h, hb, wl.targets, g)
     assert np.allclose(da, db, atol=1e-10)
+
+
+# --------------------------------------------------------- naive second path
+
+def _naive_codes(wq: np.ndarray, H: int, bits: int) -> np.ndarray:
+    """Codes by integer division: field j of a word is (w // 2^(bits j)) mod 2^bits."""
+    per = 32 // bits
+    base = 1 << bits
+    q = np.empty((wq.shape[0], H), dtype=np.int64)
+    w64 = wq.astype(np.int64)
+    for d in range(H):
+        q[:, d] = (w64[:, d // per] // (base ** (d % per))) % base
+    return q
+
+
+@pytest.mark.parametrize("bits,cap", [(4, 0.0), (4, 30.0), (8, 0.0)])
+def test_against_a_naive_second_path(bits, cap):
+    # A second fp64 path on the tiny configuration's shapes: codes by integer
+    # division, bf16 widened by placing its bits in the high half of a
+    # binary32, logsumexp as log(sum(exp(z))) with no shift (|z| is small),
+    # the first maximum by a Python scan, and dh from the definition.
+    M, H, V = 16, 256, 2048
+    head = synth.make_head(V, H, bits, softcap=cap, seed=31 + bits)
+    oh = oracle.Head(head.wq, head.scales, head.biases, bits, 64, cap)
+    hb = synth.make_hidden(M, H, seed=31)
+    t = synth.make_targets(M, V, seed=31)
+    g = synth.make_dlogp(M, seed=31).astype(np.float64)
+    h = (hb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    q = _naive_codes(head.wq, H, bits)
+    s = np.repeat(head.scales.astype(np.float64), 64, axis=1)
+    b = np.repeat(head.biases.astype(np.float64), 64, axis=1)
+    w = s * q + b
+    raw = h @ w.T
+    z = cap * np.tanh(raw / cap) if cap > 0 else raw
+    lse = np.log(np.exp(z).sum(axis=1))
+    logp = z[np.arange(M), t] - lse
+    am = np.empty(M, dtype=np.int64)
+    for m in range(M):
+        best = 0
+        for v in range(1, V):
+            if raw[m, v] > raw[m, best]:
+                best = v
+        am[m] = best
+    sech2 = 1.0 - np.tanh(raw / cap) ** 2 if cap > 0 else np.ones_like(raw)
+    onehot = np.zeros_like(raw)
+    onehot[np.arange(M), t] = 1.0
+    dh = (g[:, None] * (onehot - np.exp(z - lse[:, None])) * sech2) @ w
+
+    f = oracle.forward(hb, oh, t)
+    assert np.allclose(f.lse, lse, rtol=0, atol=1e-12)
+    assert np.allclose(f.logp, logp, rtol=0, atol=1e-12)
+    assert np.array_equal(f.argmax, am)
+    got = oracle.backward(hb, oh, t, g)
+    assert np.abs(got - dh).max() <= 1e-12 * max(1.0, np.abs(dh).max())
 
 
 # ----------------------------------------------------- library cross-check
