@@ -59,7 +59,7 @@ extern "C" {
 /* Status codes. */
 #define QHEAD_OK 0
 #define QHEAD_EINVAL 1        /* null required pointer, misalignment, bad size, small workspace */
-#define QHEAD_EUNSUPPORTED 2  /* bits / group / H / dtype this build does not implement */
+#define QHEAD_EUNSUPPORTED 2  /* bits / group / H / dtype the library does not implement */
 #define QHEAD_ECUDA 3         /* a CUDA launch or runtime call failed */
 
 /* Element type of scales and biases. */
