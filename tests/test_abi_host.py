@@ -1,9 +1,12 @@
 """Host-side checks of the C ABI: the library builds, loads and exports every
-symbol include/qhead.h declares, and argument errors come back as the
-documented status codes before anything touches a GPU."""
+symbol include/qhead.h declares, argument errors come back as the
+documented status codes before anything touches a GPU, and a plain C program
+(tests/c/abi_from_c.c) compiles against the header and links the library."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -198,3 +201,18 @@ def test_bad_filter_args(L):
     assert L.qhead_bwd_filter(hd, None, 0, None, None, None, None, ctypes.c_float(1e-5), None,
                               None, None, 0, None) == qhead.QHEAD_OK
     # workspace sizes need the device's SM count: checked in the GPU tests
+
+
+def test_the_abi_is_usable_from_plain_c(L, tmp_path):
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(qhead.LIB_PATH)
+    exe = str(tmp_path / "abi_from_c")
+    cmd = [cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I" + os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c", "abi_from_c.c"), "-L" + libdir, "-lqhead",
+           "-Wl,-rpath," + libdir, "-lm", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
