@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py: the replica aggregation over ranks (gloo,
-world size 2), the algorithmic byte count, the reference arm's JSON line and
+world size 2), the algorithmic byte count, the reference arm's JSON line (also
+under torchrun with two ranks) and
 the code hash that keys recorded DRAM traffic."""
 import json
 import os
@@ -57,6 +58,23 @@ def test_reference_arm_line():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    # Launched the way the driver launches N > 1: rank 0 alone runs the
+    # oracle and prints; the other rank exits 0 without work.
+    port = 29700 + (os.getpid() % 200)
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--config", "tiny", "--gpus", "2",
+                        "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0
 
 
 def test_recorded_traffic_is_keyed_by_code_not_comments():
