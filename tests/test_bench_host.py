@@ -1,7 +1,7 @@
 """Host-side pieces of bench.py: the replica aggregation over ranks (gloo,
 world size 2), the algorithmic byte count, the reference arm's JSON line (also
-under torchrun with two ranks) and
-the code hash that keys recorded DRAM traffic."""
+under torchrun with two ranks) and the code hash that keys recorded DRAM
+traffic."""
 import json
 import os
 import subprocess
