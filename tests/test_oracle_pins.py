@@ -589,12 +589,13 @@ def _torch_softmax_terms(h64, head: oracle.Head):
     return torch.softmax(z, dim=1).numpy(), sech2.numpy(), w.numpy()
 
 
-def _filter_case(seed=41):
+def _filter_case(seed=41, bits=4, cap=30.0, V=640):
     # 52 of 70 rows active: row blocks of 32 and 20; V = 640: 20 vocab blocks;
     # peaked logits so that some blocks are cold and others warm
-    V, H, M = 640, 128, 70
-    head, hot = synth.make_peaked_head(V, H, 4, n_hot=6, bias_shift=0.3, softcap=30.0, seed=seed)
-    oh = oracle.Head(head.wq, head.scales, head.biases, 4, 64, 30.0)
+    H, M = 128, 70
+    head, hot = synth.make_peaked_head(V, H, bits, n_hot=6, bias_shift=0.3, softcap=cap,
+                                       seed=seed)
+    oh = oracle.Head(head.wq, head.scales, head.biases, bits, 64, cap)
     h = synth.make_hidden(M, H, seed=seed, mean=0.5)
     t = synth.make_targets(M, V, seed=seed)
     g = synth.make_dlogp(M, seed=seed).astype(np.float64)
@@ -626,10 +627,12 @@ def _brute_decisions(oh, h, t, g, mask, eps):
     return cold, cmax, p, sech2, act
 
 
-def test_filter_decisions_match_brute_force():
-    oh, h, t, g, mask = _filter_case()
-    dec0 = oracle.filter_blocks(np.zeros((70, 640)), t, 1.0, mask)  # shape only
-    assert dec0.cold.shape == (2, 20)
+@pytest.mark.parametrize("seed,bits,cap,V", [(41, 4, 30.0, 640), (45, 8, 0.0, 600),
+                                            (46, 4, 0.0, 333)])
+def test_filter_decisions_match_brute_force(seed, bits, cap, V):
+    oh, h, t, g, mask = _filter_case(seed, bits, cap, V)
+    dec0 = oracle.filter_blocks(np.zeros((70, V)), t, 1.0, mask)  # shape only
+    assert dec0.cold.shape == (2, (V + 31) // 32)
     _, dec = oracle.backward_filter(h, oh, t, g, 0.0, mask=mask)
     eps = float(np.median(dec.cmax))
     cold_b, cmax_b, *_ = _brute_decisions(oh, h, t, g, mask, eps)
