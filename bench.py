@@ -4,10 +4,13 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
 One step is one pass of the whole hot path over one batch of synthetic input:
-  * verify (default; the gamma+1 speculative-decode window): one forward
-    (lse + argmax of every position) over M = 5 rows;
-  * training configs (gemma512, mid8, gemma8k_masked, tiny): forward (logp,
-    lse, argmax) + backward (dh) over all rows.
+  * training configs (gemma8k_masked, the default; gemma512, mid8, tiny):
+    forward (logp, lse, argmax) + backward (dh) over all rows;
+  * verify (the gamma+1 speculative-decode window): one forward (lse + argmax
+    of every position) over M = 5 rows.
+The default line is the 8192-row masked Gemma-class training step; it also
+carries, under "verify_window", the verify window measured in the same run on
+the same head, with its own HBM roofline.
 `value` is tokens/s over all ranks with inputs already resident in HBM;
 `e2e` is the same metric through the C ABI with the step's inputs copied from
 pinned host memory and its results read back inside the timed region.
@@ -37,12 +40,16 @@ from verify_vocab_blocked_gb300 import synth  # noqa: E402
 
 METRIC = "fused qhead logp tokens/s (fwd, fwd+bwd) + % of tensor-core / HBM roofline"
 UNIT = "tokens/s"
-DEFAULT_CONFIG = "verify"
+DEFAULT_CONFIG = "gemma8k_masked"
 EVENT_STRIDE = 16
-# The pages' own time for the e4b-class head at M=512 (forward 180 ms, backward
-# 754 ms, Apple M1 Max, fp32 operands): the only workload they time that
-# matches one of ours (gemma512, forward + backward).
-PAGES_TOKENS_PER_S = {"gemma512": 512 / (0.180 + 0.754)}
+# The pages' own timing, for context only (another machine, another precision,
+# a real head): the e4b-class head at M = 512, forward 180 ms + backward 754 ms
+# on an Apple M1 Max with fp32 operands.  It is not a baseline for any
+# workload here, so vs_baseline stays null.
+PAGES_CONTEXT = {"workload": "e4b-class head (V=262144, H=2560, 4-bit), M=512, fwd+bwd",
+                 "hardware": "Apple M1 Max (Metal), fp32 operands",
+                 "ms_fwd": 180.0, "ms_bwd": 754.0, "tokens_per_s": 512 / (0.180 + 0.754),
+                 "note": "context only, not a baseline"}
 
 
 def _peaks():
@@ -167,7 +174,8 @@ class Runner:
     """Device buffers for one workload and the C-ABI calls of one step."""
 
     def __init__(self, wl: synth.Workload, device, with_dw: bool = False,
-                 blockskip: float | None = None, filter_eps: float | None = None):
+                 blockskip: float | None = None, filter_eps: float | None = None,
+                 head=None):
         import ctypes
 
         import torch
@@ -175,9 +183,11 @@ class Runner:
         self.torch, self.q = torch, qhead
         self.wl = wl
         self.dev = device
-        self.head = qhead.Head.from_numpy(wl.head.wq, wl.head.scales, wl.head.biases,
-                                          wl.head.bits, wl.head.group, wl.head.softcap,
-                                          device=device)
+        # `head`: the same head already resident on the device (another
+        # workload's with identical head parameters), shared instead of copied.
+        self.head = head if head is not None else qhead.Head.from_numpy(
+            wl.head.wq, wl.head.scales, wl.head.biases, wl.head.bits, wl.head.group,
+            wl.head.softcap, device=device)
         M = wl.M
         self.M = M
         self.h_host = torch.from_numpy(wl.h.astype(np.int16)).view(torch.bfloat16).pin_memory()
@@ -386,6 +396,97 @@ def cpu_baseline(wl: synth.Workload, budget_s: float = 12.0, max_reps: int = 64,
                       f"{el:.1f} s"}
 
 
+def event_stride(K: int) -> int:
+    """Every how many timed steps the head kernel is bracketed by events: a
+    stream event between two launches costs the step the overlap of the next
+    launch (~9 us of a 90 us verify step when every step carries a pair)."""
+    return EVENT_STRIDE if K >= 4 * EVENT_STRIDE else 4 if K >= 8 else 1
+
+
+def timed_region(R: Runner, K: int, W: int, dist=None, local: int = 0):
+    """W untimed steps, then K steps timed on the device between barriers and
+    synchronizes, with the head kernel (and the backward chain) timed by CUDA
+    events on every event_stride(K)-th step.  Returns (elapsed ms, forward
+    kernel ms per sample, backward chain ms per sample, clock summary)."""
+    import torch
+    mk_ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    stride = event_stride(K)
+    sampled = [i % stride == 0 for i in range(K)]
+    ev_f = [(mk_ev(), mk_ev()) if sampled[i] else None for i in range(K)]
+    ev_b = [(mk_ev(), mk_ev()) if sampled[i] and R.bwd else None for i in range(K)]
+    for pair in [p for p in ev_f + ev_b if p]:  # create the events before timing
+        pair[0].record()
+        pair[1].record()
+    for _ in range(W):
+        R.step()
+    torch.cuda.synchronize()
+    t0, t1 = mk_ev(), mk_ev()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record()
+        for i in range(K):
+            R.step(ev_f[i], ev_b[i])
+        t1.record()
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    return (t0.elapsed_time(t1), [p[0].elapsed_time(p[1]) for p in ev_f if p],
+            [p[0].elapsed_time(p[1]) for p in ev_b if p], clk.summary())
+
+
+def e2e_region(R: Runner, K: int, dist=None):
+    """K steps through the C ABI from pinned host inputs to host outputs, the
+    copies inside the timed region.  Returns (elapsed ms, h2d bytes per step,
+    d2h bytes per step)."""
+    import torch
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e0.record()
+    h2d = d2h = 0
+    for _ in range(K):
+        h2d = R.h2d()
+        R.step()
+        d2h = R.d2h()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), h2d, d2h
+
+
+def hbm_roofline(cfg: dict, kms: float, hbm: float, peak_src: str, workload: str) -> dict:
+    """The weight-streaming kernel against the measured copy bandwidth."""
+    nbytes = head_bytes(cfg)
+    achieved = nbytes / (kms / 1e3) / 1e9
+    tr = _traffic("stream_fwd_kernel", workload)
+    return {"kernel": "stream_fwd_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
+            "unit": "GB/s", "frac": achieved / hbm,
+            "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+            "work_per_launch": f"{nbytes} bytes (packed head + fp16 scales/biases)",
+            "ms_per_launch": kms, "traffic": tr["dram_bytes_per_launch"] if tr else None}
+
+
+def verify_window(dev, head_dev, head_np, local: int, count: bool = True, steps: int = 2000,
+                  warmup: int = 50):
+    """The gamma+1 verify window on the same head, measured in the same run:
+    tokens/s, the step time and the streaming kernel's HBM roofline."""
+    cfg = synth.CONFIGS["verify"]
+    wl = synth.make_workload("verify", seed=0, head=head_np)
+    R = Runner(wl, dev, head=head_dev)
+    el, fwd_ms, _, clk = timed_region(R, steps, warmup, None, local)
+    hbm, _, _, peak_src = _peaks()
+    launches = count_launches(R)[1] if count else {"note": "not counted (--no-launch-count)"}
+    return {"workload": workload_desc("verify", cfg)["workload"], "metric": "tokens/s",
+            "value": R.active * steps / (el / 1e3), "ms_per_step": el / steps, "steps": steps,
+            "warmup": warmup,
+            "roofline": dict(hbm_roofline(cfg, statistics.mean(fwd_ms), hbm, peak_src, "verify"),
+                             kernel_timing=f"CUDA events around the kernel on every "
+                                           f"{event_stride(steps)}th timed step"),
+            "launches_per_step": launches, "clocks": clk}
+
+
 def run_ours(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -402,22 +503,10 @@ def run_ours(args):
     R = Runner(wl, dev, with_dw=args.with_dw, blockskip=args.blockskip,
                filter_eps=args.filter)
     K, W = args.steps, args.warmup
+    stride = event_stride(K)
 
-    # warm-up (also creates the timing events)
-    mk_ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    # The head kernel is timed by events the library records around it on its
-    # stream, on every EVENT_STRIDE-th timed step of long runs: a stream event
-    # between two launches costs the step the overlap of the next launch
-    # (~9 us of a 90 us verify step when every step carries a pair).
-    stride = EVENT_STRIDE if K >= 4 * EVENT_STRIDE else 1
-    sampled = [i % stride == 0 for i in range(K)]
-    ev_f = [(mk_ev(), mk_ev()) if sampled[i] else None for i in range(K)]
-    ev_b = [(mk_ev(), mk_ev()) if sampled[i] and R.bwd else None for i in range(K)]
-    for pair in [p for p in ev_f + ev_b if p]:
-        pair[0].record()
-        pair[1].record()
-    for _ in range(W):
-        R.step()
+    # launches of one step, counted after a first warm-up step
+    R.step()
     torch.cuda.synchronize()
     if args.no_launch_count:
         n_launch, launch_list = None, {"note": "not counted (--no-launch-count)"}
@@ -426,48 +515,26 @@ def run_ours(args):
     R.launches_per_step = n_launch
 
     # device-resident timed region
-    t0, t1 = mk_ev(), mk_ev()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0.record()
-        for i in range(K):
-            R.step(ev_f[i], ev_b[i])
-        t1.record()
-        torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    el = t0.elapsed_time(t1)
+    el, fwd_ms, bwd_ms, clocks = timed_region(R, K, W, dist, local)
     el_max, units = aggregate(el, R.active * K, world, dist)
     value = units / (el_max / 1e3)
-    fwd_ms = [p[0].elapsed_time(p[1]) for p in ev_f if p]
-    bwd_ms = [p[0].elapsed_time(p[1]) for p in ev_b if p]
 
     # end-to-end timed region: pinned host inputs -> C ABI -> host outputs
-    Ke = K
-    torch.cuda.synchronize()
-    e0, e1 = mk_ev(), mk_ev()
-    if dist:
-        dist.barrier()
-    e0.record()
-    h2d = d2h = 0
-    for _ in range(Ke):
-        h2d = R.h2d()
-        R.step()
-        d2h = R.d2h()
-    e1.record()
-    torch.cuda.synchronize()
-    el_e = e0.elapsed_time(e1)
-    el_e_max, units_e = aggregate(el_e, R.active * Ke, world, dist)
+    el_e, h2d, d2h = e2e_region(R, K, dist)
+    el_e_max, units_e = aggregate(el_e, R.active * K, world, dist)
 
     hbm, tf_burst, tf_sus, peak_src = _peaks()
+    timing = ("CUDA events around the head kernel on every "
+              + (f"{stride}th timed step" if stride > 1 else "timed step"))
     if R.bwd:
         # dominant work: the backward head phase (logits recomputed, 2*Ma*V*H,
         # and the dh contraction, 2*Ma*V*H).  On the tensor-core path (M >= 64)
         # it is a chain of two kernels per vocab chunk, timed as one region.
         # With the head gradient (--with-dw) a third contraction per chunk,
         # 2*Ma*V*H more, joins the chain (which then runs for every M).
+        # The kernels are event-timed inside a run of well under a second, so
+        # the denominator is the burst GEMM rate, not the power-capped
+        # sustained one (which needs seconds of back-to-back work).
         tc = R.M >= 64 or R.with_dw or R.blockskip is not None or R.filter_eps is not None
         dom = ("tc_bwd_chain_dw" if R.with_dw else "tc_bwd_chain") if tc else "bwd_simt_kernel"
         nmul = 6.0 if R.with_dw else 4.0
@@ -481,40 +548,35 @@ def run_ours(args):
             dom = "tc_bwd_chain_blockskip"
         if R.filter_eps is not None:
             dom = "tc_bwd_chain_filter"
+        psrc = (f"{peak_src} bf16_tflops (burst; dense, the same rate as fp16): the kernels "
+                f"are event-timed inside a {el_max / 1e3:.2f} s run")
         roof = {"kernel": (kname + " per vocab chunk" if tc else dom),
-                "bound": "tensor", "achieved": achieved, "peak": tf_sus,
-                "unit": "TFLOP/s", "frac": achieved / tf_sus,
-                "peak_source": f"{peak_src} bf16_tflops_sustained (dense, same rate as fp16)",
-                "work_per_launch": f"{flops:.3e} flop ({int(nmul)}*Ma*V*H, Ma = active rows)",
-                "ms_per_launch": kms}
+                "bound": "tensor", "achieved": achieved, "peak": tf_burst,
+                "unit": "TFLOP/s", "frac": achieved / tf_burst, "peak_source": psrc,
+                "work_per_launch": f"{flops:.3e} flop ({int(nmul)}*Ma*V*H, Ma = active rows; "
+                                   "one launch = one backward call's kernel chain)",
+                "ms_per_launch": kms, "kernel_timing": timing}
         fms = statistics.mean(fwd_ms)
         ff = 2.0 * R.active * cfg["V"] * cfg["H"]
         roof["fwd_kernel"] = {"kernel": "tc_fwd_kernel" if tc else "stream_fwd_kernel",
                               "ms_per_launch": fms,
                               "achieved_tflops": ff / (fms / 1e3) / 1e12,
-                              "frac": ff / (fms / 1e3) / 1e12 / tf_sus}
+                              "frac": ff / (fms / 1e3) / 1e12 / tf_burst}
         step_ms = el_max / K
         sf = (nmul + 2.0) * R.active * cfg["V"] * cfg["H"]
         roof["step"] = {"flop": sf, "ms": step_ms,
                         "achieved_tflops": sf / (step_ms / 1e3) / 1e12,
-                        "frac": sf / (step_ms / 1e3) / 1e12 / tf_sus}
+                        "frac": sf / (step_ms / 1e3) / 1e12 / tf_burst}
+        tr = _traffic(dom, args.config)
+        roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
     else:
-        dom = "stream_fwd_kernel"
-        nbytes = head_bytes(cfg)
-        kms = statistics.mean(fwd_ms)
-        achieved = nbytes / (kms / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                "work_per_launch": f"{nbytes} bytes (packed head + fp16 scales/biases)",
-                "ms_per_launch": kms}
-    tr = _traffic(dom, args.config)
-    roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
+        roof = dict(hbm_roofline(cfg, statistics.mean(fwd_ms), hbm, peak_src, args.config),
+                    kernel_timing=timing)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": el_max / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": (value / PAGES_TOKENS_PER_S[args.config]
-                        if args.config in PAGES_TOKENS_PER_S else None),
+        "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded; no real weights or data)",
         "config": dict(workload_desc(args.config, cfg),
                        **({"pass": "fwd+bwd (dh and dW)"} if R.with_dw else {}),
@@ -527,17 +589,23 @@ def run_ours(args):
                            "filter_eps": R.filter_eps,
                            "flop_accounting": "exact-equivalent (skipped dh steps counted as "
                                               "done): an effective rate"}
-                          if R.filter_eps is not None else {}),
-                       kernel_timing="CUDA events around the head kernel on every "
-                                     + (f"{stride}th timed step" if stride > 1 else "timed step")),
+                          if R.filter_eps is not None else {})),
         "roofline": roof,
         "e2e": {"value": units_e / (el_e_max / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": R.launches_per_step * K if R.launches_per_step is not None else None,
         "launches_per_step": launch_list,
-        "clocks": clk.summary(),
+        "clocks": clocks,
+        "pages_context": PAGES_CONTEXT,
         "impl": "ours",
     }
+    if (R.bwd and not args.no_verify and world == 1 and rank == 0
+            and synth.CONFIGS["verify"]["H"] == cfg["H"] and cfg.get("peaked") is None):
+        try:
+            line["verify_window"] = verify_window(dev, R.head, wl.head, local,
+                                                  count=not args.no_launch_count)
+        except ValueError:  # a head with other parameters: no shared verify line
+            pass
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, with_dw=R.with_dw)
     if rank == 0:
@@ -620,15 +688,18 @@ def main(argv=None):
                          "(qhead_bwd_dw)")
     ap.add_argument("--no-launch-count", action="store_true",
                     help="skip the CUPTI launch count (for runs under a profiler)")
+    ap.add_argument("--no-verify", action="store_true",
+                    help="training configs: leave out the verify-window measurement on the "
+                         "same head")
     args = ap.parse_args(argv)
     if (args.blockskip is not None) + (args.filter is not None) + args.with_dw > 1:
         ap.error("--blockskip, --filter and --with-dw select different backward entry points: "
                  "give at most one")
     fwd_only = not synth.CONFIGS[args.config]["bwd"]
     if args.steps is None:
-        args.steps = 3000 if fwd_only else 5
+        args.steps = 3000 if fwd_only else 20
     if args.warmup is None:
-        args.warmup = 50 if fwd_only else 3
+        args.warmup = 50 if fwd_only else 5
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
         run_reference(args)

@@ -277,13 +277,16 @@ int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t
  * start-up, and latency-critical loops that must not enter the allocator
  * cannot call cudaMalloc to provide qhead_fwd's workspace.  This call takes
  * the same arguments as qhead_fwd minus the workspace and computes the same
- * outputs, using instead a fixed scratch array of 8 MiB (8388608 bytes) that
- * lives in the library on every device that loads it, until the process
- * exits.  It allocates
- * nothing and calls no allocating routine.
+ * outputs, bit for bit, using instead a fixed scratch array of 8 MiB
+ * (8388608 bytes) that lives in the library on every device that loads it,
+ * until the process exits.  It allocates nothing and calls no allocating
+ * routine.
  *   - The first call with a given device current looks up the array's device
- *     address (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture on the device.
+ *     address (cudaGetSymbolAddress) and caches it by device ordinal; make
+ *     that first call before any stream capture on the device.  The cached
+ *     address belongs to the device's primary context as it was then: after
+ *     cudaDeviceReset on that device, or with a non-primary context current
+ *     on it, the cached address is stale and this call must not be used.
  *   - M rows whose workspace (qhead_fwd_workspace) exceeds the scratch size
  *     are rejected with QHEAD_EINVAL and a message; nothing is launched.
  *     In practice the scratch holds the weight-streaming path (M < 64, a few
@@ -293,6 +296,9 @@ int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t
  *     (a call writes all scratch it reads), but calls whose kernels may
  *     overlap on the GPU (e.g. issued on different streams without ordering)
  *     race on it: order them on one stream or with events.
+ *   - A call rejected by the size check disarms the thread's one-shot hooks
+ *     (qhead_time_next_head_kernel, qhead_test_stall_next_call) as a forward
+ *     call would.
  */
 int qhead_fwd_noalloc(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
                       const uint8_t* mask, float* logp, float* lse, int32_t* argmax,
@@ -304,18 +310,22 @@ const char* qhead_last_error(void);
 
 /*
  * Instrumentation (no counterpart on the pages): arm a one-shot hook on the
- * calling thread.  The thread's next qhead_fwd or qhead_bwd call records the
- * CUDA event `start` on its stream immediately before its head kernel (the
- * vocab-streaming contraction that dominates the call) and `stop`
- * immediately after it, then disarms the hook.  start and stop are
+ * calling thread.  The thread's next forward or backward call (qhead_fwd,
+ * qhead_verify, qhead_fwd_noalloc, qhead_fwd_blockmax, qhead_bwd and the
+ * other backward entry points) records the CUDA event `start` on its stream
+ * immediately before its head kernel (the vocab-streaming contraction that
+ * dominates the call; for a backward on the tensor-core path, the chain of
+ * its per-chunk kernels) and `stop` immediately after it, then disarms the
+ * hook.  A call rejected before it launches anything disarms it too.  start and stop are
  * cudaEvent_t handles passed as void*; passing NULL for both disarms.
  */
 void qhead_time_next_head_kernel(void* start, void* stop);
 
 /*
  * Test instrumentation (no counterpart on the pages): arm a one-shot switch
- * on the calling thread.  The thread's next qhead_fwd or qhead_bwd call
- * launches its pipelined head kernel with the TMA producer issuing no loads,
+ * on the calling thread.  The thread's next forward or backward call (the
+ * entry points listed for qhead_time_next_head_kernel) launches its
+ * pipelined head kernel with the TMA producer issuing no loads,
  * so the consumers' bounded waits expire and the call ends as described under
  * "Kernel time limits" (about 2 s later, without a fault).  A qhead_bwd call
  * on the SIMT path (fewer than 64 rows) has no pipelined kernel and ignores

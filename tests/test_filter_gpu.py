@@ -7,9 +7,10 @@
   wherever the oracle's largest softmax term of the block lies more than 5 %
   away from eps (closer blocks may go either way: the kernel decides in fp32
   on its own logits); the approximate dh matches the oracle's approximate dh
-  taken with the GPU's decisions as closely as the exact path matches the
-  exact oracle (at least the 2e-3 dh tolerance), and the exact dh within the
-  bound eps * sum_v |w_v| plus that tolerance; several vocab chunks, a mask,
+  taken with the GPU's decisions, and the exact dh the exact oracle, both
+  within the 2e-3 dh tolerance measured against the terms (the "peaked"
+  cancellation case of the parity rule), and the approximate dh lies within
+  eps * sum_v |w_v| plus that tolerance of the exact one; several vocab chunks, a mask,
   8-bit heads, M below the tensor-core threshold and zero cotangents;
 * dropping blocks changes the result, within the bound.
 """
@@ -59,7 +60,8 @@ def _run(wl, eps):
 
 
 def _scale(wl, ref_exact, w):
-    # the dh scale of the parity rule: max(|dh|, |dlogp| |w_target|)
+    # the dh scale of the "peaked" cancellation case of the parity rule:
+    # max(|dh|, |dlogp| |w_target|) (the hot targets hold most of the mass)
     return np.maximum(np.linalg.norm(ref_exact, axis=1),
                       np.abs(wl.dlogp) * np.linalg.norm(w[wl.targets], axis=1))
 
@@ -92,9 +94,11 @@ def test_infinite_eps_keeps_exactly_the_target_blocks():
     w = oracle.dequant(oh)
     scale = _scale(wl, ref_exact, w)
     exact = exact.cpu().numpy().astype(np.float64)
-    tol = max(DH_REL_TOL, 1.5 * _rel_rows(exact[act], ref_exact[act], scale[act]).max())
+    rel_exact = _rel_rows(exact[act], ref_exact[act], scale[act])
     rel = _rel_rows(approx.cpu().numpy().astype(np.float64)[act], ref[act], scale[act])
-    assert rel.max() <= tol, f"rel-L2 {rel.max():.3e} (tolerance {tol:.3e})"
+    print(f"filter eps=inf: exact path {rel_exact.max():.3e}, approximate {rel.max():.3e}")
+    assert rel_exact.max() <= DH_REL_TOL, f"exact dh rel-L2 {rel_exact.max():.3e}"
+    assert rel.max() <= DH_REL_TOL, f"rel-L2 {rel.max():.3e}"
 
 
 @pytest.mark.parametrize("M,H,V,bits,cap,eps,masked", [
@@ -127,12 +131,14 @@ def test_peaked_filter(M, H, V, bits, cap, eps, masked):
     assert (approx[~act] == 0.0).all()
     w = oracle.dequant(oh)
     scale = _scale(wl, ref_exact, w)
-    tol = max(DH_REL_TOL, 1.5 * _rel_rows(exact[act], ref_exact[act], scale[act]).max())
+    rel_exact = _rel_rows(exact[act], ref_exact[act], scale[act])
     rel = _rel_rows(approx[act], ref_approx[act], scale[act])
-    assert rel.max() <= tol, f"approx dh rel-L2 {rel.max():.3e} (tolerance {tol:.3e})"
+    print(f"peaked filter: exact path {rel_exact.max():.3e}, approximate {rel.max():.3e}")
+    assert rel_exact.max() <= DH_REL_TOL, f"exact dh rel-L2 {rel_exact.max():.3e}"
+    assert rel.max() <= DH_REL_TOL, f"approx dh rel-L2 {rel.max():.3e}"
     bound = eps * np.linalg.norm(w, axis=1).sum()
     diff = np.linalg.norm(approx[act] - ref_exact[act], axis=1)
-    assert (diff <= bound + tol * scale[act]).all()
+    assert (diff <= bound + DH_REL_TOL * scale[act]).all()
 
 
 def test_filtering_changes_the_result():

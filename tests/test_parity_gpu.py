@@ -1,8 +1,11 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
-Small cases are compared on every row; the full-size workloads on sampled rows
-(rows are independent, so a sampled row is an exact check of that row) plus
-properties that hold on every row.
+Small cases are compared on every row.  The full-size workloads run whole on
+the GPU and are compared on every forward row of the 512-row Gemma workload
+and of the verify window, and on 256 seeded rows plus every row next to a
+mask boundary (forward and dh) of the 8192-row workloads: rows are
+independent, so a compared row is an exact check of that row.  Properties
+that hold at any size are checked on every row besides.
 """
 import ctypes
 
@@ -34,7 +37,7 @@ def _custom(M, H, V, bits, cap, seed=0, mask=None, targets=None, dlogp=None):
     return synth.Workload("custom", head, h, t, mask, g, dict(M=M, H=H, V=V, bits=bits))
 
 
-def _run_all(wl, bwd=True):
+def _run_all(wl, bwd=True, case=None):
     head, h, t, mk, g = to_dev(wl)
     logp, lse, am = gpu_fwd(head, h, t, mk)
     rows = np.arange(wl.M)
@@ -43,7 +46,7 @@ def _run_all(wl, bwd=True):
         lse_d = torch.from_numpy(lse).cuda()
         dh = qhead.bwd(head, h, t, lse_d, g, mk)
         torch.cuda.synchronize()
-        check_dh(wl, rows, dh.cpu().numpy())
+        check_dh(wl, rows, dh.cpu().numpy(), case=case)
 
 
 def test_tiny_config():
@@ -78,7 +81,9 @@ EDGE = [
 
 @pytest.mark.parametrize("M,H,V,bits,cap", EDGE)
 def test_edge_shapes(M, H, V, bits, cap):
-    _run_all(_custom(M, H, V, bits, cap, seed=M + V))
+    # V = 1: softmax = onehot, so dh = 0 exactly and only the terms-relative
+    # error is defined.
+    _run_all(_custom(M, H, V, bits, cap, seed=M + V), case="V=1" if V == 1 else None)
 
 
 # Shapes on the tensor-core forward (M >= 64): partial 128-row tiles, vocab
@@ -232,37 +237,63 @@ def _full(name):
 
 
 def _sample_rows(wl, n, seed=0):
+    """n seeded active rows, rows 0 and M - 1, and both sides of every mask
+    boundary of every sequence."""
     rng = np.random.default_rng(seed)
-    rows = set(rng.choice(wl.M, size=min(n, wl.M), replace=False).tolist())
+    act = np.arange(wl.M) if wl.mask is None else np.nonzero(wl.mask)[0]
+    rows = set(rng.choice(act, size=min(n, len(act)), replace=False).tolist())
     rows |= {0, wl.M - 1}
+    n_boundary = 0
     if wl.mask is not None:
-        # both sides of every prompt / response boundary in the first sequence
-        idx = np.nonzero(np.diff(wl.mask.astype(int)))[0]
-        for i in idx[:4]:
+        for i in np.nonzero(np.diff(wl.mask.astype(int)))[0]:
             rows |= {int(i), int(i) + 1}
-    return np.array(sorted(rows))
+            n_boundary += 1
+    return np.array(sorted(rows)), n_boundary
 
 
 def test_full_verify_window():
     wl, (head, h, t, mk, g) = _full("verify")
     logp, lse, am = qhead.fwd(head, h, None, None)
     torch.cuda.synchronize()
-    check_fwd(wl, np.arange(wl.M), None, lse.cpu().numpy(), am.cpu().numpy())
+    assert check_fwd(wl, np.arange(wl.M), None, lse.cpu().numpy(), am.cpu().numpy()) == wl.M
 
 
-@pytest.mark.parametrize("name,n", [("gemma512", 24), ("mid8", 16), ("gemma8k_masked", 16)])
-def test_full_training_configs(name, n):
+def _full_step(name):
+    """The workload's forward and backward on the GPU, exactly as the bench
+    runs them, with the every-row properties checked."""
     wl, (head, h, t, mk, g) = _full(name)
     logp, lse, am = qhead.fwd(head, h, t, mk)
     dh = qhead.bwd(head, h, t, lse, g, mk)
     torch.cuda.synchronize()
     logp, lse_h, am = logp.cpu().numpy(), lse.cpu().numpy(), am.cpu().numpy()
+    dh_h = dh.cpu().numpy()
     act = np.ones(wl.M, bool) if wl.mask is None else wl.mask.astype(bool)
     # properties on every row
     assert np.all(np.isfinite(logp)) and np.all(logp[act] <= 1e-6)
+    assert np.all(np.isfinite(lse_h)) and np.all(lse_h[~act] == 0.0)
     assert np.all((am[act] >= 0) & (am[act] < wl.head.V)) and np.all(am[~act] == -1)
-    dh_h = dh.cpu().numpy()
     assert np.all(dh_h[~act] == 0.0) and np.all(np.isfinite(dh_h))
-    rows = _sample_rows(wl, n)
-    check_fwd(wl, rows, logp, lse_h, am)
-    check_dh(wl, rows[:8], dh_h)
+    return wl, logp, lse_h, am, dh_h
+
+
+def test_full_gemma512_every_forward_row():
+    wl, logp, lse, am, dh = _full_step("gemma512")
+    assert check_fwd(wl, np.arange(wl.M), logp, lse, am) == 512
+    rows, _ = _sample_rows(wl, 256, seed=1)
+    assert len(rows) >= 256
+    check_dh(wl, rows, dh, label="gemma512")
+
+
+def test_full_mid8_sampled_rows():
+    wl, logp, lse, am, dh = _full_step("mid8")
+    rows, _ = _sample_rows(wl, 256, seed=2)
+    assert check_fwd(wl, rows, logp, lse, am) >= 256
+    check_dh(wl, rows, dh, label="mid8")
+
+
+def test_full_gemma8k_masked_sampled_rows():
+    wl, logp, lse, am, dh = _full_step("gemma8k_masked")
+    rows, n_boundary = _sample_rows(wl, 256, seed=3)
+    assert n_boundary == 2 * 8 - 1  # prompt/response and response/next-prompt edges
+    assert check_fwd(wl, rows, logp, lse, am) >= 256
+    check_dh(wl, rows, dh, label="gemma8k_masked")

@@ -40,6 +40,16 @@ void hook_after(cudaStream_t st) {
     g_ev_start = g_ev_stop = nullptr;
 }
 
+// Disarms both one-shot hooks when the entry point that holds it returns, so
+// that a call rejected before its kernels ran does not leave them armed for
+// the thread's next call.
+struct HookScope {
+    ~HookScope() {
+        g_ev_start = g_ev_stop = nullptr;
+        g_stall = false;
+    }
+};
+
 int fail(int code, const std::string& msg) {
     g_err = msg;
     return code;
@@ -305,6 +315,7 @@ size_t qhead_fwd_blockmax_workspace(const qhead_head* head, int64_t M) {
 static int fwd_impl(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
                     const uint8_t* mask, float* logp, float* lse, int32_t* argmax, float* bmax,
                     void* workspace, size_t workspace_bytes, void* stream) {
+    HookScope hooks;
     g_err.clear();
     const int stall = take_stall();
     int rc = check_head(head);
@@ -402,6 +413,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
                     const uint8_t* mask, const float* lse, const float* dlogp, float* dh,
                     float* dw, const float* bmax, float eps, bool filter, uint8_t* cold_out,
                     void* workspace, size_t workspace_bytes, void* stream) {
+    HookScope hooks;
     g_err.clear();
     const int stall = take_stall();
     int rc = check_head(head);
@@ -582,6 +594,7 @@ int qhead_fwd(const qhead_head* head, const void* h, int64_t M, const int32_t* t
 int qhead_fwd_blockmax(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
                        const uint8_t* mask, float* logp, float* lse, int32_t* argmax,
                        float* block_max, void* workspace, size_t workspace_bytes, void* stream) {
+    HookScope hooks;
     if (!block_max && M > 0) {
         g_err.clear();
         return fail(QHEAD_EINVAL, "block_max is required");
@@ -593,6 +606,7 @@ int qhead_fwd_blockmax(const qhead_head* head, const void* h, int64_t M, const i
 int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t* targets,
                  const uint8_t* mask, const float* lse, const float* dlogp, float* dh, float* dw,
                  void* workspace, size_t workspace_bytes, void* stream) {
+    HookScope hooks;
     if (!dw) {
         g_err.clear();
         return fail(QHEAD_EINVAL, "dw is required (qhead_bwd computes dh alone)");
@@ -616,6 +630,7 @@ int qhead_bwd_blockskip(const qhead_head* head, const void* h, int64_t M,
                         const int32_t* targets, const uint8_t* mask, const float* lse,
                         const float* dlogp, const float* block_max, float eps, float* dh,
                         void* workspace, size_t workspace_bytes, void* stream) {
+    HookScope hooks;
     if (M > 0 && !block_max) {
         g_err.clear();
         return fail(QHEAD_EINVAL, "block_max is required");
@@ -643,6 +658,7 @@ int qhead_bwd_filter(const qhead_head* head, const void* h, int64_t M, const int
                      const uint8_t* mask, const float* lse, const float* dlogp, float eps,
                      float* dh, uint8_t* cold, void* workspace, size_t workspace_bytes,
                      void* stream) {
+    HookScope hooks;
     if (!(eps >= 0.f)) {
         g_err.clear();
         return fail(QHEAD_EINVAL, "eps must be >= 0");
@@ -655,6 +671,7 @@ int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,
                  const int32_t* draft, const uint8_t* mask, float* lse, int32_t* argmax,
                  int32_t* n_accept, int32_t* next_token, void* workspace, size_t workspace_bytes,
                  void* stream) {
+    HookScope hooks;
     g_err.clear();
     if (B < 0) return fail(QHEAD_EINVAL, "B < 0");
     if (W < 1 || W > (int64_t)1 << 20) return fail(QHEAD_EINVAL, "W must be in [1, 2^20]");

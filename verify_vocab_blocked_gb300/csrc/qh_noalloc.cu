@@ -14,7 +14,9 @@
 // library holds it until the process exits.  In host code its name is only a
 // host-side stand-in, never a device address, so the address is looked up
 // once per device with cudaGetSymbolAddress (with that device current) and
-// cached.  All calls share the one array: nothing in it has to start at zero
+// cached by device ordinal.  The cached address belongs to the device's
+// primary context as it was at that first call: after cudaDeviceReset, or
+// under another context made current on the same device, it is stale.  All calls share the one array: nothing in it has to start at zero
 // (each call writes every scratch byte it later reads), but two calls whose
 // kernels overlap on the GPU -- e.g. on two streams -- race on it and must be
 // serialised by the caller.
@@ -73,6 +75,11 @@ extern "C" int qhead_fwd_noalloc(const qhead_head* head, const void* h, int64_t 
     // below then rejects them with the precise code and launches nothing.
     const size_t need = qhead_fwd_workspace(head, M);
     if (need != (size_t)-1 && need > kScratchBytes) {
+        // The call ends here without reaching qhead_fwd: disarm the thread's
+        // one-shot hooks as a forward call would, so that they do not fire
+        // on its next call instead.
+        qhead_time_next_head_kernel(nullptr, nullptr);
+        qhead_test_stall_next_call(0);
         qh::set_error("qhead_fwd_noalloc: " + std::to_string(M) + " rows need " +
                       std::to_string(need) + " bytes of scratch, more than the fixed " +
                       std::to_string(kScratchBytes) +

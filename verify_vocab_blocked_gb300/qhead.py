@@ -162,6 +162,52 @@ def _stream(stream) -> int:
     return s.cuda_stream
 
 
+def _check_h(head: Head, h: torch.Tensor, what: str = "[M, H]") -> int:
+    """h must be a contiguous bf16 matrix with head.H columns, on the head's
+    device; returns M."""
+    if not isinstance(h, torch.Tensor) or h.dtype != torch.bfloat16 or h.dim() != 2 \
+            or not h.is_contiguous():
+        raise ValueError(f"h must be a contiguous bf16 {what} tensor")
+    if h.shape[1] != head.H:
+        raise ValueError(f"h has {h.shape[1]} columns but the head's hidden size H is {head.H}")
+    if head.wq.device != h.device:
+        raise ValueError(f"h is on {h.device} but the head is on {head.wq.device}")
+    return int(h.shape[0])
+
+
+def _check_vec(name: str, t: torch.Tensor | None, n: int, dtypes, dev, required: bool = True):
+    """A per-row argument: contiguous, shape [n], one of `dtypes`, on `dev`.
+    Returns the tensor to pass (bool masks are passed as their uint8 bytes)."""
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch tensor")
+    if t.dtype not in dtypes:
+        names = " or ".join(str(d).replace("torch.", "") for d in dtypes)
+        raise ValueError(f"{name} must be {names}, got {str(t.dtype).replace('torch.', '')}")
+    if t.dim() != 1 or t.shape[0] != n:
+        raise ValueError(f"{name} must have shape [{n}], got {list(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, h on {dev}")
+    return t.view(torch.uint8) if t.dtype == torch.bool else t
+
+
+def _targets(t, M, dev, required):
+    return _check_vec("targets", t, M, (torch.int32,), dev, required)
+
+
+def _mask(mk, M, dev):
+    return _check_vec("mask", mk, M, (torch.uint8, torch.bool), dev, required=False)
+
+
+def _f32(name, t, M, dev):
+    return _check_vec(name, t, M, (torch.float32,), dev)
+
+
 def fwd_workspace(head: Head, M: int) -> int:
     n = lib().qhead_fwd_workspace(ctypes.byref(head.c()), M)
     if n == ctypes.c_size_t(-1).value:
@@ -192,10 +238,10 @@ def fwd(head: Head, h: torch.Tensor, targets: torch.Tensor | None = None,
         mask: torch.Tensor | None = None, *, want_logp: bool = True, want_lse: bool = True,
         want_argmax: bool = True, workspace: torch.Tensor | None = None, stream=None):
     """Returns (logp or None, lse or None, argmax or None) for every row of h."""
-    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
-        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
-    M = h.shape[0]
+    M = _check_h(head, h)
     dev = h.device
+    targets = _targets(targets, M, dev, required=False)
+    mask = _mask(mask, M, dev)
     want_logp = want_logp and targets is not None
     logp = torch.empty(M, dtype=torch.float32, device=dev) if want_logp else None
     lse = torch.empty(M, dtype=torch.float32, device=dev) if want_lse else None
@@ -212,10 +258,11 @@ def bwd(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
         dlogp: torch.Tensor, mask: torch.Tensor | None = None, *,
         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """dh [M, H] float32 of sum_m dlogp[m] * logp[m]."""
-    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
-        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
-    M = h.shape[0]
+    M = _check_h(head, h)
     dev = h.device
+    targets = _targets(targets, M, dev, required=True)
+    mask = _mask(mask, M, dev)
+    lse, dlogp = _f32("lse", lse, M, dev), _f32("dlogp", dlogp, M, dev)
     dh = torch.empty(M, head.H, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = alloc_workspace(bwd_workspace(head, M), dev)
@@ -230,10 +277,11 @@ def bwd_dw(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor
            workspace: torch.Tensor | None = None, stream=None):
     """(dh [M, H] float32 or None, dw [V, H] float32): the gradients of
     sum_m dlogp[m] * logp[m] with respect to h and to the dequantized head."""
-    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
-        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
-    M = h.shape[0]
+    M = _check_h(head, h)
     dev = h.device
+    targets = _targets(targets, M, dev, required=True)
+    mask = _mask(mask, M, dev)
+    lse, dlogp = _f32("lse", lse, M, dev), _f32("dlogp", dlogp, M, dev)
     dh = torch.empty(M, head.H, dtype=torch.float32, device=dev) if want_dh else None
     dw = torch.empty(head.V, head.H, dtype=torch.float32, device=dev)
     if workspace is None:
@@ -257,10 +305,10 @@ def fwd_blockmax(head: Head, h: torch.Tensor, targets: torch.Tensor | None = Non
                  stream=None):
     """(logp or None, lse, argmax, block_max [M, ceil(V / 256)]): the forward
     plus each row's maximum capped logit per 256-row vocab tile."""
-    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
-        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
-    M = h.shape[0]
+    M = _check_h(head, h)
     dev = h.device
+    targets = _targets(targets, M, dev, required=False)
+    mask = _mask(mask, M, dev)
     logp = torch.empty(M, dtype=torch.float32, device=dev) if targets is not None else None
     lse = torch.empty(M, dtype=torch.float32, device=dev)
     am = torch.empty(M, dtype=torch.int32, device=dev)
@@ -280,10 +328,16 @@ def bwd_blockskip(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch
                   stream=None) -> torch.Tensor:
     """Approximate dh [M, H] float32: the blocks below eps (see
     qhead_bwd_blockskip) are left out of both backward phases."""
-    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
-        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
-    M = h.shape[0]
+    M = _check_h(head, h)
     dev = h.device
+    targets = _targets(targets, M, dev, required=True)
+    mask = _mask(mask, M, dev)
+    lse, dlogp = _f32("lse", lse, M, dev), _f32("dlogp", dlogp, M, dev)
+    nvt = (head.V + 255) // 256
+    if (not isinstance(block_max, torch.Tensor) or block_max.dtype != torch.float32
+            or tuple(block_max.shape) != (M, nvt) or not block_max.is_contiguous()
+            or block_max.device != dev):
+        raise ValueError(f"block_max must be a contiguous float32 [{M}, {nvt}] tensor on {dev}")
     dh = torch.empty(M, head.H, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = alloc_workspace(_ws_size("qhead_bwd_blockskip_workspace", head, M), dev)
@@ -300,10 +354,11 @@ def bwd_filter(head: Head, h: torch.Tensor, targets: torch.Tensor, lse: torch.Te
     """(dh [M, H] float32, cold or None): the approximate dh of the
     coefficient filter (see qhead_bwd_filter) and, when asked for, its block
     decisions uint8 [ceil(M / 32), ceil(V / 32)] (1 = cold)."""
-    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
-        raise ValueError("h must be a contiguous bf16 [M, H] tensor")
-    M = h.shape[0]
+    M = _check_h(head, h)
     dev = h.device
+    targets = _targets(targets, M, dev, required=True)
+    mask = _mask(mask, M, dev)
+    lse, dlogp = _f32("lse", lse, M, dev), _f32("dlogp", dlogp, M, dev)
     dh = torch.empty(M, head.H, dtype=torch.float32, device=dev)
     cold = (torch.empty(((M + 31) // 32, (head.V + 31) // 32), dtype=torch.uint8, device=dev)
             if want_cold else None)
@@ -322,9 +377,7 @@ def verify(head: Head, h: torch.Tensor, W: int, draft: torch.Tensor | None,
     """Verify B = h.shape[0] / W windows of W = gamma + 1 rows against their
     drafts (int32 [B, W - 1]).  Returns (n_accept [B], next_token [B],
     argmax [B * W], lse [B * W] or None), all on the device."""
-    if h.dtype != torch.bfloat16 or not h.is_contiguous() or h.dim() != 2:
-        raise ValueError("h must be a contiguous bf16 [B * W, H] tensor")
-    M = h.shape[0]
+    M = _check_h(head, h, "[B * W, H]")
     if W < 1 or M % W:
         raise ValueError("the row count must be a multiple of W >= 1")
     B = M // W
@@ -332,6 +385,9 @@ def verify(head: Head, h: torch.Tensor, W: int, draft: torch.Tensor | None,
                               or draft.numel() != B * (W - 1)):
         raise ValueError("draft must be a contiguous int32 [B, W - 1] tensor")
     dev = h.device
+    if draft is not None and draft.device != dev:
+        raise ValueError(f"draft is on {draft.device}, h on {dev}")
+    mask = _mask(mask, M, dev)
     am = torch.empty(M, dtype=torch.int32, device=dev)
     lse = torch.empty(M, dtype=torch.float32, device=dev) if want_lse else None
     n_acc = torch.empty(B, dtype=torch.int32, device=dev)

@@ -173,11 +173,20 @@ class Workload:
         return int(self.h.shape[0])
 
 
-def make_workload(name: str, seed: int = 0, M: int | None = None) -> Workload:
+def make_workload(name: str, seed: int = 0, M: int | None = None,
+                  head: SynthHead | None = None) -> Workload:
+    """The named workload.  `head`, if given, replaces the head this call would
+    draw (it must be the one make_head draws for the same shape and seed, e.g.
+    from another workload with the same head parameters)."""
     cfg = dict(CONFIGS[name])
     M = cfg["M"] if M is None else M
     pk = cfg.get("peaked")
-    if pk:
+    if head is not None:
+        if pk or (head.V, head.H, head.bits, head.group, head.softcap) != (
+                cfg["V"], cfg["H"], cfg["bits"], cfg["group"], cfg["softcap"]):
+            raise ValueError(f"the given head does not have {name}'s parameters")
+        h = make_hidden(M, cfg["H"], seed)
+    elif pk:
         head, hot = make_peaked_head(cfg["V"], cfg["H"], cfg["bits"], pk["n_hot"],
                                      pk["bias_shift"], cfg["softcap"], seed)
         h = make_hidden(M, cfg["H"], seed, mean=pk["h_mean"])
