@@ -59,11 +59,13 @@ extern "C" {
 /* Status codes. */
 #define QHEAD_OK 0
 #define QHEAD_EINVAL 1        /* null required pointer, misalignment, bad size, small workspace */
-#define QHEAD_EUNSUPPORTED 2  /* bits / group / H / dtype the library does not implement */
+#define QHEAD_EUNSUPPORTED 2  /* bits / group / H / sb_dtype the library does not implement */
 #define QHEAD_ECUDA 3         /* a CUDA launch or runtime call failed */
 
 /* Element type of scales and biases. */
 #define QHEAD_SB_F16 0
+#define QHEAD_SB_BF16 1
+#define QHEAD_SB_F32 2
 
 /*
  * The frozen quantized head (FlashCceHead on the page "mlx-bun 0.0.4 ->
@@ -72,13 +74,23 @@ extern "C" {
  *            elements j*(32/bits) + k, k = 0 .. 32/bits - 1, element k in bits
  *            bits*k .. bits*k + bits - 1 (least-significant field first).
  *            16-byte aligned.
- *   scales   device, fp16 [V, H/group], row-major.  16-byte aligned.
- *   biases   device, fp16 [V, H/group], row-major.  16-byte aligned.
+ *   scales   device, [V, H/group] row-major, of type sb_dtype.  16-byte aligned.
+ *   biases   device, [V, H/group] row-major, of type sb_dtype.  16-byte aligned.
  *   V        vocab rows, 1 <= V < 2^31.
  *   H        hidden size: a multiple of 128, 128 <= H <= 8192.
  *   bits     4 or 8.
  *   group    64 (the only group size implemented).
- *   sb_dtype QHEAD_SB_F16.
+ *   sb_dtype QHEAD_SB_F16, QHEAD_SB_BF16 or QHEAD_SB_F32: the element type of
+ *            scales and biases (the page casts any float type to f32).  The
+ *            exact fp32 parts of the path (the target logit, the argmax
+ *            recheck, the backward's one-hot term) widen the given values
+ *            exactly.  The tensor-core and weight-streaming kernels take fp16
+ *            operands: for a bf16 or fp32 head each call first rounds scales
+ *            and biases to fp16 (nearest) into its workspace -- exact for bf16
+ *            values of magnitude in [2^-17, 65504] or zero, one rounding for
+ *            fp32 -- which costs a pass over 2 * V * H/64 elements and
+ *            2 * 2 * V * H/64 bytes of workspace.  Magnitudes above 65504
+ *            become infinite there (results NaN).
  *   softcap  final-logit soft cap; <= 0 turns it off.
  */
 typedef struct qhead_head {
@@ -108,7 +120,10 @@ size_t qhead_bwd_workspace(const qhead_head* head, int64_t M);
  * (src/train/flash-cce.ts, per-vocab-block partials merged into lse and
  * logp = target logit - lse); argmax as in picksBatched on the page
  * "mlx-bun 0.0.8 -> 0.0.10" (src/spec/generate.ts).
- *   h         device, bf16 [M, H] row-major, 16-byte aligned.
+ *   h         device, bf16 [M, H] row-major, 16-byte aligned.  Every |h|
+ *             must be below 65504: the kernels stage h as fp16 operands, so a
+ *             larger magnitude becomes infinite there and the row's lse, logp
+ *             (and dh) come out inf or NaN; no error is returned.
  *   M         rows, >= 0 (M == 0 returns QHEAD_OK and launches nothing).
  *   targets   device, int32 [M], or NULL (verify: no logp).  Each active
  *             row's target must lie in [0, V); a row whose target does not
@@ -160,7 +175,8 @@ int qhead_verify(const qhead_head* head, const void* h, int64_t B, int64_t W,
  * (src/train/flash-cce.ts: logits recomputed per vocab tile, coefficient
  * dlogp * (onehot - softmax) * sech2, dh accumulated over all vocab blocks),
  * with the forward's lse reused.
- *   h, M, targets, mask  as for qhead_fwd; targets is required.
+ *   h, M, targets, mask  as for qhead_fwd (including |h| < 65504); targets
+ *             is required.
  *   lse       device, float [M]: the lse qhead_fwd returned for the same
  *             h / head / mask.
  *   dlogp     device, float [M]: the cotangent of each row's logp.
@@ -291,7 +307,9 @@ int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t
  *     are rejected with QHEAD_EINVAL and a message; nothing is launched.
  *     In practice the scratch holds the weight-streaming path (M < 64, a few
  *     hundred KB at H = 2560); the tensor-core path (M >= 64) needs tens of
- *     MB of per-segment partials and is rejected.
+ *     MB of per-segment partials and is rejected, and so is a bf16 or fp32
+ *     head whose fp16 copies of scales and biases (4 * V * H/64 bytes) do not
+ *     fit beside the rest (at V = 262144, H = 2560 they take 42 MB).
  *   - Every call shares the one array.  No byte of it needs to start at zero
  *     (a call writes all scratch it reads), but calls whose kernels may
  *     overlap on the GPU (e.g. issued on different streams without ordering)

@@ -130,13 +130,25 @@ def _as_f64_h(h: np.ndarray) -> np.ndarray:
     raise TypeError(f"oracle: h must be bf16 bits (uint16) or float64, got {h.dtype}")
 
 
-def _as_f64_sb(x: np.ndarray) -> np.ndarray:
-    """Scales/biases: float16 (or its uint16 bits) is widened; float64 is taken as is."""
-    if x.dtype in (np.float16, np.uint16):
-        return widen_f16(x)
+def _as_f64_sb(x: np.ndarray, sb_dtype: str = "f16") -> np.ndarray:
+    """Scales/biases widened exactly to float64 (the page casts any float type
+    to f32 before the dequantization): float16 (or its uint16 bits, with
+    sb_dtype "f16"), bf16 bit patterns (uint16, sb_dtype "bf16"), float32
+    (every binary32 value is a binary64 value); float64 is taken as is."""
     if x.dtype == np.float64:
         return np.ascontiguousarray(x)
-    raise TypeError(f"oracle: scales/biases must be float16 or float64, got {x.dtype}")
+    if sb_dtype == "bf16":
+        if x.dtype != np.uint16:
+            raise TypeError(f"oracle: bf16 scales/biases are uint16 bit patterns, got {x.dtype}")
+        return widen_bf16(x)
+    if sb_dtype == "f32":
+        if x.dtype != np.float32:
+            raise TypeError(f"oracle: f32 scales/biases must be float32, got {x.dtype}")
+        return np.ascontiguousarray(x, dtype=np.float64)
+    if x.dtype in (np.float16, np.uint16):
+        return widen_f16(x)
+    raise TypeError(f"oracle: scales/biases must be float16, bf16 bits, float32 or float64, "
+                    f"got {x.dtype}")
 
 
 # -------------------------------------------------------------------- head
@@ -146,11 +158,16 @@ class Head:
     """The quantized head (FlashCceHead on the page): packed codes, per-group
     affine scale and bias, bit width, group size and the optional soft cap."""
     wq: np.ndarray          # uint32 [V, H*bits/32]
-    scales: np.ndarray      # float16 or float64 [V, H/group]
-    biases: np.ndarray      # float16 or float64 [V, H/group]
+    scales: np.ndarray      # [V, H/group]: float16, bf16 bits (uint16), float32 or float64
+    biases: np.ndarray      # [V, H/group], the same type as scales
     bits: int
     group: int = 64
     softcap: float = 0.0
+    sb_dtype: str = "f16"   # "f16", "bf16" or "f32": how uint16 / float32 arrays are read
+
+    def sb(self):
+        """(scales, biases) widened exactly to float64."""
+        return _as_f64_sb(self.scales, self.sb_dtype), _as_f64_sb(self.biases, self.sb_dtype)
 
     @property
     def V(self) -> int:
@@ -173,7 +190,7 @@ def codes(wq: np.ndarray, H: int, bits: int) -> np.ndarray:
 def dequant(head: Head) -> np.ndarray:
     """Dense fp64 head w[v,d] (for small heads only: V*H doubles)."""
     wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
-    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    s, b = head.sb()
     out = np.empty((head.V, head.H), dtype=np.float64)
     _load().oracle_dequant(_ptr(wq, _u32p), _ptr(s, _f64p), _ptr(b, _f64p), head.V, head.H,
                            head.bits, head.group, _ptr(out, _f64p))
@@ -194,7 +211,7 @@ def logits(h: np.ndarray, head: Head, threads: int = 0) -> np.ndarray:
     hf = _as_f64_h(h)
     _check(head, hf)
     wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
-    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    s, b = head.sb()
     M = hf.shape[0]
     raw = np.empty((M, head.V), dtype=np.float64)
     _load().oracle_logits(M, head.H, head.V, head.bits, head.group, _ptr(hf, _f64p),
@@ -280,7 +297,7 @@ def backward(h: np.ndarray, head: Head, targets, dlogp, mask=None, lse=None,
     raw = _coeff(h, head, targets, dlogp, mask, lse, threads)
     M, V = raw.shape
     wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
-    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    s, b = head.sb()
     dh = np.empty((M, head.H), dtype=np.float64)
     _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
                       _ptr(b, _f64p), _ptr(raw, _f64p), _ptr(dh, _f64p), threads)
@@ -352,7 +369,7 @@ def backward_blockskip(h: np.ndarray, head: Head, targets, dlogp, bm, eps: float
         for k in np.nonzero(drop)[0]:
             coeff[rows, k * tile:(k + 1) * tile] = 0.0
     wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
-    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    s, b = head.sb()
     dh = np.empty((M, head.H), dtype=np.float64)
     _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
                       _ptr(b, _f64p), _ptr(coeff, _f64p), _ptr(dh, _f64p), threads)
@@ -418,7 +435,7 @@ def backward_filter(h: np.ndarray, head: Head, targets, dlogp, eps: float, mask=
         rows = act[32 * j:32 * (j + 1)]
         coeff[rows, 32 * k:32 * (k + 1)] = 0.0
     wq = np.ascontiguousarray(head.wq, dtype=np.uint32)
-    s, b = _as_f64_sb(head.scales), _as_f64_sb(head.biases)
+    s, b = head.sb()
     dh = np.empty((M, head.H), dtype=np.float64)
     _load().oracle_dh(M, head.H, V, head.bits, head.group, _ptr(wq, _u32p), _ptr(s, _f64p),
                       _ptr(b, _f64p), _ptr(coeff, _f64p), _ptr(dh, _f64p), threads)

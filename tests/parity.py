@@ -32,7 +32,8 @@ DH_REL_TOL = 2e-3
 
 def to_dev(wl: synth.Workload, device="cuda"):
     head = qhead.Head.from_numpy(wl.head.wq, wl.head.scales, wl.head.biases, wl.head.bits,
-                                 wl.head.group, wl.head.softcap, device=device)
+                                 wl.head.group, wl.head.softcap, device=device,
+                                 sb_dtype=wl.head.sb_dtype)
     h = torch.from_numpy(wl.h.astype(np.int16)).view(torch.bfloat16).to(device)
     t = torch.from_numpy(wl.targets).to(device) if wl.targets is not None else None
     mk = torch.from_numpy(wl.mask).to(device) if wl.mask is not None else None
@@ -41,7 +42,7 @@ def to_dev(wl: synth.Workload, device="cuda"):
 
 
 def oracle_head(sh: synth.SynthHead) -> oracle.Head:
-    return oracle.Head(sh.wq, sh.scales, sh.biases, sh.bits, sh.group, sh.softcap)
+    return oracle.Head(sh.wq, sh.scales, sh.biases, sh.bits, sh.group, sh.softcap, sh.sb_dtype)
 
 
 def gpu_fwd(head, h, t, mk):
@@ -145,7 +146,7 @@ def _dh_batch(wl, rows, g_dh, threads, case):
     if case is not None and act.any():
         tg = wl.targets[rows][act]
         sub = oracle.Head(wl.head.wq[tg], wl.head.scales[tg], wl.head.biases[tg], wl.head.bits,
-                          wl.head.group, wl.head.softcap)
+                          wl.head.group, wl.head.softcap, wl.head.sb_dtype)
         wt_norm = np.linalg.norm(oracle.dequant(sub), axis=1)
         den = np.maximum(den, np.abs(wl.dlogp[rows][act].astype(np.float64)) * wt_norm)
     return err, den, rows[act]

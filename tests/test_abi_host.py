@@ -68,6 +68,8 @@ def _fwd(L, head, **kw):
     (dict(bits=2), qhead.QHEAD_EUNSUPPORTED),
     (dict(group=32), qhead.QHEAD_EUNSUPPORTED),
     (dict(sb_dtype=7), qhead.QHEAD_EUNSUPPORTED),
+    (dict(sb_dtype=3), qhead.QHEAD_EUNSUPPORTED),
+    (dict(sb_dtype=-1), qhead.QHEAD_EUNSUPPORTED),
     (dict(H=192), qhead.QHEAD_EUNSUPPORTED),
     (dict(H=64), qhead.QHEAD_EUNSUPPORTED),
     (dict(H=8320), qhead.QHEAD_EUNSUPPORTED),
@@ -216,3 +218,11 @@ def test_the_abi_is_usable_from_plain_c(L, tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("sbt", [qhead.QHEAD_SB_BF16, qhead.QHEAD_SB_F32])
+def test_bf16_and_f32_scales_pass_the_head_checks(L, sbt):
+    # The head is accepted; the call then fails later (no workspace here), not
+    # on the element type of its scales and biases.
+    rc = _fwd(L, _head(sb_dtype=sbt), ws=None)
+    assert rc == qhead.QHEAD_EINVAL and "workspace" in L.qhead_last_error().decode()

@@ -86,3 +86,24 @@ def test_autograd_wrapper_validates_through_the_binding():
     h = _h().requires_grad_(True)
     with pytest.raises(ValueError, match="targets must be int32"):
         autograd.head_logp(h, _head(), _t(torch.int64))
+
+
+def test_scale_types_map_to_the_abi_codes():
+    for dt, code in ((torch.float16, qhead.QHEAD_SB_F16), (torch.bfloat16, qhead.QHEAD_SB_BF16),
+                     (torch.float32, qhead.QHEAD_SB_F32)):
+        hd = qhead.Head(torch.zeros(V, H * BITS // 32, dtype=torch.int32),
+                        torch.zeros(V, H // 64, dtype=dt), torch.zeros(V, H // 64, dtype=dt), BITS)
+        assert hd.c().sb_dtype == code
+    mixed = qhead.Head(torch.zeros(V, H * BITS // 32, dtype=torch.int32),
+                       torch.zeros(V, H // 64, dtype=torch.float16),
+                       torch.zeros(V, H // 64, dtype=torch.float32), BITS)
+    with pytest.raises(ValueError, match="share one type"):
+        mixed.c()
+
+
+def test_bf16_scales_from_numpy_keep_their_bits():
+    from verify_vocab_blocked_gb300 import synth
+    sh = synth.make_head(300, 128, 4, seed=2, sb_dtype="bf16")
+    hd = qhead.Head.from_numpy(sh.wq, sh.scales, sh.biases, 4, device="cpu", sb_dtype="bf16")
+    assert hd.scales.dtype == torch.bfloat16
+    assert (hd.scales.view(torch.int16).numpy().view("uint16") == sh.scales).all()

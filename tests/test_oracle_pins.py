@@ -286,8 +286,13 @@ def test_against_a_naive_second_path(bits, cap):
 def _torch_reference(h64, head: oracle.Head, targets, dlogp):
     """torch fp64: dense head from the bit-string unpack, log_softmax, autograd."""
     q = torch.from_numpy(_unpack_independent(head.wq, head.bits)).double()
-    s = torch.from_numpy(head.scales.astype(np.float64))
-    b = torch.from_numpy(head.biases.astype(np.float64))
+
+    def widen(x):  # torch's own conversions, independent of the oracle's C widening
+        if head.sb_dtype == "bf16":
+            return torch.from_numpy(x.astype(np.uint16).view(np.int16)).view(torch.bfloat16).double()
+        return torch.from_numpy(x).double()
+
+    s, b = widen(head.scales), widen(head.biases)
     w = q * s.repeat_interleave(head.group, 1) + b.repeat_interleave(head.group, 1)
     h = torch.from_numpy(h64).clone().requires_grad_(True)
     raw = h @ w.T
@@ -300,14 +305,20 @@ def _torch_reference(h64, head: oracle.Head, targets, dlogp):
             torch.argmax(raw, 1).numpy(), h.grad.numpy())
 
 
-@pytest.mark.parametrize("name,V,cap", [("tiny", None, None), ("gemma512", 4096, None),
-                                        ("mid8", 2048, None), ("gemma512", 1500, 0.0)])
-def test_against_torch_autograd(name, V, cap):
+@pytest.mark.parametrize("name,V,cap,sbt", [("tiny", None, None, "f16"),
+                                            ("gemma512", 4096, None, "f16"),
+                                            ("mid8", 2048, None, "f16"),
+                                            ("gemma512", 1500, 0.0, "f16"),
+                                            ("gemma512", 1500, None, "bf16"),
+                                            ("mid8", 1000, None, "bf16"),
+                                            ("gemma512", 1500, None, "f32"),
+                                            ("mid8", 1000, None, "f32")])
+def test_against_torch_autograd(name, V, cap, sbt):
     cfg = synth.CONFIGS[name]
     V = V or cfg["V"]
     cap = cfg["softcap"] if cap is None else cap
-    head = synth.make_head(V, cfg["H"], cfg["bits"], softcap=cap, seed=11)
-    ohead = oracle.Head(head.wq, head.scales, head.biases, cfg["bits"], 64, cap)
+    head = synth.make_head(V, cfg["H"], cfg["bits"], softcap=cap, seed=11, sb_dtype=sbt)
+    ohead = oracle.Head(head.wq, head.scales, head.biases, cfg["bits"], 64, cap, sbt)
     M = 6
     h = synth.make_hidden(M, cfg["H"], seed=11)
     t = synth.make_targets(M, V, seed=11)
@@ -577,8 +588,13 @@ def _torch_softmax_terms(h64, head: oracle.Head):
     """torch fp64 on the independently unpacked dense head: p[m, v] and
     sech2[m, v] (1 without a cap), and the dense head itself."""
     q = torch.from_numpy(_unpack_independent(head.wq, head.bits)).double()
-    s = torch.from_numpy(head.scales.astype(np.float64))
-    b = torch.from_numpy(head.biases.astype(np.float64))
+
+    def widen(x):  # torch's own conversions, independent of the oracle's C widening
+        if head.sb_dtype == "bf16":
+            return torch.from_numpy(x.astype(np.uint16).view(np.int16)).view(torch.bfloat16).double()
+        return torch.from_numpy(x).double()
+
+    s, b = widen(head.scales), widen(head.biases)
     w = q * s.repeat_interleave(head.group, 1) + b.repeat_interleave(head.group, 1)
     raw = torch.from_numpy(h64) @ w.T
     if head.softcap > 0:
@@ -705,3 +721,37 @@ def test_filter_keeps_target_blocks():
     c[:64] = 0.0
     c[96:] = 0.0
     assert np.allclose(got[32], c @ oracle.dequant(oh), atol=1e-12)
+
+
+# ------------------------------------------------- scale / bias element types
+
+def test_bf16_scales_equal_the_fp16_head_they_round_to():
+    # bf16 values of magnitude in [2^-14, 65504] have 8 significant bits and
+    # are exactly fp16 values too: the bf16 head and the fp16 head holding the
+    # same numbers must give identical results (the fp16 path is pinned above).
+    hb = synth.make_head(700, 256, 4, softcap=30.0, seed=31, sb_dtype="bf16")
+    sv, bv = oracle.widen_bf16(hb.scales), oracle.widen_bf16(hb.biases)
+    assert (np.abs(sv) >= 2.0 ** -14).all() and (np.abs(bv) >= 2.0 ** -14).all()
+    s16, b16 = sv.astype(np.float16), bv.astype(np.float16)
+    assert np.array_equal(s16.astype(np.float64), sv) and np.array_equal(b16.astype(np.float64), bv)
+    o_bf = oracle.Head(hb.wq, hb.scales, hb.biases, 4, 64, 30.0, "bf16")
+    o_16 = oracle.Head(hb.wq, s16, b16, 4, 64, 30.0, "f16")
+    h = synth.make_hidden(7, 256, seed=31)
+    t = synth.make_targets(7, 700, seed=31)
+    g = synth.make_dlogp(7, seed=31).astype(np.float64)
+    fa, fb = oracle.forward(h, o_bf, t), oracle.forward(h, o_16, t)
+    assert np.array_equal(fa.lse, fb.lse) and np.array_equal(fa.logp, fb.logp)
+    assert np.array_equal(oracle.backward(h, o_bf, t, g), oracle.backward(h, o_16, t, g))
+
+
+def test_f32_scales_are_used_unrounded():
+    # A scale no fp16 (or bf16) can hold: 1/64 * (1 + 2^-20).  With every code
+    # 15 and h = ones(64), raw = 64 * (15 s + b) exactly (fp64 holds it).
+    s = np.float32(1.0 / 64) * np.float32(1.0 + 2.0 ** -20)
+    b = np.float32(-0.1)
+    wq = np.full((1, 8), 0xFFFFFFFF, dtype=np.uint32)
+    head = oracle.Head(wq, np.array([[s]], np.float32), np.array([[b]], np.float32), 4, 64, 0.0,
+                       "f32")
+    raw = oracle.logits(np.ones((1, 64)), head)
+    assert raw[0, 0] == 64.0 * (15.0 * float(s) + float(b))
+    assert float(s) != float(np.float16(s))

@@ -29,8 +29,8 @@ def _lib():
     qhead.lib()
 
 
-def _custom(M, H, V, bits, cap, seed=0, mask=None, targets=None, dlogp=None):
-    head = synth.make_head(V, H, bits, softcap=cap, seed=seed)
+def _custom(M, H, V, bits, cap, seed=0, mask=None, targets=None, dlogp=None, sb_dtype="f16"):
+    head = synth.make_head(V, H, bits, softcap=cap, seed=seed, sb_dtype=sb_dtype)
     h = synth.make_hidden(M, H, seed=seed)
     t = synth.make_targets(M, V, seed=seed) if targets is None else np.asarray(targets, np.int32)
     g = synth.make_dlogp(M, seed=seed) if dlogp is None else np.asarray(dlogp, np.float32)
@@ -119,6 +119,25 @@ def test_stream_forward_shapes(M, H, V, bits, cap):
 @pytest.mark.parametrize("M,H,V,bits,cap", TC_SHAPES)
 def test_tensor_core_forward_shapes(M, H, V, bits, cap):
     _run_all(_custom(M, H, V, bits, cap, seed=M * 7 + V))
+
+
+# Scales and biases in bf16 and fp32 (the page widens any float type): the
+# weight-streaming forward (TMA-staged scales at H = 2560, cp.async at 1280)
+# with the CUDA-core backward, and the tensor-core forward and backward.
+SB_SHAPES = [
+    (5, 2560, 3001, 4, 30.0, "bf16"),
+    (13, 1280, 2000, 8, 0.0, "f32"),
+    (40, 256, 1500, 4, 30.0, "f32"),
+    (130, 384, 4099, 8, 30.0, "bf16"),
+    (300, 512, 3000, 4, 5.0, "f32"),
+    (257, 256, 2049, 4, 0.0, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,H,V,bits,cap,sbt", SB_SHAPES)
+def test_scale_bias_types(M, H, V, bits, cap, sbt):
+    mask = synth.make_mask(M, 32, 0.25) if M > 100 else None
+    _run_all(_custom(M, H, V, bits, cap, seed=M * 5 + V, mask=mask, sb_dtype=sbt))
 
 
 def test_tensor_core_forward_masked():

@@ -18,6 +18,10 @@
 #include "qh_internal.cuh"
 #include "qh_tmap.h"
 
+static_assert(QHEAD_SB_F16 == qh::kSbF16 && QHEAD_SB_BF16 == qh::kSbBf16 &&
+                  QHEAD_SB_F32 == qh::kSbF32,
+              "scale/bias element type codes");
+
 namespace {
 
 thread_local std::string g_err;
@@ -57,6 +61,14 @@ int fail(int code, const std::string& msg) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// The caller's scales and biases in their own type (the exact fp32 parts).
+qh::SbView sb_view(const qhead_head* hd) { return qh::SbView{hd->scales, hd->biases, hd->sb_dtype}; }
+
 struct DevInfo {
     int sms = 0;
 };
@@ -72,7 +84,9 @@ int check_head(const qhead_head* hd) {
     if (!hd->wq || !hd->scales || !hd->biases) return fail(QHEAD_EINVAL, "head pointer is NULL");
     if (hd->bits != 4 && hd->bits != 8) return fail(QHEAD_EUNSUPPORTED, "bits must be 4 or 8");
     if (hd->group != 64) return fail(QHEAD_EUNSUPPORTED, "group size must be 64");
-    if (hd->sb_dtype != QHEAD_SB_F16) return fail(QHEAD_EUNSUPPORTED, "scales/biases must be fp16");
+    if (hd->sb_dtype != QHEAD_SB_F16 && hd->sb_dtype != QHEAD_SB_BF16 &&
+        hd->sb_dtype != QHEAD_SB_F32)
+        return fail(QHEAD_EUNSUPPORTED, "sb_dtype must be QHEAD_SB_F16, QHEAD_SB_BF16 or QHEAD_SB_F32");
     if (hd->H < 128 || hd->H > qh::kMaxH || hd->H % 128)
         return fail(QHEAD_EUNSUPPORTED, "H must be a multiple of 128 in [128, 8192]");
     if (hd->V < 1 || hd->V >= ((int64_t)1 << 31)) return fail(QHEAD_EINVAL, "V must be in [1, 2^31)");
@@ -85,6 +99,33 @@ int check_head(const qhead_head* hd) {
 
 // ---------------------------------------------------------------- plans
 
+// Workspace for the fp16 copies of a bf16 / fp32 head's scales and biases
+// (two [V, H/64] arrays, each 256-byte aligned); none for an fp16 head.
+size_t sb_copy_bytes(const qhead_head* hd) {
+    if (hd->sb_dtype == QHEAD_SB_F16) return 0;
+    return 2 * align_up(2 * (size_t)hd->V * (size_t)(hd->H / 64), 256);
+}
+
+// The scales and biases the kernels with fp16 operands read: the caller's
+// arrays for an fp16 head, else their fp16 copies in the workspace region at
+// `off`, written by a conversion launch on `st` (which this queues).
+int sb_operands(const qhead_head* hd, void* ws, size_t off, cudaStream_t st, const __half** sc,
+                const __half** bi) {
+    if (hd->sb_dtype == QHEAD_SB_F16) {
+        *sc = static_cast<const __half*>(hd->scales);
+        *bi = static_cast<const __half*>(hd->biases);
+        return QHEAD_OK;
+    }
+    const size_t n = (size_t)hd->V * (size_t)(hd->H / 64);
+    __half* s16 = at<__half>(ws, off);
+    __half* b16 = at<__half>(ws, off + align_up(2 * n, 256));
+    const cudaError_t e = qh::launch_sb_to_f16(sb_view(hd), (int64_t)n, s16, b16, st);
+    if (e) return fail(QHEAD_ECUDA, std::string("sb_to_f16: ") + cudaGetErrorString(e));
+    *sc = s16;
+    *bi = b16;
+    return QHEAD_OK;
+}
+
 // Rows from which the forward runs on the tensor-core kernel (below: the
 // weight-streaming kernel, whose cost is one pass over the head per 8 rows).
 constexpr int64_t kTcMinM = 64;
@@ -96,6 +137,7 @@ struct FwdPlan {
     int S = 1;           // vocab splits of the partials (weight-streaming path)
     size_t records = 0;  // partial records
     size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_part = 0, total = 0;
+    size_t off_sb = 0;   // fp16 copies of bf16 / fp32 scales and biases (else unused)
 };
 
 struct BwdPlan {
@@ -112,6 +154,7 @@ struct BwdPlan {
     size_t off_count = 0, off_rows = 0, off_pos = 0, off_h16 = 0, off_coeff = 0, off_dhp = 0,
            off_hp = 0, off_g = 0, off_dmax = 0, off_cnt = 0, off_offs = 0, off_cursor = 0,
            off_idx = 0, off_skip = 0, off_kbits = 0, total = 0;
+    size_t off_sb = 0;       // fp16 copies of bf16 / fp32 scales and biases (else unused)
 };
 
 // Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block is
@@ -174,6 +217,7 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p, bool force_tc = false)
     // fp16 h for the tensor-core path; the streaming kernel converts its rows itself.
     p->off_h16 = off;   if (p->tc) off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
     p->off_part = off;  off = align_up(off + sizeof(qh::Partial) * p->records, 256);
+    p->off_sb = off;    off += sb_copy_bytes(hd);
     p->total = off;
     return QHEAD_OK;
 }
@@ -250,14 +294,12 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false,
         p->S = (int)S;
         p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 256);
     }
+    off = align_up(off, 256);
+    p->off_sb = off;    off += sb_copy_bytes(hd);
     p->total = off;
     return QHEAD_OK;
 }
 
-template <typename T>
-T* at(void* ws, size_t off) {
-    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
-}
 
 int cuda_fail(cudaError_t e, const char* what) {
     return fail(QHEAD_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
@@ -340,8 +382,9 @@ static int fwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const auto* wq = head->wq;
-    const auto* sc = static_cast<const __half*>(head->scales);
-    const auto* bi = static_cast<const __half*>(head->biases);
+    const __half *sc = nullptr, *bi = nullptr;
+    if ((rc = sb_operands(head, workspace, p.off_sb, st, &sc, &bi))) return rc;
+    const qh::SbView sbx = sb_view(head);
     const auto* hb = static_cast<const __nv_bfloat16*>(h);
     int* count = at<int>(workspace, p.off_count);
     int* err = count + 1;
@@ -391,7 +434,7 @@ static int fwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
         hook_after(st);
         if (e) return cuda_fail(e, "stream_fwd");
     }
-    if ((e = qh::launch_fwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+    if ((e = qh::launch_fwd_finalize(wq, sbx, head->V, head->H, head->bits, head->softcap, hb,
                                      pos, targets, part, p.S, p.tc ? S_dev : nullptr, err,
                                      logp, lse, argmax, M, st)))
         return cuda_fail(e, "fwd_finalize");
@@ -446,8 +489,9 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const auto* wq = head->wq;
-    const auto* sc = static_cast<const __half*>(head->scales);
-    const auto* bi = static_cast<const __half*>(head->biases);
+    const __half *sc = nullptr, *bi = nullptr;
+    if ((rc = sb_operands(head, workspace, p.off_sb, st, &sc, &bi))) return rc;
+    const qh::SbView sbx = sb_view(head);
     const auto* hb = static_cast<const __nv_bfloat16*>(h);
     int* count = at<int>(workspace, p.off_count);
     int* err = count + 1;
@@ -492,7 +536,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
         int* offs = p.dw ? at<int>(workspace, p.off_offs) : nullptr;
         int* idx = p.dw ? at<int>(workspace, p.off_idx) : nullptr;
         if (p.dw &&
-            (e = qh::launch_dw_prep(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+            (e = qh::launch_dw_prep(wq, sbx, head->V, head->H, head->bits, head->softcap, hb,
                                     rows, count, targets, dlogp, p.Mpad, dmax, hp, g,
                                     at<int>(workspace, p.off_cnt), offs,
                                     at<int>(workspace, p.off_cursor), idx, st)))
@@ -570,7 +614,7 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
         if (e) return cuda_fail(e, "bwd_simt");
     }
     if (dh &&
-        (e = qh::launch_bwd_finalize(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb,
+        (e = qh::launch_bwd_finalize(wq, sbx, head->V, head->H, head->bits, head->softcap, hb,
                                      pos, targets, dlogp, dhp, p.S, p.Mpad, err, dh, M, st)))
         return cuda_fail(e, "bwd_finalize");
     return QHEAD_OK;

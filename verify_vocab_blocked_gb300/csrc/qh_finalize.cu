@@ -6,8 +6,9 @@
 // -> 0.0.6", src/train/flash-cce.ts, done here on device in a fixed order
 // instead of in MLX ops), then
 //   * the target logit is recomputed exactly in fp32 (h widened from bf16,
-//     w = fmaf(scale, q, bias)), so logp = softcap(raw_target) - lse carries
-//     no fp16 operand rounding;
+//     w = fmaf(scale, q, bias) from the caller's scales and biases in their
+//     own type), so logp = softcap(raw_target) - lse carries no fp16 operand
+//     rounding;
 //   * the two argmax candidates (the best two raw logits over all splits)
 //     are recomputed the same way and the better exact value wins, lowest index on ties (argmax over the raw logits, which
 //     picksBatched on the page "mlx-bun 0.0.8 -> 0.0.10" notes is the argmax of
@@ -26,8 +27,7 @@ namespace {
 constexpr int kFinThreads = 128;
 
 __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
-    const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
-    const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
+    const uint32_t* __restrict__ wq, SbView sb, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
     const int32_t* __restrict__ targets, const Partial* __restrict__ part, int S,
     const int* __restrict__ S_dev, const int* __restrict__ err,
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
         else if (it < n1 + n2) v = fin.i2;
         else v = t_ok ? t : -1;
         float x = 0.f;
-        if (v >= 0) x = warp_exact_logit<10>(hrow, wq, scales, biases, v, H, bits);
+        if (v >= 0) x = warp_exact_logit<10>(hrow, wq, sb, v, H, bits);
         if (lane == 0) exact[it] = x;
     }
     __syncthreads();
@@ -125,8 +125,7 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
 constexpr int kBwdFinThreads = 256;
 
 __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
-    const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
-    const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
+    const uint32_t* __restrict__ wq, SbView sb, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
     const int32_t* __restrict__ targets, const float* __restrict__ dlogp,
     const float* __restrict__ dhp, int S, int64_t Mpad, const int* __restrict__ err,
@@ -148,7 +147,7 @@ __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
     const bool t_ok = t >= 0 && (int64_t)t < V;
     if (threadIdx.x < 32) {
         float raw = 0.f;
-        if (t_ok) raw = warp_exact_logit(h + r * (int64_t)H, wq, scales, biases, t, H, bits);
+        if (t_ok) raw = warp_exact_logit(h + r * (int64_t)H, wq, sb, t, H, bits);
         if (threadIdx.x == 0) {
             float sech2 = 1.f;
             if (cap > 0.f) {
@@ -163,19 +162,19 @@ __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
     for (int d = threadIdx.x; d < H; d += kBwdFinThreads) {
         float acc = 0.f;
         for (int s = 0; s < S; ++s) acc += dhp[((int64_t)s * Mpad + i) * H + d];
-        const float wt = t_ok ? dequant_elem(wq, scales, biases, t, d, H, bits) : 0.f;
+        const float wt = t_ok ? dequant_elem(wq, sb, t, d, H, bits) : 0.f;
         out[d] = fmaf(coef, wt, acc);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+cudaError_t launch_fwd_finalize(const uint32_t* wq, SbView sb,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
                                 const int* S_dev, const int* err, float* logp,
                                 float* lse, int32_t* argmax, int64_t M, cudaStream_t st) {
-    void* args[] = {&wq, &scales, &biases, &V,     &H,   &bits,  &cap,   &h,      &pos,
+    void* args[] = {&wq, &sb, &V,     &H,   &bits,  &cap,   &h,      &pos,
                     &targets, &part, &S, &S_dev, &err, &logp, &lse, &argmax};
     return launch_dependent(reinterpret_cast<const void*>(fwd_finalize_kernel), dim3((unsigned)M),
                             dim3(kFinThreads), 0, st, args);
@@ -221,12 +220,12 @@ cudaError_t launch_accept_prefix(const int32_t* argmax, const int32_t* draft, in
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+cudaError_t launch_bwd_finalize(const uint32_t* wq, SbView sb,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const float* dlogp,
                                 const float* dhp, int S, int64_t Mpad, const int* err, float* dh,
                                 int64_t M, cudaStream_t st) {
-    bwd_finalize_kernel<<<(unsigned)M, kBwdFinThreads, 0, st>>>(wq, scales, biases, V, H, bits,
+    bwd_finalize_kernel<<<(unsigned)M, kBwdFinThreads, 0, st>>>(wq, sb, V, H, bits,
                                                                  cap, h, pos, targets, dlogp, dhp,
                                                                  S, Mpad, err, dh);
     return cudaGetLastError();

@@ -25,6 +25,28 @@ struct __align__(32) Partial {
     int i1, i2, status, pad1;
 };
 
+// Element types of the head's scales and biases (the values of QHEAD_SB_* in
+// the public header).
+constexpr int kSbF16 = 0, kSbBf16 = 1, kSbF32 = 2;
+
+// The caller's scales and biases, each [V, H/64], in their own element type.
+// The exact fp32 parts of the path (target logit, argmax recheck, one-hot
+// term) read them through sb_elem; the tensor-core and streaming kernels read
+// an fp16 copy when the type is not fp16 (launch_sb_to_f16).
+struct SbView {
+    const void* s;
+    const void* b;
+    int type;
+};
+
+// Element i of a scale or bias array, widened to fp32 exactly.
+__device__ __forceinline__ float sb_elem(const void* p, int64_t i, int type) {
+    if (type == kSbF32) return static_cast<const float*>(p)[i];
+    const unsigned short u = static_cast<const unsigned short*>(p)[i];
+    if (type == kSbBf16) return __uint_as_float(static_cast<uint32_t>(u) << 16);
+    return __half2float(__ushort_as_half(u));
+}
+
 constexpr int kTokGroup = 8;      // tokens per weight-streaming CTA (mma n = 8)
 constexpr int kMaxH = 8192;
 constexpr int kRowPad = 128;      // compacted row count is padded to this
@@ -91,16 +113,13 @@ struct RowState {
 // whose loads are issued together (one round trip per round).
 template <int U = 4>
 __device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restrict__ hrow,
-                                                  const uint32_t* __restrict__ wq,
-                                                  const __half* __restrict__ scales,
-                                                  const __half* __restrict__ biases,
+                                                  const uint32_t* __restrict__ wq, SbView sb,
                                                   int64_t v, int H, int bits) {
     const int lane = threadIdx.x & 31;
     const int wpr = H * bits / 32;
     const int G = H / 64;
     const uint32_t* wrow = wq + v * (int64_t)wpr;
-    const __half* srow = scales + v * (int64_t)G;
-    const __half* brow = biases + v * (int64_t)G;
+    const int64_t g0 = v * (int64_t)G;
     float acc = 0.f;
     // Units of 8 consecutive elements, U per lane per round, loads of a round
     // issued together.
@@ -113,8 +132,8 @@ __device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restric
             const int u = u0 + 32 * i;
             if (u < H / 8) {
                 hv[i] = *reinterpret_cast<const uint4*>(hrow + 8 * u);
-                s[i] = __half2float(srow[u / 8]);
-                b[i] = __half2float(brow[u / 8]);
+                s[i] = sb_elem(sb.s, g0 + u / 8, sb.type);
+                b[i] = sb_elem(sb.b, g0 + u / 8, sb.type);
                 if (bits == 4) { w0[i] = wrow[u]; w1[i] = 0u; }
                 else { w0[i] = wrow[2 * u]; w1[i] = wrow[2 * u + 1]; }
             }
@@ -139,15 +158,13 @@ __device__ __forceinline__ float warp_exact_logit(const __nv_bfloat16* __restric
 }
 
 // fp32 dequantized element w[v,d].
-__device__ __forceinline__ float dequant_elem(const uint32_t* __restrict__ wq,
-                                              const __half* __restrict__ scales,
-                                              const __half* __restrict__ biases,
+__device__ __forceinline__ float dequant_elem(const uint32_t* __restrict__ wq, SbView sb,
                                               int64_t v, int d, int H, int bits) {
     const int per = 32 / bits;
     const uint32_t word = wq[v * (int64_t)(H * bits / 32) + d / per];
     const uint32_t q = (word >> (bits * (d % per))) & ((1u << bits) - 1u);
     const int64_t gi = v * (int64_t)(H / 64) + d / 64;
-    return fmaf(__half2float(scales[gi]), (float)q, __half2float(biases[gi]));
+    return fmaf(sb_elem(sb.s, gi, sb.type), (float)q, sb_elem(sb.b, gi, sb.type));
 }
 
 // ------------------------------------------------------------- launchers
@@ -160,6 +177,9 @@ constexpr int64_t kFusedPrologueMaxM = 256;
 cudaError_t launch_prologue_fused(const uint8_t* mask, const __nv_bfloat16* h, int64_t M,
                                   int64_t Mpad, int H, int bits, int* rows, int* pos, int* count,
                                   __half* h16, int64_t nrows, int* err, cudaStream_t st);
+// Scales and biases of another element type rounded to fp16 (nearest, ties
+// to even) for the tensor-core and streaming kernels: n elements of each.
+cudaError_t launch_sb_to_f16(SbView sb, int64_t n, __half* s16, __half* b16, cudaStream_t st);
 cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
                              const int* count, __half* h16, cudaStream_t st);
 // Launches `fn` with programmatic stream serialization: its CTAs may start
@@ -178,7 +198,7 @@ cudaError_t launch_skip_map(const float* bmax, int64_t ld, const float* lse,
                             const int32_t* targets, const int* rows, const int* count,
                             int64_t n_mt, int64_t n_vt, float eps, uint8_t* skip,
                             cudaStream_t st);
-cudaError_t launch_fwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+cudaError_t launch_fwd_finalize(const uint32_t* wq, SbView sb,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
                                 const int* S_dev, const int* err, float* logp,
@@ -188,7 +208,7 @@ cudaError_t launch_bwd_simt(const uint32_t* wq, const __half* scales, const __ha
                             const int* rows, const int* count, const float* lse,
                             const float* dlogp, float* dhp, int S, int64_t M, int64_t Mpad,
                             cudaStream_t st);
-cudaError_t launch_bwd_finalize(const uint32_t* wq, const __half* scales, const __half* biases,
+cudaError_t launch_bwd_finalize(const uint32_t* wq, SbView sb,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const float* dlogp,
                                 const float* dhp, int S, int64_t Mpad, const int* err, float* dh,

@@ -128,6 +128,28 @@ cudaError_t launch_compact(const uint8_t* mask, int64_t M, int64_t Mpad, int* ro
     return cudaGetLastError();
 }
 
+// Scales and biases of a bf16 or fp32 head rounded to fp16 (nearest, ties to
+// even) for the kernels that read fp16 operands: exact for bf16 values in
+// [2^-17, 65504] (bf16 has 8 significant bits, fp16 11), one rounding for fp32
+// values.  Grid-stride over the n elements of each array.
+__global__ void sb_to_f16_kernel(SbView sb, int64_t n, __half* __restrict__ s16,
+                                 __half* __restrict__ b16) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        s16[i] = __float2half_rn(sb_elem(sb.s, i, sb.type));
+        b16[i] = __float2half_rn(sb_elem(sb.b, i, sb.type));
+    }
+}
+
+cudaError_t launch_sb_to_f16(SbView sb, int64_t n, __half* s16, __half* b16, cudaStream_t st) {
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = (int64_t)device_sms() * 8;
+    if (blocks > cap && cap > 0) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    sb_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(sb, n, s16, b16);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_convert_h(const __nv_bfloat16* h, int64_t Mpad, int H, int bits, const int* rows,
                              const int* count, __half* h16, cudaStream_t st) {
     const int threads = ((H / 8) + 31) / 32 * 32;

@@ -314,8 +314,7 @@ __global__ void __launch_bounds__(1024) dw_dmax_kernel(const float* __restrict__
 constexpr int kPrepThreads = 128;
 
 __global__ void __launch_bounds__(kPrepThreads) dw_hprime_kernel(
-    const uint32_t* __restrict__ wq, const __half* __restrict__ scales,
-    const __half* __restrict__ biases, int64_t V, int H, int bits, float cap,
+    const uint32_t* __restrict__ wq, SbView sb, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ rows,
     const int* __restrict__ count, const int32_t* __restrict__ targets,
     const float* __restrict__ dlogp, const float* __restrict__ dmax, __half* __restrict__ hp,
@@ -343,7 +342,7 @@ __global__ void __launch_bounds__(kPrepThreads) dw_hprime_kernel(
             const int32_t t = targets[r];
             if (t >= 0 && (int64_t)t < V) {
                 const float raw =
-                    warp_exact_logit<10>(h + (int64_t)r * H, wq, scales, biases, t, H, bits);
+                    warp_exact_logit<10>(h + (int64_t)r * H, wq, sb, t, H, bits);
                 float sech2 = 1.f;
                 if (cap > 0.f) {
                     const float th = tanhf(raw / cap);
@@ -443,7 +442,7 @@ int tc_dw_smem_bytes(int H) {
     return tc_dh_cols(H) == 256 ? DwLayout<256>::SMEM : DwLayout<128>::SMEM;
 }
 
-cudaError_t launch_dw_prep(const uint32_t* wq, const __half* scales, const __half* biases,
+cudaError_t launch_dw_prep(const uint32_t* wq, SbView sb,
                            int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                            const int* rows, const int* count, const int32_t* targets,
                            const float* dlogp, int64_t Mpad, float* dmax, __half* hp, float* g,
@@ -451,7 +450,7 @@ cudaError_t launch_dw_prep(const uint32_t* wq, const __half* scales, const __hal
     cudaError_t e;
     dw_dmax_kernel<<<1, 1024, 0, st>>>(dlogp, rows, count, dmax);
     if ((e = cudaGetLastError())) return e;
-    dw_hprime_kernel<<<(unsigned)Mpad, kPrepThreads, 0, st>>>(wq, scales, biases, V, H, bits, cap,
+    dw_hprime_kernel<<<(unsigned)Mpad, kPrepThreads, 0, st>>>(wq, sb, V, H, bits, cap,
                                                               h, rows, count, targets, dlogp, dmax,
                                                               hp, g);
     if ((e = cudaGetLastError())) return e;

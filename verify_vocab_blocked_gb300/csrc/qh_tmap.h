@@ -145,7 +145,7 @@ int tc_fwd_smem_bytes(int bits);
 int tc_dw_smem_bytes(int H);
 // max |dlogp|, the scaled fp16 copy h' and the one-hot terms g, and the
 // per-target row lists (counting sort, stable in row order).
-cudaError_t launch_dw_prep(const uint32_t* wq, const __half* scales, const __half* biases,
+cudaError_t launch_dw_prep(const uint32_t* wq, SbView sb,
                            int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                            const int* rows, const int* count, const int32_t* targets,
                            const float* dlogp, int64_t Mpad, float* dmax, __half* hp, float* g,

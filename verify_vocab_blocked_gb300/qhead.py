@@ -16,7 +16,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqhead.so")
 
 QHEAD_OK, QHEAD_EINVAL, QHEAD_EUNSUPPORTED, QHEAD_ECUDA = 0, 1, 2, 3
-QHEAD_SB_F16 = 0
+QHEAD_SB_F16, QHEAD_SB_BF16, QHEAD_SB_F32 = 0, 1, 2
+_SB_CODE = {torch.float16: QHEAD_SB_F16, torch.bfloat16: QHEAD_SB_BF16,
+            torch.float32: QHEAD_SB_F32}
 
 # Every symbol include/qhead.h declares.
 EXPORTS = ("qhead_fwd_workspace", "qhead_bwd_workspace", "qhead_fwd", "qhead_bwd",
@@ -121,8 +123,8 @@ def _check(rc: int):
 class Head:
     """A quantized head resident on the GPU (FlashCceHead layout)."""
     wq: torch.Tensor        # int32 (uint32 bit patterns) [V, H*bits/32]
-    scales: torch.Tensor    # float16 [V, H/group]
-    biases: torch.Tensor    # float16 [V, H/group]
+    scales: torch.Tensor    # float16, bfloat16 or float32 [V, H/group]
+    biases: torch.Tensor    # the same type as scales, [V, H/group]
     bits: int
     group: int = 64
     softcap: float = 0.0
@@ -139,18 +141,32 @@ class Head:
         for t in (self.wq, self.scales, self.biases):
             if not t.is_contiguous():
                 raise ValueError("head tensors must be contiguous")
-        if self.scales.dtype != torch.float16 or self.biases.dtype != torch.float16:
-            raise ValueError("scales/biases must be float16")
+        if self.scales.dtype not in _SB_CODE or self.biases.dtype != self.scales.dtype:
+            raise ValueError("scales and biases must share one type: float16, bfloat16 or "
+                             "float32")
         return CHead(self.wq.data_ptr(), self.scales.data_ptr(), self.biases.data_ptr(),
-                     self.V, self.H, self.bits, self.group, QHEAD_SB_F16, float(self.softcap))
+                     self.V, self.H, self.bits, self.group, _SB_CODE[self.scales.dtype],
+                     float(self.softcap))
 
     @staticmethod
-    def from_numpy(wq, scales, biases, bits, group=64, softcap=0.0, device="cuda"):
+    def from_numpy(wq, scales, biases, bits, group=64, softcap=0.0, device="cuda",
+                   sb_dtype: str = "f16"):
+        """Scales and biases: float16 or float32 arrays, or uint16 bf16 bit
+        patterns with sb_dtype="bf16"."""
         import numpy as np
+
+        def sb(x):
+            x = np.ascontiguousarray(x)
+            if sb_dtype == "bf16":
+                return torch.from_numpy(x.astype(np.uint16).view(np.int16)).view(
+                    torch.bfloat16).to(device)
+            want = {"f16": np.float16, "f32": np.float32}[sb_dtype]
+            if x.dtype != want:
+                raise ValueError(f"scales/biases are {x.dtype}, sb_dtype is {sb_dtype}")
+            return torch.from_numpy(x).to(device)
+
         return Head(torch.from_numpy(np.ascontiguousarray(wq).view(np.int32)).to(device),
-                    torch.from_numpy(np.ascontiguousarray(scales)).to(device),
-                    torch.from_numpy(np.ascontiguousarray(biases)).to(device),
-                    bits, group, softcap)
+                    sb(scales), sb(biases), bits, group, softcap)
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:

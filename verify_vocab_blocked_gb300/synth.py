@@ -74,14 +74,25 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return u.astype(np.uint16)
 
 
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to bf16 (nearest, ties to even, in one rounding);
+    returns uint16 bits.  Inputs must be finite and within bf16's normal range
+    or zero."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                     # x = m * 2^e, 0.5 <= |m| < 1
+    q = np.round(m * 256.0) / 256.0        # 8 significant bits, ties to even
+    return f32_to_bf16_bits(np.ldexp(q, e).astype(np.float32))
+
+
 @dataclass
 class SynthHead:
     wq: np.ndarray        # uint32 [V, H*bits/32]
-    scales: np.ndarray    # float16 [V, H/group]
-    biases: np.ndarray    # float16 [V, H/group]
+    scales: np.ndarray    # [V, H/group]: float16, bf16 bits (uint16) or float32
+    biases: np.ndarray    # [V, H/group], the same type as scales
     bits: int
     group: int
     softcap: float
+    sb_dtype: str = "f16"
 
     @property
     def V(self) -> int:
@@ -93,7 +104,10 @@ class SynthHead:
 
 
 def make_head(V: int, H: int, bits: int, group: int = 64, softcap: float = 0.0,
-              seed: int = 0, chunk_rows: int = 1 << 16) -> SynthHead:
+              seed: int = 0, chunk_rows: int = 1 << 16, sb_dtype: str = "f16") -> SynthHead:
+    """sb_dtype: the element type scales and biases are rounded to from their
+    unrounded draws -- "f16" (float16 arrays), "bf16" (uint16 bit patterns)
+    or "f32" (float32 arrays)."""
     if bits not in (4, 8):
         raise ValueError("bits must be 4 or 8")
     if H % group:
@@ -113,8 +127,15 @@ def make_head(V: int, H: int, bits: int, group: int = 64, softcap: float = 0.0,
     else:
         s = rs.uniform(1e-4, 1e-3, size=(V, G))
         b = -128.0 * s
-    return SynthHead(wq, s.astype(np.float16), b.astype(np.float16), bits, group,
-                     float(softcap))
+    if sb_dtype == "f16":
+        sr, br = s.astype(np.float16), b.astype(np.float16)
+    elif sb_dtype == "f32":
+        sr, br = s.astype(np.float32), b.astype(np.float32)
+    elif sb_dtype == "bf16":
+        sr, br = f64_to_bf16_bits(s), f64_to_bf16_bits(b)
+    else:
+        raise ValueError("sb_dtype must be f16, bf16 or f32")
+    return SynthHead(wq, sr, br, bits, group, float(softcap), sb_dtype)
 
 
 def make_hidden(M: int, H: int, seed: int = 0, mean: float = 0.0) -> np.ndarray:
