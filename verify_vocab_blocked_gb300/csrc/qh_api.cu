@@ -409,8 +409,8 @@ static int fwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
         CUtensorMap th, tw;
         const int words = 64 * head->bits / 32;
         if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
-            !(head->bits == 8 ? qh::tmap_packed_rows_swz : qh::tmap_packed_rows)(
-                &tw, wq, head->H * head->bits / 32, head->V, words, qh::kTcFwdTileRows))
+            !qh::tmap_packed_rows(&tw, wq, head->H * head->bits / 32, head->V, words,
+                                  qh::kTcFwdBoxRows))
             return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
         qh::TcFwdArgs ta{};
         ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H; ta.cap = head->softcap;
@@ -548,9 +548,8 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
             return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
         const int wpr = head->H * head->bits / 32;
         if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
-            !(head->bits == 8 ? qh::tmap_packed_rows_swz : qh::tmap_packed_rows)(
-                &tw_logit, wq, wpr, head->V, 64 * head->bits / 32,
-                                  qh::kTcFwdTileRows) ||
+            !qh::tmap_packed_rows(&tw_logit, wq, wpr, head->V, 64 * head->bits / 32,
+                                  qh::kTcFwdBoxRows) ||
             !qh::tmap_rows_f16_sw128(&tcoef, coeff, p.chunk, p.Mpad, 128) ||
             !(qh::tc_dh_swizzled(head->H, head->bits)
                   ? qh::tmap_packed_rows_sw128(&tw_dh, wq, wpr, head->V, 64)

@@ -4,23 +4,33 @@
 // forward on the page "mlx-bun 0.0.4 -> 0.0.6" (src/train/flash-cce.ts,
 // FWD_STEEL_SOURCE: a quantized block GEMM whose epilogue soft-caps each
 // logit tile and folds it into a running max / sum-exp), re-designed for
-// sm_103a:
+// sm_103a around a pair of CTAs on two SMs (a cluster of two):
 //
-//   * one persistent CTA per SM walks units (128 token rows x a segment of
-//     256-row vocab tiles), chosen on the device from the active-row count;
-//   * a TMA warp streams the fp16 h tile (128 x 64, 128-byte swizzle) and the
-//     packed weight tile (256 rows x 64 codes) into a 3-stage ring;
+//   * the pair walks units (256 token rows x a segment of 256-row vocab
+//     tiles), chosen on the device from the active-row count; the even CTA
+//     holds token rows 0-127 of the unit and vocab rows 0-127 of each tile,
+//     the odd CTA rows 128-255 of both;
+//   * in each CTA a TMA warp streams its fp16 h tile (128 x 64, 128-byte
+//     swizzle) and its half of the packed weight tile (128 rows x 64 codes);
 //   * eight (4-bit heads) or sixteen (8-bit heads) dequant warps turn the
-//     packed tile into fp16 in the tensor core's K-major 128-byte-swizzled
-//     layout (w = fma(q, scale, bias), one rounding);
-//   * one thread issues tcgen05.mma (M=128, N=256, K=16, fp32 accumulate) into
-//     one of two 256-column TMEM accumulators;
-//   * four epilogue warps read the accumulator with tcgen05.ld (one row per
-//     thread), apply the soft cap, update the row's online softmax and track
-//     the maxima of the two 32-column slices with the largest raw logit, each
-//     with the lowest column holding it (argmax candidates, rechecked exactly
-//     by the finalize kernel).
-// The [M,V] logits and the dequantized head never leave the SM.
+//     CTA's packed half-tile into fp16 in the tensor core's K-major
+//     128-byte-swizzled layout (w = fma(q, scale, bias), one rounding), two
+//     or four threads per vocab row so that the packed rows are read with
+//     conflict-free 16-byte loads; the TMA warp also stages the half-tile's
+//     scales and biases, eight groups per box, so that the dequant warps
+//     hold no global loads in flight (a barrier arrival, a release, would
+//     wait for them);
+//   * one thread of the even CTA issues tcgen05.mma.cta_group::2 (M = 256
+//     across the pair, N = 256, K = 16, fp32 accumulate) into one of two
+//     256-column accumulators: each SM dequantizes only the half of every
+//     weight tile its own B operand holds, half of what a one-CTA M = 128 MMA
+//     would need per flop;
+//   * four epilogue warps per CTA read their 128 accumulator rows with
+//     tcgen05.ld (one row per thread), apply the soft cap, update the row's
+//     online softmax and track the maxima of the two 32-column slices with
+//     the largest raw logit, each with the lowest column holding it (argmax
+//     candidates, rechecked exactly by the finalize kernel).
+// The [M,V] logits and the dequantized head never leave the SMs.
 //
 // The same kernel is phase 1 of the backward: its coefficient epilogue writes
 // p * sech2 * 2^14 as fp16 per logit into the chunk's [rows x chunk] block;
@@ -28,7 +38,22 @@
 // per 32 x 32 block whether any term reaches eps, writes a cold block as
 // zeros and clears, for a warm one, the dh step's bit in the filter's map
 // (the backward's near-zero coefficient filter on the same page).
+//
+// Synchronisation of the pair: each CTA's dequant warps, once their B half
+// and (having waited for it) their TMA-loaded A tile are in place, arrive on
+// their own CTA's dequant barrier (CTA scope: a cluster-scope release in every
+// dequant warp at every stage would wait for the warp's prefetched scale
+// loads); in the odd CTA one otherwise idle thread waits for that barrier and
+// forwards a single cluster-scope arrival to the even CTA's, whose MMA thread
+// thus waits for both CTAs.  Each commit of the MMAs is multicast to the
+// barriers of both CTAs (input stage free, B stage free, accumulator full).
+// Each CTA's epilogue warps arrive on the even CTA's accumulator-empty
+// barrier (once per tile).
 #include <stdio.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "qh_dequant.cuh"
 #include "qh_tc.cuh"
@@ -38,55 +63,66 @@ namespace qh {
 
 namespace {
 
-constexpr int BM = 128;   // token rows per tile (MMA M)
-constexpr int BN = kTcFwdTileRows;  // vocab rows per tile (MMA N)
+constexpr int BM = 128;   // token rows per CTA per unit (the pair: 256, the MMA's M)
+constexpr int BMU = 2 * BM;
+constexpr int BN = kTcFwdTileRows;  // vocab rows per tile (MMA N); each CTA holds BN / 2
+constexpr int BNH = BN / 2;
 constexpr int BK = 64;    // K per stage (one quantization group, one swizzle atom)
-constexpr int NB = 3;     // dequantized-tile stages
-// Warp roles: 0 TMA, 1 MMA, 2 .. 2 + dequant warps - 1 dequantize, then four
-// epilogue warps.  Dequant warps: one thread per vocab row at 4 bits; two per
-// row at 8 bits (twice the words per row; measured faster).
+// Warp roles: 0 TMA, 1 MMA (issues in the even CTA; allocates TMEM in both),
+// 2 .. 2 + dequant warps - 1 dequantize, then four epilogue warps.
 template <int BITS>
 struct Warps {
     static constexpr int kDq = BITS == 4 ? 8 : 16;
-    static constexpr int kTpr = kDq * 32 / 256;  // dequant threads per vocab row
+    static constexpr int kTpr = kDq * 32 / BNH;  // dequant threads per vocab row (2 or 4)
     static constexpr int kEpi0 = 2 + kDq;        // first epilogue warp
     static constexpr int kThreads = 32 * (kEpi0 + 4);
+    static_assert(kTpr * 16 == BK * BITS / 8, "one 16-byte part of the packed row per thread");
 };
 constexpr int kTmemCols = 512;  // two 256-column fp32 accumulators
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr uint32_t kIdesc = tc::idesc_f16_f32(BM, BN, false, false);
+constexpr int B_BYTES = BNH * BK * 2;  // this CTA's half of the dequantized tile
+constexpr uint32_t kIdesc = tc::idesc_f16_f32(BMU, BN, false, false);
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint16_t kPairMask = 0x3;
 
-// Two rings: NS stages of TMA inputs (h tile + packed tile, small, deep enough
-// to cover HBM latency) and NB stages of dequantized tiles (large).
+// Two rings: NS stages of TMA inputs (h tile + packed half-tile) and NB
+// stages of dequantized half-tiles.
+// Scales and biases: boxes of kSbGroups groups x BNH rows of fp16, one box
+// of each per kSbGroups stages, in a ring of NSB slots.
+constexpr int kSbGroups = 8;
+constexpr int SB_BOX = kSbGroups * 2 * BNH;  // bytes of one box (16-byte rows)
+
 template <int BITS>
 struct Layout {
     static constexpr int NS = BITS == 4 ? 5 : 4;
+    static constexpr int NB = 4;
+    static constexpr int NSB = 2;
     static constexpr int P_ROW = BK * BITS / 8;  // packed bytes per row per stage
-    static constexpr int P_BYTES = BN * P_ROW;
+    static constexpr int P_BYTES = BNH * P_ROW;
     static constexpr int WORDS = BK * BITS / 32;
     static constexpr int OFF_B = 0;
     static constexpr int OFF_A = OFF_B + NB * B_BYTES;
     static constexpr int OFF_P = OFF_A + NS * A_BYTES;
-    static constexpr int OFF_BAR = OFF_P + NS * P_BYTES;
-    static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 4) + 16;
+    static constexpr int OFF_SB = OFF_P + NS * P_BYTES;  // slot i: scales, then biases
+    static constexpr int OFF_BAR = OFF_SB + NSB * 2 * SB_BOX;
+    static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 2 * NSB + 5) + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct Work {
     int n_mt, n_vt, n_seg, units;
 };
 
-// Units (128 rows x a segment of vocab tiles) per CTA: many small units keep
-// the per-CTA totals within a few percent of each other.
-constexpr int kUnitsPerCta = 32;
+// Units (256 rows x a segment of vocab tiles) per CTA pair: many small units
+// keep the per-pair totals within a few percent of each other.
+constexpr int kUnitsPerPair = 32;
 
-__device__ __forceinline__ Work plan_work(int n_active, int n_vt) {
+__device__ __forceinline__ Work plan_work(int n_active, int n_vt, int n_pairs) {
     Work w;
-    w.n_mt = (n_active + BM - 1) / BM;
+    w.n_mt = (n_active + BMU - 1) / BMU;
     w.n_vt = n_vt;
-    const int target = kUnitsPerCta * (int)gridDim.x;
+    const int target = kUnitsPerPair * n_pairs;
     int seg = w.n_mt > 0 ? (target + w.n_mt - 1) / w.n_mt : 1;
     if (seg > w.n_vt) seg = w.n_vt;
     if (seg < 1) seg = 1;
@@ -110,13 +146,23 @@ __device__ __forceinline__ void unit_coords(const Work& w, int vt_begin, int u, 
 //             vocab rows below filter_eps are written as zeros; a.kbits).
 constexpr int EPI_SOFTMAX = 0, EPI_COEFF = 1, EPI_FILTER = 2;
 
+// The pair's sequence of (unit, vocab tile) steps, the tiles every role
+// processes in the same order (skipped tiles left out).
+struct TileIt {
+    int u, mt, seg, vt, vt1;
+    bool valid;
+};
+
 template <int BITS, int EPI>
 __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+    const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_b,
     const TcFwdArgs a) {
     using L = Layout<BITS>;
     using WR = Warps<BITS>;
     constexpr int NS = L::NS;
+    constexpr int NB = L::NB;
+    constexpr int NSB = L::NSB;
     const __half* __restrict__ scales = a.scales;
     const __half* __restrict__ biases = a.biases;
     const int64_t V = a.V;
@@ -127,28 +173,66 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     unsigned char* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     // (offsetting the shared array itself keeps the accesses in the shared
     // address space; a round trip through an integer would make them generic)
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);  // TMA inputs landed
-    uint64_t* empty = full + NS;  // inputs consumed (MMA commit + each dequant warp)
-    uint64_t* dq = empty + NS;    // dequantized tile written
-    uint64_t* bfree = dq + NB;    // dequantized tile consumed (MMA commit)
-    uint64_t* accf = bfree + NB;
-    uint64_t* acce = accf + 2;
-    uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(acce + 2);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);  // own TMA inputs landed
+    uint64_t* empty = full + NS;  // inputs consumed (pair MMA commit + own dequant warps)
+    uint64_t* dq = empty + NS;    // own dequant warps done (even CTA: and the odd CTA's relay)
+    uint64_t* bfree = dq + NB;    // B stage consumed (pair MMA commit)
+    uint64_t* accf = bfree + NB;  // accumulator full (pair MMA commit)
+    uint64_t* acce = accf + 2;    // even CTA: both CTAs' epilogues drained the accumulator
+    uint64_t* mdrain = acce + 2;  // MMA drain on the abort path
+    uint64_t* sbf = mdrain + 1;   // scale / bias boxes landed
+    uint64_t* sbe = sbf + NSB;    // scale / bias boxes consumed (own dequant warps)
+    uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(sbe + NSB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
-    uint64_t* mdrain = acce + 3;  // MMA drain on the abort path
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int cid = (int)tc::cluster_id_x(), n_pairs = (int)tc::nclusters_x();
     const int n_active = *a.count;
-    const Work W = plan_work(n_active, a.vt_end - a.vt_begin);
+    const Work W = plan_work(n_active, a.vt_end - a.vt_begin, n_pairs);
     if (EPI == EPI_SOFTMAX && blockIdx.x == 0 && threadIdx.x == 0) *a.S_out = W.n_seg;
-    if (W.units == 0 || (int)blockIdx.x >= W.units) return;
+    // (the same decision in both CTAs of the pair: nothing below has run yet)
+    if (W.units == 0 || cid >= W.units) return;
     const int KSTEPS = H / BK;
     const int G = H / 64;
-    // Backward with the blockMax early exit: every role skips the same
-    // (row tile, vocab tile) pairs (no loads, dequantization or MMAs; the
-    // epilogue writes the tile's coefficients as zeros).
+    // Scales and biases staged by TMA (rows of whole 16-byte blocks of 8
+    // groups); otherwise each dequant thread loads its own, stage by stage.
+    const bool sb_tma = a.sb_tma != 0;
+    // Backward with the blockMax early exit: skip_half: the 128-row tile t of
+    // the map skips vocab tile vt (tiles past the map's rows hold no row);
+    // skipped: both 128-row tiles of 256-row unit mt do, and every role of
+    // both CTAs leaves the vocab tile out (no loads, dequantization or MMAs).
+    auto skip_half = [&](int t, int vt) {
+        return t >= a.skip_rows || a.skip[(int64_t)t * a.skip_ld + vt] != 0;
+    };
     auto skipped = [&](int mt, int vt) {
-        return EPI != EPI_SOFTMAX && a.skip != nullptr && a.skip[(int64_t)mt * a.skip_ld + vt] != 0;
+        return EPI != EPI_SOFTMAX && a.skip != nullptr && skip_half(2 * mt, vt) &&
+               skip_half(2 * mt + 1, vt);
+    };
+    // Tile iteration shared by the roles that look ahead (dequant warps).
+    auto tile_settle = [&](TileIt& t) {  // move to the first tile not skipped
+        while (t.valid) {
+            while (t.vt < t.vt1 && skipped(t.mt, t.vt)) ++t.vt;
+            if (t.vt < t.vt1) return;
+            t.u += n_pairs;
+            if (t.u >= W.units) { t.valid = false; return; }
+            int vt0;
+            unit_coords(W, a.vt_begin, t.u, t.mt, t.seg, vt0, t.vt1);
+            t.vt = vt0;
+        }
+    };
+    auto tile_first = [&]() {
+        TileIt t;
+        t.u = cid;
+        t.valid = true;
+        unit_coords(W, a.vt_begin, t.u, t.mt, t.seg, t.vt, t.vt1);
+        tile_settle(t);
+        return t;
+    };
+    auto tile_next = [&](TileIt t) {
+        ++t.vt;
+        tile_settle(t);
+        return t;
     };
 
     if (threadIdx.x == 0) {
@@ -157,48 +241,83 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
             tc::mbar_init(&empty[i], 1 + WR::kDq);
         }
         for (int i = 0; i < NB; ++i) {
-            tc::mbar_init(&dq[i], WR::kDq);
+            tc::mbar_init(&dq[i], WR::kDq + (rank == 0 ? 1 : 0));
             tc::mbar_init(&bfree[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&accf[i], 1);
-            tc::mbar_init(&acce[i], 4);
+            tc::mbar_init(&acce[i], 2 * 4);
         }
         tc::mbar_init(mdrain, 1);
+        for (int i = 0; i < NSB; ++i) {
+            tc::mbar_init(&sbf[i], 1);
+            tc::mbar_init(&sbe[i], WR::kDq);
+        }
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmap_h);
         tc::prefetch_tmap(&tmap_w);
+        if (sb_tma) {
+            tc::prefetch_tmap(&tmap_s);
+            tc::prefetch_tmap(&tmap_b);
+        }
     }
     if (warp == 1) {
-        tc::tmem_alloc(tmem_base_sh, kTmemCols);
-        tc::tmem_relinquish();
+        tc::tmem_alloc_pair(tmem_base_sh, kTmemCols);
+        tc::tmem_relinquish_pair();
     }
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();  // barriers initialised in both CTAs before any remote arrival
     tc::tc_fence_after();
     const uint32_t tmem_base = *tmem_base_sh;
+    // The even CTA's barriers, addressed from either CTA.
+    const uint32_t dq_lead = tc::mapa_shared(dq, 0);
+    const uint32_t acce_lead = tc::mapa_shared(acce, 0);
+    // Tiles the pair processes, in order (every role walks the same ones).
+    auto for_each_tile = [&](auto&& body) {
+        for (int u = cid; u < W.units; u += n_pairs) {
+            int mt, seg, vt0, vt1;
+            unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
+            for (int vt = vt0; vt < vt1; ++vt)
+                if (!skipped(mt, vt) && !body(mt, vt)) return;
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, fills = 0;
+            int stage = 0, sslot = 0;
+            uint32_t phase = 0, fills = 0, sphase = 0, sfills = 0;
             if (a.stall) goto producer_abort;
-            for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
+            for (int u = cid; u < W.units; u += n_pairs) {
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
                 for (int vt = vt0; vt < vt1; ++vt) {
                     if (skipped(mt, vt)) continue;
                     for (int kk = 0; kk < KSTEPS; ++kk) {
+                        if (sb_tma && kk % kSbGroups == 0) {
+                            // the scales and biases of the next 8 stages
+                            if (!tc::mbar_wait(&sbe[sslot], sphase ^ 1, abort_flag, err,
+                                               tc::kErrTimeoutEmpty))
+                                goto producer_abort;
+                            unsigned char* sd = smem + L::OFF_SB + sslot * 2 * SB_BOX;
+                            tc::mbar_arrive_expect_tx(&sbf[sslot], 2 * SB_BOX);
+                            tc::tma_load_2d(sd, &tmap_s, &sbf[sslot], kk, vt * BN + (int)rank * BNH);
+                            tc::tma_load_2d(sd + SB_BOX, &tmap_b, &sbf[sslot], kk,
+                                            vt * BN + (int)rank * BNH);
+                            ++sfills;
+                            if (++sslot == NSB) { sslot = 0; sphase ^= 1; }
+                        }
                         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag, err,
                                            tc::kErrTimeoutEmpty))
                             goto producer_abort;
                         tc::mbar_arrive_expect_tx(&full[stage], A_BYTES + L::P_BYTES);
+                        // rows past the tensor (h: the padded row count; the
+                        // head: V) read as zeros
                         tc::tma_load_2d(smem + L::OFF_A + stage * A_BYTES, &tmap_h, &full[stage],
-                                        kk * BK, mt * BM);
+                                        kk * BK, mt * BMU + (int)rank * BM);
                         tc::tma_load_2d(smem + L::OFF_P + stage * L::P_BYTES, &tmap_w,
-                                        &full[stage], kk * L::WORDS, vt * BN);
+                                        &full[stage], kk * L::WORDS, vt * BN + (int)rank * BNH);
                         ++fills;
                         if (++stage == NS) { stage = 0; phase ^= 1; }
                     }
@@ -215,29 +334,29 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
             goto producer_done;
         producer_abort:
             tc::drain_ring(full, NS, fills, err);
+            tc::drain_ring(sbf, NSB, sfills, err);
         producer_done:;
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int stage = 0, buf = 0, bs = 0;
-            uint32_t phase = 0, aphase = 0, bphase = 0;
-            for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
+            uint32_t aphase = 0, bphase = 0;
+            for (int u = cid; u < W.units; u += n_pairs) {
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
                 for (int vt = vt0; vt < vt1; ++vt) {
                     if (skipped(mt, vt)) continue;
-                    if (!tc::mbar_wait(&acce[buf], aphase ^ 1, abort_flag, err,
-                                       tc::kErrTimeoutAccEmpty))
+                    if (!tc::mbar_wait_cluster(&acce[buf], aphase ^ 1, abort_flag, err,
+                                               tc::kErrTimeoutAccEmpty))
                         goto mma_abort;
                     tc::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
                     for (int kk = 0; kk < KSTEPS; ++kk) {
-                        if (!tc::mbar_wait(&full[stage], phase, abort_flag, err,
-                                           tc::kErrTimeoutFull))
-                            goto mma_abort;
-                        if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err,
-                                           tc::kErrTimeoutDequant))
+                        // Both CTAs' dequant warps have arrived: their B halves
+                        // are written and their A tiles have landed.
+                        if (!tc::mbar_wait_cluster(&dq[bs], bphase, abort_flag, err,
+                                                   tc::kErrTimeoutDequant))
                             goto mma_abort;
                         tc::tc_fence_after();
                         const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * A_BYTES);
@@ -246,113 +365,135 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                         for (int ks = 0; ks < BK / 16; ++ks) {
                             const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks, 16, 1024);
                             const uint64_t bd = tc::sdesc_sw128(b0 + 32 * ks, 16, 1024);
-                            tc::umma_f16(d_tmem, ad, bd, kIdesc, (kk | ks) != 0);
+                            tc::umma_f16_pair(d_tmem, ad, bd, kIdesc, (kk | ks) != 0);
                         }
-                        tc::umma_commit(&empty[stage]);
-                        tc::umma_commit(&bfree[bs]);
-                        if (++stage == NS) { stage = 0; phase ^= 1; }
+                        tc::umma_commit_pair(&empty[stage], kPairMask);
+                        tc::umma_commit_pair(&bfree[bs], kPairMask);
+                        if (++stage == NS) stage = 0;
                         if (++bs == NB) { bs = 0; bphase ^= 1; }
                     }
-                    tc::umma_commit(&accf[buf]);
+                    tc::umma_commit_pair(&accf[buf], kPairMask);
                     if (++buf == 2) { buf = 0; aphase ^= 1; }
                 }
             }
             goto mma_done;
         mma_abort:
             // Let every MMA issued so far finish before TMEM is released.
-            tc::umma_commit(mdrain);
+            tc::umma_commit_pair(mdrain, 0x1);
             tc::mbar_drain(mdrain, 0, err);
         mma_done:;
+        } else if (lane == 0) {
+            // Odd CTA: forward each stage's "dequant done" to the even CTA.
+            int bs = 0;
+            uint32_t bphase = 0;
+            for_each_tile([&](int, int) {
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err, tc::kErrTimeoutDequant))
+                        return false;
+                    tc::mbar_arrive_cluster_relaxed(dq_lead + 8u * (uint32_t)bs);
+                    if (++bs == NB) { bs = 0; bphase ^= 1; }
+                }
+                return true;
+            });
         }
     } else if (warp < WR::kEpi0) {
         // ------------------------------------------------------------ dequant warps
-        // Thread: part `pt` of vocab row t of the tile (kTpr parts per row).
-        const int t = (threadIdx.x - 64) / WR::kTpr, pt = (threadIdx.x - 64) % WR::kTpr;
+        // Thread: 16-byte part `pt` of vocab row r of this CTA's half-tile.
+        const int t = threadIdx.x - 64;
+        const int r = t / WR::kTpr, pt = t % WR::kTpr;
         int stage = 0, bs = 0;
         uint32_t phase = 0, bphase = 0;
-        for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
-            int mt, seg, vt0, vt1;
-            unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
-            for (int vt = vt0; vt < vt1; ++vt) {
-                if (skipped(mt, vt)) continue;
-                const int64_t v0 = (int64_t)vt * BN + t;
-                const bool ok0 = v0 < V;
+        // One stage: wait for the inputs and a free B stage, dequantize this
+        // thread's part of row r with scale s2 / bias b2 (fp16 pairs), signal.
+        auto stage_work = [&](uint32_t s2, uint32_t b2) {
+            // Results ignored: the warp stays converged (see the abort policy).
+            tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
+            tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
+            const unsigned char* prow = smem + L::OFF_P + stage * L::P_BYTES + r * L::P_ROW;
+            unsigned char* brow = smem + L::OFF_B + bs * B_BYTES + r * 128;
+            const uint4 wv = *reinterpret_cast<const uint4*>(prow + 16 * pt);
+            const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+            if constexpr (BITS == 4) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = 4 * pt + j;  // 16-byte chunk = one word of 8 codes
+                    uint32_t p[4];
+                    deq4_word(wd[j], s2, b2, p);
+                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) =
+                        make_uint4(p[0], p[1], p[2], p[3]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int c = 2 * pt + j;  // 16-byte chunk = two words of 4 codes
+                    const uint32_t w0 = wd[2 * j], w1 = wd[2 * j + 1];
+                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) =
+                        make_uint4(deq8(w0, 0x5140u, s2, b2), deq8(w0, 0x7362u, s2, b2),
+                                   deq8(w1, 0x5140u, s2, b2), deq8(w1, 0x7362u, s2, b2));
+                }
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&dq[bs]);
+                tc::mbar_arrive(&empty[stage]);  // packed half-tile fully read
+            }
+            if (++stage == NS) { stage = 0; phase ^= 1; }
+            if (++bs == NB) { bs = 0; bphase ^= 1; }
+        };
+        // Vocab row of this thread in tile t (-1 past the head).
+        auto vrow = [&](const TileIt& ti) -> int64_t {
+            const int64_t v = (int64_t)ti.vt * BN + (int64_t)rank * BNH + r;
+            return v < V ? v : -1;
+        };
+        if (sb_tma) {
+            // Scales and biases of 8 groups per staged box: this row's 16-byte
+            // rows of the scale box and the bias box.
+            int sslot = 0;
+            uint32_t sphase = 0;
+            const int NKB = G / kSbGroups;
+            for (TileIt ti = tile_first(); ti.valid; ti = tile_next(ti)) {
+                for (int kb = 0; kb < NKB; ++kb) {
+                    tc::mbar_wait(&sbf[sslot], sphase, abort_flag, err, tc::kErrTimeoutFull);
+                    const unsigned char* sd = smem + L::OFF_SB + sslot * 2 * SB_BOX;
+                    const uint4 sc = *reinterpret_cast<const uint4*>(sd + r * 16);
+                    const uint4 bc = *reinterpret_cast<const uint4*>(sd + SB_BOX + r * 16);
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&sbe[sslot]);  // (values are in registers)
+                    if (++sslot == NSB) { sslot = 0; sphase ^= 1; }
+                    const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+                    const uint32_t bw[4] = {bc.x, bc.y, bc.z, bc.w};
+#pragma unroll
+                    for (int k8 = 0; k8 < kSbGroups; ++k8) {
+                        const uint32_t sel = (k8 & 1) ? 0x3232u : 0x1010u;
+                        stage_work(__byte_perm(sw[k8 >> 1], sw[k8 >> 1], sel),
+                                   __byte_perm(bw[k8 >> 1], bw[k8 >> 1], sel));
+                    }
+                }
+            }
+        } else {
+            for (TileIt ti = tile_first(); ti.valid; ti = tile_next(ti)) {
+                const int64_t v = vrow(ti);
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const __half z = __float2half(0.f);
-                    const __half s0 = ok0 ? scales[v0 * G + kk] : z, b0 = ok0 ? biases[v0 * G + kk] : z;
-                    // Results ignored: the warp stays converged (see the abort policy).
-                    tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
-                    tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
-                    const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
-                    unsigned char* Bs = smem + L::OFF_B + bs * B_BYTES;
-                    {
-                        const int r = t;
-                        const __half2 s2 = __half2half2(s0);
-                        const __half2 b2 = __half2half2(b0);
-                        // 8-bit packed tiles arrive with the 64-byte swizzle (16-byte
-                        // part q of row r at q ^ ((r >> 1) & 3)), so an 8-lane phase
-                        // of part loads hits 8 bank groups (measured -1.5 % at 8 bits;
-                        // the 32-byte swizzle of 4-bit tiles was not faster).
-                        const unsigned char* prow = P + r * L::P_ROW;
-                        const int pswz = BITS == 8 ? (r >> 1) & 3 : 0;
-                        unsigned char* brow = Bs + r * 128;
-                        if constexpr (BITS == 4) {
-                            static_assert(WR::kTpr == 1, "4-bit rows: one thread per row");
-#pragma unroll
-                            for (int hq = 0; hq < 2; ++hq) {
-                                const uint4 wv = *reinterpret_cast<const uint4*>(prow + ((hq ^ pswz) << 4));
-                                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const int c = hq * 4 + j;  // 16-byte chunk = one word
-                                    uint32_t p[4];
-                                    deq4_word(wd[j], s2, b2, p);
-                                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) =
-                                        make_uint4(p[0], p[1], p[2], p[3]);
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int hq0 = 0; hq0 < 4 / WR::kTpr; ++hq0) {
-                                const int hq = pt * (4 / WR::kTpr) + hq0;  // this thread's 16-byte parts
-                                const uint4 wv = *reinterpret_cast<const uint4*>(prow + ((hq ^ pswz) << 4));
-                                const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                                for (int j = 0; j < 2; ++j) {
-                                    const int c = hq * 2 + j;  // 16-byte chunk = two words
-                                    const uint32_t w0 = wd[2 * j], w1 = wd[2 * j + 1];
-                                    *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) =
-                                        make_uint4(deq8(w0, 0x5140u, s2, b2),
-                                                   deq8(w0, 0x7362u, s2, b2),
-                                                   deq8(w1, 0x5140u, s2, b2),
-                                                   deq8(w1, 0x7362u, s2, b2));
-                                }
-                            }
-                        }
-                    }
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc::mbar_arrive(&dq[bs]);
-                        tc::mbar_arrive(&empty[stage]);  // packed tile fully read
-                    }
-                    if (++stage == NS) { stage = 0; phase ^= 1; }
-                    if (++bs == NB) { bs = 0; bphase ^= 1; }
+                    const __half s0 = v >= 0 ? scales[v * G + kk] : z;
+                    const __half b0 = v >= 0 ? biases[v * G + kk] : z;
+                    stage_work(bcast_h(s0), bcast_h(b0));
                 }
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue warps
         const int sub = warp & 3;  // TMEM sub-partition of this warp
-        const int row = sub * 32 + lane;
+        const int row = (int)rank * BM + sub * 32 + lane;  // row of the pair's 256-row unit
         const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
         const float k2 = cap > 0.f ? 2.f * kLog2e / cap : 0.f;
         int buf = 0;
         uint32_t aphase = 0;
-        for (int u = blockIdx.x; u < W.units; u += gridDim.x) {
+        for (int u = cid; u < W.units; u += n_pairs) {
             int mt, seg, vt0, vt1;
             unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
-            const int i = mt * BM + row;  // compact row of this thread
+            const int i = mt * BMU + row;  // compact row of this thread
             float m = -INFINITY, s = 0.f, v1 = -INFINITY, v2 = -INFINITY;
             int i1 = INT32_MAX, i2 = INT32_MAX;
             // EPI_COEFF: log2(p * 2^14) = z * log2e - (lse * log2e - 14)
@@ -369,35 +510,38 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                 ftgt = tg >= 0 && (int64_t)tg < V ? (int64_t)tg : -1;
             }
             for (int vt = vt0; vt < vt1; ++vt) {
-                if (skipped(mt, vt)) {
-                    // The tile's coefficients of this row are written as zeros
-                    // where the dh contraction reads them: when the other
-                    // 128-row tile of its 256-row unit keeps the vocab tile.
-                    const int pm = mt ^ 1;
-                    const bool partner_skips =
-                        pm >= a.skip_rows || a.skip[(int64_t)pm * a.skip_ld + vt] != 0;
-                    if (EPI != EPI_SOFTMAX && !partner_skips && i < a.coeff_rows) {
-                        __half* dst = a.coeff + (int64_t)i * a.coeff_ld +
-                                      (int64_t)(vt - a.vt_begin) * BN;
-                        const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll 1
-                        for (int q = 0; q < BN / 16; ++q) tc::st_global_v8(dst + 16 * q, zero);
-                    }
-                    continue;
-                }
+                // Both 128-row tiles of the unit skip the vocab tile: so does
+                // the dh contraction's unit (the same pair of tiles), which
+                // reads nothing of it.
+                if (skipped(mt, vt)) continue;
                 tc::mbar_wait(&accf[buf], aphase, abort_flag, err, tc::kErrTimeoutAccFull);
                 tc::tc_fence_after();
+                // blockMax exit: this CTA's 128-row tile skips the vocab tile
+                // while the other one keeps it: its coefficients are written as
+                // zeros (the dh contraction reads them).  Warp-uniform.
+                const bool zero_half = EPI != EPI_SOFTMAX && a.skip != nullptr &&
+                                       skip_half(2 * mt + (int)rank, vt);
                 float tz = -INFINITY;  // the tile's maximum of z (blockMax)
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tc::tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, r);
-                    tc::tmem_wait_ld();
                     const int64_t col0 = (int64_t)vt * BN + c * 32;
+                    if (EPI != EPI_SOFTMAX && zero_half) {
+                        if (i < a.coeff_rows) {
+                            __half* dst = a.coeff + (int64_t)i * a.coeff_ld +
+                                          (col0 - (int64_t)a.vt_begin * BN);
+                            const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                            tc::st_global_v8(dst, zero);
+                            tc::st_global_v8(dst + 16, zero);
+                        }
+                        continue;
+                    }
+                    uint32_t rr[32];
+                    tc::tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, rr);
+                    tc::tmem_wait_ld();
                     const int nvalid = (int)min((int64_t)32, V - col0);
                     float x[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(rr[j]);
                     if constexpr (EPI != EPI_SOFTMAX) {
                         // coefficient block column = col0 - first column of the chunk
                         __half* dst = a.coeff + (int64_t)i * a.coeff_ld + (col0 - (int64_t)a.vt_begin * BN);
@@ -411,9 +555,9 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                                 const float xv = x[j + e];
                                 float lg2p, sech2 = 1.f;
                                 if (cap > 0.f) {
-                                    const float t = fmaf(-2.f, tc::rcp_approx(tc::ex2_approx(xv * k2) + 1.f), 1.f);
-                                    lg2p = fmaf(cap * t, kLog2e, -lsb);
-                                    sech2 = fmaf(-t, t, 1.f);
+                                    const float th = fmaf(-2.f, tc::rcp_approx(tc::ex2_approx(xv * k2) + 1.f), 1.f);
+                                    lg2p = fmaf(cap * th, kLog2e, -lsb);
+                                    sech2 = fmaf(-th, th, 1.f);
                                 } else {
                                     lg2p = fmaf(xv, kLog2e, -lsb);
                                 }
@@ -499,7 +643,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                     a.bmax[(int64_t)a.rows[i] * a.bmax_ld + vt] = tz;
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&acce[buf]);
+                if (lane == 0) tc::mbar_arrive_cluster(acce_lead + 8u * (uint32_t)buf);
                 if (++buf == 2) { buf = 0; aphase ^= 1; }
             }
             if (EPI == EPI_SOFTMAX && row_ok) {
@@ -510,12 +654,43 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
         }
     }
 
+    // Neither CTA releases its tensor memory or shared memory (which the other
+    // CTA's MMAs and arrivals use) before both are done.
     tc::tc_fence_before();
-    __syncthreads();
+    tc::cluster_sync();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem_base, kTmemCols);
+        tc::tmem_dealloc_pair(tmem_base, kTmemCols);
     }
+}
+
+// Pairs that can be resident at once for a kernel on the current device
+// (cluster scheduling can leave an SM of a GPC idle): cached per (kernel,
+// device).
+std::mutex g_pairs_mu;
+std::map<std::pair<const void*, int>, int> g_pairs;
+
+int resident_pairs(const void* fn, int threads, int smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(g_pairs_mu);
+    auto it = g_pairs.find({fn, dev});
+    if (it != g_pairs.end()) return it->second;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * 256);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    g_pairs[{fn, dev}] = n;
+    return n;
 }
 
 }  // namespace
@@ -523,24 +698,49 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
 int tc_fwd_smem_bytes(int bits) { return bits == 4 ? Layout<4>::SMEM : Layout<8>::SMEM; }
 
 template <int BITS, int EPI>
-static cudaError_t launch_t(const CUtensorMap& th, const CUtensorMap& tw, const TcFwdArgs& a,
-                            int grid, cudaStream_t st) {
-    if (cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_fwd_kernel<BITS, EPI>),
-                                          Layout<BITS>::SMEM))
-        return e;
-    tc_fwd_kernel<BITS, EPI><<<grid, Warps<BITS>::kThreads, Layout<BITS>::SMEM, st>>>(th, tw, a);
-    return cudaGetLastError();
+static cudaError_t launch_t(const CUtensorMap& th, const CUtensorMap& tw, const CUtensorMap& ts,
+                            const CUtensorMap& tb, const TcFwdArgs& a, int grid,
+                            cudaStream_t st) {
+    const void* fn = reinterpret_cast<const void*>(tc_fwd_kernel<BITS, EPI>);
+    constexpr int kSmem = Layout<BITS>::SMEM;
+    constexpr int kThreads = Warps<BITS>::kThreads;
+    if (cudaError_t e = ensure_smem_limit(fn, kSmem)) return e;
+    // One CTA per SM, as many pairs as fit (at most grid / 2).
+    int pairs = resident_pairs(fn, kThreads, kSmem);
+    if (pairs > grid / 2) pairs = grid / 2;
+    if (pairs < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_fwd_kernel<BITS, EPI>, th, tw, ts, tb, a);
 }
 
-cudaError_t launch_tc_fwd(const CUtensorMap& th, const CUtensorMap& tw, const TcFwdArgs& a,
+cudaError_t launch_tc_fwd(const CUtensorMap& th, const CUtensorMap& tw, const TcFwdArgs& in,
                           int bits, bool coeff_epilogue, int grid, cudaStream_t st) {
+    // Tensor maps of the scale and bias tables (boxes of 8 groups x the CTA's
+    // 128 vocab rows) when their rows are whole 16-byte blocks.
+    TcFwdArgs a = in;
+    CUtensorMap ts{}, tb{};
+    const uint64_t G = (uint64_t)a.H / 64;
+    a.sb_tma = G % kSbGroups == 0 &&
+               tmap_group_rows(&ts, a.scales, G, (uint64_t)a.V, kSbGroups, BNH) &&
+               tmap_group_rows(&tb, a.biases, G, (uint64_t)a.V, kSbGroups, BNH);
     if (bits == 4)
-        return !coeff_epilogue ? launch_t<4, EPI_SOFTMAX>(th, tw, a, grid, st)
-               : a.kbits != nullptr ? launch_t<4, EPI_FILTER>(th, tw, a, grid, st)
-                                    : launch_t<4, EPI_COEFF>(th, tw, a, grid, st);
-    return !coeff_epilogue ? launch_t<8, EPI_SOFTMAX>(th, tw, a, grid, st)
-           : a.kbits != nullptr ? launch_t<8, EPI_FILTER>(th, tw, a, grid, st)
-                                : launch_t<8, EPI_COEFF>(th, tw, a, grid, st);
+        return !coeff_epilogue ? launch_t<4, EPI_SOFTMAX>(th, tw, ts, tb, a, grid, st)
+               : a.kbits != nullptr ? launch_t<4, EPI_FILTER>(th, tw, ts, tb, a, grid, st)
+                                    : launch_t<4, EPI_COEFF>(th, tw, ts, tb, a, grid, st);
+    return !coeff_epilogue ? launch_t<8, EPI_SOFTMAX>(th, tw, ts, tb, a, grid, st)
+           : a.kbits != nullptr ? launch_t<8, EPI_FILTER>(th, tw, ts, tb, a, grid, st)
+                                : launch_t<8, EPI_COEFF>(th, tw, ts, tb, a, grid, st);
 }
 
 }  // namespace qh

@@ -39,6 +39,9 @@ bool tmap_group_rows(CUtensorMap* map, const void* scales, uint64_t groups, uint
 // Vocab rows per tile of the tensor-core logit kernel (its MMA N); vocab
 // ranges handed to it are counted in these tiles.
 constexpr int kTcFwdTileRows = 256;
+// Vocab rows of a tile each CTA of the logit kernel's CTA pair loads (the
+// packed head's tensor map box height; unswizzled rows of 64 codes).
+constexpr int kTcFwdBoxRows = 128;
 
 // Arguments of the tensor-core logit kernel (forward and backward phase 1).
 struct TcFwdArgs {
@@ -83,6 +86,8 @@ struct TcFwdArgs {
     uint8_t* cold_out;
     int64_t cold_out_ld;
     int64_t cold_out_rows;
+    // Set by launch_tc_fwd: the scale and bias tables are staged by TMA.
+    int sb_tma;
 };
 
 // Arguments of the tensor-core dh contraction (backward phase 2).
