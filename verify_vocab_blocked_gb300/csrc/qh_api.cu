@@ -158,12 +158,16 @@ struct BwdPlan {
 };
 
 // Vocab rows per backward chunk: the [rows x chunk] fp16 coefficient block is
-// sized to about 96 MB (mostly L2-resident between the two phases at a few
-// hundred rows), and at least 16384 rows: at thousands of rows longer chunks
-// give the coefficient pass several vocab tiles per work unit and halve the
-// launches and dh accumulation rounds (measured: 8192 -> 16384 rows took the
-// 8192-row Gemma backward from 15.8 to 14.2 ms; 32768 gained nothing more).
-constexpr int64_t kBwdCoeffBudget = (int64_t)96 << 20;
+// sized up to 4 GiB of workspace, so that the 8192-row workloads run the
+// whole vocabulary as one chunk (3 GB at 5736 active rows x 262144): the dh
+// contraction then accumulates each output tile over the entire vocabulary
+// in tensor memory and writes its K-slice partials once, instead of adding
+// them into dh after every chunk.  Measured on the masked 8192-row Gemma
+// workload: backward 11.9 ms with 96 MB chunks (16 chunks), 11.4 ms with
+// 384 MB, 10.8 ms with 1 GiB, 10.5 ms with one chunk; 7.0 vs 7.6 ms per step
+// on the 8-bit head.  Larger heads or row counts fall back to chunks of at
+// least 16384 rows.
+constexpr int64_t kBwdCoeffBudget = (int64_t)4 << 30;
 constexpr int64_t kBwdChunkMin = 16384;
 constexpr int64_t kBwdSkipChunkMin = 65536;
 
