@@ -528,15 +528,13 @@ def run_ours(args):
               + (f"{stride}th timed step" if stride > 1 else "timed step"))
     if R.bwd:
         # dominant work: the backward head phase (logits recomputed, 2*Ma*V*H,
-        # and the dh contraction, 2*Ma*V*H).  On the tensor-core path (M >= 64)
-        # it is a chain of two kernels per vocab chunk, timed as one region.
-        # With the head gradient (--with-dw) a third contraction per chunk,
-        # 2*Ma*V*H more, joins the chain (which then runs for every M).
+        # and the dh contraction, 2*Ma*V*H): a chain of two tensor-core kernels
+        # per vocab chunk, timed as one region.  With the head gradient
+        # (--with-dw) a third contraction per chunk, 2*Ma*V*H more, joins it.
         # The kernels are event-timed inside a run of well under a second, so
         # the denominator is the burst GEMM rate, not the power-capped
         # sustained one (which needs seconds of back-to-back work).
-        tc = R.M >= 64 or R.with_dw or R.blockskip is not None or R.filter_eps is not None
-        dom = ("tc_bwd_chain_dw" if R.with_dw else "tc_bwd_chain") if tc else "bwd_simt_kernel"
+        dom = "tc_bwd_chain_dw" if R.with_dw else "tc_bwd_chain"
         nmul = 6.0 if R.with_dw else 4.0
         flops = nmul * R.active * cfg["V"] * cfg["H"]
         kms = statistics.mean(bwd_ms)
@@ -550,7 +548,7 @@ def run_ours(args):
             dom = "tc_bwd_chain_filter"
         psrc = (f"{peak_src} bf16_tflops (burst; dense, the same rate as fp16): the kernels "
                 f"are event-timed inside a {el_max / 1e3:.2f} s run")
-        roof = {"kernel": (kname + " per vocab chunk" if tc else dom),
+        roof = {"kernel": kname + " per vocab chunk",
                 "bound": "tensor", "achieved": achieved, "peak": tf_burst,
                 "unit": "TFLOP/s", "frac": achieved / tf_burst, "peak_source": psrc,
                 "work_per_launch": f"{flops:.3e} flop ({int(nmul)}*Ma*V*H, Ma = active rows; "
@@ -558,7 +556,7 @@ def run_ours(args):
                 "ms_per_launch": kms, "kernel_timing": timing}
         fms = statistics.mean(fwd_ms)
         ff = 2.0 * R.active * cfg["V"] * cfg["H"]
-        roof["fwd_kernel"] = {"kernel": "tc_fwd_kernel" if tc else "stream_fwd_kernel",
+        roof["fwd_kernel"] = {"kernel": "tc_fwd_kernel" if R.M >= 17 else "stream_fwd_kernel",
                               "ms_per_launch": fms,
                               "achieved_tflops": ff / (fms / 1e3) / 1e12,
                               "frac": ff / (fms / 1e3) / 1e12 / tf_burst}

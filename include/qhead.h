@@ -305,11 +305,12 @@ int qhead_bwd_dw(const qhead_head* head, const void* h, int64_t M, const int32_t
  *     on it, the cached address is stale and this call must not be used.
  *   - M rows whose workspace (qhead_fwd_workspace) exceeds the scratch size
  *     are rejected with QHEAD_EINVAL and a message; nothing is launched.
- *     In practice the scratch holds the weight-streaming path (M < 64, a few
- *     hundred KB at H = 2560); the tensor-core path (M >= 64) needs tens of
- *     MB of per-segment partials and is rejected, and so is a bf16 or fp32
- *     head whose fp16 copies of scales and biases (4 * V * H/64 bytes) do not
- *     fit beside the rest (at V = 262144, H = 2560 they take 42 MB).
+ *     In practice the scratch holds up to about 200 rows at H = 2560,
+ *     V = 262144 (the weight-streaming path up to 16 rows needs a few hundred
+ *     KB; the tensor-core path from 17 rows 32 bytes per row and 256-row
+ *     vocab tile of partials); a bf16 or fp32 head's fp16 copies of scales
+ *     and biases (4 * V * H/64 bytes, 42 MB at that shape) do not fit, so
+ *     such heads are rejected.
  *   - Every call shares the one array.  No byte of it needs to start at zero
  *     (a call writes all scratch it reads), but calls whose kernels may
  *     overlap on the GPU (e.g. issued on different streams without ordering)
@@ -345,9 +346,8 @@ void qhead_time_next_head_kernel(void* start, void* stop);
  * entry points listed for qhead_time_next_head_kernel) launches its
  * pipelined head kernel with the TMA producer issuing no loads,
  * so the consumers' bounded waits expire and the call ends as described under
- * "Kernel time limits" (about 2 s later, without a fault).  A qhead_bwd call
- * on the SIMT path (fewer than 64 rows) has no pipelined kernel and ignores
- * the switch.  armed = 0 disarms.  Exists so that the time-limit path can be
+ * "Kernel time limits" (about 2 s later, without a fault).  armed = 0
+ * disarms.  Exists so that the time-limit path can be
  * tested.
  */
 void qhead_test_stall_next_call(int armed);

@@ -86,10 +86,12 @@ def test_edge_shapes(M, H, V, bits, cap):
     _run_all(_custom(M, H, V, bits, cap, seed=M + V), case="V=1" if V == 1 else None)
 
 
-# Shapes on the tensor-core forward (M >= 64): partial 128-row tiles, vocab
+# Shapes on the tensor-core forward (M >= 17): partial 256-row units, vocab
 # sizes that are not multiples of the 256-row tile or of the 32-column argmax
 # chunk, 4 and 8 bits, cap on and off.
 TC_SHAPES = [
+    (17, 256, 2000, 4, 30.0),   # the fewest rows that take the tensor-core forward
+    (40, 2560, 1500, 4, 0.0),
     (64, 256, 1000, 4, 30.0),
     (128, 128, 256, 4, 0.0),
     (130, 384, 4099, 8, 30.0),
@@ -99,14 +101,14 @@ TC_SHAPES = [
 ]
 
 
-# Shapes on the weight-streaming forward (M < 64) whose tiles span 5 or 20
+# Shapes on the weight-streaming forward (M <= 16) whose tiles span 5 or 20
 # stages and whose scale table has 8k groups: the variant with compile-time
 # ring slots and TMA-staged scales (4 and 8 bits, vocab sizes off the 256-row
-# tile, one to five token groups); H = 1280 (20 groups) takes the other one.
+# tile, one and two token groups); H = 1280 (20 groups) takes the other one.
 STREAM_SHAPES = [
     (5, 2560, 3001, 4, 30.0),
     (13, 2560, 2000, 8, 0.0),
-    (40, 2560, 1500, 4, 0.0),
+    (16, 2560, 1500, 4, 0.0),
     (6, 1280, 2500, 4, 30.0),
 ]
 

@@ -56,6 +56,7 @@ def _assert_poisoned_fwd(wl, logp, lse, am):
     (5, 256, 3000, 4, 30.0, False),    # weight-streaming kernel (scales by cp.async)
     (5, 2560, 1200, 4, 30.0, False),   # weight-streaming kernel, TMA-staged scales
     (200, 256, 2000, 8, 0.0, True),    # tensor-core kernel, some rows inactive
+    (300, 512, 3000, 4, 30.0, True),   # tensor-core kernel, TMA-staged scale and bias boxes
 ])
 def test_forward_wait_expires_then_recovers(M, H, V, bits, cap, masked):
     mask = synth.make_mask(M, 16, 0.3) if masked else None
@@ -70,9 +71,9 @@ def test_forward_wait_expires_then_recovers(M, H, V, bits, cap, masked):
     check_fwd(wl, np.arange(wl.M), logp, lse, am)
 
 
-def test_backward_wait_expires_then_recovers():
-    M = 160
-    mask = synth.make_mask(M, 16, 0.3)
+@pytest.mark.parametrize("M", [160, 5])  # every M runs the pipelined tensor-core backward
+def test_backward_wait_expires_then_recovers(M):
+    mask = synth.make_mask(M, 16, 0.3) if M > 16 else None
     wl = _workload(M, 256, 2500, 4, 30.0, seed=41, mask=mask)
     head, h, t, mk, g = to_dev(wl)
     logp, lse, am = gpu_fwd(head, h, t, mk)

@@ -61,9 +61,9 @@ def _compare(a, b):
 def test_noalloc_matches_workspace_forward_on_consecutive_calls(L):
     # Two different workloads back to back: the second call must not see
     # anything the first one left in the shared scratch.
-    # The last case is the shape the entry point exists for at its largest:
-    # the Gemma-class verify head (H = 2560, V = 262144, cap 30) with the most
-    # rows the scratch accepts (63: the largest split count and scratch use).
+    # The last case is the Gemma-class verify head (H = 2560, V = 262144,
+    # cap 30) with 63 rows: the tensor-core forward (from 17 rows), whose
+    # per-segment partials are the largest use of the scratch in these cases.
     for M, H, V, cap, seed, masked in [(5, 2560, 20000, 30.0, 1, False),
                                        (37, 1024, 7001, 0.0, 2, True),
                                        (5, 2560, 20000, 30.0, 1, False),

@@ -128,7 +128,14 @@ int sb_operands(const qhead_head* hd, void* ws, size_t off, cudaStream_t st, con
 
 // Rows from which the forward runs on the tensor-core kernel (below: the
 // weight-streaming kernel, whose cost is one pass over the head per 8 rows).
-constexpr int64_t kTcMinM = 64;
+// Measured on the Gemma-class head (V = 262144, H = 2560, 4-bit): the
+// streaming forward takes 0.084 ms at 1-8 rows and 0.14 ms at 16, the
+// tensor-core forward 0.27-0.28 ms from 1 to 128 rows; from 17 rows (three
+// token groups) the streaming kernel is the slower one (0.36 ms at 24, 0.47
+// at 63).  The backward always runs on the tensor cores (0.49-0.52 ms from
+// 1 to 128 rows; the CUDA-core backward it replaced took 7.7 ms at 1-8 rows
+// and 56 ms at 63).
+constexpr int64_t kTcMinFwdM = 17;
 
 struct FwdPlan {
     int64_t M = 0, Mpad = 0;
@@ -142,9 +149,8 @@ struct FwdPlan {
 
 struct BwdPlan {
     int64_t M = 0, Mpad = 0;
-    bool tc = false;
     int grid = 0;
-    int S = 1;               // vocab splits of the CUDA-core path
+    int S = 1;               // K slices of the dh contraction
     int64_t chunk = 0;       // vocab rows per coefficient block (tensor-core path)
     bool dw = false;         // head gradient requested: the regions below are planned
     bool skip = false;       // blockMax early exit: the skip map is planned
@@ -195,13 +201,20 @@ int plan_fwd(const qhead_head* hd, int64_t M, FwdPlan* p, bool force_tc = false)
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    p->tc = M >= kTcMinM || force_tc;
+    p->tc = M >= kTcMinFwdM || force_tc;
     if (p->tc) {
         // One persistent CTA per SM; the kernel picks the number of vocab
         // segments S from the active-row count so that n_tiles * S is about
         // 32 * grid, hence at most 128 * (32 * grid + n_tiles) records.
+        // Partial records: the kernel writes record i * S + s for compact
+        // rows i < the active count and vocab segments s < S, where S is at
+        // most the number of 256-row vocab tiles and S * (256-row units) is
+        // about 32 per CTA pair; either bound caps the records.
         p->grid = di.sms;
-        p->records = (size_t)128 * (32 * (size_t)p->grid + (size_t)(p->Mpad / 128));
+        const size_t n_vt = (size_t)((hd->V + 255) / 256);
+        const size_t by_rows = (size_t)p->Mpad * n_vt;
+        const size_t by_units = (size_t)128 * (32 * (size_t)p->grid + (size_t)(p->Mpad / 128));
+        p->records = by_rows < by_units ? by_rows : by_units;
     } else {
         const int64_t groups = (M + qh::kTokGroup - 1) / qh::kTokGroup;
         // One full wave: every SM holds as many CTAs as fit; each split keeps at
@@ -238,7 +251,6 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false,
     if (rc) return rc;
     p->M = M;
     p->Mpad = (M + qh::kRowPad - 1) / qh::kRowPad * qh::kRowPad;
-    p->tc = M >= kTcMinM || with_dw || with_skip || with_filter;
     p->dw = with_dw;
     p->skip = with_skip;
     p->filter = with_filter;
@@ -248,55 +260,43 @@ int plan_bwd(const qhead_head* hd, int64_t M, BwdPlan* p, bool with_dw = false,
     p->off_rows = off;  off = align_up(off + 4 * (size_t)p->Mpad, 256);
     p->off_pos = off;   off = align_up(off + 4 * (size_t)M, 1024);
     // (dh_slices is declared above plan_fwd)
-    if (p->tc) {
-        p->grid = di.sms;
-        p->S = 1;
-        // Vocab rows rounded to the logit kernel's tiles; the slice count S is
-        // kept within the K steps of the shortest (last) chunk, so every chunk
-        // writes or adds every slice.
-        const int64_t tr = qh::kTcFwdTileRows;
-        const int64_t vr = (hd->V + tr - 1) / tr * tr;
-        int64_t chunk = kBwdCoeffBudget / (2 * p->Mpad) / 256 * 256;
-        if (chunk < kBwdChunkMin) chunk = kBwdChunkMin;
-        // With the blockMax early exit most tiles are skipped: fewer, longer
-        // chunks (fewer launches of mostly empty kernels) pay more than L2
-        // residency (measured 4.69 -> 3.28 ms per call at 8192 peaked rows).
-        if (with_skip && chunk < kBwdSkipChunkMin) chunk = kBwdSkipChunkMin;
-        if (chunk > vr) chunk = vr;
-        p->chunk = chunk;
-        const int64_t last = vr - (vr - 1) / chunk * chunk;  // rows of the last chunk
-        p->S = dh_slices(p->Mpad, hd->H, p->grid, (last < chunk ? last : chunk) / 64);
-        p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
-        p->off_coeff = off; off = align_up(off + 2 * (size_t)p->Mpad * p->chunk, 1024);
-        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 1024);
-        if (with_dw) {
-            p->off_hp = off;     off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
-            p->off_g = off;      off = align_up(off + 4 * (size_t)p->Mpad, 256);
-            p->off_dmax = off;   off = align_up(off + 16, 256);
-            p->off_cnt = off;    off = align_up(off + 4 * (size_t)hd->V, 256);
-            p->off_offs = off;   off = align_up(off + 4 * ((size_t)hd->V + 1), 256);
-            p->off_cursor = off; off = align_up(off + 4 * (size_t)hd->V, 256);
-            p->off_idx = off;    off = align_up(off + 4 * (size_t)p->Mpad, 256);
-        }
-        if (with_skip) {
-            p->off_skip = off;   off = align_up(off + (size_t)(p->Mpad / 128) * p->n_vt, 256);
-        }
-        if (with_filter) {
-            // one bit per (256-row dh unit, 64-row vocab step of the head)
-            p->kbits_ld = (p->n_vt * 4 + 63) / 64;
-            p->off_kbits = off;
-            off = align_up(off + 8 * (size_t)((p->Mpad + 255) / 256) * p->kbits_ld, 256);
-        }
-    } else {
-        const int tb = qh::bwd_simt_tokens(hd->H);
-        const int64_t groups = (M + tb - 1) / tb;
-        const int64_t want = (int64_t)di.sms * 4;
-        int64_t S = (want + groups - 1) / groups;
-        const int64_t max_s = (hd->V + 255) / 256;
-        if (S > max_s) S = max_s;
-        if (S < 1) S = 1;
-        p->S = (int)S;
-        p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 256);
+    p->grid = di.sms;
+    p->S = 1;
+    // Vocab rows rounded to the logit kernel's tiles; the slice count S is
+    // kept within the K steps of the shortest (last) chunk, so every chunk
+    // writes or adds every slice.
+    const int64_t tr = qh::kTcFwdTileRows;
+    const int64_t vr = (hd->V + tr - 1) / tr * tr;
+    int64_t chunk = kBwdCoeffBudget / (2 * p->Mpad) / 256 * 256;
+    if (chunk < kBwdChunkMin) chunk = kBwdChunkMin;
+    // With the blockMax early exit most tiles are skipped: fewer, longer
+    // chunks (fewer launches of mostly empty kernels) pay more than L2
+    // residency (measured 4.69 -> 3.28 ms per call at 8192 peaked rows).
+    if (with_skip && chunk < kBwdSkipChunkMin) chunk = kBwdSkipChunkMin;
+    if (chunk > vr) chunk = vr;
+    p->chunk = chunk;
+    const int64_t last = vr - (vr - 1) / chunk * chunk;  // rows of the last chunk
+    p->S = dh_slices(p->Mpad, hd->H, p->grid, (last < chunk ? last : chunk) / 64);
+    p->off_h16 = off;   off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
+    p->off_coeff = off; off = align_up(off + 2 * (size_t)p->Mpad * p->chunk, 1024);
+    p->off_dhp = off;   off = align_up(off + 4 * (size_t)p->S * p->Mpad * hd->H, 1024);
+    if (with_dw) {
+        p->off_hp = off;     off = align_up(off + 2 * (size_t)p->Mpad * hd->H, 1024);
+        p->off_g = off;      off = align_up(off + 4 * (size_t)p->Mpad, 256);
+        p->off_dmax = off;   off = align_up(off + 16, 256);
+        p->off_cnt = off;    off = align_up(off + 4 * (size_t)hd->V, 256);
+        p->off_offs = off;   off = align_up(off + 4 * ((size_t)hd->V + 1), 256);
+        p->off_cursor = off; off = align_up(off + 4 * (size_t)hd->V, 256);
+        p->off_idx = off;    off = align_up(off + 4 * (size_t)p->Mpad, 256);
+    }
+    if (with_skip) {
+        p->off_skip = off;   off = align_up(off + (size_t)(p->Mpad / 128) * p->n_vt, 256);
+    }
+    if (with_filter) {
+        // one bit per (256-row dh unit, 64-row vocab step of the head)
+        p->kbits_ld = (p->n_vt * 4 + 63) / 64;
+        p->off_kbits = off;
+        off = align_up(off + 8 * (size_t)((p->Mpad + 255) / 256) * p->kbits_ld, 256);
     }
     off = align_up(off, 256);
     p->off_sb = off;    off += sb_copy_bytes(hd);
@@ -504,118 +504,108 @@ static int bwd_impl(const qhead_head* head, const void* h, int64_t M, const int3
     float* dhp = at<float>(workspace, p.off_dhp);
 
     cudaError_t e;
-    if (p.tc) {
-        __half* h16 = at<__half>(workspace, p.off_h16);
-        __half* coeff = at<__half>(workspace, p.off_coeff);
-        if (M <= qh::kFusedPrologueMaxM) {
-            if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
-                                               count, h16, p.Mpad, err, st)))
-                return cuda_fail(e, "prologue");
-        } else {
-            if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
-                return cuda_fail(e, "compact");
-            if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
-                return cuda_fail(e, "convert_h");
-        }
-        // blockMax early exit: the (row tile, vocab tile) pairs both phases skip.
-        uint8_t* skip = p.skip ? at<uint8_t>(workspace, p.off_skip) : nullptr;
-        if (skip && (e = qh::launch_skip_map(bmax, p.n_vt, lse, targets, rows, count, p.Mpad / 128,
-                                             p.n_vt, eps, skip, st)))
-            return cuda_fail(e, "skip_map");
-        // Coefficient filter: every dh step starts skipped and every block cold
-        // (rows past the active ones stay so); the coefficient pass clears the
-        // bits of the steps that hold a warm block.
-        auto* kbits = p.filter ? at<unsigned long long>(workspace, p.off_kbits) : nullptr;
-        const int64_t n_vb = (head->V + 31) / 32, n_rb = (M + 31) / 32;
-        if (kbits && (e = cudaMemsetAsync(kbits, 0xff,
-                                          8 * (size_t)((p.Mpad + 255) / 256) * p.kbits_ld, st)))
-            return cuda_fail(e, "filter bits");
-        if (kbits && cold_out && (e = cudaMemsetAsync(cold_out, 1, (size_t)(n_rb * n_vb), st)))
-            return cuda_fail(e, "cold output");
-        // Head gradient: max |dlogp|, the scaled fp16 h', the one-hot terms and
-        // the per-target row lists, once per call.
-        __half* hp = p.dw ? at<__half>(workspace, p.off_hp) : nullptr;
-        float* g = p.dw ? at<float>(workspace, p.off_g) : nullptr;
-        float* dmax = p.dw ? at<float>(workspace, p.off_dmax) : nullptr;
-        int* offs = p.dw ? at<int>(workspace, p.off_offs) : nullptr;
-        int* idx = p.dw ? at<int>(workspace, p.off_idx) : nullptr;
-        if (p.dw &&
-            (e = qh::launch_dw_prep(wq, sbx, head->V, head->H, head->bits, head->softcap, hb,
-                                    rows, count, targets, dlogp, p.Mpad, dmax, hp, g,
-                                    at<int>(workspace, p.off_cnt), offs,
-                                    at<int>(workspace, p.off_cursor), idx, st)))
-            return cuda_fail(e, "dw_prep");
-        CUtensorMap th, tw_logit, tcoef, tw_dh, tcoef_t{}, thp{};
-        if (p.dw && (!qh::tmap_rows_f16_sw128(&tcoef_t, at<__half>(workspace, p.off_coeff),
-                                               p.chunk, p.Mpad, 64) ||
-                     !qh::tmap_rows_f16_sw128(&thp, hp, head->H, p.Mpad, 64)))
-            return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
-        const int wpr = head->H * head->bits / 32;
-        if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
-            !qh::tmap_packed_rows(&tw_logit, wq, wpr, head->V, 64 * head->bits / 32,
-                                  qh::kTcFwdBoxRows) ||
-            !qh::tmap_rows_f16_sw128(&tcoef, coeff, p.chunk, p.Mpad, 128) ||
-            !(qh::tc_dh_swizzled(head->H, head->bits)
-                  ? qh::tmap_packed_rows_sw128(&tw_dh, wq, wpr, head->V, 64)
-                  : qh::tmap_packed_rows(&tw_dh, wq, wpr, head->V,
-                                         qh::tc_dh_words(head->H, head->bits), 64)))
-            return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
-        const int tr = qh::kTcFwdTileRows;
-        const int n_vt = (int)((head->V + tr - 1) / tr);
-        const int vt_chunk = (int)(p.chunk / tr);
-        hook_before(st);
-        for (int vt0 = 0, c = 0; vt0 < n_vt; vt0 += vt_chunk, ++c) {
-            const int vt1 = vt0 + vt_chunk < n_vt ? vt0 + vt_chunk : n_vt;
-            qh::TcFwdArgs ta{};
-            ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H;
-            ta.cap = head->softcap; ta.count = count; ta.err = err;
-            ta.stall = vt0 == 0 ? stall : 0;
-            ta.vt_begin = vt0; ta.vt_end = vt1;
-            ta.lse = lse; ta.rows = rows; ta.coeff = coeff; ta.coeff_ld = p.chunk;
-            ta.coeff_rows = (int)p.Mpad;
-            ta.skip = skip; ta.skip_ld = p.n_vt; ta.skip_rows = (int)(p.Mpad / 128);
-            ta.dlogp = dlogp; ta.targets = targets; ta.filter_eps = eps;
-            ta.kbits = kbits; ta.kbits_ld = p.kbits_ld;
-            ta.cold_out = cold_out; ta.cold_out_ld = n_vb; ta.cold_out_rows = n_rb;
-            if ((e = qh::launch_tc_fwd(th, tw_logit, ta, head->bits, true, p.grid, st)))
-                return cuda_fail(e, "tc_coeff");
-            if (dh) {
-                qh::TcDhArgs da{};
-                da.scales = sc; da.biases = bi; da.V = head->V; da.H = head->H;
-                da.count = count; da.err = err; da.rows = rows; da.dlogp = dlogp; da.dh_acc = dhp;
-                da.slice_stride = p.Mpad * head->H;
-                da.v_begin = (int64_t)vt0 * tr;
-                da.n_k = (vt1 - vt0) * tr / 64;
-                da.ks = p.S;  // <= the K steps of every chunk (plan_bwd)
-                da.accumulate = c > 0;
-                da.skip = skip; da.skip_ld = p.n_vt; da.skip_rows = (int)(p.Mpad / 128);
-                da.kbits = kbits; da.kbits_ld = p.kbits_ld;
-                if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
-                    return cuda_fail(e, "tc_dh");
-            }
-            if (dw) {
-                qh::TcDwArgs wa{};
-                wa.V = head->V; wa.H = head->H; wa.count = count; wa.err = err;
-                wa.v_begin = (int64_t)vt0 * tr;
-                wa.chunk_rows = (vt1 - vt0) * tr;
-                wa.dmax = dmax; wa.offs = offs; wa.idx = idx; wa.g = g; wa.rows = rows;
-                wa.h = hb; wa.dw = dw;
-                if ((e = qh::launch_tc_dw(tcoef_t, thp, wa, p.grid, st)))
-                    return cuda_fail(e, "tc_dw");
-            }
-        }
-        hook_after(st);
-        if (dw && (e = qh::launch_dw_poison(err, dw, head->V * (int64_t)head->H, st)))
-            return cuda_fail(e, "dw_poison");
+    __half* h16 = at<__half>(workspace, p.off_h16);
+    __half* coeff = at<__half>(workspace, p.off_coeff);
+    if (M <= qh::kFusedPrologueMaxM) {
+        if ((e = qh::launch_prologue_fused(mask, hb, M, p.Mpad, head->H, head->bits, rows, pos,
+                                           count, h16, p.Mpad, err, st)))
+            return cuda_fail(e, "prologue");
     } else {
         if ((e = qh::launch_compact(mask, M, p.Mpad, rows, pos, count, err, st)))
             return cuda_fail(e, "compact");
-        hook_before(st);
-        e = qh::launch_bwd_simt(wq, sc, bi, head->V, head->H, head->bits, head->softcap, hb, rows,
-                                count, lse, dlogp, dhp, p.S, M, p.Mpad, st);
-        hook_after(st);
-        if (e) return cuda_fail(e, "bwd_simt");
+        if ((e = qh::launch_convert_h(hb, p.Mpad, head->H, head->bits, rows, count, h16, st)))
+            return cuda_fail(e, "convert_h");
     }
+    // blockMax early exit: the (row tile, vocab tile) pairs both phases skip.
+    uint8_t* skip = p.skip ? at<uint8_t>(workspace, p.off_skip) : nullptr;
+    if (skip && (e = qh::launch_skip_map(bmax, p.n_vt, lse, targets, rows, count, p.Mpad / 128,
+                                         p.n_vt, eps, skip, st)))
+        return cuda_fail(e, "skip_map");
+    // Coefficient filter: every dh step starts skipped and every block cold
+    // (rows past the active ones stay so); the coefficient pass clears the
+    // bits of the steps that hold a warm block.
+    auto* kbits = p.filter ? at<unsigned long long>(workspace, p.off_kbits) : nullptr;
+    const int64_t n_vb = (head->V + 31) / 32, n_rb = (M + 31) / 32;
+    if (kbits && (e = cudaMemsetAsync(kbits, 0xff,
+                                      8 * (size_t)((p.Mpad + 255) / 256) * p.kbits_ld, st)))
+        return cuda_fail(e, "filter bits");
+    if (kbits && cold_out && (e = cudaMemsetAsync(cold_out, 1, (size_t)(n_rb * n_vb), st)))
+        return cuda_fail(e, "cold output");
+    // Head gradient: max |dlogp|, the scaled fp16 h', the one-hot terms and
+    // the per-target row lists, once per call.
+    __half* hp = p.dw ? at<__half>(workspace, p.off_hp) : nullptr;
+    float* g = p.dw ? at<float>(workspace, p.off_g) : nullptr;
+    float* dmax = p.dw ? at<float>(workspace, p.off_dmax) : nullptr;
+    int* offs = p.dw ? at<int>(workspace, p.off_offs) : nullptr;
+    int* idx = p.dw ? at<int>(workspace, p.off_idx) : nullptr;
+    if (p.dw &&
+        (e = qh::launch_dw_prep(wq, sbx, head->V, head->H, head->bits, head->softcap, hb,
+                                rows, count, targets, dlogp, p.Mpad, dmax, hp, g,
+                                at<int>(workspace, p.off_cnt), offs,
+                                at<int>(workspace, p.off_cursor), idx, st)))
+        return cuda_fail(e, "dw_prep");
+    CUtensorMap th, tw_logit, tcoef, tw_dh, tcoef_t{}, thp{};
+    if (p.dw && (!qh::tmap_rows_f16_sw128(&tcoef_t, at<__half>(workspace, p.off_coeff),
+                                           p.chunk, p.Mpad, 64) ||
+                 !qh::tmap_rows_f16_sw128(&thp, hp, head->H, p.Mpad, 64)))
+        return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
+    const int wpr = head->H * head->bits / 32;
+    if (!qh::tmap_rows_f16_sw128(&th, h16, head->H, p.Mpad, 128) ||
+        !qh::tmap_packed_rows(&tw_logit, wq, wpr, head->V, 64 * head->bits / 32,
+                              qh::kTcFwdBoxRows) ||
+        !qh::tmap_rows_f16_sw128(&tcoef, coeff, p.chunk, p.Mpad, 128) ||
+        !(qh::tc_dh_swizzled(head->H, head->bits)
+              ? qh::tmap_packed_rows_sw128(&tw_dh, wq, wpr, head->V, 64)
+              : qh::tmap_packed_rows(&tw_dh, wq, wpr, head->V,
+                                     qh::tc_dh_words(head->H, head->bits), 64)))
+        return fail(QHEAD_ECUDA, "TMA tensor map encoding failed");
+    const int tr = qh::kTcFwdTileRows;
+    const int n_vt = (int)((head->V + tr - 1) / tr);
+    const int vt_chunk = (int)(p.chunk / tr);
+    hook_before(st);
+    for (int vt0 = 0, c = 0; vt0 < n_vt; vt0 += vt_chunk, ++c) {
+        const int vt1 = vt0 + vt_chunk < n_vt ? vt0 + vt_chunk : n_vt;
+        qh::TcFwdArgs ta{};
+        ta.scales = sc; ta.biases = bi; ta.V = head->V; ta.H = head->H;
+        ta.cap = head->softcap; ta.count = count; ta.err = err;
+        ta.stall = vt0 == 0 ? stall : 0;
+        ta.vt_begin = vt0; ta.vt_end = vt1;
+        ta.lse = lse; ta.rows = rows; ta.coeff = coeff; ta.coeff_ld = p.chunk;
+        ta.coeff_rows = (int)p.Mpad;
+        ta.skip = skip; ta.skip_ld = p.n_vt; ta.skip_rows = (int)(p.Mpad / 128);
+        ta.dlogp = dlogp; ta.targets = targets; ta.filter_eps = eps;
+        ta.kbits = kbits; ta.kbits_ld = p.kbits_ld;
+        ta.cold_out = cold_out; ta.cold_out_ld = n_vb; ta.cold_out_rows = n_rb;
+        if ((e = qh::launch_tc_fwd(th, tw_logit, ta, head->bits, true, p.grid, st)))
+            return cuda_fail(e, "tc_coeff");
+        if (dh) {
+            qh::TcDhArgs da{};
+            da.scales = sc; da.biases = bi; da.V = head->V; da.H = head->H;
+            da.count = count; da.err = err; da.rows = rows; da.dlogp = dlogp; da.dh_acc = dhp;
+            da.slice_stride = p.Mpad * head->H;
+            da.v_begin = (int64_t)vt0 * tr;
+            da.n_k = (vt1 - vt0) * tr / 64;
+            da.ks = p.S;  // <= the K steps of every chunk (plan_bwd)
+            da.accumulate = c > 0;
+            da.skip = skip; da.skip_ld = p.n_vt; da.skip_rows = (int)(p.Mpad / 128);
+            da.kbits = kbits; da.kbits_ld = p.kbits_ld;
+            if ((e = qh::launch_tc_dh(tcoef, tw_dh, da, head->bits, p.grid, st)))
+                return cuda_fail(e, "tc_dh");
+        }
+        if (dw) {
+            qh::TcDwArgs wa{};
+            wa.V = head->V; wa.H = head->H; wa.count = count; wa.err = err;
+            wa.v_begin = (int64_t)vt0 * tr;
+            wa.chunk_rows = (vt1 - vt0) * tr;
+            wa.dmax = dmax; wa.offs = offs; wa.idx = idx; wa.g = g; wa.rows = rows;
+            wa.h = hb; wa.dw = dw;
+            if ((e = qh::launch_tc_dw(tcoef_t, thp, wa, p.grid, st)))
+                return cuda_fail(e, "tc_dw");
+        }
+    }
+    hook_after(st);
+    if (dw && (e = qh::launch_dw_poison(err, dw, head->V * (int64_t)head->H, st)))
+        return cuda_fail(e, "dw_poison");
     if (dh &&
         (e = qh::launch_bwd_finalize(wq, sbx, head->V, head->H, head->bits, head->softcap, hb,
                                      pos, targets, dlogp, dhp, p.S, p.Mpad, err, dh, M, st)))

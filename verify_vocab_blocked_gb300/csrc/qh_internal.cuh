@@ -203,11 +203,6 @@ cudaError_t launch_fwd_finalize(const uint32_t* wq, SbView sb,
                                 const int* pos, const int32_t* targets, const Partial* part, int S,
                                 const int* S_dev, const int* err, float* logp,
                                 float* lse, int32_t* argmax, int64_t M, cudaStream_t st);
-cudaError_t launch_bwd_simt(const uint32_t* wq, const __half* scales, const __half* biases,
-                            int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
-                            const int* rows, const int* count, const float* lse,
-                            const float* dlogp, float* dhp, int S, int64_t M, int64_t Mpad,
-                            cudaStream_t st);
 cudaError_t launch_bwd_finalize(const uint32_t* wq, SbView sb,
                                 int64_t V, int H, int bits, float cap, const __nv_bfloat16* h,
                                 const int* pos, const int32_t* targets, const float* dlogp,
@@ -224,7 +219,6 @@ int device_sms();
 cudaError_t launch_accept_prefix(const int32_t* argmax, const int32_t* draft, int64_t B, int W,
                                  int32_t* n_accept, int32_t* next_token, cudaStream_t st);
 
-int bwd_simt_tokens(int H);                   // tokens per CTA of the SIMT backward
 int stream_fwd_ctas_per_sm(int bits, int H);  // occupancy of the weight-streaming kernel
 
 }  // namespace qh
