@@ -83,7 +83,7 @@ def test_backward_wait_expires_then_recovers(M):
     dh = qhead.bwd(head, h, t, lse_d, g, mk)
     torch.cuda.synchronize()
     dh = dh.cpu().numpy()
-    act = mask.astype(bool)
+    act = mask.astype(bool) if mask is not None else np.ones(M, bool)
     assert np.all(np.isnan(dh[act]))
     assert np.all(dh[~act] == 0.0)
     dh = qhead.bwd(head, h, t, lse_d, g, mk)
