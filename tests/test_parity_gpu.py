@@ -1,11 +1,10 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
 Small cases are compared on every row.  The full-size workloads run whole on
-the GPU and are compared on every forward row of the 512-row Gemma workload
-and of the verify window, and on 256 seeded rows plus every row next to a
-mask boundary (forward and dh) of the 8192-row workloads: rows are
-independent, so a compared row is an exact check of that row.  Properties
-that hold at any size are checked on every row besides.
+the GPU and are compared on every forward row (all five workloads), and dh
+on 256 seeded rows plus rows 0 and M - 1 and every row next to a mask
+boundary: rows are independent, so a compared row is an exact check of that
+row.  Properties that hold at any size are checked on every row besides.
 """
 import ctypes
 
@@ -279,6 +278,23 @@ def test_full_verify_window():
     assert check_fwd(wl, np.arange(wl.M), None, lse.cpu().numpy(), am.cpu().numpy()) == wl.M
 
 
+@pytest.mark.parametrize("sbt", ["bf16", "f32"])
+def test_full_verify_window_bf16_and_f32_scales(sbt):
+    # The verify head with its scales and biases in bf16 or fp32 (the
+    # streaming kernel reads their per-call fp16 copy, the finalize the
+    # caller's values): every position against the oracle.
+    cfg = synth.CONFIGS["verify"]
+    head = synth.make_head(cfg["V"], cfg["H"], cfg["bits"], softcap=cfg["softcap"], seed=0,
+                           sb_dtype=sbt)
+    wl = synth.Workload(
+        "verify", head, synth.make_hidden(cfg["M"], cfg["H"], seed=0), None, None,
+        np.ones(cfg["M"], np.float32), cfg)
+    dhead, h, t, mk, g = to_dev(wl)
+    logp, lse, am = qhead.fwd(dhead, h, None, None)
+    torch.cuda.synchronize()
+    assert check_fwd(wl, np.arange(wl.M), None, lse.cpu().numpy(), am.cpu().numpy()) == wl.M
+
+
 def _full_step(name):
     """The workload's forward and backward on the GPU, exactly as the bench
     runs them, with the every-row properties checked."""
@@ -305,16 +321,18 @@ def test_full_gemma512_every_forward_row():
     check_dh(wl, rows, dh, label="gemma512")
 
 
-def test_full_mid8_sampled_rows():
+def test_full_mid8_every_forward_row():
     wl, logp, lse, am, dh = _full_step("mid8")
+    assert check_fwd(wl, np.arange(wl.M), logp, lse, am) == 8192
     rows, _ = _sample_rows(wl, 256, seed=2)
-    assert check_fwd(wl, rows, logp, lse, am) >= 256
     check_dh(wl, rows, dh, label="mid8")
 
 
-def test_full_gemma8k_masked_sampled_rows():
+def test_full_gemma8k_masked_every_forward_row():
     wl, logp, lse, am, dh = _full_step("gemma8k_masked")
+    # every row: the 5736 active ones against the oracle, the masked ones
+    # against their sentinels
+    assert check_fwd(wl, np.arange(wl.M), logp, lse, am) == 5736
     rows, n_boundary = _sample_rows(wl, 256, seed=3)
     assert n_boundary == 2 * 8 - 1  # prompt/response and response/next-prompt edges
-    assert check_fwd(wl, rows, logp, lse, am) >= 256
     check_dh(wl, rows, dh, label="gemma8k_masked")
