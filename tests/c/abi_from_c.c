@@ -52,6 +52,18 @@ int main(void) {
     CHECK(qhead_fwd(NULL, h, 4, NULL, NULL, NULL, f, NULL, ws, 1 << 20, NULL) == QHEAD_EINVAL);
     CHECK(qhead_fwd_workspace(&bad, 4) == (size_t)-1);
 
+    /* the element types of scales and biases: fp16, bf16 and fp32 pass the
+       head checks (the call then stops at the missing workspace); others are
+       unsupported */
+    bad = hd;
+    bad.sb_dtype = QHEAD_SB_BF16;
+    CHECK(qhead_fwd(&bad, h, 4, NULL, NULL, NULL, f, NULL, NULL, 0, NULL) == QHEAD_EINVAL);
+    bad.sb_dtype = QHEAD_SB_F32;
+    CHECK(qhead_fwd(&bad, h, 4, NULL, NULL, NULL, f, NULL, NULL, 0, NULL) == QHEAD_EINVAL);
+    CHECK(strstr(qhead_last_error(), "workspace") != NULL);
+    bad.sb_dtype = 3;
+    CHECK(qhead_fwd(&bad, h, 4, NULL, NULL, NULL, f, NULL, NULL, 0, NULL) == QHEAD_EUNSUPPORTED);
+
     /* M == 0 is a no-op everywhere */
     CHECK(qhead_fwd(&hd, NULL, 0, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL) == QHEAD_OK);
     CHECK(qhead_bwd(&hd, NULL, 0, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL) == QHEAD_OK);
