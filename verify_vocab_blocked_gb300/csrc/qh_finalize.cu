@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
         return;
     }
     __shared__ Partial red[kFinThreads / 32];
-    __shared__ float exact[2 * 32 + 1];
+    __shared__ float exact[3 * (kFinThreads / 32)];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     RowState st;
@@ -94,36 +94,73 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
     const __nv_bfloat16* hrow = h + r * (int64_t)H;
     const int32_t t = targets ? targets[r] : -1;
     const bool t_ok = t >= 0 && (int64_t)t < V;
-    // Work items: candidate 1, candidate 2 (if any), then the target.
+    // The exact logits of candidate 1, candidate 2 (if any) and the target,
+    // shared by the whole block: each thread takes the 8-element units
+    // u = threadIdx.x, + 128, ... of all three rows (one load of h per unit),
+    // then the block sums them in a fixed order.
     const int n1 = fin.i1 < V ? 1 : 0;  // (an empty slot holds INT32_MAX)
     const int n2 = fin.i2 < V ? 1 : 0;
-    const int nitems = n1 + n2 + 1;
-    for (int it = warp; it < nitems; it += kFinThreads / 32) {
-        int64_t v;
-        if (it < n1) v = fin.i1;
-        else if (it < n1 + n2) v = fin.i2;
-        else v = t_ok ? t : -1;
-        float x = 0.f;
-        if (v >= 0) x = warp_exact_logit<10>(hrow, wq, sb, v, H, bits);
-        if (lane == 0) exact[it] = x;
+    const int64_t vr[3] = {n1 ? (int64_t)fin.i1 : -1, n2 ? (int64_t)fin.i2 : -1,
+                           t_ok ? (int64_t)t : -1};
+    const int units = H / 8, G = H / 64, wpr = H * bits / 32;
+    float dot[3] = {0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int u = threadIdx.x; u < units; u += kFinThreads) {
+        const uint4 hv = *reinterpret_cast<const uint4*>(hrow + 8 * u);
+        const __nv_bfloat16* hp = reinterpret_cast<const __nv_bfloat16*>(&hv);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+            if (vr[c] < 0) continue;
+            const uint32_t* wrow = wq + vr[c] * wpr;
+            const int64_t gi = vr[c] * G + u / 8;
+            const float sc = sb_elem(sb.s, gi, sb.type), bi = sb_elem(sb.b, gi, sb.type);
+            const uint32_t w0 = bits == 4 ? wrow[u] : wrow[2 * u];
+            const uint32_t w1 = bits == 4 ? 0u : wrow[2 * u + 1];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t q = bits == 4 ? (w0 >> (4 * e)) & 15u
+                                             : ((e < 4 ? w0 : w1) >> (8 * (e & 3))) & 255u;
+                dot[c] = fmaf(__bfloat162float(hp[e]), fmaf(sc, (float)q, bi), dot[c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) dot[c] += __shfl_xor_sync(0xffffffffu, dot[c], o);
+        if (lane == 0) exact[warp * 3 + c] = dot[c];
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        float x[3];
+        for (int c = 0; c < 3; ++c) {
+            x[c] = 0.f;
+            for (int w = 0; w < kFinThreads / 32; ++w) x[c] += exact[w * 3 + c];
+        }
         const float l = fin.m + logf(fin.s);
         float best = -INFINITY;
         int bi = INT32_MAX;
-        for (int it = 0; it < n1 + n2; ++it) {
-            const int v = it < n1 ? fin.i1 : fin.i2;
-            if (better(exact[it], v, best, bi)) { best = exact[it]; bi = v; }
+        for (int c = 0; c < 2; ++c) {
+            const int v = c == 0 ? fin.i1 : fin.i2;
+            if (vr[c] >= 0 && better(x[c], v, best, bi)) { best = x[c]; bi = v; }
         }
         if (lse) lse[r] = l;
         if (argmax) argmax[r] = bi == INT32_MAX ? -1 : bi;
-        if (logp) logp[r] = t_ok ? softcap_exact(exact[n1 + n2], cap) - l : __int_as_float(0x7fc00000);
+        if (logp) logp[r] = t_ok ? softcap_exact(x[2], cap) - l : __int_as_float(0x7fc00000);
     }
 }
 
-constexpr int kBwdFinThreads = 256;
+constexpr int kBwdFinThreads = 512;
+// 8-element units of a row per thread: H <= kMaxH = 8192 is at most 1024 units.
+constexpr int kBwdFinUnits = kMaxH / 8 / kBwdFinThreads;
 
+// One row per block.  Every thread takes the row's 8-element units u = t,
+// t + 512, ...: in one round of loads it reads, per unit, the S partial-dh
+// slices (the sums it will write) and the target's weights and the hidden
+// states (its part of the exact target logit), so the row costs one global
+// latency, not a dot product by one warp followed by the sums.  The target
+// logit is reduced over the block in a fixed order (deterministic), then
+// dh = sum of slices + dlogp * sech2(target logit) * w_target, exactly in fp32.
 __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
     const uint32_t* __restrict__ wq, SbView sb, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
@@ -142,28 +179,71 @@ __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
         for (int d = threadIdx.x; d < H; d += kBwdFinThreads) out[d] = __int_as_float(0x7fc00000);
         return;
     }
+    __shared__ float part_sh[kBwdFinThreads / 32];
     __shared__ float coef_sh;
     const int32_t t = targets[r];
     const bool t_ok = t >= 0 && (int64_t)t < V;
-    if (threadIdx.x < 32) {
-        float raw = 0.f;
-        if (t_ok) raw = warp_exact_logit(h + r * (int64_t)H, wq, sb, t, H, bits);
-        if (threadIdx.x == 0) {
-            float sech2 = 1.f;
-            if (cap > 0.f) {
-                const float th = tanhf(raw / cap);
-                sech2 = 1.f - th * th;
-            }
-            coef_sh = t_ok ? dlogp[r] * sech2 : __int_as_float(0x7fc00000);
+    const int units = H / 8, G = H / 64, wpr = H * bits / 32;
+    const uint32_t* wrow = wq + (t_ok ? (int64_t)t : 0) * wpr;
+    const __nv_bfloat16* hrow = h + r * (int64_t)H;
+    float acc[kBwdFinUnits][8];  // the slice sums of this thread's units
+    float wt[kBwdFinUnits][8];   // the target's weights of those units
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < kBwdFinUnits; ++k) {
+        const int u = threadIdx.x + k * kBwdFinThreads;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[k][e] = wt[k][e] = 0.f;
+        if (u >= units) continue;
+        for (int sl = 0; sl < S; ++sl) {
+            const float4* src = reinterpret_cast<const float4*>(dhp + ((int64_t)sl * Mpad + i) * H + 8 * u);
+            const float4 a0 = src[0], a1 = src[1];
+            acc[k][0] += a0.x; acc[k][1] += a0.y; acc[k][2] += a0.z; acc[k][3] += a0.w;
+            acc[k][4] += a1.x; acc[k][5] += a1.y; acc[k][6] += a1.z; acc[k][7] += a1.w;
         }
+        if (t_ok) {
+            const int64_t gi = (int64_t)t * G + u / 8;
+            const float sc = sb_elem(sb.s, gi, sb.type), bi = sb_elem(sb.b, gi, sb.type);
+            const uint4 hv = *reinterpret_cast<const uint4*>(hrow + 8 * u);
+            const __nv_bfloat16* hp = reinterpret_cast<const __nv_bfloat16*>(&hv);
+            const uint32_t w0 = bits == 4 ? wrow[u] : wrow[2 * u];
+            const uint32_t w1 = bits == 4 ? 0u : wrow[2 * u + 1];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t q = bits == 4 ? (w0 >> (4 * e)) & 15u
+                                             : ((e < 4 ? w0 : w1) >> (8 * (e & 3))) & 255u;
+                wt[k][e] = fmaf(sc, (float)q, bi);
+                dot = fmaf(__bfloat162float(hp[e]), wt[k][e], dot);
+            }
+        }
+    }
+    // The target logit: warp sums, then the warps in order.
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if ((threadIdx.x & 31) == 0) part_sh[threadIdx.x >> 5] = dot;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float raw = 0.f;
+        for (int w = 0; w < kBwdFinThreads / 32; ++w) raw += part_sh[w];
+        float sech2 = 1.f;
+        if (cap > 0.f) {
+            const float th = tanhf(raw / cap);
+            sech2 = 1.f - th * th;
+        }
+        coef_sh = t_ok ? dlogp[r] * sech2 : __int_as_float(0x7fc00000);
     }
     __syncthreads();
     const float coef = coef_sh;
-    for (int d = threadIdx.x; d < H; d += kBwdFinThreads) {
-        float acc = 0.f;
-        for (int s = 0; s < S; ++s) acc += dhp[((int64_t)s * Mpad + i) * H + d];
-        const float wt = t_ok ? dequant_elem(wq, sb, t, d, H, bits) : 0.f;
-        out[d] = fmaf(coef, wt, acc);
+#pragma unroll
+    for (int k = 0; k < kBwdFinUnits; ++k) {
+        const int u = threadIdx.x + k * kBwdFinThreads;
+        if (u >= units) continue;
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = fmaf(coef, wt[k][e], acc[k][e]);
+        float4* dst = reinterpret_cast<float4*>(out + 8 * u);
+        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
     }
 }
 
