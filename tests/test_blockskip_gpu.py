@@ -33,9 +33,9 @@ def _lib():
     qhead.lib()
 
 
-def _peaked(M, H, V, bits, cap, seed, hot_frac=0.9, mask=None, bias_shift=0.3):
+def _peaked(M, H, V, bits, cap, seed, hot_frac=0.9, mask=None, bias_shift=0.3, sb_dtype="f16"):
     head, hot = synth.make_peaked_head(V, H, bits, n_hot=8, bias_shift=bias_shift, softcap=cap,
-                                       seed=seed)
+                                       seed=seed, sb_dtype=sb_dtype)
     h = synth.make_hidden(M, H, seed=seed, mean=0.5)
     t = synth.make_targets(M, V, seed=seed)
     rng = np.random.default_rng(seed)
@@ -81,14 +81,16 @@ def test_eps_zero_is_the_exact_backward():
     assert torch.equal(exact, approx)
 
 
-@pytest.mark.parametrize("M,H,V,bits,cap,eps", [
-    (300, 256, 20000, 4, 30.0, 1e-6),
-    (170, 384, 15000, 8, 0.0, 1e-5),
-    (20, 256, 9000, 4, 30.0, 1e-6),   # below the tensor-core threshold
+@pytest.mark.parametrize("M,H,V,bits,cap,eps,sbt", [
+    (300, 256, 20000, 4, 30.0, 1e-6, "f16"),
+    (170, 384, 15000, 8, 0.0, 1e-5, "f16"),
+    (20, 256, 9000, 4, 30.0, 1e-6, "f16"),   # a 20-row batch
+    (260, 256, 12000, 4, 30.0, 1e-6, "bf16"),
+    (150, 384, 9000, 8, 0.0, 1e-5, "f32"),
 ])
-def test_peaked_blockskip(M, H, V, bits, cap, eps):
+def test_peaked_blockskip(M, H, V, bits, cap, eps, sbt):
     mask = synth.make_mask(M, 20, 0.25)
-    wl = _peaked(M, H, V, bits, cap, seed=M * 3 + V, mask=mask)
+    wl = _peaked(M, H, V, bits, cap, seed=M * 3 + V, mask=mask, sb_dtype=sbt)
     head, h, t, mk, g = to_dev(wl)
     _, lse, _, bm = qhead.fwd_blockmax(head, h, t, mk)
     approx = qhead.bwd_blockskip(head, h, t, lse, g, bm, eps, mk)

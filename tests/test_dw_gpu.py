@@ -6,7 +6,8 @@ sum_m |dlogp_m| (onehot + p) sech2 |h_m| (rows with no target are sums of
 small softmax terms of both signs; the GPU rounds each term's coefficient and
 h once to fp16).  Shapes cover 256- and 128-column tiles, 4 and 8 bits, the
 soft cap on and off, a masked batch, rows sharing a target, several vocab
-chunks, a batch below the tensor-core threshold and one with no active row.
+chunks, a 5-row batch, bf16 and fp32 scales and biases, and a batch with no
+active row.
 """
 import numpy as np
 import pytest
@@ -28,8 +29,8 @@ def _lib():
     qhead.lib()
 
 
-def _workload(M, H, V, bits, cap, seed, mask=None, shared=False):
-    head = synth.make_head(V, H, bits, softcap=cap, seed=seed)
+def _workload(M, H, V, bits, cap, seed, mask=None, shared=False, sb_dtype="f16"):
+    head = synth.make_head(V, H, bits, softcap=cap, seed=seed, sb_dtype=sb_dtype)
     h = synth.make_hidden(M, H, seed=seed)
     t = synth.make_targets(M, V, seed=seed)
     if shared:
@@ -75,15 +76,17 @@ def _run(wl, want_dh=False):
     return head, (h, t, mk, g, lse), dh, dw
 
 
-@pytest.mark.parametrize("M,H,V,bits,cap,masked,shared", [
-    (150, 256, 1800, 4, 30.0, True, False),   # 256-column tiles, partial vocab unit
-    (130, 384, 2100, 8, 0.0, False, True),    # 128-column tiles, 8 bits, shared targets
-    (5, 256, 3000, 4, 30.0, False, False),    # below the tensor-core threshold
-    (70, 512, 1025, 8, 5.0, True, True),
+@pytest.mark.parametrize("M,H,V,bits,cap,masked,shared,sbt", [
+    (150, 256, 1800, 4, 30.0, True, False, "f16"),   # 256-column tiles, partial vocab unit
+    (130, 384, 2100, 8, 0.0, False, True, "f16"),    # 128-column tiles, 8 bits, shared targets
+    (5, 256, 3000, 4, 30.0, False, False, "f16"),    # a 5-row batch
+    (70, 512, 1025, 8, 5.0, True, True, "f16"),
+    (150, 256, 1800, 4, 30.0, True, True, "bf16"),
+    (70, 384, 2100, 8, 5.0, False, False, "f32"),
 ])
-def test_dw_parity(M, H, V, bits, cap, masked, shared):
+def test_dw_parity(M, H, V, bits, cap, masked, shared, sbt):
     mask = synth.make_mask(M, 16, 0.3) if masked else None
-    wl = _workload(M, H, V, bits, cap, seed=M + V, mask=mask, shared=shared)
+    wl = _workload(M, H, V, bits, cap, seed=M + V, mask=mask, shared=shared, sb_dtype=sbt)
     _, _, _, dw = _run(wl)
     _check_dw(wl, dw.cpu().numpy())
 

@@ -34,9 +34,9 @@ def _lib():
     qhead.lib()
 
 
-def _peaked(M, H, V, bits, cap, seed, hot_frac=0.9, mask=None, bias_shift=0.3):
+def _peaked(M, H, V, bits, cap, seed, hot_frac=0.9, mask=None, bias_shift=0.3, sb_dtype="f16"):
     head, hot = synth.make_peaked_head(V, H, bits, n_hot=8, bias_shift=bias_shift, softcap=cap,
-                                       seed=seed)
+                                       seed=seed, sb_dtype=sb_dtype)
     h = synth.make_hidden(M, H, seed=seed, mean=0.5)
     t = synth.make_targets(M, V, seed=seed)
     rng = np.random.default_rng(seed)
@@ -101,15 +101,17 @@ def test_infinite_eps_keeps_exactly_the_target_blocks():
     assert rel.max() <= DH_REL_TOL, f"rel-L2 {rel.max():.3e}"
 
 
-@pytest.mark.parametrize("M,H,V,bits,cap,eps,masked", [
-    (300, 256, 20000, 4, 30.0, 1e-6, True),
-    (170, 384, 15000, 8, 0.0, 1e-5, True),
-    (20, 256, 9000, 4, 30.0, 1e-6, False),     # below the tensor-core threshold
-    (3200, 128, 33000, 4, 30.0, 1e-6, False),  # three vocab chunks
+@pytest.mark.parametrize("M,H,V,bits,cap,eps,masked,sbt", [
+    (300, 256, 20000, 4, 30.0, 1e-6, True, "f16"),
+    (170, 384, 15000, 8, 0.0, 1e-5, True, "f16"),
+    (20, 256, 9000, 4, 30.0, 1e-6, False, "f16"),     # a 20-row batch
+    (3200, 128, 33000, 4, 30.0, 1e-6, False, "f16"),  # three vocab chunks
+    (260, 256, 12000, 4, 30.0, 1e-6, True, "bf16"),
+    (150, 384, 9000, 8, 0.0, 1e-5, False, "f32"),
 ])
-def test_peaked_filter(M, H, V, bits, cap, eps, masked):
+def test_peaked_filter(M, H, V, bits, cap, eps, masked, sbt):
     mask = synth.make_mask(M, 20, 0.25) if masked else None
-    wl = _peaked(M, H, V, bits, cap, seed=M * 7 + V, mask=mask)
+    wl = _peaked(M, H, V, bits, cap, seed=M * 7 + V, mask=mask, sb_dtype=sbt)
     wl.dlogp[::17] = 0.0  # rows that hold nothing warm
     approx, exact, cold = _run(wl, eps)
     approx = approx.cpu().numpy().astype(np.float64)

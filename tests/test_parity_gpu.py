@@ -124,7 +124,7 @@ def test_tensor_core_forward_shapes(M, H, V, bits, cap):
 
 # Scales and biases in bf16 and fp32 (the page widens any float type): the
 # weight-streaming forward (TMA-staged scales at H = 2560, cp.async at 1280)
-# with the CUDA-core backward, and the tensor-core forward and backward.
+# and the tensor-core forward, each with the tensor-core backward.
 SB_SHAPES = [
     (5, 2560, 3001, 4, 30.0, "bf16"),
     (13, 1280, 2000, 8, 0.0, "f32"),

@@ -147,17 +147,23 @@ def make_hidden(M: int, H: int, seed: int = 0, mean: float = 0.0) -> np.ndarray:
 
 
 def make_peaked_head(V: int, H: int, bits: int, n_hot: int, bias_shift: float,
-                     softcap: float = 0.0, seed: int = 0) -> tuple[SynthHead, np.ndarray]:
+                     softcap: float = 0.0, seed: int = 0,
+                     sb_dtype: str = "f16") -> tuple[SynthHead, np.ndarray]:
     """A head as make_head draws it, with every group bias of n_hot vocab rows
     (drawn uniformly without replacement) raised by bias_shift (rounded to
-    fp16).  With hidden states of positive mean (make_hidden(mean=...)), those
-    rows dominate every token's softmax: a peaked distribution, where most
-    vocab tiles carry negligible probability.  Returns (head, hot rows)."""
-    head = make_head(V, H, bits, softcap=softcap, seed=seed)
+    the scales' type).  With hidden states of positive mean
+    (make_hidden(mean=...)), those rows dominate every token's softmax: a
+    peaked distribution, where most vocab tiles carry negligible probability.
+    Returns (head, hot rows)."""
+    head = make_head(V, H, bits, softcap=softcap, seed=seed, sb_dtype=sb_dtype)
     hot = np.sort(_rng(seed, "hot").choice(V, size=n_hot, replace=False))
-    b = head.biases.astype(np.float32)
+    if sb_dtype == "bf16":
+        b = (head.biases.astype(np.uint32) << 16).view(np.float32).copy()
+    else:
+        b = head.biases.astype(np.float32)
     b[hot] += np.float32(bias_shift)
-    head.biases = b.astype(np.float16)
+    head.biases = (f32_to_bf16_bits(b) if sb_dtype == "bf16"
+                   else b.astype(np.float32 if sb_dtype == "f32" else np.float16))
     return head, hot
 
 
