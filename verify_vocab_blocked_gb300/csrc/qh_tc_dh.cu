@@ -232,6 +232,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
         if (lane == 0) {
             int stage = 0, bs = 0;
             uint32_t phase = 0, aphase = 0, bphase = 0;
+            // The operand descriptors of ring slot 0: a slot's are these plus
+            // its byte offset >> 4 in the 14-bit address field, which never
+            // carries (shared addresses stay below 256 KB).  One thread issues
+            // every MMA, so its per-stage instruction latency is on the
+            // tensor pipe's critical path.
+            const uint64_t ad_base = tc::sdesc_sw128(tc::smem_u32(smem + L::OFF_A), 16, 1024);
+            const uint64_t bd_base =
+                tc::sdesc_sw128(tc::smem_u32(smem + L::OFF_B), (BK / 8) * 1024, 1024);
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
                 const int mt = u / (n_nt * KS), ks = u % KS;
                 const int k0 = ks * a.n_k / KS, k1 = (ks + 1) * a.n_k / KS;
@@ -249,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                     if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err, tc::kErrTimeoutDequant))
                         goto mma_abort;
                     tc::tc_fence_after();
-                    const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * L::A_BYTES);
-                    const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
+                    const uint64_t ad0 = ad_base + (uint32_t)(stage * (L::A_BYTES >> 4));
+                    const uint64_t bd0 = bd_base + (uint32_t)(bs * (L::B_BYTES >> 4));
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         if (hh == 1 && first) {
@@ -261,12 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                         }
 #pragma unroll
                         for (int ks2 = 0; ks2 < BK / 16; ++ks2) {
-                            // A: K-major, 32 bytes per 16-element K step inside the swizzle atom.
-                            const uint64_t ad = tc::sdesc_sw128(a0 + hh * L::A_HALF + 32 * ks2, 16, 1024);
-                            // B: MN-major, two 8-row K groups (2 x 1024 B) per K step;
-                            // 64-column blocks along N are BK/8 * 1024 bytes apart.
-                            const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks2, (BK / 8) * 1024, 1024);
-                            tc::umma_f16(tmem_base + hh * BNH, ad, bd, L::IDESC,
+                            // A: K-major, 32 bytes per 16-element K step inside the
+                            // swizzle atom.  B: MN-major, two 8-row K groups (2 x 1024 B)
+                            // per K step; 64-column blocks along N are BK/8 * 1024
+                            // bytes apart (the leading offset).
+                            tc::umma_f16(tmem_base + hh * BNH, ad0 + ((hh * L::A_HALF + 32 * ks2) >> 4),
+                                         bd0 + ((2048 * ks2) >> 4), L::IDESC,
                                          (!first || ks2 > 0) ? 1u : 0u);
                         }
                     }

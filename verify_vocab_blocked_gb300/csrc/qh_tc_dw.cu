@@ -149,6 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dw_kernel(
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, aphase = 0;
+            // The operand descriptors of ring slot 0 (both MN-major: 64-element
+            // MN blocks 8 KB apart); a slot's are these plus its byte offset
+            // >> 4 in the 14-bit address field, which never carries (shared
+            // addresses stay below 256 KB).
+            const uint64_t ad_base = tc::sdesc_sw128(tc::smem_u32(smem + L::OFF_A), 8192, 1024);
+            const uint64_t bd_base = tc::sdesc_sw128(tc::smem_u32(smem + L::OFF_B), 8192, 1024);
             for (int u = blockIdx.x; u < units && !no_k; u += gridDim.x) {
                 // Half h's accumulator may be overwritten once the epilogue has
                 // read it out: half 0 before the unit starts, half 1 before its
@@ -160,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dw_kernel(
                     if (!tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull))
                         goto mma_abort;
                     tc::tc_fence_after();
-                    const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * L::A_BYTES);
-                    const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + stage * L::B_BYTES);
+                    const uint64_t ad0 = ad_base + (uint32_t)(stage * (L::A_BYTES >> 4));
+                    const uint64_t bd0 = bd_base + (uint32_t)(stage * (L::B_BYTES >> 4));
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         if (hh == 1 && kk == 0) {
@@ -171,15 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dw_kernel(
                             tc::tc_fence_after();
                         }
 #pragma unroll
-                        for (int ks2 = 0; ks2 < BK / 16; ++ks2) {
-                            // Both operands MN-major: two 8-row K groups (2 x 1024 B) per
-                            // K step; 64-element MN blocks 8 KB apart.
-                            const uint64_t ad = tc::sdesc_sw128(a0 + hh * L::A_HALF + 2048 * ks2,
-                                                                8192, 1024);
-                            const uint64_t bd = tc::sdesc_sw128(b0 + 2048 * ks2, 8192, 1024);
-                            tc::umma_f16(tmem_base + hh * BN, ad, bd, L::IDESC,
+                        for (int ks2 = 0; ks2 < BK / 16; ++ks2)  // two 8-row K groups per K step
+                            tc::umma_f16(tmem_base + hh * BN, ad0 + ((hh * L::A_HALF + 2048 * ks2) >> 4),
+                                         bd0 + ((2048 * ks2) >> 4), L::IDESC,
                                          (kk > 0 || ks2 > 0) ? 1u : 0u);
-                        }
                     }
                     tc::umma_commit(&empty[stage]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }

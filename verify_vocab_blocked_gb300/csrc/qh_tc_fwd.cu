@@ -342,6 +342,13 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
         if (lane == 0 && rank == 0) {
             int stage = 0, buf = 0, bs = 0;
             uint32_t aphase = 0, bphase = 0;
+            // The operand descriptors of ring slot 0: a slot's are these plus
+            // its byte offset >> 4 in the 14-bit address field, which never
+            // carries (shared addresses stay below 256 KB).  One thread issues
+            // every MMA, so its per-stage instruction latency is on the
+            // tensor pipe's critical path.
+            const uint64_t ad_base = tc::sdesc_sw128(tc::smem_u32(smem + L::OFF_A), 16, 1024);
+            const uint64_t bd_base = tc::sdesc_sw128(tc::smem_u32(smem + L::OFF_B), 16, 1024);
             for (int u = cid; u < W.units; u += n_pairs) {
                 int mt, seg, vt0, vt1;
                 unit_coords(W, a.vt_begin, u, mt, seg, vt0, vt1);
@@ -359,14 +366,11 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                                                    tc::kErrTimeoutDequant))
                             goto mma_abort;
                         tc::tc_fence_after();
-                        const uint32_t a0 = tc::smem_u32(smem + L::OFF_A + stage * A_BYTES);
-                        const uint32_t b0 = tc::smem_u32(smem + L::OFF_B + bs * B_BYTES);
+                        const uint64_t ad = ad_base + (uint32_t)(stage * (A_BYTES >> 4));
+                        const uint64_t bd = bd_base + (uint32_t)(bs * (B_BYTES >> 4));
 #pragma unroll
-                        for (int ks = 0; ks < BK / 16; ++ks) {
-                            const uint64_t ad = tc::sdesc_sw128(a0 + 32 * ks, 16, 1024);
-                            const uint64_t bd = tc::sdesc_sw128(b0 + 32 * ks, 16, 1024);
-                            tc::umma_f16_pair(d_tmem, ad, bd, kIdesc, (kk | ks) != 0);
-                        }
+                        for (int ks = 0; ks < BK / 16; ++ks)  // 32 bytes per 16-element K step
+                            tc::umma_f16_pair(d_tmem, ad + 2 * ks, bd + 2 * ks, kIdesc, (kk | ks) != 0);
                         tc::umma_commit_pair(&empty[stage], kPairMask);
                         tc::umma_commit_pair(&bfree[bs], kPairMask);
                         if (++stage == NS) stage = 0;
