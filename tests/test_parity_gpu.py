@@ -122,6 +122,23 @@ def test_tensor_core_forward_shapes(M, H, V, bits, cap):
     _run_all(_custom(M, H, V, bits, cap, seed=M * 7 + V))
 
 
+# The largest hidden sizes the library accepts (H up to 8192): the
+# weight-streaming forward with its shallowest ring (the staged h rows take
+# most of shared memory), the tensor-core forward with 128 K steps per unit,
+# and the backward with the finalize's widest rows.
+MAX_H_SHAPES = [
+    (5, 8192, 700, 4, 30.0),
+    (9, 4096, 900, 8, 0.0),
+    (40, 8192, 600, 8, 30.0),
+    (130, 4096, 1100, 4, 5.0),
+]
+
+
+@pytest.mark.parametrize("M,H,V,bits,cap", MAX_H_SHAPES)
+def test_max_hidden_sizes(M, H, V, bits, cap):
+    _run_all(_custom(M, H, V, bits, cap, seed=M * 13 + V))
+
+
 # Scales and biases in bf16 and fp32 (the page widens any float type): the
 # weight-streaming forward (TMA-staged scales at H = 2560, cp.async at 1280)
 # and the tensor-core forward, each with the tensor-core backward.
