@@ -139,6 +139,16 @@ def test_max_hidden_sizes(M, H, V, bits, cap):
     _run_all(_custom(M, H, V, bits, cap, seed=M * 13 + V))
 
 
+# Vocabularies of about a million rows (indices past 2^20; the streaming
+# forward's splits and the tensor-core forward's 256-row tiles both ragged).
+@pytest.mark.parametrize("M,H,V,bits,cap", [
+    (5, 128, 1_000_003, 4, 30.0),
+    (20, 128, 600_001, 8, 0.0),
+])
+def test_large_vocabularies(M, H, V, bits, cap):
+    _run_all(_custom(M, H, V, bits, cap, seed=M + 17))
+
+
 # Scales and biases in bf16 and fp32 (the page widens any float type): the
 # weight-streaming forward (TMA-staged scales at H = 2560, cp.async at 1280)
 # and the tensor-core forward, each with the tensor-core backward.
