@@ -227,6 +227,30 @@ def test_invalid_target_gives_nan_not_a_fault():
     assert np.isfinite(logp[0]) and np.isfinite(logp[3])
 
 
+def test_empty_batch_every_entry_point():
+    # M = 0: every entry point returns empty results (and a zero head
+    # gradient) without launching anything that could read past the inputs.
+    wl = _custom(3, 256, 1000, 4, 30.0, seed=14)
+    head, *_ = to_dev(wl)
+    h = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    t = torch.empty(0, dtype=torch.int32, device="cuda")
+    f = torch.empty(0, dtype=torch.float32, device="cuda")
+    logp, lse, am = qhead.fwd(head, h, t)
+    assert logp.numel() == 0 and lse.numel() == 0 and am.numel() == 0
+    assert qhead.bwd(head, h, t, f, f).shape == (0, 256)
+    dh, dw = qhead.bwd_dw(head, h, t, f, f, want_dh=True)
+    torch.cuda.synchronize()
+    assert dh.shape == (0, 256) and dw.shape == (1000, 256)
+    assert torch.count_nonzero(dw).item() == 0
+    dh, cold = qhead.bwd_filter(head, h, t, f, f, 1e-5)
+    assert dh.shape == (0, 256)
+    _, lse, _, bm = qhead.fwd_blockmax(head, h, t)
+    assert bm.shape[0] == 0
+    assert qhead.bwd_blockskip(head, h, t, f, f, bm, 1e-5).shape == (0, 256)
+    n_acc, nxt, am, _ = qhead.verify(head, h, 5, torch.empty(0, 4, dtype=torch.int32, device="cuda"))
+    assert n_acc.numel() == 0 and nxt.numel() == 0 and am.numel() == 0
+
+
 def test_deterministic():
     wl = _custom(70, 256, 4000, 4, 30.0, seed=12, mask=synth.make_mask(70, 32, 0.25))
     head, h, t, mk, g = to_dev(wl)
