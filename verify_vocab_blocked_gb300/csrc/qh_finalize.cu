@@ -24,8 +24,12 @@ namespace qh {
 
 namespace {
 
-constexpr int kFinThreads = 128;
+// Threads per row: 128 for small batches (the verify window: each row's
+// latency is the call's), 64 from 1024 rows (twice the rows in flight; each
+// row one more round of its exact dot products).
+constexpr int kFwdFinRowsWide = 1024;
 
+template <int kFinThreads>
 __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
     const uint32_t* __restrict__ wq, SbView sb, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
@@ -150,17 +154,20 @@ __global__ void __launch_bounds__(kFinThreads) fwd_finalize_kernel(
     }
 }
 
-constexpr int kBwdFinThreads = 512;
-// 8-element units of a row per thread: H <= kMaxH = 8192 is at most 1024 units.
-constexpr int kBwdFinUnits = kMaxH / 8 / kBwdFinThreads;
+// 8-element units of a row per thread (at most two): H <= kMaxH = 8192 is at
+// most 1024 units, 512 threads; rows of H <= 4096 take 256 threads, so that
+// twice as many rows (each a latency-bound round of loads) are in flight.
+constexpr int kBwdFinUnits = 2;
+constexpr int kBwdFinThreadsMax = kMaxH / 8 / kBwdFinUnits;
 
 // One row per block.  Every thread takes the row's 8-element units u = t,
-// t + 512, ...: in one round of loads it reads, per unit, the S partial-dh
+// t + THREADS: in one round of loads it reads, per unit, the S partial-dh
 // slices (the sums it will write) and the target's weights and the hidden
 // states (its part of the exact target logit), so the row costs one global
 // latency, not a dot product by one warp followed by the sums.  The target
 // logit is reduced over the block in a fixed order (deterministic), then
 // dh = sum of slices + dlogp * sech2(target logit) * w_target, exactly in fp32.
+template <int kBwdFinThreads>
 __global__ void __launch_bounds__(kBwdFinThreads) bwd_finalize_kernel(
     const uint32_t* __restrict__ wq, SbView sb, int64_t V, int H, int bits, float cap,
     const __nv_bfloat16* __restrict__ h, const int* __restrict__ pos,
@@ -256,8 +263,11 @@ cudaError_t launch_fwd_finalize(const uint32_t* wq, SbView sb,
                                 float* lse, int32_t* argmax, int64_t M, cudaStream_t st) {
     void* args[] = {&wq, &sb, &V,     &H,   &bits,  &cap,   &h,      &pos,
                     &targets, &part, &S, &S_dev, &err, &logp, &lse, &argmax};
-    return launch_dependent(reinterpret_cast<const void*>(fwd_finalize_kernel), dim3((unsigned)M),
-                            dim3(kFinThreads), 0, st, args);
+    if (M >= kFwdFinRowsWide)
+        return launch_dependent(reinterpret_cast<const void*>(fwd_finalize_kernel<64>),
+                                dim3((unsigned)M), dim3(64), 0, st, args);
+    return launch_dependent(reinterpret_cast<const void*>(fwd_finalize_kernel<128>),
+                            dim3((unsigned)M), dim3(128), 0, st, args);
 }
 
 // Longest accepted draft prefix per verify window (page "mlx-bun 0.0.8 ->
@@ -305,9 +315,13 @@ cudaError_t launch_bwd_finalize(const uint32_t* wq, SbView sb,
                                 const int* pos, const int32_t* targets, const float* dlogp,
                                 const float* dhp, int S, int64_t Mpad, const int* err, float* dh,
                                 int64_t M, cudaStream_t st) {
-    bwd_finalize_kernel<<<(unsigned)M, kBwdFinThreads, 0, st>>>(wq, sb, V, H, bits,
-                                                                 cap, h, pos, targets, dlogp, dhp,
-                                                                 S, Mpad, err, dh);
+    static_assert(kBwdFinThreadsMax == 512, "two units per thread cover kMaxH with 512 threads");
+    if (H <= 4096)
+        bwd_finalize_kernel<256><<<(unsigned)M, 256, 0, st>>>(wq, sb, V, H, bits, cap, h, pos,
+                                                              targets, dlogp, dhp, S, Mpad, err, dh);
+    else
+        bwd_finalize_kernel<512><<<(unsigned)M, 512, 0, st>>>(wq, sb, V, H, bits, cap, h, pos,
+                                                              targets, dlogp, dhp, S, Mpad, err, dh);
     return cudaGetLastError();
 }
 
