@@ -100,3 +100,26 @@ def test_logit_scale_of_the_flat_workloads():
         x = (synth.make_hidden(64, H, seed=10).astype(np.uint32) << 16).view(np.float32)
         raw = x.astype(np.float64) @ w.T
         assert abs(raw.std() - want) < 0.05 * want, (bits, raw.std())
+
+
+@pytest.mark.parametrize("sb_dtype", ["f16", "bf16", "f32"])
+def test_peaked_head_raises_only_the_hot_rows_biases(sb_dtype):
+    # The peaked head is make_head's head with the group biases of n_hot rows
+    # raised by bias_shift, rounded to the scales' own type; nothing else moves.
+    base = synth.make_head(3000, 256, 4, softcap=30.0, seed=41, sb_dtype=sb_dtype)
+    head, hot = synth.make_peaked_head(3000, 256, 4, n_hot=8, bias_shift=0.3, softcap=30.0,
+                                       seed=41, sb_dtype=sb_dtype)
+    assert head.biases.dtype == base.biases.dtype and head.sb_dtype == sb_dtype
+    assert (head.wq == base.wq).all() and (head.scales == base.scales).all()
+
+    def as_f64(b):
+        if sb_dtype == "bf16":
+            return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        return b.astype(np.float64)
+
+    diff = as_f64(head.biases) - as_f64(base.biases)
+    changed = np.flatnonzero(np.abs(diff).max(axis=1) > 0)
+    assert np.array_equal(changed, np.sort(hot)) and len(hot) == 8
+    step = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7, "f32": 2.0 ** -23}[sb_dtype]
+    # raised by 0.3 up to one rounding of the sum (|bias| < 1 here)
+    assert np.allclose(diff[hot], 0.3, atol=step)
