@@ -46,7 +46,8 @@
 // loads); in the odd CTA one otherwise idle thread waits for that barrier and
 // forwards a single cluster-scope arrival to the even CTA's, whose MMA thread
 // thus waits for both CTAs.  Each commit of the MMAs is multicast to the
-// barriers of both CTAs (input stage free, B stage free, accumulator full).
+// barriers of both CTAs (stage free: its inputs and its B slot; accumulator
+// full).
 // Each CTA's epilogue warps arrive on the even CTA's accumulator-empty
 // barrier (once per tile).
 #include <stdio.h>
@@ -85,8 +86,12 @@ constexpr uint32_t kIdesc = tc::idesc_f16_f32(BMU, BN, false, false);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint16_t kPairMask = 0x3;
 
-// Two rings: NS stages of TMA inputs (h tile + packed half-tile) and NB
-// stages of dequantized half-tiles.
+// One ring of NS stages, each the TMA inputs (h tile + packed half-tile) and
+// the dequantized half-tile made from them: a stage's B slot is free again
+// once its inputs are (the MMAs that read A also read B), so the dequant
+// warps wait for the stage's inputs alone and the MMA thread commits once
+// per stage (two rings, with a separate barrier for the B slots, were 2-5 %
+// slower).
 // Scales and biases: boxes of kSbGroups groups x BNH rows of fp16, one box
 // of each per kSbGroups stages, in a ring of NSB slots.
 constexpr int kSbGroups = 8;
@@ -95,17 +100,16 @@ constexpr int SB_BOX = kSbGroups * 2 * BNH;  // bytes of one box (16-byte rows)
 template <int BITS>
 struct Layout {
     static constexpr int NS = BITS == 4 ? 5 : 4;
-    static constexpr int NB = 4;
     static constexpr int NSB = 2;
     static constexpr int P_ROW = BK * BITS / 8;  // packed bytes per row per stage
     static constexpr int P_BYTES = BNH * P_ROW;
     static constexpr int WORDS = BK * BITS / 32;
     static constexpr int OFF_B = 0;
-    static constexpr int OFF_A = OFF_B + NB * B_BYTES;
+    static constexpr int OFF_A = OFF_B + NS * B_BYTES;
     static constexpr int OFF_P = OFF_A + NS * A_BYTES;
     static constexpr int OFF_SB = OFF_P + NS * P_BYTES;  // slot i: scales, then biases
     static constexpr int OFF_BAR = OFF_SB + NSB * 2 * SB_BOX;
-    static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 2 * NSB + 5) + 16;
+    static constexpr int BAR_BYTES = 8 * (3 * NS + 2 * NSB + 5) + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -161,7 +165,6 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     using L = Layout<BITS>;
     using WR = Warps<BITS>;
     constexpr int NS = L::NS;
-    constexpr int NB = L::NB;
     constexpr int NSB = L::NSB;
     const __half* __restrict__ scales = a.scales;
     const __half* __restrict__ biases = a.biases;
@@ -174,10 +177,9 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     // (offsetting the shared array itself keeps the accesses in the shared
     // address space; a round trip through an integer would make them generic)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);  // own TMA inputs landed
-    uint64_t* empty = full + NS;  // inputs consumed (pair MMA commit + own dequant warps)
+    uint64_t* empty = full + NS;  // stage consumed (pair MMA commit + own dequant warps)
     uint64_t* dq = empty + NS;    // own dequant warps done (even CTA: and the odd CTA's relay)
-    uint64_t* bfree = dq + NB;    // B stage consumed (pair MMA commit)
-    uint64_t* accf = bfree + NB;  // accumulator full (pair MMA commit)
+    uint64_t* accf = dq + NS;     // accumulator full (pair MMA commit)
     uint64_t* acce = accf + 2;    // even CTA: both CTAs' epilogues drained the accumulator
     uint64_t* mdrain = acce + 2;  // MMA drain on the abort path
     uint64_t* sbf = mdrain + 1;   // scale / bias boxes landed
@@ -239,10 +241,7 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
         for (int i = 0; i < NS; ++i) {
             tc::mbar_init(&full[i], 1);
             tc::mbar_init(&empty[i], 1 + WR::kDq);
-        }
-        for (int i = 0; i < NB; ++i) {
             tc::mbar_init(&dq[i], WR::kDq + (rank == 0 ? 1 : 0));
-            tc::mbar_init(&bfree[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&accf[i], 1);
@@ -340,8 +339,8 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
-            int stage = 0, buf = 0, bs = 0;
-            uint32_t aphase = 0, bphase = 0;
+            int stage = 0, buf = 0;
+            uint32_t aphase = 0, phase = 0;
             // The operand descriptors of ring slot 0: a slot's are these plus
             // its byte offset >> 4 in the 14-bit address field, which never
             // carries (shared addresses stay below 256 KB).  One thread issues
@@ -362,19 +361,17 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
                     for (int kk = 0; kk < KSTEPS; ++kk) {
                         // Both CTAs' dequant warps have arrived: their B halves
                         // are written and their A tiles have landed.
-                        if (!tc::mbar_wait_cluster(&dq[bs], bphase, abort_flag, err,
+                        if (!tc::mbar_wait_cluster(&dq[stage], phase, abort_flag, err,
                                                    tc::kErrTimeoutDequant))
                             goto mma_abort;
                         tc::tc_fence_after();
                         const uint64_t ad = ad_base + (uint32_t)(stage * (A_BYTES >> 4));
-                        const uint64_t bd = bd_base + (uint32_t)(bs * (B_BYTES >> 4));
+                        const uint64_t bd = bd_base + (uint32_t)(stage * (B_BYTES >> 4));
 #pragma unroll
                         for (int ks = 0; ks < BK / 16; ++ks)  // 32 bytes per 16-element K step
                             tc::umma_f16_pair(d_tmem, ad + 2 * ks, bd + 2 * ks, kIdesc, (kk | ks) != 0);
-                        tc::umma_commit_pair(&empty[stage], kPairMask);
-                        tc::umma_commit_pair(&bfree[bs], kPairMask);
-                        if (++stage == NS) stage = 0;
-                        if (++bs == NB) { bs = 0; bphase ^= 1; }
+                        tc::umma_commit_pair(&empty[stage], kPairMask);  // A, P and B free
+                        if (++stage == NS) { stage = 0; phase ^= 1; }
                     }
                     tc::umma_commit_pair(&accf[buf], kPairMask);
                     if (++buf == 2) { buf = 0; aphase ^= 1; }
@@ -388,14 +385,14 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
         mma_done:;
         } else if (lane == 0) {
             // Odd CTA: forward each stage's "dequant done" to the even CTA.
-            int bs = 0;
-            uint32_t bphase = 0;
+            int stage = 0;
+            uint32_t phase = 0;
             for_each_tile([&](int, int) {
                 for (int kk = 0; kk < KSTEPS; ++kk) {
-                    if (!tc::mbar_wait(&dq[bs], bphase, abort_flag, err, tc::kErrTimeoutDequant))
+                    if (!tc::mbar_wait(&dq[stage], phase, abort_flag, err, tc::kErrTimeoutDequant))
                         return false;
-                    tc::mbar_arrive_cluster_relaxed(dq_lead + 8u * (uint32_t)bs);
-                    if (++bs == NB) { bs = 0; bphase ^= 1; }
+                    tc::mbar_arrive_cluster_relaxed(dq_lead + 8u * (uint32_t)stage);
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
                 return true;
             });
@@ -405,16 +402,16 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
         // Thread: 16-byte part `pt` of vocab row r of this CTA's half-tile.
         const int t = threadIdx.x - 64;
         const int r = t / WR::kTpr, pt = t % WR::kTpr;
-        int stage = 0, bs = 0;
-        uint32_t phase = 0, bphase = 0;
-        // One stage: wait for the inputs and a free B stage, dequantize this
-        // thread's part of row r with scale s2 / bias b2 (fp16 pairs), signal.
+        int stage = 0;
+        uint32_t phase = 0;
+        // One stage: wait for its inputs (its B slot was freed with them),
+        // dequantize this thread's part of row r with scale s2 / bias b2 (fp16
+        // pairs), signal.
         auto stage_work = [&](uint32_t s2, uint32_t b2) {
-            // Results ignored: the warp stays converged (see the abort policy).
+            // Result ignored: the warp stays converged (see the abort policy).
             tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
-            tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
             const unsigned char* prow = smem + L::OFF_P + stage * L::P_BYTES + r * L::P_ROW;
-            unsigned char* brow = smem + L::OFF_B + bs * B_BYTES + r * 128;
+            unsigned char* brow = smem + L::OFF_B + stage * B_BYTES + r * 128;
             const uint4 wv = *reinterpret_cast<const uint4*>(prow + 16 * pt);
             const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
             if constexpr (BITS == 4) {
@@ -439,11 +436,10 @@ __global__ void __launch_bounds__(Warps<BITS>::kThreads, 1) tc_fwd_kernel(
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tc::mbar_arrive(&dq[bs]);
+                tc::mbar_arrive(&dq[stage]);
                 tc::mbar_arrive(&empty[stage]);  // packed half-tile fully read
             }
             if (++stage == NS) { stage = 0; phase ^= 1; }
-            if (++bs == NB) { bs = 0; bphase ^= 1; }
         };
         // Vocab row of this thread in tile t (-1 past the head).
         auto vrow = [&](const TileIt& ti) -> int64_t {
