@@ -31,8 +31,13 @@ namespace {
 constexpr int BM = 128;   // token rows per MMA (M); a unit covers two halves
 constexpr int BMU = 2 * BM;
 constexpr int BK = 64;    // vocab rows per stage
-template <int BITS>
-constexpr int dh_nb() { return BITS == 4 ? 3 : 2; }  // dequantized-tile stages
+// Dequantized-tile stages: as many as input stages for 4-bit heads, so that
+// the two rings are one (a stage's B slot is freed with its inputs: the
+// dequant warps wait for the inputs alone and the MMA thread commits once per
+// step); 8-bit heads, whose packed tiles are twice as large, keep a shorter
+// B ring of their own.
+template <int BITS, int BNH>
+constexpr int dh_nb() { return BITS == 4 ? (BNH == 256 ? 3 : 4) : 2; }
 constexpr int kDqWarps = 8;             // warps 2 .. 9 dequantize
 constexpr int kDqThreads = 32 * kDqWarps;
 constexpr int kEpiWarp0 = 2 + kDqWarps; // warps 10 .. 13 run the epilogue
@@ -45,7 +50,8 @@ constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 template <int BITS, int BNH>
 struct DhLayout {
     static constexpr int NS = BNH == 256 ? 3 : 4;
-    static constexpr int NB = dh_nb<BITS>();
+    static constexpr int NB = dh_nb<BITS, BNH>();
+    static constexpr bool ONE_RING = NB == NS;
     static constexpr int A_BYTES = 2 * BM * BK * 2;         // coeff tiles of both halves, K-major SW128
     static constexpr int A_HALF = BM * BK * 2;
     static constexpr int B_BYTES = BNH * BK * 2;            // weight tile, MN-major SW128
@@ -61,6 +67,7 @@ struct DhLayout {
     static constexpr int OFF_BAR = OFF_SB + NS * SB_BYTES;
     static constexpr int BAR_BYTES = 8 * (2 * NS + 2 * NB + 4) + 16;
     static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
     static constexpr int TMEM_COLS = 2 * BNH;               // the two halves' accumulators
     // Dequant work split: a packed row is PIECES 16-byte pieces; thread t takes
     // piece t % PIECES of rows t / PIECES + RPP * pass.
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                         }
                     }
                     tc::umma_commit(&empty[stage]);
-                    tc::umma_commit(&bfree[bs]);
+                    if constexpr (!L::ONE_RING) tc::umma_commit(&bfree[bs]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                     if (++bs == NB) { bs = 0; bphase ^= 1; }
                     first = false;
@@ -311,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dh_kernel(
                 if (kskip(mt, kk)) continue;
                 // Results ignored: the warp stays converged (see the abort policy).
                 tc::mbar_wait(&full[stage], phase, abort_flag, err, tc::kErrTimeoutFull);
-                tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
+                if constexpr (!L::ONE_RING)
+                    tc::mbar_wait(&bfree[bs], bphase ^ 1, abort_flag, err, tc::kErrTimeoutDequant);
                 const unsigned char* P = smem + L::OFF_P + stage * L::P_BYTES;
                 const __half* sb = reinterpret_cast<const __half*>(smem + L::OFF_SB + stage * L::SB_BYTES);
                 unsigned char* Bs = smem + L::OFF_B + bs * L::B_BYTES;
