@@ -58,6 +58,18 @@ def test_reference_arm_line():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the contract's keys, with the arm's own metric, unit and direction
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert k in line, k
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["higher_is_better"] is True and line["vs_baseline"] is None
+    assert line["config"]["workload"].startswith("tiny")
+    cb = line["cpu_baseline"]
+    assert cb["value"] == line["value"] and cb["unit"] == line["unit"] and cb["cores"] >= 1
+    assert cb["sample"]
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
+    assert line["e2e"]["d2h_bytes_per_step"] == 0
 
 
 def test_reference_arm_under_torchrun_prints_once():
